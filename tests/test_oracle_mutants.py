@@ -1,0 +1,58 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each.
+
+Every mutant is compiled from a patched copy of ``oracle/pa_oracle.c`` into a
+temporary directory and the whole pin suite (test_oracle_pins.py) is run against
+it in a child process; the suite must fail.  The oracle itself is never changed.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pa_oracle.c")
+
+MUTANTS = {
+    "k-layout-group-and-lane-swapped": ("* (D / x) + d / x) * bs + t) * x + d % x",
+                                        "* (D / x) + d % x) * bs + t) * x + d / x"),
+    "v-layout-transposed": ("(((int64_t)b * Hkv + h) * D + d) * bs + t",
+                            "(((int64_t)b * Hkv + h) * bs + t) * D + d"),
+    "fp16-exponent-bias": ("e - 25", "e - 24"),
+    "fp16-subnormal-scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "bf16-shift": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
+    "scale-dropped": ("z[t] = scale * acc;", "z[t] = acc;"),
+    "softmax-sign": ("z[t] = exp(z[t] - m);", "z[t] = exp(m - z[t]);"),
+    "softmax-not-normalised": ("z[t] /= Z;", "z[t] /= 1.0;"),
+    "gqa-mapping-modulo": ("const int kvh = h / G;", "const int kvh = h % num_kv_heads;"),
+    "table-index-offset": ("table_row[t / bs]", "table_row[t % bs]"),
+    "in-block-offset-shifted": ("const int off = t % bs;", "const int off = (t + 1) % bs;"),
+    "length-off-by-one": ("const int L = seq_lens[s];", "const int L = seq_lens[s] - (seq_lens[s] > 1);"),
+    "value-uses-keys": ("acc += z[t] * V[(int64_t)t * D + d];", "acc += z[t] * K[(int64_t)t * D + d];"),
+    "query-not-indexed": ("load(q, qo + d, dtype)", "load(q, qo, dtype)"),
+    "slot-block-from-modulo": ("const int64_t blk = slot / block_size;",
+                               "const int64_t blk = slot % block_size;"),
+    "slot-offset-from-division": ("const int off = (int)(slot % block_size);",
+                                  "const int off = (int)(slot / block_size % block_size);"),
+    "copy-direction-swapped": ("memmove((char*)k_cache + (size_t)dst * blk_bytes, (const char*)k_cache + (size_t)src * blk_bytes",
+                               "memmove((char*)k_cache + (size_t)src * blk_bytes, (const char*)k_cache + (size_t)dst * blk_bytes"),
+    "padding-slot-written": ("if (slot < 0) continue;\n    const int64_t blk", "if (slot < -1) continue;\n    const int64_t blk"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor not unique for {name}"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(text.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    r = subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", str(mutant_c), "-o", str(lib), "-lm"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    env = dict(os.environ, PA_ORACLE_LIB=str(lib), OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
