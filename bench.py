@@ -1,0 +1,448 @@
+"""Benchmark of one decode step of one attention layer over a paged KV pool.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload qwen|llama|long|mixed|tiny] [--block-size 16|32]
+
+A step is the whole hot path on one batch: copy-on-write block copies (the
+mixed workload only), reshape_and_cache of every sequence's new token, and
+decode attention (plus the partition merge when the planner splits).
+`value` is algorithmic bytes per step / step time (inputs resident in HBM, pool
+copies rotated so K/V always come from HBM); `e2e` is the same metric through
+the Python API with the step's inputs copied from pinned host memory and the
+output copied back inside the timed region.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle on the host cores instead: each step is a
+bounded sample of the same workload (one sequence, a subset of its heads).
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged-decode KV read GB/s (% of GB300 HBM peak) and decode tokens/s per layer"
+WORKLOADS = {"tiny": 1, "qwen": 2, "llama": 3, "long": 4, "mixed": 5}
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --- byte accounting ------------------------------------------------------------------------
+
+def decode_bytes(wl, unique=False):
+    """Algorithmic bytes of one decode call: K and V of the valid tokens (per kv head),
+    q and out, the block-table entries walked and seq_lens.  unique=True counts
+    shared physical blocks once (prefix sharing)."""
+    e = W.ELEM_BYTES[wl.dtype]
+    tokens = wl.unique_tokens if unique else wl.total_tokens
+    kv = tokens * wl.num_kv_heads * wl.head_size * e * 2
+    qo = 2 * wl.num_seqs * wl.num_heads * wl.head_size * e
+    tables = int(np.sum(-(-wl.seq_lens.astype(np.int64) // wl.block_size))) * 4 + 4 * wl.num_seqs
+    return kv + qo + tables
+
+
+def write_bytes(wl):
+    """reshape_and_cache (read key/value, write the slots) and block copies (read + write)."""
+    e = W.ELEM_BYTES[wl.dtype]
+    tok = wl.num_seqs * wl.num_kv_heads * wl.head_size * e * 2 * 2 + wl.num_seqs * 8
+    blk = wl.num_kv_heads * wl.head_size * wl.block_size * e * 2
+    return tok + len(wl.cow) * blk * 2 + len(wl.cow) * 16
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# --- clocks --------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# --- distributed plumbing (one process per GPU; replicas, no data-path collective) ---------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, world_size, device=None):
+    """MAX of a per-rank scalar (the timed duration) over all ranks."""
+    if world_size <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world_size, device=None):
+    if world_size > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --- our arm ---------------------------------------------------------------------------------
+
+def describe(wl, cfg):
+    L = wl.seq_lens
+    return {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_size": wl.head_size, "block_size": wl.block_size,
+            "seq_lens": {"min": int(L.min()), "max": int(L.max()), "total": int(L.sum())},
+            "num_blocks": wl.num_blocks, "cow_copies": int(len(wl.cow)), "seed": 306 + cfg}
+
+
+def run_ours(args, wl, cfg, world_size, rank, local_rank):
+    import torch
+    import paged_kv_cache_306_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    e = W.ELEM_BYTES[wl.dtype]
+    pool_bytes = wl.num_blocks * wl.num_kv_heads * wl.head_size * wl.block_size * e * 2
+    copies = max(2, math.ceil(4 * L2_BYTES / pool_bytes))
+    copies = min(copies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // pool_bytes)))
+
+    sets = []
+    for _ in range(copies):
+        sets.append({
+            "q": W.to_torch(wl.q, wl.dtype, dev), "key": W.to_torch(wl.key, wl.dtype, dev),
+            "value": W.to_torch(wl.value, wl.dtype, dev), "k": W.to_torch(wl.k_cache, wl.dtype, dev),
+            "v": W.to_torch(wl.v_cache, wl.dtype, dev), "out": torch.empty(wl.q.shape, dtype=pa_dtype(wl), device=dev),
+        })
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    cow = torch.from_numpy(np.ascontiguousarray(wl.cow)).to(dev)
+    ps = wl.partition_size if args.partition is None else args.partition
+    code = pa.PA_F32 if wl.dtype == "f32" else pa.PA_F16 if wl.dtype == "f16" else pa.PA_BF16
+    resolved = pa.pa_decode_plan_partition(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
+                                           wl.max_seq_len, wl.block_size, code) if ps == -1 else ps
+    ws_bytes = pa.pa_decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
+                                           wl.max_seq_len, wl.block_size, resolved, code)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def step(i, ev=None):
+        s = sets[i % copies]
+        if len(wl.cow):
+            pa.pa_copy_blocks(s["k"], s["v"], cow, stream=stream)
+        pa.pa_reshape_and_cache(s["key"], s["value"], s["k"], s["v"], slots, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.pa_decode(s["out"], s["q"], s["k"], s["v"], bt, sl, wl.scale, wl.max_seq_len, resolved, ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if pa.pa_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # timed region: K steps, events around the whole loop and around every decode call
+    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world_size, dev)
+    torch.cuda.synchronize(dev)
+    launches0 = pa.pa_launch_count()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i, dec_events[i])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    launches = pa.pa_launch_count() - launches0
+    barrier(world_size, dev)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    if pa.pa_get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    ms_total = max_over_ranks(start.elapsed_time(stop), world_size, dev)
+    ms_step = ms_total / args.steps
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_events]))
+
+    # end to end through the API: pinned host inputs in, result out, every step
+    e2e = run_e2e(args, wl, dev, stream, sets[0], bt, sl, resolved, ws)
+
+    step_bytes = decode_bytes(wl) + write_bytes(wl)
+    dbytes = decode_bytes(wl)
+    peak, peak_kind = measured_peaks()
+    achieved = dbytes / (dec_ms * 1e-3) / 1e9
+    traffic = load_traffic(wl)
+    cfgd = describe(wl, cfg)
+    cfgd.update({"partition_size": int(resolved), "pool_copies_rotated": copies,
+                 "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e6:.0f} MB rotated",
+                 "decode_bytes": int(dbytes), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
+                 "step_bytes": int(step_bytes), "decode_us": round(dec_ms * 1e3, 2),
+                 "tokens_per_s_per_layer": round(world_size * wl.num_seqs / (ms_step * 1e-3), 1),
+                 "pct_of_hbm_peak_step": round(100 * step_bytes / (ms_step * 1e-3) / 1e9 / peak, 2),
+                 "peak_gbs": peak, "peak_kind": peak_kind, "parallelism": f"replicas x{world_size}"})
+    line = {
+        "metric": METRIC, "value": round(world_size * step_bytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfgd,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "pa_decode (main kernel + partition merge when split)",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
+    }
+    return line
+
+
+def pa_dtype(wl):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+
+
+def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws):
+    """Same step through the Python API, inputs from pinned host memory each step."""
+    import torch
+    import paged_kv_cache_306_gb300 as pa
+    host = {
+        "q": W.to_torch(wl.q, wl.dtype, "cpu").pin_memory(),
+        "key": W.to_torch(wl.key, wl.dtype, "cpu").pin_memory(),
+        "value": W.to_torch(wl.value, wl.dtype, "cpu").pin_memory(),
+        "bt": torch.from_numpy(wl.block_tables).pin_memory(),
+        "sl": torch.from_numpy(wl.seq_lens).pin_memory(),
+        "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
+        "cow": torch.from_numpy(np.ascontiguousarray(wl.cow)).pin_memory(),
+    }
+    devt = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(wl.q.shape, dtype=pa_dtype(wl)).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    steps = min(args.steps, 2000)
+
+    def step():
+        for k in host:
+            devt[k].copy_(host[k], non_blocking=True)
+        if len(wl.cow):
+            pa.pa_copy_blocks(s["k"], s["v"], devt["cow"], stream=stream)
+        pa.pa_reshape_and_cache(devt["key"], devt["value"], s["k"], s["v"], devt["slots"], stream=stream)
+        pa.pa_decode(s["out"], devt["q"], s["k"], s["v"], devt["bt"], devt["sl"], wl.scale, wl.max_seq_len,
+                     resolved, ws, stream=stream)
+        out_host.copy_(s["out"], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    return {"value": round((decode_bytes(wl) + write_bytes(wl)) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "steps": steps, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def load_traffic(wl):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel source; otherwise null."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        import hashlib
+        d = json.load(open(p))
+        src = open(os.path.join(ROOT, "paged_kv_cache_306_gb300", "csrc", "decode_kernels.cuh"), "rb").read()
+        if d.get("kernel_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        ent = d.get("workloads", {}).get(wl.name)
+        return ent.get("dram_bytes_per_launch") if ent else None
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+# --- the CPU oracle (reference arm and cpu_baseline) ------------------------------------------
+
+def cpu_baseline(wl, seconds=12.0):
+    """The oracle on the host cores over a bounded sample: whole sequences, all heads."""
+    import oracle
+    # the oracle sees the pool after the step's write (as the GPU does)
+    k, v = wl.clone_pools()
+    oracle.copy_blocks(k, v, wl.cow, wl.dtype)
+    oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
+    done, nbytes, t0 = 0, 0, time.perf_counter()
+    order = np.argsort(wl.seq_lens)             # shortest first keeps the sample bounded
+    e = W.ELEM_BYTES[wl.dtype]
+    while time.perf_counter() - t0 < seconds and done < wl.num_seqs:
+        s = int(order[done])
+        sub = W.subset(wl, [s])
+        oracle.decode(sub.q, k, v, sub.block_tables, sub.seq_lens, wl.scale, wl.dtype)
+        nbytes += int(wl.seq_lens[s]) * wl.num_kv_heads * wl.head_size * e * 2
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{done} of {wl.num_seqs} sequences (shortest first), all heads, "
+                                        f"{dt:.1f} s, fp64 C oracle"}
+
+
+def run_reference(args, wl, cfg, world_size, rank):
+    """The CPU oracle as the reference arm: each step is one sequence of the workload."""
+    import oracle
+    k, v = wl.clone_pools()
+    oracle.copy_blocks(k, v, wl.cow, wl.dtype)
+    oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
+    e = W.ELEM_BYTES[wl.dtype]
+    G = wl.num_heads // wl.num_kv_heads
+
+    def one(i, kvh):
+        s = i % wl.num_seqs
+        sub = W.subset(wl, [s])
+        q = np.ascontiguousarray(sub.q[:, :kvh * G])
+        kk = np.ascontiguousarray(k[:, :kvh]) if kvh < wl.num_kv_heads else k
+        vv = np.ascontiguousarray(v[:, :kvh]) if kvh < wl.num_kv_heads else v
+        oracle.decode(q, kk, vv, sub.block_tables, sub.seq_lens, wl.scale, wl.dtype)
+        return int(wl.seq_lens[s]) * kvh * wl.head_size * e * 2
+
+    # size the per-step sample (kv heads of one sequence) so the run stays within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    t = time.perf_counter()
+    one(0, 1)
+    per_head = time.perf_counter() - t
+    kv_sub = int(max(1, min(wl.num_kv_heads, budget // max(per_head, 1e-6))))
+    if kv_sub < wl.num_kv_heads:
+        k = np.ascontiguousarray(k[:, :kv_sub])
+        v = np.ascontiguousarray(v[:, :kv_sub])
+    for i in range(args.warmup):
+        one(i, kv_sub)
+    nbytes, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        nbytes += one(i, kv_sub)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = (f"per step one sequence of the workload (rotating), {kv_sub} of {wl.num_kv_heads} kv heads "
+              f"with their {G} query heads each; fp64 C oracle")
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world_size, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "impl": "reference",
+            "config": describe(wl, cfg),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen")
+    ap.add_argument("--block-size", type=int, default=None, help="mixed workload only: 16 or 32")
+    ap.add_argument("--partition", type=int, default=None, help="override the workload's partition size")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world_size, rank, local_rank = dist_env()
+    cfg = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        wl = W.config(cfg, poison=False, block_size=args.block_size)
+        print(json.dumps(run_reference(args, wl, cfg, world_size, rank)), flush=True)
+        return 0
+
+    if world_size > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    # every rank holds its own replica of the workload (weak scaling)
+    wl = W.config(cfg, poison=False, block_size=args.block_size)
+    line = run_ours(args, wl, cfg, world_size, rank, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+/*
+ * pa.h -- C ABI of the GB300 paged-attention decode library (libpa.so).
+ *
+ * The library implements the two directions of a paged KV cache that the
+ * source pages describe:
+ *   - the write path, which scatters each new token's K/V rows into a pool of
+ *     fixed-size physical blocks through a flat slot number ("Reading vLLM's
+ *     PagedAttention kernel", §3.2), plus the whole-block copy that
+ *     copy-on-write needs ("vLLM's PagedAttention: why the KV cache is paged",
+ *     §4.2);
+ *   - the read path, decode attention: every query row walks its sequence's
+ *     block-table row, gathers K/V from the scattered blocks and folds them
+ *     into an online softmax, optionally split into partitions of
+ *     `partition_size` tokens whose partial results a second pass merges
+ *     ("Reading vLLM's PagedAttention kernel", §2, §3.3, §3.4).
+ *
+ * Memory layouts (all C-contiguous, element type `pa_dtype`):
+ *   q, out        [num_seqs, num_heads, head_size]
+ *   key, value    [num_tokens, num_kv_heads, head_size]
+ *   k_cache       [num_blocks, num_kv_heads, head_size / x, block_size, x],
+ *                 x = 16 / element_size (fp32: 4, fp16 and bf16: 8)
+ *   v_cache       [num_blocks, num_kv_heads, head_size, block_size]
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]; entry i of row s is the
+ *                 physical block that holds tokens i*block_size .. of sequence s
+ *   seq_lens      int32 [num_seqs], the number of valid tokens per sequence
+ *   slot_mapping  int64 [num_tokens], physical_block * block_size + offset
+ *   (cache layouts: "Reading vLLM's PagedAttention kernel", §3.1)
+ *
+ * Query head h reads kv head h / (num_heads / num_kv_heads).
+ *
+ * Conventions for every call:
+ *   - Every buffer is owned by the caller and lives in device memory of the
+ *     current device; the library allocates nothing and keeps no pointer.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  A call validates its host-side arguments, enqueues its
+ *     kernels and returns; it never synchronizes, except
+ *     pa_get_device_error().  A return of PA_OK means the work was enqueued.
+ *   - q, out, key, value, k_cache, v_cache and workspace must be 16-byte
+ *     aligned; block_tables and seq_lens 4-byte; slot_mapping and the
+ *     copy list 8-byte (PA_ERR_ALIGNMENT otherwise).
+ *   - Conditions the host cannot see (a block id outside the pool, a seq_len
+ *     outside [1, max_seq_len], a slot beyond the pool) are checked on the
+ *     device: the offending access is skipped or clamped into the pool, the
+ *     affected outputs are unspecified, and the first such error is recorded
+ *     for pa_get_device_error().
+ *   - Thread safety: calls may be made from several host threads; the
+ *     device-error word and the launch counter are shared per process.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* a size, pointer or combination is invalid */
+  PA_ERR_UNSUPPORTED = 2,  /* valid, but outside what the kernels are built for */
+  PA_ERR_ALIGNMENT = 3,    /* a pointer breaks the alignment rule above */
+  PA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+  PA_ERR_CUDA = 5          /* a CUDA runtime call failed (see pa_last_error_message) */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* partition_size values for pa_decode */
+#define PA_PARTITION_NONE 0    /* one pass over each whole sequence */
+#define PA_PARTITION_AUTO (-1) /* the planner picks from the shape and the SM count */
+
+/* device-side error codes returned by pa_get_device_error */
+#define PA_DEVERR_NONE 0
+#define PA_DEVERR_BLOCK_ID 1   /* a block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN 2    /* a seq_lens entry outside [1, max_seq_len] */
+#define PA_DEVERR_SLOT 3       /* a slot_mapping entry >= num_blocks * block_size */
+#define PA_DEVERR_TIMEOUT 4    /* a pipeline wait in a kernel gave up after ~1 s */
+#define PA_DEVERR_COPY_ID 5    /* a copy_blocks id outside [0, num_blocks) */
+
+/* Human-readable name of a status. Never NULL. */
+PA_API const char* pa_status_string(pa_status s);
+
+/* Detail of the last non-OK status returned on the calling host thread. */
+PA_API const char* pa_last_error_message(void);
+
+/*
+ * Write path ("Reading vLLM's PagedAttention kernel", §3.2): for every token t
+ * with slot = slot_mapping[t] >= 0, copy key[t, h, :] into
+ * k_cache[slot / block_size, h, :, slot % block_size, :] and value[t, h, :] into
+ * v_cache[slot / block_size, h, :, slot % block_size] for all kv heads h.
+ * A pure copy: the bytes of the cache equal the bytes of key/value.
+ * A negative slot marks a padding token, which is skipped.  Two tokens of one
+ * call must not share a slot (the result would be either token's row).
+ * head_size must be a multiple of x; block_size >= 1.
+ */
+PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                               int head_size, int block_size, int64_t num_blocks, pa_dtype dtype,
+                               void* stream);
+
+/*
+ * Copy-on-write block copy ("vLLM's PagedAttention: why the KV cache is paged",
+ * §4.2): for each pair i, physical block src_dst[2i] is copied to block
+ * src_dst[2i+1] -- every kv head, K and V.  The pairs run in parallel: no
+ * destination may repeat and no destination may be a source of the same call.
+ */
+PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int64_t num_pairs,
+                         int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                         pa_dtype dtype, void* stream);
+
+/*
+ * The partition size pa_decode uses for PA_PARTITION_AUTO on the current
+ * device: PA_PARTITION_NONE or a positive multiple of block_size.  The choice
+ * depends only on the arguments and the device's SM count.  Returns -1 for
+ * arguments pa_decode would reject.
+ */
+PA_API int pa_decode_plan_partition(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                             int max_seq_len, int block_size, pa_dtype dtype);
+
+/*
+ * Bytes of workspace pa_decode needs for these arguments (partition_size may be
+ * PA_PARTITION_AUTO; it is resolved as pa_decode_plan_partition does).  Zero
+ * when no split is made.  The workspace holds per-partition maxima, sums and
+ * partial outputs in fp32; its contents need no initialisation and are
+ * meaningless between calls.
+ */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                int max_seq_len, int block_size, int partition_size,
+                                pa_dtype dtype);
+
+/*
+ * Decode attention over the paged pool ("Reading vLLM's PagedAttention
+ * kernel", §2 flowchart, §3.3, §3.4; "KV Cache and PagedAttention memory
+ * management", attention formula): for each sequence s and query head h,
+ *     out[s, h, :] = sum_t softmax_t(scale * <q[s, h, :], K_s[t, :]>) V_s[t, :]
+ * over the tokens t < seq_lens[s], with K_s and V_s gathered in logical order
+ * through block_tables[s] from kv head h / (num_heads / num_kv_heads).
+ * Scores, softmax statistics and the weighted sum are kept in fp32; out is
+ * rounded once to `dtype` (round to nearest even).
+ *
+ * max_seq_len is a host-side bound on every seq_lens entry and must not exceed
+ * max_blocks_per_seq * block_size.  partition_size is PA_PARTITION_NONE,
+ * PA_PARTITION_AUTO or a positive multiple of block_size: a sequence longer
+ * than one partition is processed as independent partitions of that many
+ * tokens whose (max, sum, partial output) results are merged by a second
+ * kernel; the merged result equals the unsplit one up to fp32 rounding, and a
+ * sequence that fits in one partition gives bit-identical output to
+ * PA_PARTITION_NONE.  workspace must hold pa_decode_workspace_size() bytes
+ * (it may be NULL when that is 0).
+ *
+ * Supported: head_size 64 or 128; block_size 16 or 32; num_heads a multiple
+ * of num_kv_heads; num_seqs and num_heads at most 65535.  Output for a given
+ * set of arguments is deterministic and does not depend on the physical
+ * placement of the blocks.
+ */
+PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                    int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
+                    int block_size, int64_t num_blocks, float scale, int partition_size,
+                    void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * Read and clear the first device-side error recorded on the current device
+ * (PA_DEVERR_*; 0 if none).  Synchronizes `stream` first.
+ */
+PA_API pa_status pa_get_device_error(int* code, void* stream);
+
+/* Number of kernels this library has launched in this process (all devices). */
+PA_API uint64_t pa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

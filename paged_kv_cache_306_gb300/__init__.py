@@ -1,0 +1,26 @@
+"""GB300-native paged-attention decode.
+
+A small C-ABI library (``_build/libpa.so``, sources in ``csrc/``, interface in
+``include/pa.h``) with hand-written sm_103a kernels for the two directions of a
+paged KV cache: the write path (``pa_reshape_and_cache``, ``pa_copy_blocks``)
+and decode attention over the block pool (``pa_decode``).  This package is the
+thin Python binding; PyTorch supplies device memory and streams only.
+"""
+from ._binding import (  # noqa: F401
+    DEVICE_ERRORS,
+    LIB_PATH,
+    PA_BF16,
+    PA_F16,
+    PA_F32,
+    PARTITION_AUTO,
+    PARTITION_NONE,
+    PAError,
+    load,
+    pa_copy_blocks,
+    pa_decode,
+    pa_decode_plan_partition,
+    pa_decode_workspace_size,
+    pa_get_device_error,
+    pa_launch_count,
+    pa_reshape_and_cache,
+)

@@ -1,0 +1,170 @@
+"""ctypes binding of libpa.so: argument marshalling only.
+
+Each function takes torch tensors, checks that they match the call's contract
+(device, dtype, shape, contiguity), and passes raw pointers, sizes and the
+current CUDA stream to the C entry point of the same name (include/pa.h).
+Every step of the computation runs in the library's kernels; there is no
+fallback path, and a missing library is an error.
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libpa.so")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_ALIGNMENT, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(6)
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PARTITION_NONE = 0
+PARTITION_AUTO = -1
+DEVICE_ERRORS = {0: "none", 1: "block id outside the pool", 2: "seq_len outside [1, max_seq_len]",
+                 3: "slot outside the pool", 4: "pipeline wait timed out", 5: "copy id outside the pool"}
+
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(message)
+        self.status = status
+
+
+def load():
+    """Load libpa.so (built by ``python -m paged_kv_cache_306_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise PAError(-1, f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_306_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_error_message.argtypes = []
+    lib.pa_last_error_message.restype = ctypes.c_char_p
+    lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i64, i32, P]
+    lib.pa_copy_blocks.argtypes = [P, P, P, i64, i32, i32, i32, i64, i32, P]
+    lib.pa_decode_plan_partition.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.pa_decode_plan_partition.restype = i32
+    lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.pa_decode_workspace_size.restype = sz
+    lib.pa_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, P, sz, i32, P]
+    lib.pa_get_device_error.argtypes = [ctypes.POINTER(i32), P]
+    lib.pa_launch_count.argtypes = []
+    lib.pa_launch_count.restype = ctypes.c_uint64
+    for f in (lib.pa_reshape_and_cache, lib.pa_copy_blocks, lib.pa_decode, lib.pa_get_device_error):
+        f.restype = i32
+    _lib = lib
+    return lib
+
+
+def check(status):
+    if status != PA_OK:
+        lib = load()
+        name = lib.pa_status_string(status).decode()
+        msg = lib.pa_last_error_message().decode()
+        raise PAError(status, f"{name}: {msg}")
+
+
+def dtype_code(torch_dtype):
+    import torch
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    if torch_dtype not in codes:
+        raise PAError(PA_ERR_UNSUPPORTED, f"unsupported dtype {torch_dtype}")
+    return codes[torch_dtype]
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() else ctypes.c_void_p(0)
+
+
+def _need_cuda(name, t, dtype=None, dims=None):
+    if not t.is_cuda:
+        raise PAError(PA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise PAError(PA_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise PAError(PA_ERR_INVALID_ARG, f"{name} has dtype {t.dtype}, expected {dtype}")
+    if dims is not None and t.dim() != dims:
+        raise PAError(PA_ERR_INVALID_ARG, f"{name} must have {dims} dims")
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
+    """Scatter key/value [T, Hkv, D] into the paged pools through slot_mapping (int64 [T])."""
+    import torch
+    for n, t in (("key", key), ("value", value), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("slot_mapping", slot_mapping, torch.int64, 1)
+    T, hkv, d = key.shape
+    nb, bs = v_cache.shape[0], v_cache.shape[3]
+    check(load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                                      T, hkv, d, bs, nb, dtype_code(k_cache.dtype), _stream(stream)))
+
+
+def pa_copy_blocks(k_cache, v_cache, src_dst, stream=None):
+    """Copy whole physical blocks: src_dst is int64 [n, 2] of (src, dst)."""
+    import torch
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("src_dst", src_dst, torch.int64)
+    nb, hkv, d, bs = v_cache.shape
+    check(load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst), src_dst.numel() // 2, hkv, d, bs, nb,
+                                dtype_code(k_cache.dtype), _stream(stream)))
+
+
+def pa_decode_plan_partition(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype):
+    return load().pa_decode_plan_partition(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size,
+                                           dtype if isinstance(dtype, int) else dtype_code(dtype))
+
+
+def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, partition_size,
+                             dtype):
+    return load().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size,
+                                           partition_size, dtype if isinstance(dtype, int) else dtype_code(dtype))
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len,
+              partition_size=PARTITION_AUTO, workspace=None, stream=None):
+    """Decode attention over the paged pool; writes out [S, H, D].
+
+    max_seq_len is a host-side bound on seq_lens.  When the call needs a
+    workspace and none is given, one is taken from torch's allocator.
+    Returns the workspace tensor used (or None).
+    """
+    import torch
+    dt = q.dtype
+    _need_cuda("q", q, dt, 3)
+    _need_cuda("out", out, dt, 3)
+    _need_cuda("k_cache", k_cache, dt, 5)
+    _need_cuda("v_cache", v_cache, dt, 4)
+    _need_cuda("block_tables", block_tables, torch.int32, 2)
+    _need_cuda("seq_lens", seq_lens, torch.int32, 1)
+    S, H, D = q.shape
+    nb, hkv, _, bs = v_cache.shape
+    code = dtype_code(dt)
+    lib = load()
+    need = lib.pa_decode_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, code)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                        block_tables.shape[1], _ptr(seq_lens), S, max_seq_len, H, hkv, D, bs, nb, float(scale),
+                        partition_size, _ptr(workspace), ws_bytes, code, _stream(stream)))
+    return workspace
+
+
+def pa_get_device_error(stream=None):
+    """Read and clear the first device-side error (0 if none); synchronizes the stream."""
+    code = ctypes.c_int(0)
+    check(load().pa_get_device_error(ctypes.byref(code), _stream(stream)))
+    return code.value
+
+
+def pa_launch_count():
+    return load().pa_launch_count()

@@ -1,0 +1,322 @@
+// api.cu -- the C ABI of libpa (include/pa.h): argument validation, the
+// partition planner and launch dispatch.  No call allocates device memory or
+// synchronizes, except pa_get_device_error.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_launch.h"
+
+namespace {
+
+// The first device-side error of the process on each device (PA_DEVERR_*).
+__device__ unsigned g_device_error;
+
+thread_local char t_message[512] = "";
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+
+pa_status fail(pa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_message, sizeof t_message, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device address of g_device_error on the current device (looked up once per device).
+pa_status device_error_ptr(unsigned** out) {
+  static std::mutex mu;
+  static unsigned* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  *out = ptrs[dev];
+  return PA_OK;
+}
+
+int sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int elem_bytes(pa_dtype d) { return d == PA_F32 ? 4 : (d == PA_F16 || d == PA_BF16) ? 2 : 0; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Shape checks shared by the planner, the workspace query and pa_decode.
+pa_status check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len,
+                             int block_size, pa_dtype dtype) {
+  if (!elem_bytes(dtype)) return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (num_seqs < 0 || num_seqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_seqs %d outside [0, 65535]", num_seqs);
+  if (num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "num_heads %d must be a positive multiple of num_kv_heads %d", num_heads,
+                num_kv_heads);
+  if (num_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_heads %d > 65535", num_heads);
+  if (head_size != 64 && head_size != 128) return fail(PA_ERR_UNSUPPORTED, "head_size %d not in {64, 128}", head_size);
+  if (block_size != 16 && block_size != 32)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d not in {16, 32}", block_size);
+  if (max_seq_len < 1) return fail(PA_ERR_INVALID_ARG, "max_seq_len %d < 1", max_seq_len);
+  return PA_OK;
+}
+
+// Blocks per partition for a resolved partition size (NONE: the whole sequence).
+int partition_blocks(int partition_size, int max_seq_len, int block_size) {
+  const int nblk = ceil_div(max_seq_len, block_size);
+  return partition_size == PA_PARTITION_NONE ? nblk : partition_size / block_size;
+}
+
+// The planner: split sequences into partitions so that the grid holds about
+// eight waves of resident CTAs (a ragged batch averages about half of that),
+// but never below 256 tokens per partition, where the partial results would
+// start to cost a visible share of the traffic.
+int plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len, int block_size,
+         pa_dtype dtype) {
+  const int group = num_heads / num_kv_heads;
+  const pa::DecodeKind kind = pa::decode_kind(static_cast<int>(dtype), group);
+  const long long units_per_seq =
+      kind == pa::DecodeKind::kMma ? (long long)num_kv_heads * ((group + 15) / 16) : num_heads;
+  const int ctas = pa::decode_ctas_per_sm(static_cast<int>(dtype), head_size, block_size, kind);
+  const long long slots = (long long)sm_count() * (ctas > 0 ? ctas : 1);
+  const int nblk = ceil_div(max_seq_len, block_size);
+  const int min_pb = 256 / block_size;
+  const long long base = (long long)num_seqs * units_per_seq;
+  if (nblk <= min_pb || base == 0) return PA_PARTITION_NONE;
+  const long long want = (8 * slots + base - 1) / base;
+  if (want <= 1) return PA_PARTITION_NONE;
+  int pb = ceil_div(nblk, want);
+  if (pb < min_pb) pb = min_pb;
+  const int nparts = ceil_div(nblk, pb);
+  if (nparts <= 1) return PA_PARTITION_NONE;
+  pb = ceil_div(nblk, nparts);
+  return pb * block_size;
+}
+
+size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int num_parts) {
+  if (num_parts <= 1) return 0;
+  const size_t n = (size_t)num_seqs * num_heads * num_parts;
+  const size_t ml = (n * 2 * sizeof(float) + 255) / 256 * 256;
+  return ml + n * head_size * sizeof(float);
+}
+
+}  // namespace
+
+namespace pa {
+
+int decode_ctas_per_sm(int dtype, int head_size, int block_size, DecodeKind kind) {
+  switch (dtype) {
+    case PA_F32: return decode_ctas_per_sm_f32(head_size, block_size, kind);
+    case PA_F16: return decode_ctas_per_sm_f16(head_size, block_size, kind);
+    case PA_BF16: return decode_ctas_per_sm_bf16(head_size, block_size, kind);
+    default: return 0;
+  }
+}
+
+cudaError_t launch_decode(int dtype, int head_size, const DecodeParams& p, DecodeKind kind, cudaStream_t stream,
+                          int* launches) {
+  switch (dtype) {
+    case PA_F32: return launch_decode_f32(head_size, p, kind, stream, launches);
+    case PA_F16: return launch_decode_f16(head_size, p, kind, stream, launches);
+    case PA_BF16: return launch_decode_bf16(head_size, p, kind, stream, launches);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_ALIGNMENT: return "PA_ERR_ALIGNMENT";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+const char* pa_last_error_message(void) { return t_message; }
+
+uint64_t pa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_size,
+                               int block_size, int64_t num_blocks, pa_dtype dtype, void* stream) {
+  const int e = elem_bytes(dtype);
+  if (!e) return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (num_tokens < 0 || num_tokens > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_tokens %lld", (long long)num_tokens);
+  if (num_kv_heads < 1 || head_size < 1 || block_size < 1 || num_blocks < 1)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads, head_size, block_size and num_blocks must be positive");
+  if (head_size % (16 / e)) return fail(PA_ERR_INVALID_ARG, "head_size %d not a multiple of x = %d", head_size, 16 / e);
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return fail(PA_ERR_ALIGNMENT, "key/value/caches need 16-byte, slot_mapping 8-byte alignment");
+  unsigned* err = nullptr;
+  pa_status st = device_error_ptr(&err);
+  if (st != PA_OK) return st;
+  int n = 0;
+  cudaError_t ce = pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads,
+                                                head_size, block_size, num_blocks, e, err,
+                                                static_cast<cudaStream_t>(stream), &n);
+  g_launches.fetch_add(n, std::memory_order_relaxed);
+  return ce == cudaSuccess ? PA_OK : cuda_fail(ce, "reshape_and_cache launch");
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int64_t num_pairs, int num_kv_heads,
+                         int head_size, int block_size, int64_t num_blocks, pa_dtype dtype, void* stream) {
+  const int e = elem_bytes(dtype);
+  if (!e) return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (num_pairs < 0 || num_pairs > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_pairs %lld", (long long)num_pairs);
+  if (num_kv_heads < 1 || head_size < 1 || block_size < 1 || num_blocks < 1)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads, head_size, block_size and num_blocks must be positive");
+  const long long block_bytes = (long long)num_kv_heads * head_size * block_size * e;
+  if (block_bytes % 16) return fail(PA_ERR_INVALID_ARG, "a block of %lld bytes is not a multiple of 16", block_bytes);
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_dst) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst, 8))
+    return fail(PA_ERR_ALIGNMENT, "caches need 16-byte, src_dst 8-byte alignment");
+  unsigned* err = nullptr;
+  pa_status st = device_error_ptr(&err);
+  if (st != PA_OK) return st;
+  int n = 0;
+  cudaError_t ce = pa::launch_copy_blocks(k_cache, v_cache, src_dst, num_pairs, block_bytes, num_blocks, err,
+                                          static_cast<cudaStream_t>(stream), &n);
+  g_launches.fetch_add(n, std::memory_order_relaxed);
+  return ce == cudaSuccess ? PA_OK : cuda_fail(ce, "copy_blocks launch");
+}
+
+int pa_decode_plan_partition(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len,
+                             int block_size, pa_dtype dtype) {
+  if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype) != PA_OK)
+    return -1;
+  return plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len,
+                                int block_size, int partition_size, pa_dtype dtype) {
+  if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype) != PA_OK)
+    return 0;
+  if (partition_size == PA_PARTITION_AUTO)
+    partition_size = plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
+  if (partition_size < 0 || (partition_size > 0 && partition_size % block_size)) return 0;
+  const int pb = partition_blocks(partition_size, max_seq_len, block_size);
+  return workspace_bytes_for(num_seqs, num_heads, head_size, ceil_div(ceil_div(max_seq_len, block_size), pb));
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                    int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int max_seq_len, int num_heads,
+                    int num_kv_heads, int head_size, int block_size, int64_t num_blocks, float scale,
+                    int partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  pa_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
+  if (st != PA_OK) return st;
+  if (max_blocks_per_seq < 1 || (long long)max_seq_len > (long long)max_blocks_per_seq * block_size)
+    return fail(PA_ERR_INVALID_ARG, "max_seq_len %d exceeds max_blocks_per_seq %d * block_size %d", max_seq_len,
+                max_blocks_per_seq, block_size);
+  if (num_blocks < 1) return fail(PA_ERR_INVALID_ARG, "num_blocks %lld < 1", (long long)num_blocks);
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+  if (partition_size == PA_PARTITION_AUTO)
+    partition_size = plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
+  if (partition_size < 0 || (partition_size > 0 && partition_size % block_size))
+    return fail(PA_ERR_INVALID_ARG, "partition_size %d must be NONE, AUTO or a positive multiple of block_size %d",
+                partition_size, block_size);
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return fail(PA_ERR_ALIGNMENT, "q/out/caches need 16-byte, block_tables/seq_lens 4-byte alignment");
+
+  const int nblk = ceil_div(max_seq_len, block_size);
+  const int pb = partition_blocks(partition_size, max_seq_len, block_size);
+  const int num_parts = ceil_div(nblk, pb);
+  if (num_parts > 12 * 1024)
+    return fail(PA_ERR_UNSUPPORTED, "%d partitions per sequence (more than 12288); use a larger partition_size",
+                num_parts);
+  const size_t need = workspace_bytes_for(num_seqs, num_heads, head_size, num_parts);
+  if (need) {
+    if (!workspace || workspace_bytes < need)
+      return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
+    if (!aligned(workspace, 16)) return fail(PA_ERR_ALIGNMENT, "workspace needs 16-byte alignment");
+  }
+
+  pa::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  if (need) {
+    const size_t n = (size_t)num_seqs * num_heads * num_parts;
+    p.part_ml = static_cast<float*>(workspace);
+    p.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + (n * 2 * sizeof(float) + 255) / 256 * 256);
+  }
+  st = device_error_ptr(&p.err);
+  if (st != PA_OK) return st;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.max_seq_len = max_seq_len;
+  p.block_size = block_size;
+  p.part_blocks = pb;
+  p.num_parts = num_parts;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+  int n = 0;
+  const cudaError_t ce = pa::launch_decode(static_cast<int>(dtype), head_size, p,
+                                           pa::decode_kind(static_cast<int>(dtype), p.group),
+                                           static_cast<cudaStream_t>(stream), &n);
+  g_launches.fetch_add(n, std::memory_order_relaxed);
+  return ce == cudaSuccess ? PA_OK : cuda_fail(ce, "decode launch");
+}
+
+pa_status pa_get_device_error(int* code, void* stream) {
+  if (!code) return fail(PA_ERR_INVALID_ARG, "null code pointer");
+  unsigned* err = nullptr;
+  pa_status st = device_error_ptr(&err);
+  if (st != PA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  const unsigned zero = 0;
+  e = cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  *code = static_cast<int>(v);
+  return PA_OK;
+}
+
+}  // extern "C"

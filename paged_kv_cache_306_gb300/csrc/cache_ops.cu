@@ -1,0 +1,116 @@
+// cache_ops.cu -- the write side of the paged KV cache.
+//
+// reshape_and_cache ("Reading vLLM's PagedAttention kernel", §3.2): each new
+// token carries a flat slot (physical block * block_size + offset); its K and V
+// rows are copied into that slot of the pools.  In the K pool a token's row is
+// head_size/x runs of 16 bytes (one per x-element group), so every 16-byte
+// group of the key row lands as one 16-byte store; the V pool stores a token's
+// row with a stride of block_size elements, so V is an element scatter.
+//
+// copy_blocks ("vLLM's PagedAttention: why the KV cache is paged", §4.2): before
+// a shared block is written it is copied whole to a fresh block; a physical
+// block of one pool is one contiguous run of bytes, copied with 16-byte vectors.
+#include <stdint.h>
+
+#include "pa_device.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+
+template <int E> struct Word;
+template <> struct Word<2> { using type = uint16_t; };
+template <> struct Word<4> { using type = uint32_t; };
+
+// One CTA per token.
+template <int E>
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_kernel(const unsigned char* __restrict__ key, const unsigned char* __restrict__ value,
+                             unsigned char* __restrict__ k_cache, unsigned char* __restrict__ v_cache,
+                             const int64_t* __restrict__ slot_mapping, int num_kv_heads, int head_size,
+                             int block_size, long long num_blocks, unsigned* err) {
+  using W = typename Word<E>::type;
+  constexpr int X = 16 / E;
+  const long long t = blockIdx.x;
+  const long long slot = slot_mapping[t];
+  if (slot < 0) return;  // padding token
+  if (slot >= num_blocks * block_size) {
+    if (threadIdx.x == 0) set_error(err, kErrSlot);
+    return;
+  }
+  const long long blk = slot / block_size;
+  const int off = static_cast<int>(slot - blk * block_size);
+  const int groups_per_head = head_size / X;
+  const long long row = t * num_kv_heads * head_size;  // first element of token t's rows
+
+  // K: 16-byte group g of head h -> k_cache[blk, h, g, off, :]
+  for (int c = threadIdx.x; c < num_kv_heads * groups_per_head; c += blockDim.x) {
+    const int h = c / groups_per_head, g = c - h * groups_per_head;
+    const uint4 v = *reinterpret_cast<const uint4*>(key + (row + (long long)c * X) * E);
+    const long long dst = (((blk * num_kv_heads + h) * groups_per_head + g) * block_size + off) * X;
+    *reinterpret_cast<uint4*>(k_cache + dst * E) = v;
+  }
+  // V: element (h, d) -> v_cache[blk, h, d, off]
+  for (int i = threadIdx.x; i < num_kv_heads * head_size; i += blockDim.x) {
+    const int h = i / head_size, d = i - h * head_size;
+    const W v = reinterpret_cast<const W*>(value)[row + i];
+    reinterpret_cast<W*>(v_cache)[((blk * num_kv_heads + h) * head_size + d) * block_size + off] = v;
+  }
+}
+
+// grid = (num_pairs, 2 [K, V], chunks)
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(unsigned char* k_cache, unsigned char* v_cache, const int64_t* __restrict__ src_dst,
+                       long long block_bytes, long long num_blocks, unsigned* err) {
+  const long long i = blockIdx.x;
+  const long long src = src_dst[2 * i], dst = src_dst[2 * i + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_error(err, kErrCopyId);
+    return;
+  }
+  unsigned char* base = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint4* s = reinterpret_cast<const uint4*>(base + src * block_bytes);
+  uint4* d = reinterpret_cast<uint4*>(base + dst * block_bytes);
+  const long long nvec = block_bytes / 16;
+  for (long long v = (long long)blockIdx.z * blockDim.x + threadIdx.x; v < nvec; v += (long long)gridDim.z * blockDim.x)
+    d[v] = s[v];
+}
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                                     int head_size, int block_size, int64_t num_blocks, int elem_bytes,
+                                     unsigned* err, cudaStream_t stream, int* launches) {
+  *launches = 0;
+  if (num_tokens == 0) return cudaSuccess;
+  const auto* kp = static_cast<const unsigned char*>(key);
+  const auto* vp = static_cast<const unsigned char*>(value);
+  auto* kc = static_cast<unsigned char*>(k_cache);
+  auto* vc = static_cast<unsigned char*>(v_cache);
+  if (elem_bytes == 4)
+    reshape_and_cache_kernel<4><<<static_cast<unsigned>(num_tokens), 128, 0, stream>>>(
+        kp, vp, kc, vc, slot_mapping, num_kv_heads, head_size, block_size, num_blocks, err);
+  else
+    reshape_and_cache_kernel<2><<<static_cast<unsigned>(num_tokens), 128, 0, stream>>>(
+        kp, vp, kc, vc, slot_mapping, num_kv_heads, head_size, block_size, num_blocks, err);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) *launches = 1;
+  return e;
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int64_t num_pairs,
+                               int64_t block_bytes, int64_t num_blocks, unsigned* err, cudaStream_t stream,
+                               int* launches) {
+  *launches = 0;
+  if (num_pairs == 0) return cudaSuccess;
+  const long long nvec = block_bytes / 16;
+  long long chunks = (nvec + 256 * 4 - 1) / (256 * 4);
+  if (chunks > 64) chunks = 64;
+  dim3 grid(static_cast<unsigned>(num_pairs), 2, static_cast<unsigned>(chunks));
+  copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<unsigned char*>(k_cache),
+                                               static_cast<unsigned char*>(v_cache), src_dst, block_bytes,
+                                               num_blocks, err);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) *launches = 1;
+  return e;
+}
+
+}  // namespace pa

@@ -1,0 +1,127 @@
+"""The C-ABI library builds, loads and exports what include/pa.h declares (no GPU).
+
+Only host-side argument checks are exercised here: each call below is rejected
+before any CUDA call is made.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_306_gb300 as pa
+from paged_kv_cache_306_gb300 import _binding as B
+from paged_kv_cache_306_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(pa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return B.load()
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for n in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_size",
+              "pa_decode_plan_partition", "pa_get_device_error", "pa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    # nothing else with the pa_ prefix leaks out as a C symbol
+    raw = ctypes.CDLL(B.LIB_PATH)
+    assert raw.pa_decode is not None
+
+
+def test_status_strings(lib):
+    assert lib.pa_status_string(0) == b"PA_OK"
+    assert lib.pa_status_string(4) == b"PA_ERR_WORKSPACE"
+    assert lib.pa_status_string(99) == b"PA_ERR_UNKNOWN"
+
+
+def _decode(lib, **kw):
+    a = dict(out=8192, q=8192, k=8192, v=8192, bt=8192, mb=4, sl=8192, S=1, msl=16, H=4, Hkv=4, D=128, bs=16,
+             nb=8, scale=0.1, ps=0, ws=None, wsb=0, dt=B.PA_F16)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.pa_decode(P(a["out"]), P(a["q"]), P(a["k"]), P(a["v"]), P(a["bt"]), a["mb"], P(a["sl"]), a["S"],
+                         a["msl"], a["H"], a["Hkv"], a["D"], a["bs"], a["nb"], a["scale"], a["ps"], P(a["ws"]),
+                         a["wsb"], a["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H=6, Hkv=4), B.PA_ERR_INVALID_ARG),           # heads not a multiple of kv heads
+    (dict(D=96), B.PA_ERR_UNSUPPORTED),                 # head size outside {64, 128}
+    (dict(bs=8), B.PA_ERR_UNSUPPORTED),                 # block size outside {16, 32}
+    (dict(msl=65), B.PA_ERR_INVALID_ARG),               # max_seq_len beyond the table width
+    (dict(msl=0), B.PA_ERR_INVALID_ARG),
+    (dict(ps=24), B.PA_ERR_INVALID_ARG),                # partition not a multiple of block_size
+    (dict(ps=-2), B.PA_ERR_INVALID_ARG),
+    (dict(dt=7), B.PA_ERR_INVALID_ARG),
+    (dict(nb=0), B.PA_ERR_INVALID_ARG),
+    (dict(S=-1), B.PA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), B.PA_ERR_INVALID_ARG),
+    (dict(q=8200), B.PA_ERR_ALIGNMENT),                 # q not 16-byte aligned
+    (dict(bt=8194), B.PA_ERR_ALIGNMENT),
+    (dict(q=0), B.PA_ERR_INVALID_ARG),                  # null pointer
+    (dict(msl=64, ps=16), B.PA_ERR_WORKSPACE),          # split needs a workspace
+])
+def test_decode_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert _decode(lib, **kw) == status
+    assert lib.pa_last_error_message()
+
+
+def test_decode_with_no_sequences_is_a_no_op(lib):
+    assert _decode(lib, S=0, q=0, out=0) == B.PA_OK
+
+
+def test_workspace_size_for_an_explicit_split(lib):
+    # 2 seqs, 8 heads, 3 partitions of 32 tokens over max_seq_len 70 -> (2 + 128) floats per partial
+    n = 2 * 8 * 3
+    ml = (n * 2 * 4 + 255) // 256 * 256
+    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 32, B.PA_F16) == ml + n * 128 * 4
+    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 0, B.PA_F16) == 0
+    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 96, B.PA_F16) == 0   # one partition
+    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 24, B.PA_F16) == 0   # invalid split
+
+
+def test_plan_rejects_what_decode_rejects(lib):
+    assert lib.pa_decode_plan_partition(1, 6, 4, 128, 100, 16, B.PA_F16) == -1
+    assert lib.pa_decode_plan_partition(1, 4, 4, 96, 100, 16, B.PA_F16) == -1
+
+
+def test_write_path_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    st = lib.pa_reshape_and_cache(P(16), P(16), P(16), P(16), P(16), 4, 2, 60, 16, 8, B.PA_F16, None)
+    assert st == B.PA_ERR_INVALID_ARG                   # head size not a multiple of x
+    st = lib.pa_reshape_and_cache(P(16), P(16), P(24), P(16), P(16), 4, 2, 64, 16, 8, B.PA_F16, None)
+    assert st == B.PA_ERR_ALIGNMENT
+    st = lib.pa_reshape_and_cache(None, None, None, None, None, 0, 2, 64, 16, 8, B.PA_F16, None)
+    assert st == B.PA_OK                                # nothing to write
+    st = lib.pa_copy_blocks(P(16), P(16), P(12), 3, 2, 64, 16, 8, B.PA_F16, None)
+    assert st == B.PA_ERR_ALIGNMENT
+    st = lib.pa_copy_blocks(P(16), P(16), P(16), 3, 2, 64, 16, 8, 5, None)
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 4, 128, dtype=torch.float16)
+    with pytest.raises(pa.PAError):
+        pa.pa_decode(q, q, torch.zeros(1, 4, 16, 16, 8, dtype=torch.float16),
+                     torch.zeros(1, 4, 128, 16, dtype=torch.float16), torch.zeros(1, 1, dtype=torch.int32),
+                     torch.ones(1, dtype=torch.int32), 0.1, 1)
