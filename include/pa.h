@@ -176,6 +176,38 @@ PA_API pa_status pa_get_device_error(int* code, void* stream);
 /* Number of kernels this library has launched in this process (all devices). */
 PA_API uint64_t pa_launch_count(void);
 
+/*
+ * Decode with no allocation anywhere: the same computation, arguments and
+ * results as pa_decode, but the per-partition scratch lives in a fixed array
+ * inside the library instead of a caller-provided workspace.  This serves
+ * callers that cannot call cudaMalloc at the point where they decode -- for
+ * example a process that reserved its whole memory budget up front (weights
+ * plus the KV pool) and forbids later allocations, or a caller on a latency
+ * path where an allocation may synchronize the device.  (The pages have no
+ * counterpart to this call: it is a deployment convenience of this library.)
+ *
+ *   - The array holds PA_NOALLOC_SCRATCH_BYTES (32 MiB) and every GPU that loads
+ *     libpa keeps it until the process exits.  A shape whose split needs more
+ *     (see pa_decode_workspace_size) is rejected with PA_ERR_WORKSPACE before
+ *     anything is enqueued; pick a larger partition_size or use pa_decode.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture begins.
+ *   - Every call on a device shares the one array and it keeps whatever the last
+ *     call left there.  Nothing in it has to start at zero: each call writes
+ *     every partial result before its merge reads it.  Calls whose work overlaps
+ *     on the GPU (other streams, other host threads) race on the array and give
+ *     undefined results: order them on one stream.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                   int num_heads, int num_kv_heads, int head_size, int block_size,
+                                   int64_t num_blocks, float scale, int partition_size,
+                                   pa_dtype dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

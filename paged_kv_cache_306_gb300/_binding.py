@@ -48,6 +48,8 @@ def load():
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, P, sz, i32, P]
+    lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, i32, P]
+    lib.pa_decode_noalloc.restype = i32
     lib.pa_get_device_error.argtypes = [ctypes.POINTER(i32), P]
     lib.pa_launch_count.argtypes = []
     lib.pa_launch_count.restype = ctypes.c_uint64

@@ -128,6 +128,10 @@ size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int num_p
 
 namespace pa {
 
+// Record a failure with a message for pa_last_error_message (used by other
+// translation units of the library).
+pa_status record_failure(pa_status st, const char* message) { return fail(st, "%s", message); }
+
 int decode_ctas_per_sm(int dtype, int head_size, int block_size, DecodeKind kind) {
   switch (dtype) {
     case PA_F32: return decode_ctas_per_sm_f32(head_size, block_size, kind);
