@@ -85,43 +85,72 @@ pa_status check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int 
   return PA_OK;
 }
 
-// Blocks per partition for a resolved partition size (NONE: the whole sequence).
-int partition_blocks(int partition_size, int max_seq_len, int block_size) {
-  const int nblk = ceil_div(max_seq_len, block_size);
-  return partition_size == PA_PARTITION_NONE ? nblk : partition_size / block_size;
-}
+// How one pa_decode call is cut into launches and how its workspace is laid out.
+struct DecodePlan {
+  pa::DecodeKind kind;
+  int units;         // head units per sequence
+  int rows;          // query rows per unit
+  int part_blocks;   // caller partition in blocks (a huge value when none)
+  int chunk;         // sequences per launch
+  int grid;          // CTAs of the main kernel (all resident)
+  long long slots;   // partial-result slots
+  size_t off_tag, off_ml, off_o, off_first, off_last, bytes;
+};
 
-// The planner: split sequences into partitions so that the grid holds about
-// eight waves of resident CTAs (a ragged batch averages about half of that),
-// but never below 256 tokens per partition, where the partial results would
-// start to cost a visible share of the traffic.
-int plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len, int block_size,
-         pa_dtype dtype) {
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The schedule: the main kernel runs exactly the CTAs that fit on the GPU at once
+// (fewer for small batches, so that every warp gets a few blocks); each warp takes
+// an equal share of all blocks of the launch.  A launch covers at most
+// kMaxSeqsPerLaunch sequences.  Partial slots: one per warp plus one per segment
+// and per caller partition, the most pieces a launch can leave.
+pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len, int block_size,
+                    int partition_size, pa_dtype dtype, DecodePlan* pl) {
   const int group = num_heads / num_kv_heads;
-  const pa::DecodeKind kind = pa::decode_kind(static_cast<int>(dtype), group);
-  const long long units_per_seq =
-      kind == pa::DecodeKind::kMma ? (long long)num_kv_heads * ((group + 15) / 16) : num_heads;
-  const int ctas = pa::decode_ctas_per_sm(static_cast<int>(dtype), head_size, block_size, kind);
-  const long long slots = (long long)sm_count() * (ctas > 0 ? ctas : 1);
-  const int nblk = ceil_div(max_seq_len, block_size);
-  const int min_pb = 256 / block_size;
-  const long long base = (long long)num_seqs * units_per_seq;
-  if (nblk <= min_pb || base == 0) return PA_PARTITION_NONE;
-  const long long want = (8 * slots + base - 1) / base;
-  if (want <= 1) return PA_PARTITION_NONE;
-  int pb = ceil_div(nblk, want);
-  if (pb < min_pb) pb = min_pb;
-  const int nparts = ceil_div(nblk, pb);
-  if (nparts <= 1) return PA_PARTITION_NONE;
-  pb = ceil_div(nblk, nparts);
-  return pb * block_size;
+  pl->kind = pa::decode_kind(static_cast<int>(dtype), group);
+  pl->units = pa::decode_units(pl->kind, num_heads, num_kv_heads);
+  pl->rows = pa::decode_rows(pl->kind, num_heads, num_kv_heads);
+  const int nblk_max = ceil_div(max_seq_len, block_size);
+  pl->part_blocks = partition_size > 0 ? partition_size / block_size : (1 << 30);
+  long long chunk = num_seqs < pa::kMaxSeqsPerLaunch ? num_seqs : pa::kMaxSeqsPerLaunch;
+  if (chunk > 0x7fffffffLL / nblk_max) chunk = 0x7fffffffLL / nblk_max;
+  if (chunk < 1) chunk = 1;
+  pl->chunk = static_cast<int>(chunk);
+  const int ctas = pa::decode_ctas_per_sm(static_cast<int>(dtype), head_size, block_size, pl->kind);
+  const int sms = sm_count();
+  if (ctas <= 0 || sms <= 0) return fail(PA_ERR_CUDA, "cannot query the device (SM count %d, CTAs per SM %d)", sms, ctas);
+  const long long work = chunk * pl->units * (long long)nblk_max;
+  long long grid = (work + 4 * pa::kDecodeWarps - 1) / (4 * pa::kDecodeWarps);
+  if (grid > (long long)sms * ctas) grid = (long long)sms * ctas;
+  if (grid < 1) grid = 1;
+  pl->grid = static_cast<int>(grid);
+  const long long np_max = (nblk_max + pl->part_blocks - 1) / pl->part_blocks;
+  const long long segs = chunk * pl->units;
+  pl->slots = grid * pa::kDecodeWarps + segs * np_max;
+  if (pl->slots > 0x7fffffffLL || segs > 0x7fffffffLL)
+    return fail(PA_ERR_UNSUPPORTED, "too many partial results (%lld); use a larger partition_size", pl->slots);
+  size_t off = 0;
+  pl->off_tag = off;
+  off = align256(off + (size_t)pl->slots * 8);
+  pl->off_ml = off;
+  off = align256(off + (size_t)pl->slots * pl->rows * 2 * sizeof(float));
+  pl->off_o = off;
+  off = align256(off + (size_t)pl->slots * pl->rows * head_size * sizeof(float));
+  pl->off_first = off;
+  off = align256(off + (size_t)segs * sizeof(int));
+  pl->off_last = off;
+  off = align256(off + (size_t)segs * sizeof(int));
+  pl->bytes = off;
+  return PA_OK;
 }
 
-size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int num_parts) {
-  if (num_parts <= 1) return 0;
-  const size_t n = (size_t)num_seqs * num_heads * num_parts;
-  const size_t ml = (n * 2 * sizeof(float) + 255) / 256 * 256;
-  return ml + n * head_size * sizeof(float);
+// A fresh tag for every launch, so a launch never mistakes an earlier launch's
+// partial slot for its own.  Zero is never used.
+unsigned next_epoch() {
+  static std::atomic<unsigned> epoch{0};
+  unsigned e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
 }
 
 }  // namespace
@@ -141,12 +170,12 @@ int decode_ctas_per_sm(int dtype, int head_size, int block_size, DecodeKind kind
   }
 }
 
-cudaError_t launch_decode(int dtype, int head_size, const DecodeParams& p, DecodeKind kind, cudaStream_t stream,
-                          int* launches) {
+cudaError_t launch_decode(int dtype, int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
+                          cudaStream_t stream, int* launches) {
   switch (dtype) {
-    case PA_F32: return launch_decode_f32(head_size, p, kind, stream, launches);
-    case PA_F16: return launch_decode_f16(head_size, p, kind, stream, launches);
-    case PA_BF16: return launch_decode_bf16(head_size, p, kind, stream, launches);
+    case PA_F32: return launch_decode_f32(head_size, block_size, p, kind, grid, stream, launches);
+    case PA_F16: return launch_decode_f16(head_size, block_size, p, kind, grid, stream, launches);
+    case PA_BF16: return launch_decode_bf16(head_size, block_size, p, kind, grid, stream, launches);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -223,18 +252,22 @@ int pa_decode_plan_partition(int num_seqs, int num_heads, int num_kv_heads, int 
                              int block_size, pa_dtype dtype) {
   if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype) != PA_OK)
     return -1;
-  return plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
+  // The load-balanced schedule needs no caller partitions: every warp already gets
+  // an equal share of the blocks, and long sequences are split wherever that falls.
+  return PA_PARTITION_NONE;
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len,
                                 int block_size, int partition_size, pa_dtype dtype) {
   if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype) != PA_OK)
     return 0;
-  if (partition_size == PA_PARTITION_AUTO)
-    partition_size = plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
-  if (partition_size < 0 || (partition_size > 0 && partition_size % block_size)) return 0;
-  const int pb = partition_blocks(partition_size, max_seq_len, block_size);
-  return workspace_bytes_for(num_seqs, num_heads, head_size, ceil_div(ceil_div(max_seq_len, block_size), pb));
+  if (partition_size == PA_PARTITION_AUTO) partition_size = PA_PARTITION_NONE;
+  if (partition_size < 0 || (partition_size > 0 && partition_size % block_size) || num_seqs == 0) return 0;
+  DecodePlan pl;
+  if (make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, partition_size, dtype, &pl) !=
+      PA_OK)
+    return 0;
+  return pl.bytes;
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -248,8 +281,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                 max_blocks_per_seq, block_size);
   if (num_blocks < 1) return fail(PA_ERR_INVALID_ARG, "num_blocks %lld < 1", (long long)num_blocks);
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
-  if (partition_size == PA_PARTITION_AUTO)
-    partition_size = plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
+  if (partition_size == PA_PARTITION_AUTO) partition_size = PA_PARTITION_NONE;
   if (partition_size < 0 || (partition_size > 0 && partition_size % block_size))
     return fail(PA_ERR_INVALID_ARG, "partition_size %d must be NONE, AUTO or a positive multiple of block_size %d",
                 partition_size, block_size);
@@ -259,51 +291,51 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return fail(PA_ERR_ALIGNMENT, "q/out/caches need 16-byte, block_tables/seq_lens 4-byte alignment");
 
-  const int nblk = ceil_div(max_seq_len, block_size);
-  const int pb = partition_blocks(partition_size, max_seq_len, block_size);
-  const int num_parts = ceil_div(nblk, pb);
-  if (num_parts > 12 * 1024)
-    return fail(PA_ERR_UNSUPPORTED, "%d partitions per sequence (more than 12288); use a larger partition_size",
-                num_parts);
-  const size_t need = workspace_bytes_for(num_seqs, num_heads, head_size, num_parts);
-  if (need) {
-    if (!workspace || workspace_bytes < need)
-      return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
-    if (!aligned(workspace, 16)) return fail(PA_ERR_ALIGNMENT, "workspace needs 16-byte alignment");
-  }
+  DecodePlan pl;
+  st = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, partition_size, dtype, &pl);
+  if (st != PA_OK) return st;
+  if (!workspace || workspace_bytes < pl.bytes)
+    return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pl.bytes, workspace ? workspace_bytes : 0);
+  if (!aligned(workspace, 16)) return fail(PA_ERR_ALIGNMENT, "workspace needs 16-byte alignment");
 
   pa::DecodeParams p{};
-  p.out = out;
-  p.q = q;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.block_tables = block_tables;
-  p.seq_lens = seq_lens;
-  if (need) {
-    const size_t n = (size_t)num_seqs * num_heads * num_parts;
-    p.part_ml = static_cast<float*>(workspace);
-    p.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + (n * 2 * sizeof(float) + 255) / 256 * 256);
-  }
+  char* ws = static_cast<char*>(workspace);
+  p.part_tag = reinterpret_cast<int2*>(ws + pl.off_tag);
+  p.part_ml = reinterpret_cast<float*>(ws + pl.off_ml);
+  p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
+  p.seg_first = reinterpret_cast<int*>(ws + pl.off_first);
+  p.seg_last = reinterpret_cast<int*>(ws + pl.off_last);
   st = device_error_ptr(&p.err);
   if (st != PA_OK) return st;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
   p.num_blocks = num_blocks;
   p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_seqs = num_seqs;
   p.num_heads = num_heads;
   p.num_kv_heads = num_kv_heads;
   p.group = num_heads / num_kv_heads;
+  p.units = pl.units;
+  p.rows = pl.rows;
   p.max_seq_len = max_seq_len;
-  p.block_size = block_size;
-  p.part_blocks = pb;
-  p.num_parts = num_parts;
+  p.part_blocks = pl.part_blocks;
+  p.num_slots = static_cast<int>(pl.slots);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
-  int n = 0;
-  const cudaError_t ce = pa::launch_decode(static_cast<int>(dtype), head_size, p,
-                                           pa::decode_kind(static_cast<int>(dtype), p.group),
-                                           static_cast<cudaStream_t>(stream), &n);
-  g_launches.fetch_add(n, std::memory_order_relaxed);
-  return ce == cudaSuccess ? PA_OK : cuda_fail(ce, "decode launch");
+  const size_t row_bytes = (size_t)num_heads * head_size * elem_bytes(dtype);
+  for (int c0 = 0; c0 < num_seqs; c0 += pl.chunk) {
+    p.num_seqs = num_seqs - c0 < pl.chunk ? num_seqs - c0 : pl.chunk;
+    p.q = static_cast<const char*>(q) + (size_t)c0 * row_bytes;
+    p.out = static_cast<char*>(out) + (size_t)c0 * row_bytes;
+    p.block_tables = block_tables + (size_t)c0 * max_blocks_per_seq;
+    p.seq_lens = seq_lens + c0;
+    p.epoch = next_epoch();
+    int n = 0;
+    const cudaError_t ce = pa::launch_decode(static_cast<int>(dtype), head_size, block_size, p, pl.kind, pl.grid,
+                                             static_cast<cudaStream_t>(stream), &n);
+    g_launches.fetch_add(n, std::memory_order_relaxed);
+    if (ce != cudaSuccess) return cuda_fail(ce, "decode launch");
+  }
+  return PA_OK;
 }
 
 pa_status pa_get_device_error(int* code, void* stream) {

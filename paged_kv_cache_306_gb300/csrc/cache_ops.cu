@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(128)
                              int block_size, long long num_blocks, unsigned* err) {
   using W = typename Word<E>::type;
   constexpr int X = 16 / E;
+  // let a following decode launch start its set-up; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long t = blockIdx.x;
   const long long slot = slot_mapping[t];
   if (slot < 0) return;  // padding token
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(128)
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(unsigned char* k_cache, unsigned char* v_cache, const int64_t* __restrict__ src_dst,
                        long long block_bytes, long long num_blocks, unsigned* err) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long i = blockIdx.x;
   const long long src = src_dst[2 * i], dst = src_dst[2 * i + 1];
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {

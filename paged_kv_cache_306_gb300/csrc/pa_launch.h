@@ -7,28 +7,38 @@
 
 namespace pa {
 
+// Sequences handled by one launch of the decode kernels (their per-sequence
+// tables live in shared memory); larger batches are launched in chunks.
+constexpr int kMaxSeqsPerLaunch = 1024;
+constexpr int kDecodeWarps = 4;  // warps per decode CTA; every warp is an independent worker
+
 // Everything a decode launch needs; passed to the kernels by value.
 struct DecodeParams {
-  void* out;                 // [S, H, D] in the cache dtype
-  const void* q;             // [S, H, D]
-  const void* k_cache;       // [NB, Hkv, D/x, BS, x]
-  const void* v_cache;       // [NB, Hkv, D, BS]
+  void* out;                    // [S, H, D] in the cache dtype
+  const void* q;                // [S, H, D]
+  const void* k_cache;          // [NB, Hkv, D/x, BS, x]
+  const void* v_cache;          // [NB, Hkv, D, BS]
   const int32_t* block_tables;  // [S, max_blocks_per_seq]
   const int32_t* seq_lens;      // [S]
-  float* part_ml;            // [S, H, num_parts, 2]: (max in log2 units, sum) per partition
-  float* part_o;             // [S, H, num_parts, D]: normalised partial outputs
-  unsigned* err;             // device error word
+  float* part_ml;               // [slots, rows, 2]: (max in log2 units, sum) of a piece
+  float* part_o;                // [slots, rows, D]: normalised partial output of a piece
+  int2* part_tag;               // [slots]: (segment, epoch) that wrote the slot
+  int* seg_first;               // [S * units]: first piece's slot, or -1 when no merge is needed
+  int* seg_last;                // [S * units]: last piece's slot
+  unsigned* err;                // device error word
   long long num_blocks;
   int max_blocks_per_seq;
-  int num_seqs;
+  int num_seqs;                 // <= kMaxSeqsPerLaunch
   int num_heads;
   int num_kv_heads;
-  int group;                 // num_heads / num_kv_heads
+  int group;                    // num_heads / num_kv_heads
+  int units;                    // head units per sequence (a segment is one sequence x one unit)
+  int rows;                     // query rows per unit stored in a partial slot
   int max_seq_len;
-  int block_size;
-  int part_blocks;           // blocks per partition (>= every sequence's block count when unsplit)
-  int num_parts;             // partitions of a max_seq_len sequence
-  float scale_log2;          // scale * log2(e)
+  int part_blocks;              // blocks per caller partition; a huge value when none
+  int num_slots;                // partial-result slots in the workspace
+  unsigned epoch;               // distinguishes this launch's partial slots from stale ones
+  float scale_log2;             // scale * log2(e)
 };
 
 enum class DecodeKind { kSimt = 0, kMma = 1 };
@@ -39,21 +49,33 @@ inline DecodeKind decode_kind(int dtype, int group) {
   return (dtype != 0 && group >= 2) ? DecodeKind::kMma : DecodeKind::kSimt;
 }
 
+// Head units per sequence and query rows per unit for a kernel kind.
+inline int decode_units(DecodeKind k, int num_heads, int num_kv_heads) {
+  const int g = num_heads / num_kv_heads;
+  return k == DecodeKind::kMma ? num_kv_heads * ((g + 15) / 16) : num_heads;
+}
+inline int decode_rows(DecodeKind k, int num_heads, int num_kv_heads) {
+  const int g = num_heads / num_kv_heads;
+  return k == DecodeKind::kMma ? (g < 16 ? g : 16) : 1;
+}
+
 // Resident CTAs per SM of the main decode kernel for (dtype, D, BS, kind); 0 if unsupported.
 int decode_ctas_per_sm(int dtype, int head_size, int block_size, DecodeKind kind);
 
-// Enqueue the main decode kernel and, when some sequence spans more than one
-// partition, the merge kernel.  *launches receives the number of kernels enqueued.
-cudaError_t launch_decode(int dtype, int head_size, const DecodeParams& p, DecodeKind kind,
-                          cudaStream_t stream, int* launches);
+// Enqueue the main decode kernel (grid CTAs) and the merge kernel for one chunk of sequences.
+cudaError_t launch_decode(int dtype, int head_size, int block_size, const DecodeParams& p, DecodeKind kind,
+                          int grid, cudaStream_t stream, int* launches);
 
 // Per-dtype entry points (decode_<dtype>.cu).
 int decode_ctas_per_sm_f32(int head_size, int block_size, DecodeKind kind);
 int decode_ctas_per_sm_f16(int head_size, int block_size, DecodeKind kind);
 int decode_ctas_per_sm_bf16(int head_size, int block_size, DecodeKind kind);
-cudaError_t launch_decode_f32(int head_size, const DecodeParams& p, DecodeKind kind, cudaStream_t s, int* n);
-cudaError_t launch_decode_f16(int head_size, const DecodeParams& p, DecodeKind kind, cudaStream_t s, int* n);
-cudaError_t launch_decode_bf16(int head_size, const DecodeParams& p, DecodeKind kind, cudaStream_t s, int* n);
+cudaError_t launch_decode_f32(int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
+                              cudaStream_t s, int* n);
+cudaError_t launch_decode_f16(int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
+                              cudaStream_t s, int* n);
+cudaError_t launch_decode_bf16(int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
+                               cudaStream_t s, int* n);
 
 // Write path (cache_ops.cu).
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,

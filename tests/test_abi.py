@@ -78,7 +78,6 @@ def _decode(lib, **kw):
     (dict(q=8200), B.PA_ERR_ALIGNMENT),                 # q not 16-byte aligned
     (dict(bt=8194), B.PA_ERR_ALIGNMENT),
     (dict(q=0), B.PA_ERR_INVALID_ARG),                  # null pointer
-    (dict(msl=64, ps=16), B.PA_ERR_WORKSPACE),          # split needs a workspace
 ])
 def test_decode_rejects_bad_arguments_on_the_host(lib, kw, status):
     assert _decode(lib, **kw) == status
@@ -89,14 +88,11 @@ def test_decode_with_no_sequences_is_a_no_op(lib):
     assert _decode(lib, S=0, q=0, out=0) == B.PA_OK
 
 
-def test_workspace_size_for_an_explicit_split(lib):
-    # 2 seqs, 8 heads, 3 partitions of 32 tokens over max_seq_len 70 -> (2 + 128) floats per partial
-    n = 2 * 8 * 3
-    ml = (n * 2 * 4 + 255) // 256 * 256
-    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 32, B.PA_F16) == ml + n * 128 * 4
-    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 0, B.PA_F16) == 0
-    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 96, B.PA_F16) == 0   # one partition
-    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 24, B.PA_F16) == 0   # invalid split
+def test_workspace_size_is_zero_for_arguments_decode_rejects(lib):
+    assert lib.pa_decode_workspace_size(2, 8, 2, 96, 70, 16, 0, B.PA_F16) == 0     # head size
+    assert lib.pa_decode_workspace_size(2, 8, 3, 128, 70, 16, 0, B.PA_F16) == 0    # heads vs kv heads
+    assert lib.pa_decode_workspace_size(2, 8, 2, 128, 70, 16, 24, B.PA_F16) == 0   # partition not a block multiple
+    assert lib.pa_decode_workspace_size(0, 8, 2, 128, 70, 16, 0, B.PA_F16) == 0    # nothing to do
 
 
 def test_plan_rejects_what_decode_rejects(lib):

@@ -214,6 +214,26 @@ def test_workspace_too_small_is_rejected():
     assert st == 4
 
 
+def test_workspace_grows_with_caller_partitions_and_covers_every_call():
+    import paged_kv_cache_306_gb300 as pa
+    lib = pa.load()
+    none = lib.pa_decode_workspace_size(64, 28, 4, 128, 4096, 16, 0, pa.PA_F16)
+    auto = lib.pa_decode_workspace_size(64, 28, 4, 128, 4096, 16, -1, pa.PA_F16)
+    p256 = lib.pa_decode_workspace_size(64, 28, 4, 128, 4096, 16, 256, pa.PA_F16)
+    assert none > 0 and auto == none and p256 > none
+    assert lib.pa_decode_plan_partition(64, 28, 4, 128, 4096, 16, pa.PA_F16) == 0
+
+
+def test_more_sequences_than_one_launch_holds():
+    """Batches beyond one launch's sequence tables are cut into several launches."""
+    rng = np.random.default_rng(29)
+    L = rng.integers(1, 90, size=2100)
+    wl = W.make_private("many", "f16", L, 8, 2, 64, 16, seed=30, partition_size=-1)
+    out, _ = gpu_step(wl)
+    k, v = oracle_pools(wl)
+    assert_close(as_f64(out), oracle_out(wl, k, v), "f16", with_rounding=True)
+
+
 def test_launch_count_counts_kernels():
     import paged_kv_cache_306_gb300 as pa
     wl = W.make_private("cnt", "f16", [2000, 100], 8, 2, 128, 16, seed=28, partition_size=256)
