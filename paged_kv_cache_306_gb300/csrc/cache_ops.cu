@@ -30,8 +30,8 @@ __global__ void __launch_bounds__(128)
                              int block_size, long long num_blocks, unsigned* err) {
   using W = typename Word<E>::type;
   constexpr int X = 16 / E;
-  // let a following decode launch start its set-up; it waits for this grid to finish
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  griddep_wait();
+  griddep_launch_dependents();
   const long long t = blockIdx.x;
   const long long slot = slot_mapping[t];
   if (slot < 0) return;  // padding token
@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(128)
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(unsigned char* k_cache, unsigned char* v_cache, const int64_t* __restrict__ src_dst,
                        long long block_bytes, long long num_blocks, unsigned* err) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  griddep_wait();
+  griddep_launch_dependents();
   const long long i = blockIdx.x;
   const long long src = src_dst[2 * i], dst = src_dst[2 * i + 1];
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -88,13 +89,13 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
   const auto* vp = static_cast<const unsigned char*>(value);
   auto* kc = static_cast<unsigned char*>(k_cache);
   auto* vc = static_cast<unsigned char*>(v_cache);
-  if (elem_bytes == 4)
-    reshape_and_cache_kernel<4><<<static_cast<unsigned>(num_tokens), 128, 0, stream>>>(
-        kp, vp, kc, vc, slot_mapping, num_kv_heads, head_size, block_size, num_blocks, err);
-  else
-    reshape_and_cache_kernel<2><<<static_cast<unsigned>(num_tokens), 128, 0, stream>>>(
-        kp, vp, kc, vc, slot_mapping, num_kv_heads, head_size, block_size, num_blocks, err);
-  const cudaError_t e = cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(num_tokens));
+  const cudaError_t e =
+      elem_bytes == 4
+          ? launch_pdl(reshape_and_cache_kernel<4>, grid, dim3(128), 0, stream, kp, vp, kc, vc, slot_mapping,
+                       num_kv_heads, head_size, block_size, (long long)num_blocks, err)
+          : launch_pdl(reshape_and_cache_kernel<2>, grid, dim3(128), 0, stream, kp, vp, kc, vc, slot_mapping,
+                       num_kv_heads, head_size, block_size, (long long)num_blocks, err);
   if (e == cudaSuccess) *launches = 1;
   return e;
 }
@@ -108,10 +109,9 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_
   long long chunks = (nvec + 256 * 4 - 1) / (256 * 4);
   if (chunks > 64) chunks = 64;
   dim3 grid(static_cast<unsigned>(num_pairs), 2, static_cast<unsigned>(chunks));
-  copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<unsigned char*>(k_cache),
-                                               static_cast<unsigned char*>(v_cache), src_dst, block_bytes,
-                                               num_blocks, err);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(256), 0, stream,
+                                   static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache),
+                                   src_dst, (long long)block_bytes, (long long)num_blocks, err);
   if (e == cudaSuccess) *launches = 1;
   return e;
 }

@@ -36,9 +36,9 @@
 //   * CUDA-core math (fp32 caches, or one query head per kv head): half-warps split
 //     the head dims of the scores, lanes split V rows and token chunks for P V, and
 //     the reductions are warp shuffles.
-//   * Programmatic dependent launch: the kernels are launched so that they may start
-//     while the previous kernel in the stream finishes; they wait for it
-//     (griddepcontrol.wait) before touching any input.
+//   * Programmatic dependent launch (see pa_device.cuh): the decode kernel becomes
+//     resident while the write-path kernel before it finishes, and the merge kernel
+//     while the decode kernel finishes.
 #pragma once
 
 #include <math.h>
@@ -51,11 +51,6 @@
 namespace pa {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s, then PA_DEVERR_TIMEOUT
-
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Ring depth per warp from the bytes of one stage (K tile + V tile).
 constexpr int decode_stages(int stage_bytes) {
@@ -649,6 +644,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   __shared__ float red[NW];
   __shared__ float o_s[NW][D];
   griddep_wait();
+  griddep_launch_dependents();
   const int seg = blockIdx.x / p.rows, r = blockIdx.x - seg * p.rows;
   const int first = p.seg_first[seg];
   if (first < 0) return;
@@ -736,21 +732,6 @@ int decode_ctas_per_sm_t() {
                                                     decode_smem_bytes<T, D, BS>()) != cudaSuccess)
     return 0;
   return n;
-}
-
-template <typename K>
-cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, int smem, cudaStream_t stream, const DecodeParams& p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <typename T, int D, int BS, bool kMma>

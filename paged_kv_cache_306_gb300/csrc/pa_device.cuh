@@ -5,7 +5,10 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <utility>
 
 namespace pa {
 
@@ -16,6 +19,36 @@ enum : unsigned { kErrNone = 0, kErrBlockId = 1, kErrSeqLen = 2, kErrSlot = 3, k
 // Record `code` unless an earlier error is already recorded.
 __device__ __forceinline__ void set_error(unsigned* err, unsigned code) {
   if (err) atomicCAS(err, 0u, code);
+}
+
+// ---- programmatic dependent launch ----------------------------------------------------------
+//
+// Every kernel of the library is launched so that it may become resident while
+// the previous kernel of the stream is still running.  Before it touches any
+// memory it waits for that kernel to finish and for its writes to be visible
+// (griddep_wait); as soon as it starts it lets the next kernel do the same
+// (griddep_launch_dependents).  A kernel never waits on a later one, so the
+// chain cannot deadlock.
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- dtype traits ---------------------------------------------------------------------------
