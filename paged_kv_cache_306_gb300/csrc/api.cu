@@ -94,7 +94,7 @@ struct DecodePlan {
   int chunk;         // sequences per launch
   int grid;          // CTAs of the main kernel (all resident)
   long long slots;   // partial-result slots
-  size_t off_tag, off_ml, off_o, off_first, off_last, off_count, bytes;
+  size_t off_tag, off_ml, off_o, off_first, off_last, bytes;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -140,8 +140,6 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   off = align256(off + (size_t)segs * sizeof(int));
   pl->off_last = off;
   off = align256(off + (size_t)segs * sizeof(int));
-  pl->off_count = off;
-  off = align256(off + (size_t)segs * sizeof(unsigned long long));
   pl->bytes = off;
   return PA_OK;
 }
@@ -307,7 +305,6 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.seg_first = reinterpret_cast<int*>(ws + pl.off_first);
   p.seg_last = reinterpret_cast<int*>(ws + pl.off_last);
-  p.seg_count = reinterpret_cast<unsigned long long*>(ws + pl.off_count);
   st = device_error_ptr(&p.err);
   if (st != PA_OK) return st;
   p.k_cache = k_cache;

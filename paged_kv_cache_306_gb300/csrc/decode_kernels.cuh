@@ -19,9 +19,7 @@
 //     streams the same number of blocks from start to finish with its pipeline
 //     full: no per-CTA ramp-up, no tail wave, no idle SMs on ragged batches.
 //     A segment cut by a warp boundary (or by a caller partition boundary) leaves
-//     pieces whose (m, l, acc / l) go to partial slots.  Each piece adds its blocks
-//     to the segment's counter; the warp whose piece completes the segment merges
-//     the pieces at once when they are few, and a second kernel merges the rest.
+//     pieces whose (m, l, acc / l) go to partial slots; a second kernel merges them.
 //     A segment done wholly by one warp is written straight to the output.
 //   * Each warp owns a STAGES-deep ring of shared-memory stages.  A stage holds the
 //     K tile and the V tile of one (physical block, kv head); in this pool layout
@@ -376,96 +374,6 @@ struct SimtMath {
   }
 };
 
-// --- merging a segment in the warp that finishes it --------------------------------------------
-
-// Add n blocks to a segment's count for launch `epoch`; return the count before.
-// A count left by another launch (another epoch) counts as zero.
-__device__ __forceinline__ unsigned add_blocks(unsigned long long* c, unsigned epoch, unsigned n) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c), assumed;
-  unsigned before;
-  do {
-    assumed = old;
-    before = static_cast<unsigned>(assumed >> 32) == epoch ? static_cast<unsigned>(assumed) : 0u;
-    old = atomicCAS(c, assumed, (static_cast<unsigned long long>(epoch) << 32) | (before + n));
-  } while (old != assumed);
-  return before;
-}
-
-// Merge the pieces of a segment whose last piece this warp just finished, when
-// they are few (at most 32 pieces and 128 piece-rows); larger merges are left to
-// the merge kernel.  Lane i owns piece i for the maxima and weights; for the
-// weighted sum every lane owns D/32 head dims.  Pieces written by other SMs are
-// read through L2 (ld.cg).
-template <typename T, int D, int ROWS>
-__device__ __forceinline__ void merge_in_warp(const DecodeParams& p, int seg, int s, int h0, int nh, int lane) {
-  constexpr int CPL = D / 32;
-  const int first = __ldcg(p.seg_first + seg), last = __ldcg(p.seg_last + seg);
-  const int K = last - first + 1;
-  if (first < 0 || K < 2 || K > 32 || K * nh > 128 || last >= p.num_slots) return;
-  const int ep = static_cast<int>(p.epoch);
-  const long long sl = first + lane;
-  bool valid = false;
-  if (lane < K) {
-    const int2 tag = __ldcg(p.part_tag + sl);
-    valid = tag.x == seg && tag.y == ep;
-  }
-  float wgt[ROWS], lsum[ROWS];
-#pragma unroll
-  for (int r = 0; r < ROWS; ++r) {
-    float m = -INFINITY, l = 0.f;
-    if (valid && r < nh) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (sl * p.rows + r) * 2));
-      m = ml.x;
-      l = ml.y;
-    }
-    float M = m;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    wgt[r] = (valid && r < nh) ? l * exp2f(m - M) : 0.f;
-    float ls = wgt[r];
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-    lsum[r] = ls;
-  }
-  float acc[ROWS][CPL];
-#pragma unroll
-  for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[r][c] = 0.f;
-#pragma unroll 2
-  for (int i = 0; i < K; ++i) {
-    const long long base = (long long)(first + i) * p.rows;
-#pragma unroll
-    for (int r = 0; r < ROWS; ++r) {
-      const float wi = __shfl_sync(0xffffffffu, wgt[r], i);
-      if (r < nh && wi != 0.f) {
-        const float* po = p.part_o + (base + r) * D + lane * CPL;
-        if constexpr (CPL == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-          acc[r][0] = fmaf(wi, v.x, acc[r][0]);
-          acc[r][1] = fmaf(wi, v.y, acc[r][1]);
-          acc[r][2] = fmaf(wi, v.z, acc[r][2]);
-          acc[r][3] = fmaf(wi, v.w, acc[r][3]);
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-          acc[r][0] = fmaf(wi, v.x, acc[r][0]);
-          acc[r][1] = fmaf(wi, v.y, acc[r][1]);
-        }
-      }
-    }
-  }
-  T* out = static_cast<T*>(p.out) + ((long long)s * p.num_heads + h0) * D + lane * CPL;
-#pragma unroll
-  for (int r = 0; r < ROWS; ++r)
-    if (r < nh) {
-      const float il = 1.f / lsum[r];
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) out[r * D + c] = DType<T>::from_f32(acc[r][c] * il);
-    }
-  __syncwarp();
-  if (lane == 0) p.seg_first[seg] = -1;  // merged: the merge kernel skips this segment
-}
-
 // --- the schedule ---------------------------------------------------------------------------------
 
 // Head unit u of a sequence: its kv head, first query head and query-row count.
@@ -678,16 +586,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
           p.part_tag[slot] = make_int2(seg, static_cast<int>(p.epoch));
           if (j0 == 0) p.seg_first[seg] = static_cast<int>(slot);
           if (seg_end) p.seg_last[seg] = static_cast<int>(slot);
-        }
-        // Count the piece's blocks; the piece that completes the segment merges it.
-        __threadfence();
-        __syncwarp();
-        unsigned before = 0;
-        if (lane == 0) before = add_blocks(p.seg_count + seg, p.epoch, static_cast<unsigned>(cj - j0));
-        before = __shfl_sync(0xffffffffu, before, 0);
-        if (before + static_cast<unsigned>(cj - j0) == static_cast<unsigned>(nblk)) {
-          __threadfence();
-          merge_in_warp<T, D, kMma ? 16 : 1>(p, seg, cs, h0, nh, lane);
         }
       }
       if (!last) {

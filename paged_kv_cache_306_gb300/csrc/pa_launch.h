@@ -25,7 +25,6 @@ struct DecodeParams {
   int2* part_tag;               // [slots]: (segment, epoch) that wrote the slot
   int* seg_first;               // [S * units]: first piece's slot, or -1 when no merge is needed
   int* seg_last;                // [S * units]: last piece's slot
-  unsigned long long* seg_count;  // [S * units]: (epoch << 32) | blocks of the segment done so far
   unsigned* err;                // device error word
   long long num_blocks;
   int max_blocks_per_seq;
