@@ -119,14 +119,15 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   const int ctas = pa::decode_ctas_per_sm(static_cast<int>(dtype), head_size, block_size, pl->kind);
   const int sms = sm_count();
   if (ctas <= 0 || sms <= 0) return fail(PA_ERR_CUDA, "cannot query the device (SM count %d, CTAs per SM %d)", sms, ctas);
+  const int warps = pa::decode_warps_for(elem_bytes(dtype), head_size, block_size);
   const long long work = chunk * pl->units * (long long)nblk_max;
-  long long grid = (work + 4 * pa::kDecodeWarps - 1) / (4 * pa::kDecodeWarps);
+  long long grid = (work + 4 * warps - 1) / (4 * warps);
   if (grid > (long long)sms * ctas) grid = (long long)sms * ctas;
   if (grid < 1) grid = 1;
   pl->grid = static_cast<int>(grid);
   const long long np_max = (nblk_max + pl->part_blocks - 1) / pl->part_blocks;
   const long long segs = chunk * pl->units;
-  pl->slots = grid * pa::kDecodeWarps + segs * np_max;
+  pl->slots = grid * warps + segs * np_max;
   if (pl->slots > 0x7fffffffLL || segs > 0x7fffffffLL)
     return fail(PA_ERR_UNSUPPORTED, "too many partial results (%lld); use a larger partition_size", pl->slots);
   size_t off = 0;

@@ -52,21 +52,17 @@ namespace pa {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s, then PA_DEVERR_TIMEOUT
 
-// Ring depth per warp from the bytes of one stage (K tile + V tile).
-constexpr int decode_stages(int stage_bytes) {
-  return stage_bytes <= 4096 ? 4 : stage_bytes <= 8192 ? 3 : stage_bytes <= 16384 ? 2 : 1;
-}
-
 template <typename T, int D, int BS>
 struct DecodeShape {
   static constexpr int kElem = sizeof(T);
   static constexpr int kX = 16 / kElem;         // elements per 16-byte K group
   static constexpr int kTile = D * BS * kElem;  // bytes of one K (or V) tile
+  static constexpr int kWarps = decode_warps(2 * kTile);
   static constexpr int kStages = decode_stages(2 * kTile);
-  static constexpr int kRingBytes = kDecodeWarps * kStages * 2 * kTile;
-  static constexpr int kBarBytes = kDecodeWarps * kStages * 8;
+  static constexpr int kRingBytes = kWarps * kStages * 2 * kTile;
+  static constexpr int kBarBytes = kWarps * kStages * 8;
   // per-sequence tables: lengths, block prefix, partition-cut prefix, warp sums
-  static constexpr int kTableBytes = (kMaxSeqsPerLaunch + 2 * (kMaxSeqsPerLaunch + 1) + 2 * kDecodeWarps + 2) * 4;
+  static constexpr int kTableBytes = (kMaxSeqsPerLaunch + 2 * (kMaxSeqsPerLaunch + 1) + 2 * kWarps + 2) * 4;
 };
 
 // Wait for block i's stage.  On timeout record the error and drain the copies
@@ -410,9 +406,10 @@ __device__ __forceinline__ void locate(long long g, const int* pre, int S, int U
 
 // grid = resident CTAs (persistent); kDecodeWarps independent warps per CTA.
 template <typename T, int D, int BS, bool kMma>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+__global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
     decode_kernel(const DecodeParams p) {
   using Sh = DecodeShape<T, D, BS>;
+  constexpr int kDecodeWarps = Sh::kWarps;
   using Math = std::conditional_t<kMma, MmaMath<T, D, BS>, SimtMath<T, D, BS>>;
   constexpr int TILE = Sh::kTile, STAGES = Sh::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -438,7 +435,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   // blocks and of caller-partition cuts.  Each thread scans 8 consecutive sequences.
   const int S = p.num_seqs, U = p.units, PB = p.part_blocks;
   {
-    constexpr int PER = kMaxSeqsPerLaunch / (kDecodeWarps * 32);
+    constexpr int PER = (kMaxSeqsPerLaunch + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
     int nb[PER], ct[PER], sb = 0, sc = 0;
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
@@ -708,7 +705,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
 template <typename T, int D, int BS>
 constexpr int decode_smem_bytes() {
   using Sh = DecodeShape<T, D, BS>;
-  return Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes + kDecodeWarps * BS * 4;
+  return Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes + Sh::kWarps * BS * 4;
 }
 
 template <typename T, int D, int BS, bool kMma>
@@ -728,7 +725,7 @@ template <typename T, int D, int BS, bool kMma>
 int decode_ctas_per_sm_t() {
   if (ensure_smem_attr<T, D, BS, kMma>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<T, D, BS, kMma>, kDecodeWarps * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<T, D, BS, kMma>, DecodeShape<T, D, BS>::kWarps * 32,
                                                     decode_smem_bytes<T, D, BS>()) != cudaSuccess)
     return 0;
   return n;
@@ -739,7 +736,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream
   *launches = 0;
   cudaError_t e = ensure_smem_attr<T, D, BS, kMma>();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_kernel<T, D, BS, kMma>, dim3(grid), dim3(kDecodeWarps * 32), decode_smem_bytes<T, D, BS>(),
+  e = launch_pdl(decode_kernel<T, D, BS, kMma>, dim3(grid), dim3(DecodeShape<T, D, BS>::kWarps * 32), decode_smem_bytes<T, D, BS>(),
                  stream, p);
   if (e != cudaSuccess) return e;
   *launches = 1;

@@ -10,7 +10,23 @@ namespace pa {
 // Sequences handled by one launch of the decode kernels (their per-sequence
 // tables live in shared memory); larger batches are launched in chunks.
 constexpr int kMaxSeqsPerLaunch = 1024;
-constexpr int kDecodeWarps = 4;  // warps per decode CTA; every warp is an independent worker
+
+// Shape of the decode CTA.  One CTA per SM; every warp is an independent worker
+// with a ring of stages, one stage = the K tile and the V tile of one block.
+// Measured on GB300: about 128 KiB of copies in flight per SM streams the pool
+// fastest (more in flight queues up in the memory system, less leaves it idle),
+// with 8 warps to hide the math.  The largest tiles (32 KiB stages) use 4 warps.
+constexpr int kInFlightBytes = 128 * 1024;
+__host__ __device__ constexpr int decode_warps(int stage_bytes) { return stage_bytes <= 16384 ? 8 : 4; }
+__host__ __device__ constexpr int decode_stages(int stage_bytes) {
+  return kInFlightBytes / (decode_warps(stage_bytes) * stage_bytes) > 1
+             ? kInFlightBytes / (decode_warps(stage_bytes) * stage_bytes)
+             : 1;
+}
+// Warps per decode CTA for a cache dtype size, head size and block size.
+inline int decode_warps_for(int elem_bytes, int head_size, int block_size) {
+  return decode_warps(2 * head_size * block_size * elem_bytes);
+}
 
 // Everything a decode launch needs; passed to the kernels by value.
 struct DecodeParams {
