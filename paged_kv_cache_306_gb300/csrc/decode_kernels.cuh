@@ -611,92 +611,77 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
 
 // --- merge of pieces --------------------------------------------------------------------------------
 //
-// One CTA per (segment, query row) whose segment was cut into pieces.  Every load
-// is issued in parallel: threads over the pieces for the maxima and weights,
-// warps over the pieces and lanes over the head dims for the weighted sum.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeChunk = 1024;  // pieces whose weights are staged in shared memory at once
-
-__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float x = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? fmaxf(v, x) : v + x;
-  }
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  v = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-  return v;
-}
+// One CTA per segment (sequence, head unit); warp w merges query rows w, w + 8, ...
+// of the segment on its own (shuffles only, no block-wide barrier).  For a row:
+// lanes take the pieces 32 at a time for the maximum and the weights, then every
+// lane owns D/32 head dims and sums the weighted partial outputs of all pieces,
+// with the loads of consecutive pieces in flight together.
+constexpr int kMergeWarps = 8;
 
 template <typename T, int D, bool kMma>
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
-  constexpr int NW = kMergeThreads / 32;
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
   constexpr int CPL = D / 32;  // head dims per lane
-  __shared__ float w_s[kMergeChunk];
-  __shared__ float red[NW];
-  __shared__ float o_s[NW][D];
   griddep_wait();
   griddep_launch_dependents();
-  const int seg = blockIdx.x / p.rows, r = blockIdx.x - seg * p.rows;
-  const int first = p.seg_first[seg];
-  if (first < 0) return;
-  const int last = p.seg_last[seg];
-  if (last < first || last >= p.num_slots) return;  // only after an aborted launch; the error is recorded
+  const int seg = blockIdx.x;
+  const int first = p.seg_first[seg], last = p.seg_last[seg];
+  if (first < 0 || last < first || last >= p.num_slots) return;  // no merge (or an aborted launch)
   const int s = seg / p.units, u = seg - s * p.units;
   int kvh, h0, nh;
   unit_heads<kMma>(p, u, kvh, h0, nh);
-  if (r >= nh) return;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = last - first + 1, ep = static_cast<int>(p.epoch);
 
-  float M = -INFINITY;
-  for (int i = tid; i < K; i += kMergeThreads) {
-    const int sl = first + i;
-    const int2 tag = p.part_tag[sl];
-    const float m = p.part_ml[((long long)sl * p.rows + r) * 2];
-    if (tag.x == seg && tag.y == ep) M = fmaxf(M, m);
-  }
-  M = block_reduce(M, red, true);
-
-  float lsum = 0.f, acc[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-  for (int c0 = 0; c0 < K; c0 += kMergeChunk) {
-    const int n = min(kMergeChunk, K - c0);
-    for (int i = tid; i < n; i += kMergeThreads) {
-      const int sl = first + c0 + i;
+  for (int r = warp; r < nh; r += kMergeWarps) {
+    // the maximum over this row's valid pieces
+    float M = -INFINITY;
+    for (int i = lane; i < K; i += 32) {
+      const long long sl = first + i;
       const int2 tag = p.part_tag[sl];
-      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((long long)sl * p.rows + r) * 2);
-      const float wgt = (tag.x == seg && tag.y == ep) ? ml.y * exp2f(ml.x - M) : 0.f;
-      w_s[i] = wgt;
-      lsum += wgt;
+      const float m = p.part_ml[(sl * p.rows + r) * 2];
+      if (tag.x == seg && tag.y == ep) M = fmaxf(M, m);
     }
-    __syncthreads();
-#pragma unroll 4
-    for (int i = warp; i < n; i += NW) {
-      const float wgt = w_s[i];
-      if (wgt != 0.f) {  // pieces of other launches or segments have weight 0 and are never read
-        const float* po = p.part_o + ((long long)(first + c0 + i) * p.rows + r) * D + lane * CPL;
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wgt, po[c], acc[c]);
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // weights (lane i holds piece c0 + i) and the weighted sum of the partial outputs
+    float lsum = 0.f, acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    for (int c0 = 0; c0 < K; c0 += 32) {
+      float wgt = 0.f;
+      if (c0 + lane < K) {
+        const long long sl = first + c0 + lane;
+        const int2 tag = p.part_tag[sl];
+        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (sl * p.rows + r) * 2);
+        if (tag.x == seg && tag.y == ep) wgt = ml.y * exp2f(ml.x - M);
+      }
+      lsum += wgt;
+      const int n = min(32, K - c0);
+#pragma unroll 8
+      for (int i = 0; i < n; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, wgt, i);
+        if (wi != 0.f) {  // slots of other launches or segments have weight 0 and are never read
+          const float* po = p.part_o + ((long long)(first + c0 + i) * p.rows + r) * D + lane * CPL;
+          if constexpr (CPL == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(po);
+            acc[0] = fmaf(wi, v.x, acc[0]);
+            acc[1] = fmaf(wi, v.y, acc[1]);
+            acc[2] = fmaf(wi, v.z, acc[2]);
+            acc[3] = fmaf(wi, v.w, acc[3]);
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(po);
+            acc[0] = fmaf(wi, v.x, acc[0]);
+            acc[1] = fmaf(wi, v.y, acc[1]);
+          }
+        }
       }
     }
-    __syncthreads();
-  }
-  lsum = block_reduce(lsum, red, false);
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) o_s[warp][lane * CPL + c] = acc[c];
-  __syncthreads();
-  if (tid < D) {
-    float o = 0.f;
+    for (int o = 16; o; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float il = 1.f / lsum;
+    T* out = static_cast<T*>(p.out) + ((long long)s * p.num_heads + h0 + r) * D + lane * CPL;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) o += o_s[w][tid];
-    static_cast<T*>(p.out)[((long long)s * p.num_heads + h0 + r) * D + tid] = DType<T>::from_f32(o / lsum);
+    for (int c = 0; c < CPL; ++c) out[c] = DType<T>::from_f32(acc[c] * il);
   }
 }
 
@@ -740,8 +725,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream
                  stream, p);
   if (e != cudaSuccess) return e;
   *launches = 1;
-  e = launch_pdl(decode_merge_kernel<T, D, kMma>, dim3(p.num_seqs * p.units * p.rows), dim3(kMergeThreads), 0, stream,
-                 p);
+  e = launch_pdl(decode_merge_kernel<T, D, kMma>, dim3(p.num_seqs * p.units), dim3(kMergeWarps * 32), 0, stream, p);
   if (e != cudaSuccess) return e;
   *launches = 2;
   return cudaSuccess;
