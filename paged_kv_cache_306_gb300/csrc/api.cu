@@ -102,8 +102,8 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // The schedule: the main kernel runs exactly the CTAs that fit on the GPU at once
 // (fewer for small batches, so that every warp gets a few blocks); each warp takes
 // an equal share of all blocks of the launch.  A launch covers at most
-// kMaxSeqsPerLaunch sequences.  Partial slots: one per warp plus one per segment
-// and per caller partition, the most pieces a launch can leave.
+// kMaxSeqsPerLaunch sequences.  Partial slots: one per warp plus one per segment,
+// the most pieces a launch can leave (pieces start at warp or segment boundaries).
 pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len, int block_size,
                     int partition_size, pa_dtype dtype, DecodePlan* pl) {
   const int group = num_heads / num_kv_heads;
@@ -125,9 +125,8 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   if (grid > (long long)sms * ctas) grid = (long long)sms * ctas;
   if (grid < 1) grid = 1;
   pl->grid = static_cast<int>(grid);
-  const long long np_max = (nblk_max + pl->part_blocks - 1) / pl->part_blocks;
   const long long segs = chunk * pl->units;
-  pl->slots = grid * warps + segs * np_max;
+  pl->slots = grid * warps + segs;
   if (pl->slots > 0x7fffffffLL || segs > 0x7fffffffLL)
     return fail(PA_ERR_UNSUPPORTED, "too many partial results (%lld); use a larger partition_size", pl->slots);
   size_t off = 0;

@@ -18,9 +18,11 @@
 //     blocks (W = warps in the grid), crossing segment boundaries.  Every warp thus
 //     streams the same number of blocks from start to finish with its pipeline
 //     full: no per-CTA ramp-up, no tail wave, no idle SMs on ragged batches.
-//     A segment cut by a warp boundary (or by a caller partition boundary) leaves
-//     pieces whose (m, l, acc / l) go to partial slots; a second kernel merges them.
-//     A segment done wholly by one warp is written straight to the output.
+//     A segment cut by a warp boundary leaves pieces whose (m, l, acc / l) go to
+//     partial slots; a second kernel merges them.  A segment done wholly by one
+//     warp is written straight to the output.  Caller partitions (PARTITION_SIZE)
+//     that end inside a warp's piece are merged into the piece at once with the
+//     same formula, through a running state in shared memory.
 //   * Each warp owns a STAGES-deep ring of shared-memory stages.  A stage holds the
 //     K tile and the V tile of one (physical block, kv head); in this pool layout
 //     both are contiguous runs of head_size * block_size elements, so each is one
@@ -61,8 +63,8 @@ struct DecodeShape {
   static constexpr int kStages = decode_stages(2 * kTile);
   static constexpr int kRingBytes = kWarps * kStages * 2 * kTile;
   static constexpr int kBarBytes = kWarps * kStages * 8;
-  // per-sequence tables: lengths, block prefix, partition-cut prefix, warp sums
-  static constexpr int kTableBytes = (kMaxSeqsPerLaunch + 2 * (kMaxSeqsPerLaunch + 1) + 2 * kWarps + 2) * 4;
+  // per-sequence tables: lengths, block prefix, warp sums
+  static constexpr int kTableBytes = (kMaxSeqsPerLaunch + (kMaxSeqsPerLaunch + 1) + kWarps + 3) * 4;
 };
 
 // Wait for block i's stage.  On timeout record the error and drain the copies
@@ -250,6 +252,58 @@ struct MmaMath {
       if (v1) *reinterpret_cast<float2*>(pml + 2 * (g + 8)) = make_float2(m1, l1);
     }
   }
+
+  // Merge this partition's result (m, l, o = acc / l) into the warp's running
+  // state (M, W, O) in shared memory: M' = max(M, m), O' = O 2^(M - M') + l 2^(m - M') o,
+  // W' = W 2^(M - M') + l 2^(m - M').  so: [16][D], sml: [16][2].
+  __device__ __forceinline__ void fold(float* so, float* sml, bool first) const {
+    float M[2], Wt[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      M[h] = first ? -INFINITY : sml[2 * (g + 8 * h)];
+      Wt[h] = first ? 0.f : sml[2 * (g + 8 * h) + 1];
+    }
+    __syncwarp();
+    const float mp[2] = {m0, m1}, lp[2] = {l0, l1};
+    float fo[2], fp[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float mn = fmaxf(M[h], mp[h]);
+      fo[h] = exp2f(M[h] - mn);
+      fp[h] = exp2f(mp[h] - mn);  // l 2^(m - M') times o = acc / l
+      if (t4 == 0) *reinterpret_cast<float2*>(sml + 2 * (g + 8 * h)) = make_float2(mn, Wt[h] * fo[h] + lp[h] * exp2f(mp[h] - mn));
+    }
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) {
+      const int d = dt * 8 + 2 * t4;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float2* o = reinterpret_cast<float2*>(so + (g + 8 * h) * D + d);
+        const float2 old = first ? make_float2(0.f, 0.f) : *o;
+        *o = make_float2(old.x * fo[h] + fp[h] * acc[dt][2 * h], old.y * fo[h] + fp[h] * acc[dt][2 * h + 1]);
+      }
+    }
+    __syncwarp();
+  }
+
+  // Take the running state as this piece's (m, l, acc): acc = O, l = W.
+  __device__ __forceinline__ void load_state(const float* so, const float* sml) {
+    m0 = sml[2 * g];
+    l0 = sml[2 * g + 1];
+    m1 = sml[2 * (g + 8)];
+    l1 = sml[2 * (g + 8) + 1];
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) {
+      const int d = dt * 8 + 2 * t4;
+      const float2 a = *reinterpret_cast<const float2*>(so + g * D + d);
+      const float2 b = *reinterpret_cast<const float2*>(so + (g + 8) * D + d);
+      acc[dt][0] = a.x;
+      acc[dt][1] = a.y;
+      acc[dt][2] = b.x;
+      acc[dt][3] = b.y;
+    }
+    __syncwarp();
+  }
 };
 
 // --- per-warp math: CUDA cores --------------------------------------------------------------------
@@ -368,6 +422,31 @@ struct SimtMath {
     }
     if (lane == 0) *reinterpret_cast<float2*>(pml) = make_float2(m, lpart);
   }
+
+  // As MmaMath::fold, for one row (after finish()): so: [D], sml: [2].
+  __device__ __forceinline__ void fold(float* so, float* sml, bool first) const {
+    const float M = first ? -INFINITY : sml[0], Wt = first ? 0.f : sml[1];
+    __syncwarp();
+    const float mn = fmaxf(M, m);
+    const float fo = exp2f(M - mn), fp = exp2f(m - mn), e = lpart * fp;
+    if (lane == 0) *reinterpret_cast<float2*>(sml) = make_float2(mn, Wt * fo + e);
+    if (vchunk == 0) {
+#pragma unroll
+      for (int k = 0; k < VP; ++k) {
+        float* o = so + k * RPW + vrow;
+        *o = (first ? 0.f : *o) * fo + fp * acc[k];
+      }
+    }
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void load_state(const float* so, const float* sml) {
+    m = sml[0];
+    lpart = sml[1];
+#pragma unroll
+    for (int k = 0; k < VP; ++k) acc[k] = so[k * RPW + vrow];
+    __syncwarp();
+  }
 };
 
 // --- the schedule ---------------------------------------------------------------------------------
@@ -419,9 +498,13 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kRingBytes) + warp * STAGES;
   int* s_len = reinterpret_cast<int*>(smem + Sh::kRingBytes + Sh::kBarBytes);
   int* s_pre = s_len + kMaxSeqsPerLaunch;                 // [S + 1] block prefix per unit
-  int* s_cut = s_pre + kMaxSeqsPerLaunch + 1;              // [S + 1] partition-cut prefix per unit
-  int* s_wsum = s_cut + kMaxSeqsPerLaunch + 1;             // [2 * warps]
-  float* pw = reinterpret_cast<float*>(s_wsum + 2 * kDecodeWarps + 2) + warp * BS;
+  int* s_wsum = s_pre + kMaxSeqsPerLaunch + 1;             // [warps]
+  float* pw = reinterpret_cast<float*>(smem + Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes) + warp * BS;
+  // running state of this warp's piece across caller partitions (see fold)
+  constexpr int kRows = kMma ? 16 : 1;
+  float* st_o = reinterpret_cast<float*>(smem + Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes) +
+                kDecodeWarps * BS + warp * kRows * (D + 2);
+  float* st_ml = st_o + kRows * D;
 
   if (lane == 0) {
     for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
@@ -431,12 +514,12 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
   griddep_launch_dependents();
   griddep_wait();  // every input may come from the previous kernel in the stream
 
-  // Per-sequence tables: length (0 when outside [1, max_seq_len]), prefix sums of
-  // blocks and of caller-partition cuts.  Each thread scans 8 consecutive sequences.
+  // Per-sequence tables: length (0 when outside [1, max_seq_len]) and prefix sums
+  // of blocks.  Each thread scans PER consecutive sequences.
   const int S = p.num_seqs, U = p.units, PB = p.part_blocks;
   {
     constexpr int PER = (kMaxSeqsPerLaunch + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
-    int nb[PER], ct[PER], sb = 0, sc = 0;
+    int nb[PER], sb = 0;
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
       const int i = tid * PER + k;
@@ -444,43 +527,25 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
       if (L < 1 || L > p.max_seq_len) L = 0;
       if (i < S) s_len[i] = L;
       nb[k] = (L + BS - 1) / BS;
-      ct[k] = nb[k] > 0 ? (nb[k] + PB - 1) / PB - 1 : 0;
       sb += nb[k];
-      sc += ct[k];
     }
-    int ib = sb, ic = sc;  // inclusive warp scans
+    int ib = sb;  // inclusive warp scan
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int xb = __shfl_up_sync(0xffffffffu, ib, o), xc = __shfl_up_sync(0xffffffffu, ic, o);
-      if (lane >= o) {
-        ib += xb;
-        ic += xc;
-      }
+      const int xb = __shfl_up_sync(0xffffffffu, ib, o);
+      if (lane >= o) ib += xb;
     }
-    if (lane == 31) {
-      s_wsum[warp] = ib;
-      s_wsum[kDecodeWarps + warp] = ic;
-    }
+    if (lane == 31) s_wsum[warp] = ib;
     __syncthreads();
-    int ob = ib - sb, oc = ic - sc;
-    for (int w = 0; w < warp; ++w) {
-      ob += s_wsum[w];
-      oc += s_wsum[kDecodeWarps + w];
-    }
+    int ob = ib - sb;
+    for (int w = 0; w < warp; ++w) ob += s_wsum[w];
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
       const int i = tid * PER + k;
-      if (i <= S) {
-        s_pre[i] = ob;
-        s_cut[i] = oc;
-      }
+      if (i <= S) s_pre[i] = ob;
       ob += nb[k];
-      oc += ct[k];
     }
-    if (tid == blockDim.x - 1) {  // the totals (also covers S == kMaxSeqsPerLaunch)
-      s_pre[S] = ob;
-      s_cut[S] = oc;
-    }
+    if (tid == blockDim.x - 1) s_pre[S] = ob;  // the total (also covers S == kMaxSeqsPerLaunch)
     __syncthreads();
   }
 
@@ -551,12 +616,12 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
   math.init(lane, pw);
   int cs, cu, cj;
   locate(start, s_pre, S, U, cs, cu, cj);
-  int L = 0, nblk = 0, kvh = 0, h0 = 0, nh = 0, cuts_s = 0, seg = 0, j0 = cj;
+  int L = 0, nblk = 0, kvh = 0, h0 = 0, nh = 0, seg = 0, j0 = cj;
+  bool folded = false;  // earlier partitions of this piece are in the running state
   auto enter = [&]() {
     L = s_len[cs];
     nblk = s_pre[cs + 1] - s_pre[cs];
     unit_heads<kMma>(p, cu, kvh, h0, nh);
-    cuts_s = (nblk + PB - 1) / PB - 1;
     seg = cs * U + cu;
     math.reset();
     math.load_q(static_cast<const T*>(p.q) + ((long long)cs * p.num_heads + h0) * D, nh);
@@ -571,13 +636,19 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
     math.block(stage, TILE, rem, p.scale_log2);
     ++cj;
     const bool seg_end = cj == nblk, last = k + 1 == len;
-    if (seg_end || last || cj % PB == 0) {
+    if (seg_end || last) {  // the end of a piece
       math.finish();
+      if (folded) {  // close the last caller partition and take the merged state
+        math.fold(st_o, st_ml, false);
+        math.load_state(st_o, st_ml);
+        folded = false;
+      }
       if (j0 == 0 && seg_end) {  // the whole segment: straight to the output
         math.store_out(static_cast<T*>(p.out) + ((long long)cs * p.num_heads + h0) * D, nh);
         if (lane == 0) p.seg_first[seg] = -1;
       } else {
-        const long long slot = (long long)w + seg + (long long)U * s_cut[cs] + (long long)cu * cuts_s + j0 / PB;
+        // pieces start only at warp and segment boundaries, so this slot is unique
+        const long long slot = (long long)w + seg;
         math.store_partial(p.part_o + slot * p.rows * D, p.part_ml + slot * p.rows * 2, nh);
         if (lane == 0) {
           p.part_tag[slot] = make_int2(seg, static_cast<int>(p.epoch));
@@ -586,20 +657,21 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
         }
       }
       if (!last) {
-        if (seg_end) {
-          if (++cu == U) {
-            cu = 0;
-            do {
-              ++cs;
-            } while (s_pre[cs + 1] == s_pre[cs]);
-          }
-          cj = 0;
-          enter();
-        } else {
-          math.reset();
+        if (++cu == U) {
+          cu = 0;
+          do {
+            ++cs;
+          } while (s_pre[cs + 1] == s_pre[cs]);
         }
-        j0 = cj;
+        cj = 0;
+        enter();
+        j0 = 0;
       }
+    } else if (cj % PB == 0) {  // a caller partition ends inside this piece: fold it
+      math.finish();
+      math.fold(st_o, st_ml, !folded);
+      folded = true;
+      math.reset();
     }
     __syncwarp();
     if (k + STAGES < len) {
@@ -611,16 +683,19 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
 
 // --- merge of pieces --------------------------------------------------------------------------------
 //
-// One CTA per segment (sequence, head unit); warp w merges query rows w, w + 8, ...
-// of the segment on its own (shuffles only, no block-wide barrier).  For a row:
-// lanes take the pieces 32 at a time for the maximum and the weights, then every
-// lane owns D/32 head dims and sums the weighted partial outputs of all pieces,
-// with the loads of consecutive pieces in flight together.
+// One CTA per segment (sequence, head unit).  Each query row of the segment gets
+// g = 8 / rows warps (at least one); the warps of a row split its pieces 32 at a
+// time: lanes take pieces for the maximum and the weights, then every lane owns
+// D/32 head dims and sums the weighted partial outputs, with the loads of
+// consecutive pieces in flight together.  The g warps of a row combine through
+// shared memory.
 constexpr int kMergeWarps = 8;
 
 template <typename T, int D, bool kMma>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
   constexpr int CPL = D / 32;  // head dims per lane
+  __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
+  __shared__ float s_o[kMergeWarps][D];
   griddep_wait();
   griddep_launch_dependents();
   const int seg = blockIdx.x;
@@ -631,66 +706,97 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   unit_heads<kMma>(p, u, kvh, h0, nh);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = last - first + 1, ep = static_cast<int>(p.epoch);
+  const int g = nh >= kMergeWarps ? 1 : kMergeWarps / nh;  // warps per row
+  const int per_round = kMergeWarps / g;                     // rows per round
+  const int j = warp % g, lead = warp - j;
 
-  for (int r = warp; r < nh; r += kMergeWarps) {
-    // the maximum over this row's valid pieces
+  for (int r0 = 0; r0 < nh; r0 += per_round) {
+    const int r = r0 + warp / g;
+    const bool active = warp < per_round * g && r < nh;
+    // the maximum over the row's valid pieces
     float M = -INFINITY;
-    for (int i = lane; i < K; i += 32) {
-      const long long sl = first + i;
-      const int2 tag = p.part_tag[sl];
-      const float m = p.part_ml[(sl * p.rows + r) * 2];
-      if (tag.x == seg && tag.y == ep) M = fmaxf(M, m);
+    if (active) {
+      for (int i = j * 32 + lane; i < K; i += g * 32) {
+        const long long sl = first + i;
+        const int2 tag = p.part_tag[sl];
+        const float m = p.part_ml[(sl * p.rows + r) * 2];
+        if (tag.x == seg && tag.y == ep) M = fmaxf(M, m);
+      }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (g > 1) {
+      if (lane == 0) s_m[warp] = M;
+      __syncthreads();
+      for (int jj = 0; jj < g; ++jj) M = fmaxf(M, s_m[lead + jj]);
+    }
     // weights (lane i holds piece c0 + i) and the weighted sum of the partial outputs
     float lsum = 0.f, acc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-    for (int c0 = 0; c0 < K; c0 += 32) {
-      float wgt = 0.f;
-      if (c0 + lane < K) {
-        const long long sl = first + c0 + lane;
-        const int2 tag = p.part_tag[sl];
-        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (sl * p.rows + r) * 2);
-        if (tag.x == seg && tag.y == ep) wgt = ml.y * exp2f(ml.x - M);
-      }
-      lsum += wgt;
-      const int n = min(32, K - c0);
+    if (active) {
+      for (int c0 = j * 32; c0 < K; c0 += g * 32) {
+        float wgt = 0.f;
+        if (c0 + lane < K) {
+          const long long sl = first + c0 + lane;
+          const int2 tag = p.part_tag[sl];
+          const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (sl * p.rows + r) * 2);
+          if (tag.x == seg && tag.y == ep) wgt = ml.y * exp2f(ml.x - M);
+        }
+        lsum += wgt;
+        const int n = min(32, K - c0);
 #pragma unroll 8
-      for (int i = 0; i < n; ++i) {
-        const float wi = __shfl_sync(0xffffffffu, wgt, i);
-        if (wi != 0.f) {  // slots of other launches or segments have weight 0 and are never read
-          const float* po = p.part_o + ((long long)(first + c0 + i) * p.rows + r) * D + lane * CPL;
-          if constexpr (CPL == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(po);
-            acc[0] = fmaf(wi, v.x, acc[0]);
-            acc[1] = fmaf(wi, v.y, acc[1]);
-            acc[2] = fmaf(wi, v.z, acc[2]);
-            acc[3] = fmaf(wi, v.w, acc[3]);
-          } else {
-            const float2 v = *reinterpret_cast<const float2*>(po);
-            acc[0] = fmaf(wi, v.x, acc[0]);
-            acc[1] = fmaf(wi, v.y, acc[1]);
+        for (int i = 0; i < n; ++i) {
+          const float wi = __shfl_sync(0xffffffffu, wgt, i);
+          if (wi != 0.f) {  // slots of other launches or segments have weight 0 and are never read
+            const float* po = p.part_o + ((long long)(first + c0 + i) * p.rows + r) * D + lane * CPL;
+            if constexpr (CPL == 4) {
+              const float4 v = *reinterpret_cast<const float4*>(po);
+              acc[0] = fmaf(wi, v.x, acc[0]);
+              acc[1] = fmaf(wi, v.y, acc[1]);
+              acc[2] = fmaf(wi, v.z, acc[2]);
+              acc[3] = fmaf(wi, v.w, acc[3]);
+            } else {
+              const float2 v = *reinterpret_cast<const float2*>(po);
+              acc[0] = fmaf(wi, v.x, acc[0]);
+              acc[1] = fmaf(wi, v.y, acc[1]);
+            }
           }
         }
       }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    const float il = 1.f / lsum;
-    T* out = static_cast<T*>(p.out) + ((long long)s * p.num_heads + h0 + r) * D + lane * CPL;
+    if (g > 1) {
+      if (lane == 0) s_l[warp] = lsum;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) out[c] = DType<T>::from_f32(acc[c] * il);
+      for (int c = 0; c < CPL; ++c) s_o[warp][lane * CPL + c] = acc[c];
+      __syncthreads();
+      if (j == 0) {
+        for (int jj = 1; jj < g; ++jj) {
+          lsum += s_l[lead + jj];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acc[c] += s_o[lead + jj][lane * CPL + c];
+        }
+      }
+    }
+    if (active && j == 0) {
+      const float il = 1.f / lsum;
+      T* out = static_cast<T*>(p.out) + ((long long)s * p.num_heads + h0 + r) * D + lane * CPL;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) out[c] = DType<T>::from_f32(acc[c] * il);
+    }
+    __syncthreads();  // the shared arrays are reused by the next round
   }
 }
 
 // --- host-side launch helpers (instantiated per dtype) ------------------------------------------
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool kMma>
 constexpr int decode_smem_bytes() {
   using Sh = DecodeShape<T, D, BS>;
-  return Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes + Sh::kWarps * BS * 4;
+  return Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes + Sh::kWarps * BS * 4 +
+         Sh::kWarps * (kMma ? 16 : 1) * (D + 2) * 4;
 }
 
 template <typename T, int D, int BS, bool kMma>
@@ -701,7 +807,7 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   if (dev < 32 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1u)) return cudaSuccess;
   e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&decode_kernel<T, D, BS, kMma>),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<T, D, BS>());
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<T, D, BS, kMma>());
   if (e == cudaSuccess && dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
   return e;
 }
@@ -711,7 +817,7 @@ int decode_ctas_per_sm_t() {
   if (ensure_smem_attr<T, D, BS, kMma>() != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<T, D, BS, kMma>, DecodeShape<T, D, BS>::kWarps * 32,
-                                                    decode_smem_bytes<T, D, BS>()) != cudaSuccess)
+                                                    decode_smem_bytes<T, D, BS, kMma>()) != cudaSuccess)
     return 0;
   return n;
 }
@@ -721,7 +827,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream
   *launches = 0;
   cudaError_t e = ensure_smem_attr<T, D, BS, kMma>();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_kernel<T, D, BS, kMma>, dim3(grid), dim3(DecodeShape<T, D, BS>::kWarps * 32), decode_smem_bytes<T, D, BS>(),
+  e = launch_pdl(decode_kernel<T, D, BS, kMma>, dim3(grid), dim3(DecodeShape<T, D, BS>::kWarps * 32), decode_smem_bytes<T, D, BS, kMma>(),
                  stream, p);
   if (e != cudaSuccess) return e;
   *launches = 1;
