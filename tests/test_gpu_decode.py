@@ -214,13 +214,14 @@ def test_workspace_too_small_is_rejected():
     assert st == 4
 
 
-def test_workspace_grows_with_caller_partitions_and_covers_every_call():
+def test_workspace_does_not_depend_on_caller_partitions():
+    """Caller partitions are merged inside the warps, so they need no extra partial slots."""
     import paged_kv_cache_306_gb300 as pa
     lib = pa.load()
     none = lib.pa_decode_workspace_size(64, 28, 4, 128, 4096, 16, 0, pa.PA_F16)
     auto = lib.pa_decode_workspace_size(64, 28, 4, 128, 4096, 16, -1, pa.PA_F16)
     p256 = lib.pa_decode_workspace_size(64, 28, 4, 128, 4096, 16, 256, pa.PA_F16)
-    assert none > 0 and auto == none and p256 > none
+    assert none > 0 and auto == none and p256 == none
     assert lib.pa_decode_plan_partition(64, 28, 4, 128, 4096, 16, pa.PA_F16) == 0
 
 
