@@ -92,11 +92,12 @@ def test_no_alloc_matches_the_workspace_entry_point_on_two_calls_in_a_row(lib):
 def test_no_alloc_rejects_a_split_larger_than_its_scratch(lib):
     P = ctypes.c_void_p
     n0 = lib.pa_launch_count()
-    # 256 sequences of up to 131072 tokens in partitions of 256: far beyond 32 MiB of partials
-    need = lib.pa_decode_workspace_size(256, 32, 8, 128, 131072, 16, 256, 1)
+    # 1024 sequences x 16 kv heads with 16 query heads each: one partial slot per
+    # (sequence, kv head) of 16 rows x 128 dims is far beyond 32 MiB
+    need = lib.pa_decode_workspace_size(1024, 256, 16, 128, 4096, 16, 0, 1)
     assert need > 32 * 1024 * 1024
-    st = lib.pa_decode_noalloc(P(256), P(256), P(256), P(256), P(256), 8192, P(256), 256, 131072, 32, 8, 128, 16,
-                               100000, ctypes.c_float(0.1), 256, 1, None)
+    st = lib.pa_decode_noalloc(P(256), P(256), P(256), P(256), P(256), 256, P(256), 1024, 4096, 256, 16, 128, 16,
+                               100000, ctypes.c_float(0.1), 0, 1, None)
     assert st == 4                                       # PA_ERR_WORKSPACE, nothing enqueued
     assert b"32 MiB" in lib.pa_last_error_message() or b"holds" in lib.pa_last_error_message()
     assert lib.pa_launch_count() == n0
