@@ -1,0 +1,75 @@
+"""Host-side pieces of bench.py, on CPU: the multi-rank timing reduction (2 gloo
+ranks), the algorithmic byte accounting and the CPU reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    q.put((rank, bench.max_over_ranks(1.5 + rank, world)))
+    dist.destroy_process_group()
+
+
+def test_timing_is_the_max_over_two_gloo_ranks():
+    torch = pytest.importorskip("torch")
+    mp = torch.multiprocessing.get_context("spawn")
+    q = mp.Queue()
+    port = _free_port()
+    procs = [mp.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: 2.5, 1: 2.5}
+
+
+def test_single_rank_needs_no_process_group():
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_decode_bytes_of_the_llama_layer():
+    wl = W.config(3, poison=False)
+    # K+V of 16 x 2048 tokens x 32 kv heads x 128 dims x 2 B, q and out, 128 table entries per sequence
+    expect = 536_870_912 + 2 * 16 * 32 * 128 * 2 + 16 * 128 * 4 + 16 * 4
+    assert bench.decode_bytes(wl) == expect
+
+
+def test_unique_bytes_count_shared_blocks_once():
+    wl = W.make_prefix_shared("t", "f16", 2, 4, 8, 2, 64, 16, seed=3, len_range=(300, 600),
+                              prefix_range=(200, 250))
+    assert bench.decode_bytes(wl, unique=True) < bench.decode_bytes(wl)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["steps"] == 3
