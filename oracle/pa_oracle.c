@@ -22,7 +22,9 @@
  *     the V pool v_cache[b][h][d][t], all arrays C-contiguous;
  *   - slot s decodes to block s / block_size, offset s % block_size; a negative
  *     slot is a padding token and is skipped;
- *   - query head h reads kv head h / (num_heads / num_kv_heads).
+ *   - query head h reads kv head h / (num_heads / num_kv_heads);
+ *   - a quantised (FP8 E4M3) cache stores the code of x / scale per element,
+ *     with one k_scale and one v_scale per call, and reads back code * scale.
  *
  * The decode result has a plain definition -- paging changes where K/V live,
  * not what attention computes ([ILP] §4, §6; [BHHXX] §4.3) -- so the oracle is
@@ -38,7 +40,7 @@
 #include <omp.h>
 #endif
 
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_F64 = 3 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_F64 = 3, OR_FP8 = 4 };
 
 enum {
   OR_OK = 0,
@@ -56,6 +58,7 @@ static int elem_bytes(int dtype) {
     case OR_F16: return 2;
     case OR_BF16: return 2;
     case OR_F64: return 8;
+    case OR_FP8: return 1;
     default: return 0;
   }
 }
@@ -84,12 +87,47 @@ static double bf16_bits_to_double(uint16_t b) {
   return (double)f;
 }
 
+/* OCP FP8 E4M3 (the "fn" variant): 1 sign bit, 4 exponent bits (bias 7),
+ * 3 fraction bits; exponent 0 is zero/subnormal (f * 2^-9); S.1111.111 is NaN;
+ * there are no infinities, so the largest magnitude is 1.75 * 2^8 = 448. */
+static double e4m3_bits_to_double(uint8_t b) {
+  int sign = (b >> 7) & 1;
+  int e = (b >> 3) & 0xf;
+  int f = b & 7;
+  double v;
+  if (e == 15 && f == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)f, -9);
+  else
+    v = ldexp((double)(f | 8), e - 10);
+  return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to x (ties to the even code), magnitudes beyond 448 clamped
+ * to 448: a search over the 127 non-negative finite codes. */
+static uint8_t double_to_e4m3_satfinite(double x) {
+  if (isnan(x)) return 0x7f;
+  const uint8_t sign = signbit(x) ? 0x80 : 0;
+  const double a = fabs(x);
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 126; ++c) {
+    const double d = fabs(e4m3_bits_to_double((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
 /* Element idx of an array of the given dtype, widened exactly to fp64. */
 static double load(const void* base, int64_t idx, int dtype) {
   switch (dtype) {
     case OR_F32: return (double)((const float*)base)[idx];
     case OR_F16: return half_bits_to_double(((const uint16_t*)base)[idx]);
     case OR_BF16: return bf16_bits_to_double(((const uint16_t*)base)[idx]);
+    case OR_FP8: return e4m3_bits_to_double(((const uint8_t*)base)[idx]);
     default: return ((const double*)base)[idx];
   }
 }
@@ -116,6 +154,12 @@ int oracle_num_threads(void) {
 #else
   return 1;
 #endif
+}
+
+/* E4M3 codes of n fp64 values (ties to even, clamped to +-448). */
+int oracle_encode_e4m3(uint8_t* out, const double* in, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = double_to_e4m3_satfinite(in[i]);
+  return OR_OK;
 }
 
 /* Widen n elements to fp64 (used by the tests to pin the decoders). */
@@ -166,6 +210,55 @@ int oracle_reshape_and_cache(const void* key, const void* value, void* k_cache, 
 }
 
 /*
+ * Write path with a quantised cache ([ILP] §3.2 names the kv_cache_dtype, k_scale
+ * and v_scale arguments of the write): each element x of key (value) is stored as
+ * the E4M3 code of x / k_scale (x / v_scale), the division done in fp32 as the
+ * write kernel does, rounded to nearest (ties to even) and clamped to +-448.
+ * Reading it back gives code * scale.  For a 16-bit or fp32 cache of the key's own
+ * dtype with both scales 1 this is the plain byte copy above.
+ */
+int oracle_reshape_and_cache_scaled(const void* key, const void* value, void* k_cache, void* v_cache,
+                                    const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                                    int head_size, int block_size, int64_t num_blocks, int key_dtype,
+                                    int cache_dtype, double k_scale, double v_scale) {
+  if (cache_dtype != OR_FP8) {
+    if (cache_dtype != key_dtype || k_scale != 1.0 || v_scale != 1.0) return OR_ERR_ARG;
+    return oracle_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads,
+                                    head_size, block_size, num_blocks, key_dtype);
+  }
+  if (key_dtype != OR_F32 && key_dtype != OR_F16 && key_dtype != OR_BF16) return OR_ERR_ARG;
+  if (num_tokens < 0 || num_kv_heads < 1 || block_size < 1 || head_size % 16 || !(k_scale > 0) || !(v_scale > 0))
+    return OR_ERR_ARG;
+  const int64_t n_slots = num_blocks * block_size;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= n_slots) return OR_ERR_SLOT;
+    for (int64_t u = 0; u < t; ++u)
+      if (slot_mapping[u] == slot) return OR_ERR_DUP_SLOT;
+  }
+  const float ks = (float)k_scale, vs = (float)v_scale;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / block_size;
+    const int off = (int)(slot % block_size);
+    for (int h = 0; h < num_kv_heads; ++h) {
+      for (int d = 0; d < head_size; ++d) {
+        const int64_t src = ((int64_t)t * num_kv_heads + h) * head_size + d;
+        const float kq = (float)load(key, src, key_dtype) / ks;
+        const float vq = (float)load(value, src, key_dtype) / vs;
+        ((uint8_t*)k_cache)[k_index(blk, h, d, off, num_kv_heads, head_size, block_size, 16)] =
+            double_to_e4m3_satfinite((double)kq);
+        ((uint8_t*)v_cache)[v_index(blk, h, d, off, num_kv_heads, head_size, block_size)] =
+            double_to_e4m3_satfinite((double)vq);
+      }
+    }
+  }
+  return OR_OK;
+}
+
+/*
  * Copy-on-write block copy, [BHHXX] §4.2: before a shared physical block
  * (refcount > 1) is written, it is first copied to a fresh block.  Pair i of
  * src_dst is (src, dst); the whole block -- every kv head, K and V -- is copied.
@@ -194,15 +287,15 @@ int oracle_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int
  */
 static int gather_seq(double* K, double* V, const void* k_cache, const void* v_cache,
                       const int32_t* table_row, int L, int kvh, int Hkv, int D, int bs,
-                      int64_t num_blocks, int dtype) {
+                      int64_t num_blocks, int dtype, double k_scale, double v_scale) {
   const int x = pack_x(dtype);
   for (int t = 0; t < L; ++t) {
     const int64_t phys = table_row[t / bs];
     if (phys < 0 || phys >= num_blocks) return OR_ERR_BLOCK_ID;
     const int off = t % bs;
     for (int d = 0; d < D; ++d) {
-      K[(int64_t)t * D + d] = load(k_cache, k_index(phys, kvh, d, off, Hkv, D, bs, x), dtype);
-      V[(int64_t)t * D + d] = load(v_cache, v_index(phys, kvh, d, off, Hkv, D, bs), dtype);
+      K[(int64_t)t * D + d] = k_scale * load(k_cache, k_index(phys, kvh, d, off, Hkv, D, bs, x), dtype);
+      V[(int64_t)t * D + d] = v_scale * load(v_cache, v_index(phys, kvh, d, off, Hkv, D, bs), dtype);
     }
   }
   return OR_OK;
@@ -221,13 +314,14 @@ static int gather_seq(double* K, double* V, const void* k_cache, const void* v_c
  * Positions at or beyond seq_lens[s] are never read ([ILP] §4: a partially
  * filled last block is guarded by the true sequence length).
  */
-int oracle_decode(double* out, double* weights, int64_t w_stride, const void* q,
-                  const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                  int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
-                  int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
-                  double scale, int dtype) {
-  if (!elem_bytes(dtype) || num_seqs < 0 || num_kv_heads < 1 || num_heads % num_kv_heads ||
-      block_size < 1 || head_size % pack_x(dtype))
+int oracle_decode_scaled(double* out, double* weights, int64_t w_stride, const void* q,
+                         const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                         int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
+                         int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                         double scale, int q_dtype, int cache_dtype, double k_scale, double v_scale) {
+  const int dtype = cache_dtype;
+  if (!elem_bytes(dtype) || !elem_bytes(q_dtype) || num_seqs < 0 || num_kv_heads < 1 ||
+      num_heads % num_kv_heads || block_size < 1 || head_size % pack_x(dtype))
     return OR_ERR_ARG;
   for (int s = 0; s < num_seqs; ++s)
     if (seq_lens[s] < 1 || (int64_t)seq_lens[s] > (int64_t)max_blocks_per_seq * block_size)
@@ -252,7 +346,7 @@ int oracle_decode(double* out, double* weights, int64_t w_stride, const void* q,
       continue;
     }
     int st = gather_seq(K, V, k_cache, v_cache, block_tables + (int64_t)s * max_blocks_per_seq, L,
-                        kvh, num_kv_heads, D, block_size, num_blocks, dtype);
+                        kvh, num_kv_heads, D, block_size, num_blocks, dtype, k_scale, v_scale);
     if (st != OR_OK) {
 #pragma omp critical
       status = st;
@@ -263,7 +357,7 @@ int oracle_decode(double* out, double* weights, int64_t w_stride, const void* q,
     /* scores */
     for (int t = 0; t < L; ++t) {
       double acc = 0.0;
-      for (int d = 0; d < D; ++d) acc += load(q, qo + d, dtype) * K[(int64_t)t * D + d];
+      for (int d = 0; d < D; ++d) acc += load(q, qo + d, q_dtype) * K[(int64_t)t * D + d];
       z[t] = scale * acc;
     }
     /* softmax with the maximum subtracted */
@@ -283,4 +377,17 @@ int oracle_decode(double* out, double* weights, int64_t w_stride, const void* q,
     free(K); free(V); free(z);
   }
   return status;
+}
+
+/*
+ * The decode definition above for a cache in the query's own dtype (no scales).
+ */
+int oracle_decode(double* out, double* weights, int64_t w_stride, const void* q,
+                  const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                  int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
+                  int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                  double scale, int dtype) {
+  return oracle_decode_scaled(out, weights, w_stride, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                              seq_lens, num_seqs, num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                              scale, dtype, dtype, 1.0, 1.0);
 }

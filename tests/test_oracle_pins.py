@@ -363,3 +363,98 @@ def test_kv_bytes_of_llama7b_layer_times_layers_matches_memory_formula():
     seqs, heads, D, L, e = 16, 32, 128, 2048, 2
     per_layer = 2 * seqs * L * heads * D * e
     assert per_layer * 32 == 4 * 32 * 4096 * 2048 * 16 == 17_179_869_184
+
+
+# --- FP8 E4M3 cache (kv_cache_dtype, k_scale, v_scale of the write path) ----------------------
+
+def test_e4m3_decoding_matches_torch_on_every_code():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.widen(codes, "fp8")
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_e4m3_encoding_matches_torch_within_range():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(30)
+    x = np.concatenate([rng.uniform(-464, 464, 20000), rng.standard_normal(20000) * 3,
+                        rng.standard_normal(20000) * 2.0 ** -7, [0.0, -0.0, 448.0, -448.0, 464.0, 2.0 ** -10,
+                                                                  1.5 * 2.0 ** -9, 2.5 * 2.0 ** -9]])
+    x = x.astype(np.float32).astype(np.float64)
+    ours = oracle.encode_e4m3(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_clamps_instead_of_overflowing():
+    assert oracle.encode_e4m3(np.array([1000.0, 480.0, -1e6])).tolist() == [0x7E, 0x7E, 0xFE]
+
+
+def test_e4m3_codes_round_trip():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(oracle.encode_e4m3(oracle.widen(codes, "fp8")), codes)
+
+
+def _fp8_pool(rng, NB, Hkv, D, bs, gen_scale):
+    """Random E4M3 pools drawn with torch's float8 conversion, logical [NB, Hkv, bs, D]."""
+    torch = pytest.importorskip("torch")
+    def draw():
+        x = rng.standard_normal((NB, Hkv, bs, D)).astype(np.float32) / np.float32(gen_scale)
+        return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return draw(), draw()
+
+
+def test_quantised_decode_equals_decode_of_the_dequantised_pool():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    NB, Hkv, D, bs = 24, 2, 32, 4
+    kc8, vc8 = _fp8_pool(rng, NB, Hkv, D, bs, 1 / 32)
+    ks, vs = 0.03, 0.05
+    k8, v8 = pools_from_logical(kc8, vc8, 16)
+    deq = lambda a, s: torch.from_numpy(a).view(torch.float8_e4m3fn).to(torch.float64).numpy() * s
+    k64, v64 = pools_from_logical(deq(kc8, ks), deq(vc8, vs), 2)
+    q = rng.standard_normal((3, 4, D)).astype(np.float16)
+    bt = rng.permutation(NB)[:18].reshape(3, 6).astype(np.int32)
+    L = np.array([1, 13, 24], np.int32)
+    got = oracle.decode(q, k8, v8, bt, L, 0.2, "fp8", q_dtype="f16", k_scale=ks, v_scale=vs)
+    ref = oracle.decode(q.astype(np.float64), k64, v64, bt, L, 0.2, "f64")
+    assert np.max(np.abs(got - ref)) < 1e-13
+
+
+def test_quantised_write_stores_torch_rounded_codes_of_x_over_scale():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(32)
+    NB, Hkv, D, bs, T = 10, 2, 32, 4, 9
+    k = np.zeros((NB, Hkv, D // 16, bs, 16), np.uint8)
+    v = np.zeros((NB, Hkv, D, bs), np.uint8)
+    # |x| / scale stays inside +-448 here, where torch's conversion does not saturate
+    key = rng.standard_normal((T, Hkv, D)).astype(np.float16)
+    val = rng.standard_normal((T, Hkv, D)).astype(np.float16)
+    slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+    ks, vs = 0.0125, 0.02
+    oracle.reshape_and_cache_scaled(key, val, k, v, slots, "f16", "fp8", ks, vs)
+    Kl, Vl = logical_from_pools(k, v)
+    q8 = lambda a, s: torch.from_numpy(a.astype(np.float32) / np.float32(s)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+    for t in range(T):
+        b, o = divmod(int(slots[t]), bs)
+        assert np.array_equal(Kl[b, :, o], q8(key[t], ks))
+        assert np.array_equal(Vl[b, :, o], q8(val[t], vs))
+
+
+def test_value_scale_scales_the_output_and_key_scale_acts_like_query_scale():
+    rng = np.random.default_rng(33)
+    NB, Hkv, D, bs = 16, 1, 16, 4
+    kc8, vc8 = _fp8_pool(rng, NB, Hkv, D, bs, 1 / 16)
+    k8, v8 = pools_from_logical(kc8, vc8, 16)
+    q = rng.standard_normal((2, 2, D)).astype(np.float32)
+    bt = np.arange(16, dtype=np.int32).reshape(2, 8)
+    L = np.array([30, 7], np.int32)
+    a = oracle.decode(q, k8, v8, bt, L, 0.25, "fp8", q_dtype="f32", k_scale=0.1, v_scale=0.5)
+    b = oracle.decode(q, k8, v8, bt, L, 0.25, "fp8", q_dtype="f32", k_scale=0.1, v_scale=1.0)
+    c = oracle.decode(q, k8, v8, bt, L, 0.025, "fp8", q_dtype="f32", k_scale=1.0, v_scale=0.5)
+    assert np.max(np.abs(a - 0.5 * b)) < 1e-14
+    assert np.max(np.abs(a - c)) < 1e-12
