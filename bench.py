@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload qwen|llama|long|mixed|tiny] [--block-size 16|32]
+                    [--kv-dtype fp8]
 
 A step is the whole hot path on one batch: copy-on-write block copies (the
 mixed workload only), reshape_and_cache of every sequence's new token, and
@@ -10,6 +11,10 @@ decode attention (plus the partition merge when the planner splits).
 copies rotated so K/V always come from HBM); `e2e` is the same metric through
 the Python API with the step's inputs copied from pinned host memory and the
 output copied back inside the timed region.  Rank 0 prints one JSON line.
+
+--kv-dtype fp8 keeps the workload's shapes and query dtype but stores the pool
+as FP8 E4M3 codes (quantising write, dequantising decode); bytes are counted at
+one byte per cached element.
 
 --impl reference times the CPU oracle on the host cores instead: each step is a
 bounded sample of the same workload (one sequence, a subset of its heads).
@@ -42,18 +47,18 @@ def decode_bytes(wl, unique=False):
     """Algorithmic bytes of one decode call: K and V of the valid tokens (per kv head),
     q and out, the block-table entries walked and seq_lens.  unique=True counts
     shared physical blocks once (prefix sharing)."""
-    e = W.ELEM_BYTES[wl.dtype]
+    e, eq = W.ELEM_BYTES[wl.dtype], W.ELEM_BYTES[wl.q_dtype]
     tokens = wl.unique_tokens if unique else wl.total_tokens
     kv = tokens * wl.num_kv_heads * wl.head_size * e * 2
-    qo = 2 * wl.num_seqs * wl.num_heads * wl.head_size * e
+    qo = 2 * wl.num_seqs * wl.num_heads * wl.head_size * eq
     tables = int(np.sum(-(-wl.seq_lens.astype(np.int64) // wl.block_size))) * 4 + 4 * wl.num_seqs
     return kv + qo + tables
 
 
 def write_bytes(wl):
     """reshape_and_cache (read key/value, write the slots) and block copies (read + write)."""
-    e = W.ELEM_BYTES[wl.dtype]
-    tok = wl.num_seqs * wl.num_kv_heads * wl.head_size * e * 2 * 2 + wl.num_seqs * 8
+    e, eq = W.ELEM_BYTES[wl.dtype], W.ELEM_BYTES[wl.q_dtype]
+    tok = wl.num_seqs * wl.num_kv_heads * wl.head_size * (e + eq) * 2 + wl.num_seqs * 8
     blk = wl.num_kv_heads * wl.head_size * wl.block_size * e * 2
     return tok + len(wl.cow) * blk * 2 + len(wl.cow) * 16
 
@@ -155,10 +160,53 @@ def barrier(world_size, device=None):
 
 def describe(wl, cfg):
     L = wl.seq_lens
-    return {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
-            "num_kv_heads": wl.num_kv_heads, "head_size": wl.head_size, "block_size": wl.block_size,
-            "seq_lens": {"min": int(L.min()), "max": int(L.max()), "total": int(L.sum())},
-            "num_blocks": wl.num_blocks, "cow_copies": int(len(wl.cow)), "seed": 306 + cfg}
+    d = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
+         "num_kv_heads": wl.num_kv_heads, "head_size": wl.head_size, "block_size": wl.block_size,
+         "seq_lens": {"min": int(L.min()), "max": int(L.max()), "total": int(L.sum())},
+         "num_blocks": wl.num_blocks, "cow_copies": int(len(wl.cow)), "seed": 306 + cfg}
+    if wl.dtype == "fp8":
+        d.update({"kv_cache_dtype": "fp8_e4m3", "q_dtype": wl.q_dtype, "k_scale": wl.k_scale,
+                  "v_scale": wl.v_scale})
+    return d
+
+
+def dtype_label(wl):
+    """The arithmetic type of the path: an FP8 pool is widened to the query dtype."""
+    return wl.dtype if wl.dtype != "fp8" else f"fp8_e4m3 cache, {wl.q_dtype} compute"
+
+
+def api_calls(wl):
+    """(write, decode) through the public API for the workload's cache dtype."""
+    import paged_kv_cache_306_gb300 as pa
+    if wl.dtype != "fp8":
+        return pa.pa_reshape_and_cache, pa.pa_decode
+
+    def write(key, value, k, v, slots, stream=None):
+        pa.pa_reshape_and_cache_scaled(key, value, k, v, slots, wl.k_scale, wl.v_scale, stream=stream)
+
+    def decode(out, q, k, v, bt, sl, scale, max_seq_len, partition_size, ws, stream=None):
+        return pa.pa_decode_scaled(out, q, k, v, bt, sl, scale, max_seq_len, wl.k_scale, wl.v_scale,
+                                   partition_size, ws, stream=stream)
+    return write, decode
+
+
+def oracle_pools_after_write(wl):
+    """The pool as the step leaves it (block copies, then the new tokens), by the oracle."""
+    import oracle
+    k, v = wl.clone_pools()
+    oracle.copy_blocks(k, v, wl.cow, wl.dtype)
+    if wl.dtype == "fp8":
+        oracle.reshape_and_cache_scaled(wl.key, wl.value, k, v, wl.slot_mapping, wl.q_dtype, wl.dtype, wl.k_scale,
+                                        wl.v_scale)
+    else:
+        oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
+    return k, v
+
+
+def oracle_decode(wl, q, k, v, sub):
+    import oracle
+    return oracle.decode(q, k, v, sub.block_tables, sub.seq_lens, wl.scale, wl.dtype, q_dtype=wl.q_dtype,
+                         k_scale=wl.k_scale, v_scale=wl.v_scale)
 
 
 def run_ours(args, wl, cfg, world_size, rank, local_rank):
@@ -176,8 +224,8 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     sets = []
     for _ in range(copies):
         sets.append({
-            "q": W.to_torch(wl.q, wl.dtype, dev), "key": W.to_torch(wl.key, wl.dtype, dev),
-            "value": W.to_torch(wl.value, wl.dtype, dev), "k": W.to_torch(wl.k_cache, wl.dtype, dev),
+            "q": W.to_torch(wl.q, wl.q_dtype, dev), "key": W.to_torch(wl.key, wl.q_dtype, dev),
+            "value": W.to_torch(wl.value, wl.q_dtype, dev), "k": W.to_torch(wl.k_cache, wl.dtype, dev),
             "v": W.to_torch(wl.v_cache, wl.dtype, dev), "out": torch.empty(wl.q.shape, dtype=pa_dtype(wl), device=dev),
         })
     bt = torch.from_numpy(wl.block_tables).to(dev)
@@ -185,7 +233,8 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     slots = torch.from_numpy(wl.slot_mapping).to(dev)
     cow = torch.from_numpy(np.ascontiguousarray(wl.cow)).to(dev)
     ps = wl.partition_size if args.partition is None else args.partition
-    code = pa.PA_F32 if wl.dtype == "f32" else pa.PA_F16 if wl.dtype == "f16" else pa.PA_BF16
+    code = {"f32": pa.PA_F32, "f16": pa.PA_F16, "bf16": pa.PA_BF16, "fp8": pa.PA_FP8_E4M3}[wl.dtype]
+    write, decode = api_calls(wl)
     resolved = pa.pa_decode_plan_partition(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
                                            wl.max_seq_len, wl.block_size, code) if ps == -1 else ps
     ws_bytes = pa.pa_decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
@@ -196,10 +245,10 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
         s = sets[i % copies]
         if len(wl.cow):
             pa.pa_copy_blocks(s["k"], s["v"], cow, stream=stream)
-        pa.pa_reshape_and_cache(s["key"], s["value"], s["k"], s["v"], slots, stream=stream)
+        write(s["key"], s["value"], s["k"], s["v"], slots, stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        pa.pa_decode(s["out"], s["q"], s["k"], s["v"], bt, sl, wl.scale, wl.max_seq_len, resolved, ws, stream=stream)
+        decode(s["out"], s["q"], s["k"], s["v"], bt, sl, wl.scale, wl.max_seq_len, resolved, ws, stream=stream)
         if ev is not None:
             ev[1].record(stream)
 
@@ -261,7 +310,7 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     line = {
         "metric": METRIC, "value": round(world_size * step_bytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(wl),
         "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfgd,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -275,7 +324,7 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
 
 def pa_dtype(wl):
     import torch
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.q_dtype]
 
 
 def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws):
@@ -285,9 +334,9 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws):
     import torch
     import paged_kv_cache_306_gb300 as pa
     parts = {
-        "q": W.to_torch(wl.q, wl.dtype, "cpu"),
-        "key": W.to_torch(wl.key, wl.dtype, "cpu"),
-        "value": W.to_torch(wl.value, wl.dtype, "cpu"),
+        "q": W.to_torch(wl.q, wl.q_dtype, "cpu"),
+        "key": W.to_torch(wl.key, wl.q_dtype, "cpu"),
+        "value": W.to_torch(wl.value, wl.q_dtype, "cpu"),
         "bt": torch.from_numpy(wl.block_tables),
         "sl": torch.from_numpy(wl.seq_lens),
         "slots": torch.from_numpy(wl.slot_mapping),
@@ -308,14 +357,15 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws):
     h2d = off
     d2h = out_host.numel() * out_host.element_size()
     steps = min(args.steps, 2000)
+    write, decode = api_calls(wl)
 
     def step():
         d_stage.copy_(h_stage, non_blocking=True)
         if len(wl.cow):
             pa.pa_copy_blocks(s["k"], s["v"], devt["cow"], stream=stream)
-        pa.pa_reshape_and_cache(devt["key"], devt["value"], s["k"], s["v"], devt["slots"], stream=stream)
-        pa.pa_decode(s["out"], devt["q"], s["k"], s["v"], devt["bt"], devt["sl"], wl.scale, wl.max_seq_len,
-                     resolved, ws, stream=stream)
+        write(devt["key"], devt["value"], s["k"], s["v"], devt["slots"], stream=stream)
+        decode(s["out"], devt["q"], s["k"], s["v"], devt["bt"], devt["sl"], wl.scale, wl.max_seq_len,
+               resolved, ws, stream=stream)
         out_host.copy_(s["out"], non_blocking=True)
 
     for _ in range(3):
@@ -357,16 +407,14 @@ def cpu_baseline(wl, seconds=12.0):
     """The oracle on the host cores over a bounded sample: whole sequences, all heads."""
     import oracle
     # the oracle sees the pool after the step's write (as the GPU does)
-    k, v = wl.clone_pools()
-    oracle.copy_blocks(k, v, wl.cow, wl.dtype)
-    oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
+    k, v = oracle_pools_after_write(wl)
     done, nbytes, t0 = 0, 0, time.perf_counter()
     order = np.argsort(wl.seq_lens)             # shortest first keeps the sample bounded
     e = W.ELEM_BYTES[wl.dtype]
     while time.perf_counter() - t0 < seconds and done < wl.num_seqs:
         s = int(order[done])
         sub = W.subset(wl, [s])
-        oracle.decode(sub.q, k, v, sub.block_tables, sub.seq_lens, wl.scale, wl.dtype)
+        oracle_decode(wl, sub.q, k, v, sub)
         nbytes += int(wl.seq_lens[s]) * wl.num_kv_heads * wl.head_size * e * 2
         done += 1
     dt = time.perf_counter() - t0
@@ -378,9 +426,7 @@ def cpu_baseline(wl, seconds=12.0):
 def run_reference(args, wl, cfg, world_size, rank):
     """The CPU oracle as the reference arm: each step is one sequence of the workload."""
     import oracle
-    k, v = wl.clone_pools()
-    oracle.copy_blocks(k, v, wl.cow, wl.dtype)
-    oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
+    k, v = oracle_pools_after_write(wl)
     e = W.ELEM_BYTES[wl.dtype]
     G = wl.num_heads // wl.num_kv_heads
 
@@ -390,7 +436,7 @@ def run_reference(args, wl, cfg, world_size, rank):
         q = np.ascontiguousarray(sub.q[:, :kvh * G])
         kk = np.ascontiguousarray(k[:, :kvh]) if kvh < wl.num_kv_heads else k
         vv = np.ascontiguousarray(v[:, :kvh]) if kvh < wl.num_kv_heads else v
-        oracle.decode(q, kk, vv, sub.block_tables, sub.seq_lens, wl.scale, wl.dtype)
+        oracle_decode(wl, q, kk, vv, sub)
         return int(wl.seq_lens[s]) * kvh * wl.head_size * e * 2
 
     # size the per-step sample (kv heads of one sequence) so the run stays within ~2 minutes
@@ -413,7 +459,7 @@ def run_reference(args, wl, cfg, world_size, rank):
               f"with their {G} query heads each; fp64 C oracle")
     return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world_size, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "impl": "reference",
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(wl), "data": "synthetic", "impl": "reference",
             "config": describe(wl, cfg),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
@@ -429,6 +475,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen")
     ap.add_argument("--block-size", type=int, default=None, help="mixed workload only: 16 or 32")
     ap.add_argument("--partition", type=int, default=None, help="override the workload's partition size")
+    ap.add_argument("--kv-dtype", choices=["fp8"], default=None,
+                    help="store the pool as FP8 E4M3 codes (not for the fp32 tiny workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
@@ -441,7 +489,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        wl = W.config(cfg, poison=False, block_size=args.block_size)
+        wl = W.config(cfg, poison=False, block_size=args.block_size, kv_dtype=args.kv_dtype)
         print(json.dumps(run_reference(args, wl, cfg, world_size, rank)), flush=True)
         return 0
 
@@ -451,7 +499,7 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     # every rank holds its own replica of the workload (weak scaling)
-    wl = W.config(cfg, poison=False, block_size=args.block_size)
+    wl = W.config(cfg, poison=False, block_size=args.block_size, kv_dtype=args.kv_dtype)
     line = run_ours(args, wl, cfg, world_size, rank, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:

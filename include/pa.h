@@ -24,7 +24,8 @@
  *                 physical block that holds tokens i*block_size .. of sequence s
  *   seq_lens      int32 [num_seqs], the number of valid tokens per sequence
  *   slot_mapping  int64 [num_tokens], physical_block * block_size + offset
- *   (cache layouts: "Reading vLLM's PagedAttention kernel", §3.1)
+ *   (cache layouts: "Reading vLLM's PagedAttention kernel", §3.1; an FP8 E4M3
+ *   cache has x = 16 and one byte per element)
  *
  * Query head h reads kv head h / (num_heads / num_kv_heads).
  *
@@ -71,7 +72,7 @@ typedef enum {
   PA_ERR_CUDA = 5          /* a CUDA runtime call failed (see pa_last_error_message) */
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 /* partition_size values for pa_decode */
 #define PA_PARTITION_NONE 0    /* one pass over each whole sequence */
@@ -105,6 +106,24 @@ PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, void* 
                                const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
                                int head_size, int block_size, int64_t num_blocks, pa_dtype dtype,
                                void* stream);
+
+/*
+ * Write path into a cache of another dtype ("Reading vLLM's PagedAttention
+ * kernel", §3.2: the write also takes kv_cache_dtype, k_scale and v_scale).
+ * With cache_dtype PA_FP8_E4M3 every element x of key (value) is stored as the
+ * OCP FP8 E4M3 code of x / k_scale (x / v_scale): the division correctly rounded
+ * in fp32, the code rounded to nearest with ties to even and clamped to +-448
+ * (no infinities; a NaN stays NaN).  A later read of that cache gives
+ * code * k_scale (code * v_scale).  key_dtype is PA_F32, PA_F16 or PA_BF16;
+ * scales are positive and finite; head_size is a multiple of 16.  For any other
+ * cache_dtype the call is pa_reshape_and_cache and requires key_dtype ==
+ * cache_dtype and both scales 1.  Layouts, slots and errors as there.
+ */
+PA_API pa_status pa_reshape_and_cache_scaled(const void* key, const void* value, void* k_cache, void* v_cache,
+                                             const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                                             int head_size, int block_size, int64_t num_blocks,
+                                             pa_dtype key_dtype, pa_dtype cache_dtype, float k_scale,
+                                             float v_scale, void* stream);
 
 /*
  * Copy-on-write block copy ("vLLM's PagedAttention: why the KV cache is paged",
@@ -166,6 +185,22 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                     int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
                     int block_size, int64_t num_blocks, float scale, int partition_size,
                     void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_decode over a cache whose dtype differs from the query's: with cache_dtype
+ * PA_FP8_E4M3 and q_dtype PA_F16 or PA_BF16, K and V read back as
+ * code * k_scale and code * v_scale (see pa_reshape_and_cache_scaled); out has
+ * q_dtype.  Scores, softmax and the weighted sum are fp32 as in pa_decode.  For
+ * any other cache_dtype, q_dtype must equal it and both scales be 1.  The
+ * workspace is pa_decode_workspace_size(..., cache_dtype).  pa_decode itself
+ * rejects PA_FP8_E4M3 (it has no query dtype or scales).
+ */
+PA_API pa_status pa_decode_scaled(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                  int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
+                                  int block_size, int64_t num_blocks, float scale, int partition_size,
+                                  void* workspace, size_t workspace_bytes, pa_dtype q_dtype, pa_dtype cache_dtype,
+                                  float k_scale, float v_scale, void* stream);
 
 /*
  * Read and clear the first device-side error recorded on the current device

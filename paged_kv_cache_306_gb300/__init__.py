@@ -12,15 +12,18 @@ from ._binding import (  # noqa: F401
     PA_BF16,
     PA_F16,
     PA_F32,
+    PA_FP8_E4M3,
     PARTITION_AUTO,
     PARTITION_NONE,
     PAError,
     load,
     pa_copy_blocks,
     pa_decode,
+    pa_decode_scaled,
     pa_decode_plan_partition,
     pa_decode_workspace_size,
     pa_get_device_error,
     pa_launch_count,
     pa_reshape_and_cache,
+    pa_reshape_and_cache_scaled,
 )

@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_ALIGNMENT, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(6)
-PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PARTITION_NONE = 0
 PARTITION_AUTO = -1
 DEVICE_ERRORS = {0: "none", 1: "block id outside the pool", 2: "seq_len outside [1, max_seq_len]",
@@ -48,6 +48,11 @@ def load():
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, P, sz, i32, P]
+    lib.pa_reshape_and_cache_scaled.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i64, i32, i32, f32, f32, P]
+    lib.pa_reshape_and_cache_scaled.restype = i32
+    lib.pa_decode_scaled.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, P, sz, i32,
+                                     i32, f32, f32, P]
+    lib.pa_decode_scaled.restype = i32
     lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, i32, P]
     lib.pa_decode_noalloc.restype = i32
     lib.pa_get_device_error.argtypes = [ctypes.POINTER(i32), P]
@@ -69,7 +74,8 @@ def check(status):
 
 def dtype_code(torch_dtype):
     import torch
-    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16,
+             torch.float8_e4m3fn: PA_FP8_E4M3}
     if torch_dtype not in codes:
         raise PAError(PA_ERR_UNSUPPORTED, f"unsupported dtype {torch_dtype}")
     return codes[torch_dtype]
@@ -107,6 +113,23 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None
     nb, bs = v_cache.shape[0], v_cache.shape[3]
     check(load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
                                       T, hkv, d, bs, nb, dtype_code(k_cache.dtype), _stream(stream)))
+
+
+def pa_reshape_and_cache_scaled(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale, stream=None):
+    """Write path into a cache of another dtype: for an FP8 E4M3 cache (torch.float8_e4m3fn)
+    each element is stored as the code of x / k_scale (x / v_scale)."""
+    import torch
+    for n, t in (("key", key), ("value", value)):
+        _need_cuda(n, t, key.dtype)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("slot_mapping", slot_mapping, torch.int64, 1)
+    T, hkv, d = key.shape
+    nb, bs = v_cache.shape[0], v_cache.shape[3]
+    check(load().pa_reshape_and_cache_scaled(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                             _ptr(slot_mapping), T, hkv, d, bs, nb, dtype_code(key.dtype),
+                                             dtype_code(k_cache.dtype), float(k_scale), float(v_scale),
+                                             _stream(stream)))
 
 
 def pa_copy_blocks(k_cache, v_cache, src_dst, stream=None):
@@ -158,6 +181,32 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_l
     check(lib.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                         block_tables.shape[1], _ptr(seq_lens), S, max_seq_len, H, hkv, D, bs, nb, float(scale),
                         partition_size, _ptr(workspace), ws_bytes, code, _stream(stream)))
+    return workspace
+
+
+def pa_decode_scaled(out, q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len, k_scale, v_scale,
+                     partition_size=PARTITION_AUTO, workspace=None, stream=None):
+    """pa_decode over a cache whose dtype differs from q's (FP8 E4M3 read back as code * scale)."""
+    import torch
+    dt = q.dtype
+    _need_cuda("q", q, dt, 3)
+    _need_cuda("out", out, dt, 3)
+    _need_cuda("k_cache", k_cache, None, 5)
+    _need_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _need_cuda("block_tables", block_tables, torch.int32, 2)
+    _need_cuda("seq_lens", seq_lens, torch.int32, 1)
+    S, H, D = q.shape
+    nb, hkv, _, bs = v_cache.shape
+    cc = dtype_code(k_cache.dtype)
+    lib = load()
+    need = lib.pa_decode_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, cc)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib.pa_decode_scaled(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                               block_tables.shape[1], _ptr(seq_lens), S, max_seq_len, H, hkv, D, bs, nb, float(scale),
+                               partition_size, _ptr(workspace), ws_bytes, dtype_code(dt), cc, float(k_scale),
+                               float(v_scale), _stream(stream)))
     return workspace
 
 

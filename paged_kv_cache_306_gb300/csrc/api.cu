@@ -63,7 +63,9 @@ int sm_count() {
   return n;
 }
 
-int elem_bytes(pa_dtype d) { return d == PA_F32 ? 4 : (d == PA_F16 || d == PA_BF16) ? 2 : 0; }
+int elem_bytes(pa_dtype d) {
+  return d == PA_F32 ? 4 : (d == PA_F16 || d == PA_BF16) ? 2 : d == PA_FP8_E4M3 ? 1 : 0;
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -166,12 +168,17 @@ int decode_ctas_per_sm(int dtype, int head_size, int block_size, DecodeKind kind
     case PA_F32: return decode_ctas_per_sm_f32(head_size, block_size, kind);
     case PA_F16: return decode_ctas_per_sm_f16(head_size, block_size, kind);
     case PA_BF16: return decode_ctas_per_sm_bf16(head_size, block_size, kind);
+    case PA_FP8_E4M3: return decode_ctas_per_sm_fp8(false, head_size, block_size, kind);
     default: return 0;
   }
 }
 
 cudaError_t launch_decode(int dtype, int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
                           cudaStream_t stream, int* launches) {
+  // dtype: the cache dtype for 16-bit and fp32 caches (the query's too); for an
+  // FP8 cache, 16 + the query dtype (see decode_impl)
+  if (dtype >= 16)
+    return launch_decode_fp8(dtype - 16 == PA_BF16, head_size, block_size, p, kind, grid, stream, launches);
   switch (dtype) {
     case PA_F32: return launch_decode_f32(head_size, block_size, p, kind, grid, stream, launches);
     case PA_F16: return launch_decode_f16(head_size, block_size, p, kind, grid, stream, launches);
@@ -225,6 +232,42 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   return ce == cudaSuccess ? PA_OK : cuda_fail(ce, "reshape_and_cache launch");
 }
 
+pa_status pa_reshape_and_cache_scaled(const void* key, const void* value, void* k_cache, void* v_cache,
+                                      const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_size,
+                                      int block_size, int64_t num_blocks, pa_dtype key_dtype, pa_dtype cache_dtype,
+                                      float k_scale, float v_scale, void* stream) {
+  if (cache_dtype != PA_FP8_E4M3) {
+    if (key_dtype != cache_dtype || k_scale != 1.f || v_scale != 1.f)
+      return fail(PA_ERR_INVALID_ARG, "a %s cache stores key/value as they are: same dtype, scales 1",
+                  cache_dtype == PA_F32 ? "fp32" : "16-bit");
+    return pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_size,
+                                block_size, num_blocks, cache_dtype, stream);
+  }
+  if (key_dtype != PA_F32 && key_dtype != PA_F16 && key_dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "an FP8 cache is written from fp32, fp16 or bf16 key/value");
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
+  if (num_tokens < 0 || num_tokens > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_tokens %lld", (long long)num_tokens);
+  if (num_kv_heads < 1 || head_size < 1 || block_size < 1 || num_blocks < 1)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads, head_size, block_size and num_blocks must be positive");
+  if (head_size % 16) return fail(PA_ERR_INVALID_ARG, "head_size %d not a multiple of 16", head_size);
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return fail(PA_ERR_ALIGNMENT, "key/value/caches need 16-byte, slot_mapping 8-byte alignment");
+  unsigned* err = nullptr;
+  pa_status st = device_error_ptr(&err);
+  if (st != PA_OK) return st;
+  int n = 0;
+  cudaError_t ce = pa::launch_reshape_and_cache_e4m3(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                                     num_kv_heads, head_size, block_size, num_blocks,
+                                                     static_cast<int>(key_dtype), k_scale, v_scale, err,
+                                                     static_cast<cudaStream_t>(stream), &n);
+  g_launches.fetch_add(n, std::memory_order_relaxed);
+  return ce == cudaSuccess ? PA_OK : cuda_fail(ce, "quantising reshape_and_cache launch");
+}
+
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int64_t num_pairs, int num_kv_heads,
                          int head_size, int block_size, int64_t num_blocks, pa_dtype dtype, void* stream) {
   const int e = elem_bytes(dtype);
@@ -270,12 +313,23 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
   return pl.bytes;
 }
 
-pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                    int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int max_seq_len, int num_heads,
-                    int num_kv_heads, int head_size, int block_size, int64_t num_blocks, float scale,
-                    int partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+static pa_status decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                             int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
+                             int block_size, int64_t num_blocks, float scale, int partition_size, void* workspace,
+                             size_t workspace_bytes, pa_dtype q_dtype, pa_dtype dtype, float k_scale, float v_scale,
+                             void* stream) {
+  // `dtype` is the cache dtype from here on; q and out have q_dtype.
   pa_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
   if (st != PA_OK) return st;
+  if (dtype == PA_FP8_E4M3) {
+    if (q_dtype != PA_F16 && q_dtype != PA_BF16)
+      return fail(PA_ERR_UNSUPPORTED, "an FP8 cache is read by fp16 or bf16 queries");
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+      return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
+  } else if (q_dtype != dtype || k_scale != 1.f || v_scale != 1.f) {
+    return fail(PA_ERR_INVALID_ARG, "a 16-bit or fp32 cache is read by queries of its own dtype with scales 1");
+  }
   if (max_blocks_per_seq < 1 || (long long)max_seq_len > (long long)max_blocks_per_seq * block_size)
     return fail(PA_ERR_INVALID_ARG, "max_seq_len %d exceeds max_blocks_per_seq %d * block_size %d", max_seq_len,
                 max_blocks_per_seq, block_size);
@@ -319,9 +373,11 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   p.max_seq_len = max_seq_len;
   p.part_blocks = pl.part_blocks;
   p.num_slots = static_cast<int>(pl.slots);
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * k_scale * 1.4426950408889634);
+  p.out_scale = v_scale;
 
-  const size_t row_bytes = (size_t)num_heads * head_size * elem_bytes(dtype);
+  const size_t row_bytes = (size_t)num_heads * head_size * elem_bytes(q_dtype);
+  const int launch_dtype = dtype == PA_FP8_E4M3 ? 16 + static_cast<int>(q_dtype) : static_cast<int>(dtype);
   for (int c0 = 0; c0 < num_seqs; c0 += pl.chunk) {
     p.num_seqs = num_seqs - c0 < pl.chunk ? num_seqs - c0 : pl.chunk;
     p.q = static_cast<const char*>(q) + (size_t)c0 * row_bytes;
@@ -330,12 +386,35 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     p.seq_lens = seq_lens + c0;
     p.epoch = next_epoch();
     int n = 0;
-    const cudaError_t ce = pa::launch_decode(static_cast<int>(dtype), head_size, block_size, p, pl.kind, pl.grid,
+    const cudaError_t ce = pa::launch_decode(launch_dtype, head_size, block_size, p, pl.kind, pl.grid,
                                              static_cast<cudaStream_t>(stream), &n);
     g_launches.fetch_add(n, std::memory_order_relaxed);
     if (ce != cudaSuccess) return cuda_fail(ce, "decode launch");
   }
   return PA_OK;
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                    int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int max_seq_len, int num_heads,
+                    int num_kv_heads, int head_size, int block_size, int64_t num_blocks, float scale,
+                    int partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (dtype == PA_FP8_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "an FP8 cache needs pa_decode_scaled (query dtype and k/v scales)");
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                     num_heads, num_kv_heads, head_size, block_size, num_blocks, scale, partition_size, workspace,
+                     workspace_bytes, dtype, dtype, 1.f, 1.f, stream);
+}
+
+pa_status pa_decode_scaled(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                           int max_seq_len, int num_heads, int num_kv_heads, int head_size, int block_size,
+                           int64_t num_blocks, float scale, int partition_size, void* workspace,
+                           size_t workspace_bytes, pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                           float v_scale, void* stream) {
+  if (!elem_bytes(q_dtype)) return fail(PA_ERR_INVALID_ARG, "unknown query dtype %d", static_cast<int>(q_dtype));
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                     num_heads, num_kv_heads, head_size, block_size, num_blocks, scale, partition_size, workspace,
+                     workspace_bytes, q_dtype, cache_dtype, k_scale, v_scale, stream);
 }
 
 pa_status pa_get_device_error(int* code, void* stream) {

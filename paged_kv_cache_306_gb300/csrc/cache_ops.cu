@@ -18,6 +18,7 @@
 namespace pa {
 
 template <int E> struct Word;
+template <> struct Word<1> { using type = uint8_t; };
 template <> struct Word<2> { using type = uint16_t; };
 template <> struct Word<4> { using type = uint32_t; };
 
@@ -59,6 +60,58 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// Quantising write into an FP8 E4M3 cache (the kv_cache_dtype, k_scale and v_scale
+// arguments of the write, "Reading vLLM's PagedAttention kernel" §3.2): element x
+// of the key (value) row is stored as the E4M3 code of x / k_scale (x / v_scale),
+// the division correctly rounded in fp32, the code rounded to nearest (ties to
+// even) and clamped to +-448.  One CTA per token; in the K pool a 16-element group
+// of a head is 16 contiguous codes, written with one 16-byte store.
+template <typename TS>
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_e4m3_kernel(const TS* __restrict__ key, const TS* __restrict__ value,
+                                  unsigned char* __restrict__ k_cache, unsigned char* __restrict__ v_cache,
+                                  const int64_t* __restrict__ slot_mapping, int num_kv_heads, int head_size,
+                                  int block_size, long long num_blocks, float k_scale, float v_scale, unsigned* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long t = blockIdx.x;
+  const long long slot = slot_mapping[t];
+  if (slot < 0) return;  // padding token
+  if (slot >= num_blocks * block_size) {
+    if (threadIdx.x == 0) set_error(err, kErrSlot);
+    return;
+  }
+  const long long blk = slot / block_size;
+  const int off = static_cast<int>(slot - blk * block_size);
+  const int groups = head_size / 16;
+  const long long row = t * num_kv_heads * head_size;
+  for (int c = threadIdx.x; c < num_kv_heads * groups; c += blockDim.x) {
+    const int h = c / groups, g = c - h * groups;
+    const TS* src = key + row + (long long)c * 16;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t packed = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float a = __fdiv_rn(DType<TS>::to_f32(src[4 * i + 2 * j]), k_scale);
+        const float b = __fdiv_rn(DType<TS>::to_f32(src[4 * i + 2 * j + 1]), k_scale);
+        const uint32_t two = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+        packed |= (two & 0xffffu) << (16 * j);
+      }
+      w[i] = packed;
+    }
+    *reinterpret_cast<uint4*>(k_cache + (((blk * num_kv_heads + h) * groups + g) * block_size + off) * 16) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  for (int i = threadIdx.x; i < num_kv_heads * head_size; i += blockDim.x) {
+    const int h = i / head_size, d = i - h * head_size;
+    const float x = __fdiv_rn(DType<TS>::to_f32(value[row + i]), v_scale);
+    v_cache[((blk * num_kv_heads + h) * head_size + d) * block_size + off] =
+        static_cast<unsigned char>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+  }
+}
+
 // grid = (num_pairs, 2 [K, V], chunks)
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(unsigned char* k_cache, unsigned char* v_cache, const int64_t* __restrict__ src_dst,
@@ -91,11 +144,40 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
   auto* vc = static_cast<unsigned char*>(v_cache);
   const dim3 grid(static_cast<unsigned>(num_tokens));
   const cudaError_t e =
-      elem_bytes == 4
-          ? launch_pdl(reshape_and_cache_kernel<4>, grid, dim3(128), 0, stream, kp, vp, kc, vc, slot_mapping,
-                       num_kv_heads, head_size, block_size, (long long)num_blocks, err)
-          : launch_pdl(reshape_and_cache_kernel<2>, grid, dim3(128), 0, stream, kp, vp, kc, vc, slot_mapping,
-                       num_kv_heads, head_size, block_size, (long long)num_blocks, err);
+      elem_bytes == 4   ? launch_pdl(reshape_and_cache_kernel<4>, grid, dim3(128), 0, stream, kp, vp, kc, vc,
+                                     slot_mapping, num_kv_heads, head_size, block_size, (long long)num_blocks, err)
+      : elem_bytes == 2 ? launch_pdl(reshape_and_cache_kernel<2>, grid, dim3(128), 0, stream, kp, vp, kc, vc,
+                                     slot_mapping, num_kv_heads, head_size, block_size, (long long)num_blocks, err)
+                        : launch_pdl(reshape_and_cache_kernel<1>, grid, dim3(128), 0, stream, kp, vp, kc, vc,
+                                     slot_mapping, num_kv_heads, head_size, block_size, (long long)num_blocks, err);
+  if (e == cudaSuccess) *launches = 1;
+  return e;
+}
+
+cudaError_t launch_reshape_and_cache_e4m3(const void* key, const void* value, void* k_cache, void* v_cache,
+                                           const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                                           int head_size, int block_size, int64_t num_blocks, int key_dtype,
+                                           float k_scale, float v_scale, unsigned* err, cudaStream_t stream,
+                                           int* launches) {
+  *launches = 0;
+  if (num_tokens == 0) return cudaSuccess;
+  auto* kc = static_cast<unsigned char*>(k_cache);
+  auto* vc = static_cast<unsigned char*>(v_cache);
+  const dim3 grid(static_cast<unsigned>(num_tokens));
+  const long long nb = num_blocks;
+  cudaError_t e;
+  if (key_dtype == 0)
+    e = launch_pdl(reshape_and_cache_e4m3_kernel<float>, grid, dim3(128), 0, stream, static_cast<const float*>(key),
+                   static_cast<const float*>(value), kc, vc, slot_mapping, num_kv_heads, head_size, block_size, nb,
+                   k_scale, v_scale, err);
+  else if (key_dtype == 1)
+    e = launch_pdl(reshape_and_cache_e4m3_kernel<__half>, grid, dim3(128), 0, stream,
+                   static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc, slot_mapping,
+                   num_kv_heads, head_size, block_size, nb, k_scale, v_scale, err);
+  else
+    e = launch_pdl(reshape_and_cache_e4m3_kernel<__nv_bfloat16>, grid, dim3(128), 0, stream,
+                   static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc, vc,
+                   slot_mapping, num_kv_heads, head_size, block_size, nb, k_scale, v_scale, err);
   if (e == cudaSuccess) *launches = 1;
   return e;
 }

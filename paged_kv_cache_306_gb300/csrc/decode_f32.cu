@@ -4,12 +4,12 @@
 namespace pa {
 
 int decode_ctas_per_sm_f32(int head_size, int block_size, DecodeKind kind) {
-  return decode_ctas_per_sm_dispatch<float>(head_size, block_size, kind);
+  return decode_ctas_per_sm_dispatch<float, float>(head_size, block_size, kind);
 }
 
 cudaError_t launch_decode_f32(int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
                               cudaStream_t s, int* n) {
-  return launch_decode_dispatch<float>(head_size, block_size, p, kind, grid, s, n);
+  return launch_decode_dispatch<float, float>(head_size, block_size, p, kind, grid, s, n);
 }
 
 }  // namespace pa

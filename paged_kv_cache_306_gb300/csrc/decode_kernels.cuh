@@ -94,13 +94,26 @@ __device__ __forceinline__ void zero_tail_v(unsigned char* vtile, int rem, int l
 // --- per-warp math: tensor cores ---------------------------------------------------------------
 //
 // Up to 16 query rows (the heads of one head unit) against the tokens of a block.
-template <typename T, int D, int BS>
+//
+// T is the query / output type and the type of the tensor-core operands; TC is
+// the cache element type: T itself, or FP8 E4M3 (converted to T in registers).
+// For an FP8 cache, ldmatrix over 16-byte rows hands each thread 4 consecutive
+// codes, which must become the (k, k+1) and (k+8, k+9) operand pairs of the MMA:
+// the head dims of Q are permuted to match within each 16-dim k-step, and the
+// tokens of S's n-tiles are permuted so that P's fragments line up with V's.
+template <typename T, typename TC, int D, int BS>
 struct MmaMath {
   static constexpr int NT = BS / 8;   // token n-tiles of S
   static constexpr int KS = D / 16;   // k-steps over head dims for S
   static constexpr int DT = D / 8;    // head-dim n-tiles of O
   static constexpr int KK = BS / 16;  // token k-steps for O
-  static constexpr int kElem = sizeof(T);
+  static constexpr int kElem = sizeof(TC);
+  static constexpr bool kFp8 = sizeof(TC) == 1;
+
+  // Token of column col (0..7) of S n-tile nt.
+  __device__ __forceinline__ static int token(int nt, int col) {
+    return kFp8 ? 16 * (nt >> 1) + 4 * (col >> 1) + (col & 1) + 2 * (nt & 1) : nt * 8 + col;
+  }
 
   uint32_t qf[KS][4];
   float acc[DT][4];
@@ -112,8 +125,15 @@ struct MmaMath {
     g = lane >> 2;
     t4 = lane & 3;
     const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix mi, row mr
-    k_lane_off = ((mi & 1) * BS + (mi >> 1) * 8 + mr) * 16;
-    v_lane_off = ((mi >> 1) * 8 + mr) * (BS * kElem) + (mi & 1) * 16;
+    if (kFp8) {
+      // K: matrix mi = (k-step mi & 1, n-tile mi >> 1), rows = that n-tile's tokens
+      k_lane_off = ((mi & 1) * BS + token(mi >> 1, mr)) * 16;
+      // V: matrix mi = head-dim n-tile mi, rows = 8 head dims of 16 tokens (16 bytes)
+      v_lane_off = (mi * 8 + mr) * BS;
+    } else {
+      k_lane_off = ((mi & 1) * BS + (mi >> 1) * 8 + mr) * 16;
+      v_lane_off = ((mi >> 1) * 8 + mr) * (BS * kElem) + (mi & 1) * 16;
+    }
   }
 
   __device__ __forceinline__ void reset() {
@@ -130,11 +150,13 @@ struct MmaMath {
     const bool v0 = g < nh, v1 = g + 8 < nh;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      const int d = ks * 16 + 2 * t4;
+      // operand k = 2t4, 2t4+1 and 2t4+8, 2t4+9 read head dims d, d+1 and d2, d2+1
+      const int d = ks * 16 + (kFp8 ? 4 * t4 : 2 * t4);
+      const int d2 = kFp8 ? d + 2 : d + 8;
       qf[ks][0] = v0 ? __ldg(reinterpret_cast<const unsigned int*>(q0 + d)) : 0u;
       qf[ks][1] = v1 ? __ldg(reinterpret_cast<const unsigned int*>(q1 + d)) : 0u;
-      qf[ks][2] = v0 ? __ldg(reinterpret_cast<const unsigned int*>(q0 + d + 8)) : 0u;
-      qf[ks][3] = v1 ? __ldg(reinterpret_cast<const unsigned int*>(q1 + d + 8)) : 0u;
+      qf[ks][2] = v0 ? __ldg(reinterpret_cast<const unsigned int*>(q0 + d2)) : 0u;
+      qf[ks][3] = v1 ? __ldg(reinterpret_cast<const unsigned int*>(q1 + d2)) : 0u;
     }
   }
 
@@ -144,14 +166,29 @@ struct MmaMath {
     float sc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    if constexpr (kFp8) {
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
+      for (int kp = 0; kp < KS / 2; ++kp) {
 #pragma unroll
-      for (int np = 0; np < NT; np += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + k_lane_off + (2 * ks * BS + np * 8) * 16, b0, b1, b2, b3);
-        mma_16816<T>(sc[np], qf[ks], b0, b1);
-        mma_16816<T>(sc[np + 1], qf[ks], b2, b3);
+        for (int np = 0; np < NT; np += 2) {
+          uint32_t r[4];  // (k-step 2kp, n-tile np), (2kp+1, np), (2kp, np+1), (2kp+1, np+1)
+          ldsm_x4(kb + k_lane_off + (2 * kp * BS + np * 8) * 16, r[0], r[1], r[2], r[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mma_16816<T>(sc[np + (i >> 1)], qf[2 * kp + (i & 1)], e4m3x2_to<T>(r[i] & 0xffffu),
+                         e4m3x2_to<T>(r[i] >> 16));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+        for (int np = 0; np < NT; np += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + k_lane_off + (2 * ks * BS + np * 8) * 16, b0, b1, b2, b3);
+          mma_16816<T>(sc[np], qf[ks], b0, b1);
+          mma_16816<T>(sc[np + 1], qf[ks], b2, b3);
+        }
       }
     }
     // Online softmax update (log2 domain); tokens past the sequence get -inf.
@@ -160,7 +197,7 @@ struct MmaMath {
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int tok = nt * 8 + 2 * t4 + (c & 1);
+        const int tok = token(nt, 2 * t4 + (c & 1));
         const float v = sc[nt][c] * scale_log2;
         sc[nt][c] = tok < rem ? v : -INFINITY;
       }
@@ -205,14 +242,28 @@ struct MmaMath {
         const float2 back = unpack2<T>(ahi[r]);
         alo[r] = pack2<T>(src[0] - back.x, src[1] - back.y);
       }
+      if constexpr (kFp8) {
 #pragma unroll
-      for (int dp = 0; dp < DT; dp += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(vb + v_lane_off + dp * 8 * (BS * kElem) + kk * 32, b0, b1, b2, b3);
-        mma_16816<T>(acc[dp], ahi, b0, b1);
-        mma_16816<T>(acc[dp + 1], ahi, b2, b3);
-        mma_16816<T>(acc[dp], alo, b0, b1);
-        mma_16816<T>(acc[dp + 1], alo, b2, b3);
+        for (int dp = 0; dp < DT; dp += 4) {
+          uint32_t r[4];  // head-dim n-tiles dp .. dp+3, tokens 16kk .. 16kk+15
+          ldsm_x4(vb + v_lane_off + dp * 8 * BS + kk * 16, r[0], r[1], r[2], r[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t b0 = e4m3x2_to<T>(r[i] & 0xffffu), b1 = e4m3x2_to<T>(r[i] >> 16);
+            mma_16816<T>(acc[dp + i], ahi, b0, b1);
+            mma_16816<T>(acc[dp + i], alo, b0, b1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int dp = 0; dp < DT; dp += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(vb + v_lane_off + dp * 8 * (BS * kElem) + kk * 32, b0, b1, b2, b3);
+          mma_16816<T>(acc[dp], ahi, b0, b1);
+          mma_16816<T>(acc[dp + 1], ahi, b2, b3);
+          mma_16816<T>(acc[dp], alo, b0, b1);
+          mma_16816<T>(acc[dp + 1], alo, b2, b3);
+        }
       }
     }
   }
@@ -225,9 +276,9 @@ struct MmaMath {
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   }
 
-  // out rows 0..nh-1 (row stride D) = acc / l, rounded to T.
-  __device__ __forceinline__ void store_out(T* out, int nh) const {
-    const float i0 = 1.f / l0, i1 = 1.f / l1;
+  // out rows 0..nh-1 (row stride D) = oscale * acc / l, rounded to T.
+  __device__ __forceinline__ void store_out(T* out, int nh, float oscale) const {
+    const float i0 = oscale / l0, i1 = oscale / l1;
     const bool v0 = g < nh, v1 = g + 8 < nh;
 #pragma unroll
     for (int dt = 0; dt < DT; ++dt) {
@@ -237,9 +288,9 @@ struct MmaMath {
     }
   }
 
-  // Partial result of rows 0..nh-1: o = acc / l (fp32, row stride D), (m, l).
-  __device__ __forceinline__ void store_partial(float* po, float* pml, int nh) const {
-    const float i0 = 1.f / l0, i1 = 1.f / l1;
+  // Partial result of rows 0..nh-1: o = oscale * acc / l (fp32, row stride D), (m, l).
+  __device__ __forceinline__ void store_partial(float* po, float* pml, int nh, float oscale) const {
+    const float i0 = oscale / l0, i1 = oscale / l1;
     const bool v0 = g < nh, v1 = g + 8 < nh;
 #pragma unroll
     for (int dt = 0; dt < DT; ++dt) {
@@ -309,9 +360,9 @@ struct MmaMath {
 // --- per-warp math: CUDA cores --------------------------------------------------------------------
 //
 // One query row against the tokens of a block.
-template <typename T, int D, int BS>
+template <typename T, typename TC, int D, int BS>
 struct SimtMath {
-  static constexpr int kElem = sizeof(T);
+  static constexpr int kElem = sizeof(TC);
   static constexpr int X = 16 / kElem;
   static constexpr int NGH = D / X / 2;        // 16-byte K groups per half-warp
   static constexpr int TP = BS / 16;           // 16-token passes per block
@@ -357,9 +408,9 @@ struct SimtMath {
 #pragma unroll
       for (int gi = 0; gi < NGH; ++gi) {
         const uint4 raw = *reinterpret_cast<const uint4*>(stage + ((half * NGH + gi) * BS + tok) * 16);
-        const T* kv = reinterpret_cast<const T*>(&raw);
+        const TC* kv = reinterpret_cast<const TC*>(&raw);
 #pragma unroll
-        for (int k = 0; k < X; ++k) dot = fmaf(qv[gi * X + k], DType<T>::to_f32(kv[k]), dot);
+        for (int k = 0; k < X; ++k) dot = fmaf(qv[gi * X + k], DType<TC>::to_f32(kv[k]), dot);
       }
       dot += __shfl_xor_sync(0xffffffffu, dot, 16);
       sc[tp] = tok < rem ? dot * scale_log2 : -INFINITY;
@@ -387,10 +438,10 @@ struct SimtMath {
     for (int k = 0; k < VP; ++k) {
       const int d = k * RPW + vrow;
       const uint4 raw = *reinterpret_cast<const uint4*>(vt + d * BS * kElem + vchunk * 16);
-      const T* vv = reinterpret_cast<const T*>(&raw);
+      const TC* vv = reinterpret_cast<const TC*>(&raw);
       float a = acc[k] * corr;
 #pragma unroll
-      for (int e = 0; e < X; ++e) a = fmaf(pw[vchunk * X + e], DType<T>::to_f32(vv[e]), a);
+      for (int e = 0; e < X; ++e) a = fmaf(pw[vchunk * X + e], DType<TC>::to_f32(vv[e]), a);
       acc[k] = a;
     }
     __syncwarp();
@@ -406,17 +457,17 @@ struct SimtMath {
     for (int o = 1; o < 32; o <<= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, o);
   }
 
-  __device__ __forceinline__ void store_out(T* out, int) const {
+  __device__ __forceinline__ void store_out(T* out, int, float oscale) const {
     if (vchunk == 0) {
-      const float il = 1.f / lpart;
+      const float il = oscale / lpart;
 #pragma unroll
       for (int k = 0; k < VP; ++k) out[k * RPW + vrow] = DType<T>::from_f32(acc[k] * il);
     }
   }
 
-  __device__ __forceinline__ void store_partial(float* po, float* pml, int) const {
+  __device__ __forceinline__ void store_partial(float* po, float* pml, int, float oscale) const {
     if (vchunk == 0) {
-      const float il = 1.f / lpart;
+      const float il = oscale / lpart;
 #pragma unroll
       for (int k = 0; k < VP; ++k) po[k * RPW + vrow] = acc[k] * il;
     }
@@ -484,12 +535,12 @@ __device__ __forceinline__ void locate(long long g, const int* pre, int S, int U
 }
 
 // grid = resident CTAs (persistent); kDecodeWarps independent warps per CTA.
-template <typename T, int D, int BS, bool kMma>
-__global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
+template <typename T, typename TC, int D, int BS, bool kMma>
+__global__ void __launch_bounds__(DecodeShape<TC, D, BS>::kWarps * 32)
     decode_kernel(const DecodeParams p) {
-  using Sh = DecodeShape<T, D, BS>;
+  using Sh = DecodeShape<TC, D, BS>;
   constexpr int kDecodeWarps = Sh::kWarps;
-  using Math = std::conditional_t<kMma, MmaMath<T, D, BS>, SimtMath<T, D, BS>>;
+  using Math = std::conditional_t<kMma, MmaMath<T, TC, D, BS>, SimtMath<T, TC, D, BS>>;
   constexpr int TILE = Sh::kTile, STAGES = Sh::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -632,7 +683,7 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
     if (!wait_stage<STAGES>(bars, k, len, p.err, lane)) break;
     unsigned char* stage = ring + (k % STAGES) * 2 * TILE;
     const int rem = L - cj * BS;  // valid tokens in this block (>= 1)
-    if (rem < BS) zero_tail_v<T, D, BS>(stage + TILE, rem, lane);
+    if (rem < BS) zero_tail_v<TC, D, BS>(stage + TILE, rem, lane);
     math.block(stage, TILE, rem, p.scale_log2);
     ++cj;
     const bool seg_end = cj == nblk, last = k + 1 == len;
@@ -644,12 +695,12 @@ __global__ void __launch_bounds__(DecodeShape<T, D, BS>::kWarps * 32)
         folded = false;
       }
       if (j0 == 0 && seg_end) {  // the whole segment: straight to the output
-        math.store_out(static_cast<T*>(p.out) + ((long long)cs * p.num_heads + h0) * D, nh);
+        math.store_out(static_cast<T*>(p.out) + ((long long)cs * p.num_heads + h0) * D, nh, p.out_scale);
         if (lane == 0) p.seg_first[seg] = -1;
       } else {
         // pieces start only at warp and segment boundaries, so this slot is unique
         const long long slot = (long long)w + seg;
-        math.store_partial(p.part_o + slot * p.rows * D, p.part_ml + slot * p.rows * 2, nh);
+        math.store_partial(p.part_o + slot * p.rows * D, p.part_ml + slot * p.rows * 2, nh, p.out_scale);
         if (lane == 0) {
           p.part_tag[slot] = make_int2(seg, static_cast<int>(p.epoch));
           if (j0 == 0) p.seg_first[seg] = static_cast<int>(slot);
@@ -792,43 +843,44 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
 
 // --- host-side launch helpers (instantiated per dtype) ------------------------------------------
 
-template <typename T, int D, int BS, bool kMma>
+template <typename TC, int D, int BS, bool kMma>
 constexpr int decode_smem_bytes() {
-  using Sh = DecodeShape<T, D, BS>;
+  using Sh = DecodeShape<TC, D, BS>;
   return Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes + Sh::kWarps * BS * 4 +
          Sh::kWarps * (kMma ? 16 : 1) * (D + 2) * 4;
 }
 
-template <typename T, int D, int BS, bool kMma>
+template <typename T, typename TC, int D, int BS, bool kMma>
 cudaError_t ensure_smem_attr() {
   static unsigned done = 0;  // bit d: set on device d
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 32 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1u)) return cudaSuccess;
-  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&decode_kernel<T, D, BS, kMma>),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<T, D, BS, kMma>());
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&decode_kernel<T, TC, D, BS, kMma>),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<TC, D, BS, kMma>());
   if (e == cudaSuccess && dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
   return e;
 }
 
-template <typename T, int D, int BS, bool kMma>
+template <typename T, typename TC, int D, int BS, bool kMma>
 int decode_ctas_per_sm_t() {
-  if (ensure_smem_attr<T, D, BS, kMma>() != cudaSuccess) return 0;
+  if (ensure_smem_attr<T, TC, D, BS, kMma>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<T, D, BS, kMma>, DecodeShape<T, D, BS>::kWarps * 32,
-                                                    decode_smem_bytes<T, D, BS, kMma>()) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<T, TC, D, BS, kMma>,
+                                                    DecodeShape<TC, D, BS>::kWarps * 32,
+                                                    decode_smem_bytes<TC, D, BS, kMma>()) != cudaSuccess)
     return 0;
   return n;
 }
 
-template <typename T, int D, int BS, bool kMma>
+template <typename T, typename TC, int D, int BS, bool kMma>
 cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream, int* launches) {
   *launches = 0;
-  cudaError_t e = ensure_smem_attr<T, D, BS, kMma>();
+  cudaError_t e = ensure_smem_attr<T, TC, D, BS, kMma>();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_kernel<T, D, BS, kMma>, dim3(grid), dim3(DecodeShape<T, D, BS>::kWarps * 32), decode_smem_bytes<T, D, BS, kMma>(),
-                 stream, p);
+  e = launch_pdl(decode_kernel<T, TC, D, BS, kMma>, dim3(grid), dim3(DecodeShape<TC, D, BS>::kWarps * 32),
+                 decode_smem_bytes<TC, D, BS, kMma>(), stream, p);
   if (e != cudaSuccess) return e;
   *launches = 1;
   e = launch_pdl(decode_merge_kernel<T, D, kMma>, dim3(p.num_seqs * p.units), dim3(kMergeWarps * 32), 0, stream, p);
@@ -837,41 +889,43 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream
   return cudaSuccess;
 }
 
-template <typename T, int D, int BS>
+// fp32 caches use the CUDA-core math only; 16-bit and FP8 caches both kinds.
+template <typename T, typename TC, int D, int BS>
 int ctas_for(DecodeKind kind) {
   if constexpr (sizeof(T) == 4) {
-    return decode_ctas_per_sm_t<T, D, BS, false>();
+    return decode_ctas_per_sm_t<T, TC, D, BS, false>();
   } else {
-    return kind == DecodeKind::kMma ? decode_ctas_per_sm_t<T, D, BS, true>() : decode_ctas_per_sm_t<T, D, BS, false>();
+    return kind == DecodeKind::kMma ? decode_ctas_per_sm_t<T, TC, D, BS, true>()
+                                    : decode_ctas_per_sm_t<T, TC, D, BS, false>();
   }
 }
 
-template <typename T, int D, int BS>
+template <typename T, typename TC, int D, int BS>
 cudaError_t launch_for(const DecodeParams& p, DecodeKind kind, int grid, cudaStream_t s, int* n) {
   if constexpr (sizeof(T) == 4) {
-    return launch_decode_t<T, D, BS, false>(p, grid, s, n);
+    return launch_decode_t<T, TC, D, BS, false>(p, grid, s, n);
   } else {
-    return kind == DecodeKind::kMma ? launch_decode_t<T, D, BS, true>(p, grid, s, n)
-                                    : launch_decode_t<T, D, BS, false>(p, grid, s, n);
+    return kind == DecodeKind::kMma ? launch_decode_t<T, TC, D, BS, true>(p, grid, s, n)
+                                    : launch_decode_t<T, TC, D, BS, false>(p, grid, s, n);
   }
 }
 
-template <typename T>
+template <typename T, typename TC>
 int decode_ctas_per_sm_dispatch(int head_size, int block_size, DecodeKind kind) {
-  if (head_size == 64 && block_size == 16) return ctas_for<T, 64, 16>(kind);
-  if (head_size == 64 && block_size == 32) return ctas_for<T, 64, 32>(kind);
-  if (head_size == 128 && block_size == 16) return ctas_for<T, 128, 16>(kind);
-  if (head_size == 128 && block_size == 32) return ctas_for<T, 128, 32>(kind);
+  if (head_size == 64 && block_size == 16) return ctas_for<T, TC, 64, 16>(kind);
+  if (head_size == 64 && block_size == 32) return ctas_for<T, TC, 64, 32>(kind);
+  if (head_size == 128 && block_size == 16) return ctas_for<T, TC, 128, 16>(kind);
+  if (head_size == 128 && block_size == 32) return ctas_for<T, TC, 128, 32>(kind);
   return 0;
 }
 
-template <typename T>
+template <typename T, typename TC>
 cudaError_t launch_decode_dispatch(int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
                                    cudaStream_t s, int* n) {
-  if (head_size == 64 && block_size == 16) return launch_for<T, 64, 16>(p, kind, grid, s, n);
-  if (head_size == 64 && block_size == 32) return launch_for<T, 64, 32>(p, kind, grid, s, n);
-  if (head_size == 128 && block_size == 16) return launch_for<T, 128, 16>(p, kind, grid, s, n);
-  if (head_size == 128 && block_size == 32) return launch_for<T, 128, 32>(p, kind, grid, s, n);
+  if (head_size == 64 && block_size == 16) return launch_for<T, TC, 64, 16>(p, kind, grid, s, n);
+  if (head_size == 64 && block_size == 32) return launch_for<T, TC, 64, 32>(p, kind, grid, s, n);
+  if (head_size == 128 && block_size == 16) return launch_for<T, TC, 128, 16>(p, kind, grid, s, n);
+  if (head_size == 128 && block_size == 32) return launch_for<T, TC, 128, 32>(p, kind, grid, s, n);
   return cudaErrorInvalidValue;
 }
 

@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -69,6 +70,28 @@ template <> struct DType<__nv_bfloat16> {
   __device__ __forceinline__ static float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
   __device__ __forceinline__ static __nv_bfloat16 from_f32(float v) { return __float2bfloat16_rn(v); }
 };
+
+// OCP FP8 E4M3 cache elements (read-only in decode; written by the quantising write path).
+template <> struct DType<__nv_fp8_e4m3> {
+  static constexpr int kBytes = 1;
+  __device__ __forceinline__ static float to_f32(__nv_fp8_e4m3 v) { return static_cast<float>(v); }
+  __device__ __forceinline__ static __nv_fp8_e4m3 from_f32(float v) { return __nv_fp8_e4m3(v); }
+};
+
+// Two E4M3 codes (low byte = first element) as a packed pair of 16-bit floats of
+// type T; exact, since every E4M3 value is a normal fp16 and bf16 number.
+template <typename T> __device__ __forceinline__ uint32_t e4m3x2_to(uint32_t two_codes);
+template <> __device__ __forceinline__ uint32_t e4m3x2_to<__half>(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+template <> __device__ __forceinline__ uint32_t e4m3x2_to<__nv_bfloat16>(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
+  __half2 hh;
+  *reinterpret_cast<__half2_raw*>(&hh) = h;
+  const __nv_bfloat162 b = __floats2bfloat162_rn(__low2float(hh), __high2float(hh));
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
 
 // Two fp32 values rounded to a packed pair of 16-bit floats (low half = a).
 template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);

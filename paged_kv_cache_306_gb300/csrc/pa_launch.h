@@ -54,7 +54,8 @@ struct DecodeParams {
   int part_blocks;              // blocks per caller partition; a huge value when none
   int num_slots;                // partial-result slots in the workspace
   unsigned epoch;               // distinguishes this launch's partial slots from stale ones
-  float scale_log2;             // scale * log2(e)
+  float scale_log2;             // scale * k_scale * log2(e)
+  float out_scale;              // v_scale: a quantised cache's V reads back as code * v_scale
 };
 
 enum class DecodeKind { kSimt = 0, kMma = 1 };
@@ -92,12 +93,21 @@ cudaError_t launch_decode_f16(int head_size, int block_size, const DecodeParams&
                               cudaStream_t s, int* n);
 cudaError_t launch_decode_bf16(int head_size, int block_size, const DecodeParams& p, DecodeKind kind, int grid,
                                cudaStream_t s, int* n);
+// FP8 E4M3 cache with fp16 (q_is_bf16 == false) or bf16 queries (decode_fp8.cu).
+int decode_ctas_per_sm_fp8(bool q_is_bf16, int head_size, int block_size, DecodeKind kind);
+cudaError_t launch_decode_fp8(bool q_is_bf16, int head_size, int block_size, const DecodeParams& p, DecodeKind kind,
+                              int grid, cudaStream_t s, int* n);
 
 // Write path (cache_ops.cu).
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                      const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
                                      int head_size, int block_size, int64_t num_blocks, int elem_bytes,
                                      unsigned* err, cudaStream_t stream, int* launches);
+cudaError_t launch_reshape_and_cache_e4m3(const void* key, const void* value, void* k_cache, void* v_cache,
+                                           const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                                           int head_size, int block_size, int64_t num_blocks, int key_dtype,
+                                           float k_scale, float v_scale, unsigned* err, cudaStream_t stream,
+                                           int* launches);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int64_t num_pairs,
                                int64_t block_bytes, int64_t num_blocks, unsigned* err, cudaStream_t stream,
                                int* launches);

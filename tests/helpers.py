@@ -6,8 +6,9 @@ import oracle
 import workloads as W
 
 # Max-abs tolerance on attention outputs: 2e-3 for 16-bit caches with fp32
-# accumulation, 1e-5 for fp32 caches.
-TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
+# accumulation, 1e-5 for fp32 caches.  An FP8 cache is compared with the oracle
+# reading the same codes, so only the arithmetic differs: the 16-bit bar holds.
+TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3, "fp8": 2e-3}
 
 
 def half_ulp(ref, dtype):
@@ -29,9 +30,9 @@ def torch_dtype(dtype):
 def upload(wl, device="cuda"):
     import torch
     t = {
-        "q": W.to_torch(wl.q, wl.dtype, device),
-        "key": W.to_torch(wl.key, wl.dtype, device),
-        "value": W.to_torch(wl.value, wl.dtype, device),
+        "q": W.to_torch(wl.q, wl.q_dtype, device),
+        "key": W.to_torch(wl.key, wl.q_dtype, device),
+        "value": W.to_torch(wl.value, wl.q_dtype, device),
         "k_cache": W.to_torch(wl.k_cache, wl.dtype, device),
         "v_cache": W.to_torch(wl.v_cache, wl.dtype, device),
         "block_tables": torch.from_numpy(wl.block_tables).to(device),
@@ -50,11 +51,19 @@ def gpu_step(wl, partition_size=None, t=None, write=True):
     if write:
         if len(wl.cow):
             pa.pa_copy_blocks(t["k_cache"], t["v_cache"], t["cow"])
-        pa.pa_reshape_and_cache(t["key"], t["value"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+        if wl.dtype == "fp8":
+            pa.pa_reshape_and_cache_scaled(t["key"], t["value"], t["k_cache"], t["v_cache"], t["slot_mapping"],
+                                           wl.k_scale, wl.v_scale)
+        else:
+            pa.pa_reshape_and_cache(t["key"], t["value"], t["k_cache"], t["v_cache"], t["slot_mapping"])
     out = torch.empty_like(t["q"])
     ps = wl.partition_size if partition_size is None else partition_size
-    pa.pa_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"], wl.scale,
-                 wl.max_seq_len, ps)
+    if wl.dtype == "fp8":
+        pa.pa_decode_scaled(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"], wl.scale,
+                            wl.max_seq_len, wl.k_scale, wl.v_scale, ps)
+    else:
+        pa.pa_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"], wl.scale,
+                     wl.max_seq_len, ps)
     code = pa.pa_get_device_error()
     assert code == 0, f"device error {code}: {pa.DEVICE_ERRORS.get(code)}"
     return out, t
@@ -64,13 +73,18 @@ def oracle_pools(wl, write=True):
     k, v = wl.clone_pools()
     if write:
         oracle.copy_blocks(k, v, wl.cow, wl.dtype)
-        oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
+        if wl.dtype == "fp8":
+            oracle.reshape_and_cache_scaled(wl.key, wl.value, k, v, wl.slot_mapping, wl.q_dtype, wl.dtype,
+                                            wl.k_scale, wl.v_scale)
+        else:
+            oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
     return k, v
 
 
 def oracle_out(wl, k, v, seqs=None):
     sub = wl if seqs is None else W.subset(wl, seqs)
-    return oracle.decode(sub.q, k, v, sub.block_tables, sub.seq_lens, wl.scale, wl.dtype)
+    return oracle.decode(sub.q, k, v, sub.block_tables, sub.seq_lens, wl.scale, wl.dtype, q_dtype=wl.q_dtype,
+                         k_scale=wl.k_scale, v_scale=wl.v_scale)
 
 
 def as_f64(out):
@@ -78,14 +92,14 @@ def as_f64(out):
     return out.detach().to(torch.float64).cpu().numpy()
 
 
-def max_violation(got, ref, dtype, with_rounding):
+def max_violation(got, ref, dtype, with_rounding, out_dtype=None):
     err = np.abs(got - ref)
-    tol = TOL[dtype] + (half_ulp(ref, dtype) if with_rounding else 0.0)
+    tol = TOL[dtype] + (half_ulp(ref, out_dtype or dtype) if with_rounding else 0.0)
     assert np.all(np.isfinite(got)), "non-finite output"
     return float(err.max()), float((err - tol).max())
 
 
-def assert_close(got, ref, dtype, with_rounding=True, what=""):
-    err, worst = max_violation(got, ref, dtype, with_rounding)
+def assert_close(got, ref, dtype, with_rounding=True, what="", out_dtype=None):
+    err, worst = max_violation(got, ref, dtype, with_rounding, out_dtype)
     assert worst <= 0.0, f"{what}: max abs err {err:.3e} exceeds tolerance (excess {worst:.3e})"
     return err

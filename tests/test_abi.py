@@ -121,3 +121,58 @@ def test_binding_refuses_cpu_tensors(lib):
         pa.pa_decode(q, q, torch.zeros(1, 4, 16, 16, 8, dtype=torch.float16),
                      torch.zeros(1, 4, 128, 16, dtype=torch.float16), torch.zeros(1, 1, dtype=torch.int32),
                      torch.ones(1, dtype=torch.int32), 0.1, 1)
+
+
+def _decode_scaled(lib, **kw):
+    a = dict(out=8192, q=8192, k=8192, v=8192, bt=8192, mb=4, sl=8192, S=1, msl=16, H=4, Hkv=2, D=128, bs=16,
+             nb=8, scale=0.1, ps=0, ws=None, wsb=0, qdt=B.PA_F16, cdt=B.PA_FP8_E4M3, ks=0.5, vs=0.25)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.pa_decode_scaled(P(a["out"]), P(a["q"]), P(a["k"]), P(a["v"]), P(a["bt"]), a["mb"], P(a["sl"]),
+                                a["S"], a["msl"], a["H"], a["Hkv"], a["D"], a["bs"], a["nb"], a["scale"], a["ps"],
+                                P(a["ws"]), a["wsb"], a["qdt"], a["cdt"], a["ks"], a["vs"], None)
+
+
+def test_plain_decode_refuses_an_fp8_cache(lib):
+    # the FP8 cache needs the query dtype and the scales: pa_decode_scaled
+    assert _decode(lib, dt=B.PA_FP8_E4M3) == B.PA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qdt=B.PA_F32), B.PA_ERR_UNSUPPORTED),          # FP8 cache read by fp32 queries
+    (dict(qdt=B.PA_FP8_E4M3), B.PA_ERR_UNSUPPORTED),
+    (dict(qdt=9), B.PA_ERR_INVALID_ARG),
+    (dict(ks=0.0), B.PA_ERR_INVALID_ARG),
+    (dict(vs=-1.0), B.PA_ERR_INVALID_ARG),
+    (dict(ks=float("inf")), B.PA_ERR_INVALID_ARG),
+    (dict(vs=float("nan")), B.PA_ERR_INVALID_ARG),
+    (dict(cdt=B.PA_F16, qdt=B.PA_BF16, ks=1.0, vs=1.0), B.PA_ERR_INVALID_ARG),   # 16-bit cache, other queries
+    (dict(cdt=B.PA_F16, ks=0.5, vs=1.0), B.PA_ERR_INVALID_ARG),                  # 16-bit cache, scale != 1
+    (dict(D=96), B.PA_ERR_UNSUPPORTED),
+    (dict(ps=24), B.PA_ERR_INVALID_ARG),
+    (dict(q=8200), B.PA_ERR_ALIGNMENT),
+])
+def test_scaled_decode_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert _decode_scaled(lib, **kw) == status
+    assert lib.pa_last_error_message()
+
+
+def test_scaled_decode_with_no_sequences_is_a_no_op(lib):
+    assert _decode_scaled(lib, S=0, q=0, out=0) == B.PA_OK
+
+
+def test_scaled_write_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    F8, F16 = B.PA_FP8_E4M3, B.PA_F16
+
+    def w(key_dt=F16, cache_dt=F8, ks=0.5, vs=0.5, D=128, key=16, T=4):
+        return lib.pa_reshape_and_cache_scaled(P(key), P(16), P(16), P(16), P(16), T, 2, D, 16, 8, key_dt, cache_dt,
+                                               ks, vs, None)
+    assert w(key_dt=F8) == B.PA_ERR_UNSUPPORTED           # codes are not a source dtype
+    assert w(ks=0.0) == B.PA_ERR_INVALID_ARG
+    assert w(vs=float("nan")) == B.PA_ERR_INVALID_ARG
+    assert w(D=72) == B.PA_ERR_INVALID_ARG                # x = 16 codes per K row chunk
+    assert w(key=24) == B.PA_ERR_ALIGNMENT
+    assert w(cache_dt=F16, ks=0.5) == B.PA_ERR_INVALID_ARG   # a 16-bit cache takes no scales
+    assert w(cache_dt=F16, key_dt=B.PA_BF16, ks=1.0, vs=1.0) == B.PA_ERR_INVALID_ARG
+    assert w(T=0) == B.PA_OK

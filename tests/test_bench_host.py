@@ -73,3 +73,22 @@ def test_reference_arm_prints_one_json_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["steps"] == 3
+
+
+def test_decode_bytes_of_the_llama_layer_with_an_fp8_pool():
+    wl = W.config(3, poison=False, kv_dtype="fp8")
+    # K+V at one byte per element, q and out still fp16
+    expect = 536_870_912 // 2 + 2 * 16 * 32 * 128 * 2 + 16 * 128 * 4 + 16 * 4
+    assert bench.decode_bytes(wl) == expect
+    # write: fp16 key/value in, one-byte codes out, the slot ids
+    assert bench.write_bytes(wl) == 16 * 32 * 128 * (2 + 1) * 2 + 16 * 8
+
+
+def test_reference_arm_with_an_fp8_pool():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "llama",
+                        "--kv-dtype", "fp8", "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["config"]["kv_cache_dtype"] == "fp8_e4m3" and line["value"] > 0
+    assert line["dtype"].startswith("fp8_e4m3")

@@ -109,3 +109,30 @@ def test_full_size_shapes_of_the_layer_workloads():
     assert sorted(wl.block_tables.ravel().tolist()) == list(range(2048))
     kv_bytes = wl.total_tokens * wl.num_kv_heads * wl.head_size * 2 * 2
     assert kv_bytes == 536_870_912
+
+
+def test_fp8_workload_holds_codes_of_scaled_normal_values():
+    wl = W.make_private("f8", "fp8", [40, 17, 1], 8, 2, 128, 16, seed=7, q_dtype="bf16")
+    assert wl.k_cache.dtype == np.uint8 and wl.k_cache.shape == (wl.num_blocks, 2, 8, 16, 16)
+    assert wl.q_dtype == "bf16" and wl.q.dtype == np.uint16 and wl.key.dtype == np.uint16
+    assert wl.k_scale == wl.v_scale == W.FP8_SCALE
+    m = valid_mask_k(wl)
+    for s in range(wl.num_seqs):                                 # new-token slots stay poisoned until the write
+        b, o = divmod(int(wl.slot_mapping[s]), wl.block_size)
+        m[b, o] = False
+    vals = oracle.widen(wl.v_cache, "fp8") * wl.v_scale          # [NB, Hkv, D, bs]
+    live = vals.transpose(0, 3, 1, 2)[m]                         # tokens some sequence reads
+    assert np.all(np.isfinite(live))
+    assert 0.9 < live.std() < 1.1 and abs(live.mean()) < 0.05
+    # unused slots carry the NaN code
+    dead = wl.v_cache.transpose(0, 3, 1, 2)[~m]
+    assert np.all(dead == W.FP8_NAN)
+
+
+def test_fp8_config_keeps_the_shapes_of_its_16_bit_workload():
+    a, b = W.config(3), W.config(3, kv_dtype="fp8")
+    assert b.k_cache.shape[:2] == a.k_cache.shape[:2] and b.k_cache.shape[-1] == 16
+    assert b.q_dtype == a.dtype and np.array_equal(a.seq_lens, b.seq_lens)
+    assert np.array_equal(a.block_tables, b.block_tables)
+    with pytest.raises(ValueError):
+        W.config(1, kv_dtype="fp8")

@@ -16,16 +16,21 @@ block copies (`cow`), and `seq_lens` already counts that token.  Slots that hold
 no valid token are filled with NaN when `poison` is set, so a kernel that reads
 them produces a visible error.
 
-Arrays are numpy: fp32 -> float32, fp16 -> float16, bf16 -> uint16 bit patterns.
+Arrays are numpy: fp32 -> float32, fp16 -> float16, bf16 -> uint16 bit patterns,
+FP8 E4M3 -> uint8 codes.  An FP8 pool ("fp8") holds codes whose values times the
+workload's k_scale / v_scale are the K / V values; its queries and new-token rows
+are in a 16-bit `q_dtype`.
 """
 from dataclasses import dataclass, field
 import math
 
 import numpy as np
 
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
-NP_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8": 1}
+NP_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "fp8": np.uint8}
 BF16_NAN = np.uint16(0x7FC0)
+FP8_NAN = np.uint8(0x7F)
+FP8_SCALE = 1.0 / 64   # k_scale = v_scale of the FP8 workloads: N(0,1) values span codes up to ~400
 _CHUNK = 1 << 23
 
 
@@ -40,24 +45,31 @@ def _bf16_bits(f32):
 
 
 def cast(f32, dtype):
-    """Round float32 values to the storage dtype."""
+    """Round float32 values to the storage dtype (FP8: torch's float8_e4m3fn rounding)."""
     if dtype == "f32":
         return np.ascontiguousarray(f32, dtype=np.float32)
     if dtype == "f16":
         return f32.astype(np.float16)
+    if dtype == "fp8":
+        import torch
+        x = np.clip(np.ascontiguousarray(f32, dtype=np.float32), -448.0, 448.0)
+        return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     return _bf16_bits(f32)
 
 
 def fill_value(dtype, poison):
     if not poison:
         return 0
-    return BF16_NAN if dtype == "bf16" else np.nan
+    return {"bf16": BF16_NAN, "fp8": FP8_NAN}.get(dtype, np.nan)
 
 
-def randn(rng, shape, dtype, std=1.0):
+def randn(rng, shape, dtype, std=1.0, scale=1.0):
+    """N(0, std^2) draws stored as `dtype`; FP8 stores the codes nearest to x / scale."""
     v = rng.standard_normal(shape, dtype=np.float32)
     if std != 1.0:
         v *= np.float32(std)
+    if dtype == "fp8":
+        v /= np.float32(scale)
     return cast(v, dtype)
 
 
@@ -85,6 +97,13 @@ class Workload:
     cow: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int64))
     unique_tokens: int = 0       # valid tokens summed over distinct physical blocks
     meta: dict = field(default_factory=dict)
+    q_dtype: str = None          # dtype of q, key, value and out (defaults to the cache dtype)
+    k_scale: float = 1.0         # an FP8 pool reads back as code * scale
+    v_scale: float = 1.0
+
+    def __post_init__(self):
+        if self.q_dtype is None:
+            self.q_dtype = self.dtype
 
     @property
     def max_blocks_per_seq(self):
@@ -112,15 +131,15 @@ def _empty_pools(nb, hkv, d, bs, dtype, poison):
     return k, v
 
 
-def _fill_blocks(rng, k, v, ids, dtype, std):
+def _fill_blocks(rng, k, v, ids, dtype, std, scale=1.0):
     """Random values into whole physical blocks `ids` (chunked to bound memory)."""
     ids = np.asarray(ids, dtype=np.int64)
     per = int(np.prod(k.shape[1:]))
     step = max(1, _CHUNK // per)
     for i in range(0, len(ids), step):
         c = ids[i:i + step]
-        k[c] = randn(rng, (len(c),) + k.shape[1:], dtype, std)
-        v[c] = randn(rng, (len(c),) + v.shape[1:], dtype, std)
+        k[c] = randn(rng, (len(c),) + k.shape[1:], dtype, std, scale)
+        v[c] = randn(rng, (len(c),) + v.shape[1:], dtype, std, scale)
 
 
 def _poison_tail(k, v, phys, first_invalid, dtype, poison):
@@ -131,7 +150,8 @@ def _poison_tail(k, v, phys, first_invalid, dtype, poison):
 
 
 def _finish(name, dtype, S, H, Hkv, D, bs, nb, tables, seq_lens, k, v, rng, partition_size,
-            q_std=1.0, kv_std=1.0, poison=True, cow=None, unique_tokens=None, meta=None):
+            q_std=1.0, kv_std=1.0, poison=True, cow=None, unique_tokens=None, meta=None, q_dtype=None,
+            kv_scale=1.0):
     """Common tail: new-token slots, poison, q/key/value draws."""
     mb = max(len(t) for t in tables) if S else 1
     bt = np.full((S, mb), -1, dtype=np.int32)
@@ -147,9 +167,10 @@ def _finish(name, dtype, S, H, Hkv, D, bs, nb, tables, seq_lens, k, v, rng, part
         slots[s] = phys * bs + off
         k[phys, :, :, off, :] = fv                   # written by the step itself
         v[phys, :, :, off] = fv
-    q = randn(rng, (S, H, D), dtype, q_std)
-    key = randn(rng, (S, Hkv, D), dtype, kv_std)
-    value = randn(rng, (S, Hkv, D), dtype, kv_std)
+    qd = q_dtype or dtype
+    q = randn(rng, (S, H, D), qd, q_std)
+    key = randn(rng, (S, Hkv, D), qd, kv_std)
+    value = randn(rng, (S, Hkv, D), qd, kv_std)
     if unique_tokens is None:
         unique_tokens = int(sl.astype(np.int64).sum())
     return Workload(name=name, dtype=dtype, num_seqs=S, num_heads=H, num_kv_heads=Hkv, head_size=D,
@@ -157,12 +178,21 @@ def _finish(name, dtype, S, H, Hkv, D, bs, nb, tables, seq_lens, k, v, rng, part
                     partition_size=partition_size, q=q, key=key, value=value, slot_mapping=slots,
                     k_cache=k, v_cache=v, block_tables=bt, seq_lens=sl,
                     cow=np.zeros((0, 2), np.int64) if cow is None else np.asarray(cow, np.int64).reshape(-1, 2),
-                    unique_tokens=unique_tokens, meta=meta or {})
+                    unique_tokens=unique_tokens, meta=meta or {}, q_dtype=qd, k_scale=kv_scale,
+                    v_scale=kv_scale)
+
+
+def _fp8_args(dtype, q_dtype, kv_scale):
+    if dtype == "fp8":
+        if q_dtype not in ("f16", "bf16"):
+            raise ValueError("an FP8 pool needs fp16 or bf16 queries")
+        return q_dtype, FP8_SCALE if kv_scale is None else kv_scale
+    return q_dtype, 1.0
 
 
 def make_private(name, dtype, seq_lens, num_heads, num_kv_heads, head_size, block_size, *, seed,
                  num_blocks=None, pool_factor=1.25, placement="shuffled", q_std=1.0, kv_std=1.0,
-                 poison=True, partition_size=0):
+                 poison=True, partition_size=0, q_dtype=None, kv_scale=None):
     """Sequences with private blocks only.
 
     placement:
@@ -171,6 +201,7 @@ def make_private(name, dtype, seq_lens, num_heads, num_kv_heads, head_size, bloc
                       tables, then one random relabelling of physical ids);
       "contiguous" -- the identity placement, sequence after sequence.
     """
+    q_dtype, kv_scale = _fp8_args(dtype, q_dtype, kv_scale)
     rng = np.random.default_rng(seed)
     seq_lens = [int(x) for x in seq_lens]
     S = len(seq_lens)
@@ -188,18 +219,19 @@ def make_private(name, dtype, seq_lens, num_heads, num_kv_heads, head_size, bloc
         tables.append(ids[c:c + n].astype(np.int32))
         c += n
     k, v = _empty_pools(nb, num_kv_heads, head_size, block_size, dtype, poison)
-    _fill_blocks(rng, k, v, ids, dtype, kv_std)
+    _fill_blocks(rng, k, v, ids, dtype, kv_std, kv_scale)
     for s, L in enumerate(seq_lens):
         r = L % block_size
         if r:
             _poison_tail(k, v, int(tables[s][-1]), r, dtype, poison)
     return _finish(name, dtype, S, num_heads, num_kv_heads, head_size, block_size, nb, tables, seq_lens,
-                   k, v, rng, partition_size, q_std=q_std, kv_std=kv_std, poison=poison)
+                   k, v, rng, partition_size, q_std=q_std, kv_std=kv_std, poison=poison, q_dtype=q_dtype,
+                   kv_scale=kv_scale)
 
 
 def make_prefix_shared(name, dtype, num_groups, group_size, num_heads, num_kv_heads, head_size,
                        block_size, *, seed, len_range=(16, 8192), prefix_range=(256, 2048),
-                       pool_factor=1.25, poison=True, partition_size=-1):
+                       pool_factor=1.25, poison=True, partition_size=-1, q_dtype=None, kv_scale=None):
     """Parallel-sampling groups that share prefix blocks (refcount > 1).
 
     Group g has a prefix of P_g tokens.  Sequence i of the group has L_i tokens
@@ -212,6 +244,7 @@ def make_prefix_shared(name, dtype, num_groups, group_size, num_heads, num_kv_he
     copy-on-write when the target block is shared (refcount > 1), in place
     otherwise ("vLLM's PagedAttention: why the KV cache is paged", §4.2).
     """
+    q_dtype, kv_scale = _fp8_args(dtype, q_dtype, kv_scale)
     rng = np.random.default_rng(seed)
     bs = block_size
     S = num_groups * group_size
@@ -258,11 +291,11 @@ def make_prefix_shared(name, dtype, num_groups, group_size, num_heads, num_kv_he
     k, v = _empty_pools(nb, num_kv_heads, head_size, bs, dtype, poison)
     # prefix content: the group's prefix tokens, partial last block poisoned past P_g
     for g in range(num_groups):
-        _fill_blocks(rng, k, v, shared_ids[g], dtype, 1.0)
+        _fill_blocks(rng, k, v, shared_ids[g], dtype, 1.0, kv_scale)
         r = int(P[g]) % bs
         if r:
             _poison_tail(k, v, int(shared_ids[g][-1]), r, dtype, poison)
-    _fill_blocks(rng, k, v, private_ids, dtype, 1.0)
+    _fill_blocks(rng, k, v, private_ids, dtype, 1.0, kv_scale)
 
     tables = []
     refcount = {}
@@ -315,7 +348,7 @@ def make_prefix_shared(name, dtype, num_groups, group_size, num_heads, num_kv_he
     unique_tokens = int(sum(valid.values()))
     wl = _finish(name, dtype, S, num_heads, num_kv_heads, head_size, bs, nb, tables, L, k, v, rng,
                  partition_size, poison=poison, cow=None, unique_tokens=unique_tokens,
-                 meta={"prefix_lens": P.tolist(), "group_size": group_size})
+                 meta={"prefix_lens": P.tolist(), "group_size": group_size}, q_dtype=q_dtype, kv_scale=kv_scale)
     # _finish poisons the new-token slot of the (post-copy) target block; a
     # copy-on-write destination is still unwritten before the step, so the
     # poison there is what the copy must overwrite.  The source block keeps the
@@ -335,9 +368,27 @@ CONFIG_NAMES = {
 }
 
 
-def config(i, *, poison=True, block_size=None, seed=None):
-    """Workload i (1..5) at its full size; seed defaults to 306 + i."""
+def config(i, *, poison=True, block_size=None, seed=None, kv_dtype=None):
+    """Workload i (1..5) at its full size; seed defaults to 306 + i.
+
+    kv_dtype="fp8" keeps every shape and the query dtype but stores the pool as
+    FP8 E4M3 codes (scales FP8_SCALE); the tiny fp32 workload has no FP8 form.
+    """
     sd = 306 + i if seed is None else seed
+    if kv_dtype not in (None, "fp8"):
+        raise ValueError(kv_dtype)
+    if kv_dtype == "fp8":
+        if i == 1:
+            raise ValueError("the fp32 workload has no FP8 form")
+        wl0 = {2: "f16", 3: "f16", 4: "bf16", 5: "f16"}[i]
+        return _config(i, sd, poison, block_size, cache="fp8", q_dtype=wl0)
+    return _config(i, sd, poison, block_size)
+
+
+def _config(i, sd, poison, block_size, cache=None, q_dtype=None):
+    def dt(d):
+        return cache or d
+    suffix = "-fp8kv" if cache else ""
     if i == 1:
         rng = np.random.default_rng(sd)
         L = rng.integers(1, 257, size=4)
@@ -347,19 +398,20 @@ def config(i, *, poison=True, block_size=None, seed=None):
     if i == 2:
         rng = np.random.default_rng(sd)
         L = rng.integers(512, 4097, size=64)
-        return make_private(CONFIG_NAMES[2], "f16", L, 28, 4, 128, 16, seed=sd + 1000,
-                            placement="shuffled", poison=poison, partition_size=-1)
+        return make_private(CONFIG_NAMES[2] + suffix, dt("f16"), L, 28, 4, 128, 16, seed=sd + 1000,
+                            placement="shuffled", poison=poison, partition_size=-1, q_dtype=q_dtype)
     if i == 3:
-        return make_private(CONFIG_NAMES[3], "f16", [2048] * 16, 32, 32, 128, 16, seed=sd,
+        return make_private(CONFIG_NAMES[3] + suffix, dt("f16"), [2048] * 16, 32, 32, 128, 16, seed=sd,
                             num_blocks=2048, placement="shuffled", kv_std=0.5, poison=poison,
-                            partition_size=-1)
+                            partition_size=-1, q_dtype=q_dtype)
     if i == 4:
-        return make_private(CONFIG_NAMES[4], "bf16", [32768, 65536, 98304, 131072], 32, 8, 128, 16,
-                            seed=sd, pool_factor=1.25, placement="shuffled", poison=poison,
-                            partition_size=512)
+        return make_private(CONFIG_NAMES[4] + suffix, dt("bf16"), [32768, 65536, 98304, 131072], 32, 8, 128,
+                            16, seed=sd, pool_factor=1.25, placement="shuffled", poison=poison,
+                            partition_size=512, q_dtype=q_dtype)
     if i == 5:
-        return make_prefix_shared(CONFIG_NAMES[5] + f"-bs{block_size or 16}", "f16", 32, 8, 32, 8, 128,
-                                  block_size or 16, seed=sd, poison=poison, partition_size=-1)
+        return make_prefix_shared(CONFIG_NAMES[5] + f"-bs{block_size or 16}" + suffix, dt("f16"), 32, 8, 32, 8,
+                                  128, block_size or 16, seed=sd, poison=poison, partition_size=-1,
+                                  q_dtype=q_dtype)
     raise ValueError(i)
 
 
@@ -373,7 +425,8 @@ def subset(wl, seqs):
                     key=np.ascontiguousarray(wl.key[seqs]), value=np.ascontiguousarray(wl.value[seqs]),
                     slot_mapping=np.ascontiguousarray(wl.slot_mapping[seqs]), k_cache=wl.k_cache,
                     v_cache=wl.v_cache, block_tables=np.ascontiguousarray(wl.block_tables[seqs]),
-                    seq_lens=np.ascontiguousarray(wl.seq_lens[seqs]), meta=dict(wl.meta))
+                    seq_lens=np.ascontiguousarray(wl.seq_lens[seqs]), meta=dict(wl.meta), q_dtype=wl.q_dtype,
+                    k_scale=wl.k_scale, v_scale=wl.v_scale)
 
 
 def to_torch(a, dtype, device):
@@ -381,6 +434,8 @@ def to_torch(a, dtype, device):
     import torch
     if dtype == "bf16":
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    elif dtype == "fp8":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.uint8)).view(torch.float8_e4m3fn)
     else:
         t = torch.from_numpy(np.ascontiguousarray(a))
     return t.to(device)
@@ -392,4 +447,6 @@ def from_torch(t, dtype):
     t = t.detach().cpu().contiguous()
     if dtype == "bf16":
         return t.view(torch.int16).numpy().view(np.uint16)
+    if dtype == "fp8":
+        return t.view(torch.uint8).numpy()
     return t.numpy()
