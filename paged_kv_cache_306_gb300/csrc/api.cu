@@ -121,7 +121,7 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   const int ctas = pa::decode_ctas_per_sm(static_cast<int>(dtype), head_size, block_size, pl->kind);
   const int sms = sm_count();
   if (ctas <= 0 || sms <= 0) return fail(PA_ERR_CUDA, "cannot query the device (SM count %d, CTAs per SM %d)", sms, ctas);
-  const int warps = pa::decode_warps_for(elem_bytes(dtype), head_size, block_size);
+  const int warps = pa::decode_warps_for(elem_bytes(dtype), head_size, block_size, pl->kind);
   const long long work = chunk * pl->units * (long long)nblk_max;
   long long grid = (work + 4 * warps - 1) / (4 * warps);
   if (grid > (long long)sms * ctas) grid = (long long)sms * ctas;

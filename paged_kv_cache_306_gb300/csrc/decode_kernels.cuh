@@ -29,12 +29,13 @@
 //     1-D bulk copy through the TMA unit (cp.async.bulk) that signals an mbarrier
 //     with its byte count.  Block-table entries for the next 32 blocks are fetched
 //     one group ahead, one lane per entry, so the table walk never stalls the ring.
-//   * Tensor-core math (16-bit caches, >= 2 query heads per kv head): the query
-//     heads of one kv head are the rows of m16n8k16 tiles, so one K/V read serves
-//     all of them.  S = Q K^T takes K straight from the stage with ldmatrix (a
-//     K-pool row of 8 dims is 16 B); P V takes V the same way (a V-pool row holds 8
-//     consecutive tokens per 16 B).  P stays in registers, split into a rounded
-//     16-bit high part and the rounded remainder so P V keeps ~16 significant bits.
+//   * Tensor-core math (16-bit and FP8 caches, >= 2 query heads per kv head): the
+//     query heads of one kv head are the 8-wide side of m16n8k16 tiles, tokens
+//     and head dims the 16-row side (S^T = K Q^T, O^T += V^T P^T), so one K/V read
+//     serves all of them and a kv head with up to 8 query heads wastes no
+//     tensor-core work.  K and V come straight from the stage with ldmatrix; P
+//     stays in registers, split into a rounded 16-bit high part and the rounded
+//     remainder so P V keeps ~16 significant bits.
 //   * CUDA-core math (fp32 caches, or one query head per kv head): half-warps split
 //     the head dims of the scores, lanes split V rows and token chunks for P V, and
 //     the reductions are warp shuffles.
@@ -54,13 +55,13 @@ namespace pa {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s, then PA_DEVERR_TIMEOUT
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, int kMode>
 struct DecodeShape {
   static constexpr int kElem = sizeof(T);
   static constexpr int kX = 16 / kElem;         // elements per 16-byte K group
   static constexpr int kTile = D * BS * kElem;  // bytes of one K (or V) tile
-  static constexpr int kWarps = decode_warps(2 * kTile);
-  static constexpr int kStages = decode_stages(2 * kTile);
+  static constexpr int kWarps = decode_warps(2 * kTile, kMode);
+  static constexpr int kStages = decode_stages(2 * kTile, kMode);
   static constexpr int kRingBytes = kWarps * kStages * 2 * kTile;
   static constexpr int kBarBytes = kWarps * kStages * 8;
   // per-sequence tables: lengths, block prefix, warp sums
@@ -93,266 +94,320 @@ __device__ __forceinline__ void zero_tail_v(unsigned char* vtile, int rem, int l
 
 // --- per-warp math: tensor cores ---------------------------------------------------------------
 //
-// Up to 16 query rows (the heads of one head unit) against the tokens of a block.
+// The query heads of one head unit (up to 8 * NH) against the tokens of a block,
+// with the tiles transposed so that tokens and head dims take the 16-row side of
+// the m16n8k16 shape and the query heads its 8-column side:
+//     S^T [tokens x heads] = K [tokens x dims] Q^T [dims x heads]
+//     O^T [dims x heads]  += V^T [dims x tokens] P^T [tokens x heads]
+// K and V^T are A operands read straight from the stage with ldmatrix (a K-pool
+// row holds 16 bytes of dims of one token, a V-pool row the tokens of one dim);
+// Q^T stays in registers for the whole segment.  A kv head with at most 8 query
+// heads fills one 8-column tile, so no tensor-core work goes to padding rows.
+// P^T comes from S^T's accumulators through movmatrix (8x8 transposes), split
+// into a rounded 16-bit high part and the rounded remainder, so that P V keeps
+// ~16 significant bits.
 //
-// T is the query / output type and the type of the tensor-core operands; TC is
-// the cache element type: T itself, or FP8 E4M3 (converted to T in registers).
-// For an FP8 cache, ldmatrix over 16-byte rows hands each thread 4 consecutive
-// codes, which must become the (k, k+1) and (k+8, k+9) operand pairs of the MMA:
-// the head dims of Q are permuted to match within each 16-dim k-step, and the
-// tokens of S's n-tiles are permuted so that P's fragments line up with V's.
-template <typename T, typename TC, int D, int BS>
+// T is the query / output type and the operand type; TC is the cache element
+// type: T itself, or FP8 E4M3 (widened to T in registers).  For an FP8 cache a
+// 16-byte ldmatrix row holds 16 codes and each thread receives 4 consecutive ones,
+// which must become the (k, k+1) and (k+8, k+9) operand pairs: the dims of Q^T
+// are permuted to match within each 16-dim k-step, and the token rows of K are
+// loaded in the order perm(), so that S^T's rows line up with the permuted token
+// columns of V^T.
+template <typename T, typename TC, int D, int BS, int NH>
 struct MmaMath {
-  static constexpr int NT = BS / 8;   // token n-tiles of S
-  static constexpr int KS = D / 16;   // k-steps over head dims for S
-  static constexpr int DT = D / 8;    // head-dim n-tiles of O
-  static constexpr int KK = BS / 16;  // token k-steps for O
-  static constexpr int kElem = sizeof(TC);
+  static constexpr int MT = BS / 16;  // 16-token tiles of a block
+  static constexpr int KS = D / 16;   // 16-dim k-steps of S^T, and 16-dim row tiles of O^T
   static constexpr bool kFp8 = sizeof(TC) == 1;
 
-  // Token of column col (0..7) of S n-tile nt.
-  __device__ __forceinline__ static int token(int nt, int col) {
-    return kFp8 ? 16 * (nt >> 1) + 4 * (col >> 1) + (col & 1) + 2 * (nt & 1) : nt * 8 + col;
+  // Token (within a 16-token tile) of row r of S^T, which is also k-index r of P^T.
+  __device__ __forceinline__ static int perm(int r) {
+    return kFp8 ? 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3) : r;
   }
 
-  uint32_t qf[KS][4];
-  float acc[DT][4];
-  float m0, m1, l0, l1;
+  uint32_t qb[KS][NH][2];  // Q^T B fragments
+  float acc[KS][NH][4];    // O^T accumulators
+  float m_[NH][2], l_[NH][2];  // running max (log2 units) and lane-partial sum of heads 8n + 2t4 + {0, 1}
   uint32_t k_lane_off, v_lane_off;
-  int g, t4;
+  int g, t4, tok0, tok1;   // tok0 / tok1: tokens of this lane's S^T rows g and g + 8
 
   __device__ __forceinline__ void init(int lane, float*) {
     g = lane >> 2;
     t4 = lane & 3;
-    const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix mi, row mr
+    tok0 = perm(g);
+    tok1 = perm(g + 8);
+    const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: this lane addresses row mr of matrix mi
     if (kFp8) {
-      // K: matrix mi = (k-step mi & 1, n-tile mi >> 1), rows = that n-tile's tokens
-      k_lane_off = ((mi & 1) * BS + token(mi >> 1, mr)) * 16;
-      // V: matrix mi = head-dim n-tile mi, rows = 8 head dims of 16 tokens (16 bytes)
+      // K: matrix mi = (16-dim chunk mi >> 1, token rows 8 (mi & 1) ..); V: 8 dims of 16 tokens
+      k_lane_off = ((mi >> 1) * BS + perm((mi & 1) * 8 + mr)) * 16;
       v_lane_off = (mi * 8 + mr) * BS;
     } else {
-      k_lane_off = ((mi & 1) * BS + (mi >> 1) * 8 + mr) * 16;
-      v_lane_off = ((mi >> 1) * 8 + mr) * (BS * kElem) + (mi & 1) * 16;
+      // K: matrix mi = (8-dim chunk mi >> 1, tokens 8 (mi & 1) ..); V: dims 8 (mi & 1) .., tokens 8 (mi >> 1) ..
+      k_lane_off = ((mi >> 1) * BS + (mi & 1) * 8 + mr) * 16;
+      v_lane_off = ((mi & 1) * 8 + mr) * (BS * 2) + (mi >> 1) * 16;
     }
   }
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int i = 0; i < DT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.f;
-  }
-
-  // A-operand fragments of rows 0..nh-1 of q (row stride D), zero past nh.
-  __device__ __forceinline__ void load_q(const T* q, int nh) {
-    const T* q0 = q + g * D;
-    const T* q1 = q0 + 8 * D;
-    const bool v0 = g < nh, v1 = g + 8 < nh;
+    for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      // operand k = 2t4, 2t4+1 and 2t4+8, 2t4+9 read head dims d, d+1 and d2, d2+1
-      const int d = ks * 16 + (kFp8 ? 4 * t4 : 2 * t4);
-      const int d2 = kFp8 ? d + 2 : d + 8;
-      qf[ks][0] = v0 ? __ldg(reinterpret_cast<const unsigned int*>(q0 + d)) : 0u;
-      qf[ks][1] = v1 ? __ldg(reinterpret_cast<const unsigned int*>(q1 + d)) : 0u;
-      qf[ks][2] = v0 ? __ldg(reinterpret_cast<const unsigned int*>(q0 + d2)) : 0u;
-      qf[ks][3] = v1 ? __ldg(reinterpret_cast<const unsigned int*>(q1 + d2)) : 0u;
+      for (int n = 0; n < NH; ++n) acc[ks][n][0] = acc[ks][n][1] = acc[ks][n][2] = acc[ks][n][3] = 0.f;
+#pragma unroll
+    for (int n = 0; n < NH; ++n) {
+      m_[n][0] = m_[n][1] = -INFINITY;
+      l_[n][0] = l_[n][1] = 0.f;
     }
   }
+
+  // B fragments of heads 0..nh-1 of q (row stride D), zero past nh.
+  __device__ __forceinline__ void load_q(const T* q, int nh) {
+#pragma unroll
+    for (int n = 0; n < NH; ++n) {
+      const int h = 8 * n + g;
+      const T* qh = q + h * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        // operand k = 2t4, 2t4+1 and 2t4+8, 2t4+9 read dims d0, d0+1 and d1, d1+1
+        const int d0 = ks * 16 + (kFp8 ? 4 * t4 : 2 * t4);
+        const int d1 = kFp8 ? d0 + 2 : d0 + 8;
+        qb[ks][n][0] = h < nh ? __ldg(reinterpret_cast<const unsigned int*>(qh + d0)) : 0u;
+        qb[ks][n][1] = h < nh ? __ldg(reinterpret_cast<const unsigned int*>(qh + d1)) : 0u;
+      }
+    }
+  }
+
+  // Four E4M3 codes of an ldmatrix register as the low (codes 0, 1) and high pair.
+  __device__ __forceinline__ static uint32_t lo2(uint32_t r) { return e4m3x2_to<T>(r & 0xffffu); }
+  __device__ __forceinline__ static uint32_t hi2(uint32_t r) { return e4m3x2_to<T>(r >> 16); }
 
   __device__ __forceinline__ void block(unsigned char* stage, int tile_bytes, int rem, float scale_log2) {
     const uint32_t kb = smem_addr(stage), vb = kb + tile_bytes;
-    // S = Q K^T for the block's BS tokens.
-    float sc[NT][4];
+    // S^T = K Q^T for the block's BS tokens.
+    float sc[MT][NH][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-    if constexpr (kFp8) {
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int kp = 0; kp < KS / 2; ++kp) {
+      for (int n = 0; n < NH; ++n) sc[mt][n][0] = sc[mt][n][1] = sc[mt][n][2] = sc[mt][n][3] = 0.f;
 #pragma unroll
-        for (int np = 0; np < NT; np += 2) {
-          uint32_t r[4];  // (k-step 2kp, n-tile np), (2kp+1, np), (2kp, np+1), (2kp+1, np+1)
-          ldsm_x4(kb + k_lane_off + (2 * kp * BS + np * 8) * 16, r[0], r[1], r[2], r[3]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            mma_16816<T>(sc[np + (i >> 1)], qf[2 * kp + (i & 1)], e4m3x2_to<T>(r[i] & 0xffffu),
-                         e4m3x2_to<T>(r[i] >> 16));
-        }
-      }
-    } else {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-        for (int np = 0; np < NT; np += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + k_lane_off + (2 * ks * BS + np * 8) * 16, b0, b1, b2, b3);
-          mma_16816<T>(sc[np], qf[ks], b0, b1);
-          mma_16816<T>(sc[np + 1], qf[ks], b2, b3);
-        }
-      }
-    }
-    // Online softmax update (log2 domain); tokens past the sequence get -inf.
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int tok = token(nt, 2 * t4 + (c & 1));
-        const float v = sc[nt][c] * scale_log2;
-        sc[nt][c] = tok < rem ? v : -INFINITY;
-      }
-      mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      sc[nt][0] = exp2f(sc[nt][0] - mn0);
-      sc[nt][1] = exp2f(sc[nt][1] - mn0);
-      sc[nt][2] = exp2f(sc[nt][2] - mn1);
-      sc[nt][3] = exp2f(sc[nt][3] - mn1);
-      ps0 += sc[nt][0] + sc[nt][1];
-      ps1 += sc[nt][2] + sc[nt][3];
-    }
-    l0 = l0 * c0 + ps0;
-    l1 = l1 * c1 + ps1;
-#pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
-      acc[dt][0] *= c0;
-      acc[dt][1] *= c0;
-      acc[dt][2] *= c1;
-      acc[dt][3] *= c1;
-    }
-    // O += P V, with P = hi + lo in the cache's 16-bit type.
-#pragma unroll
-    for (int kk = 0; kk < KK; ++kk) {
-      uint32_t ahi[4], alo[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float* src = sc[2 * kk + (r >> 1)] + (r & 1) * 2;
-        ahi[r] = pack2<T>(src[0], src[1]);
-        const float2 back = unpack2<T>(ahi[r]);
-        alo[r] = pack2<T>(src[0] - back.x, src[1] - back.y);
-      }
+    for (int mt = 0; mt < MT; ++mt) {
       if constexpr (kFp8) {
 #pragma unroll
-        for (int dp = 0; dp < DT; dp += 4) {
-          uint32_t r[4];  // head-dim n-tiles dp .. dp+3, tokens 16kk .. 16kk+15
-          ldsm_x4(vb + v_lane_off + dp * 8 * BS + kk * 16, r[0], r[1], r[2], r[3]);
+        for (int kp = 0; kp < KS / 2; ++kp) {
+          uint32_t r[4];  // (chunk 2kp, rows 0-7), (2kp, rows 8-15), (2kp+1, rows 0-7), (2kp+1, rows 8-15)
+          ldsm_x4(kb + k_lane_off + (2 * kp * BS + 16 * mt) * 16, r[0], r[1], r[2], r[3]);
+          const uint32_t a0[4] = {lo2(r[0]), lo2(r[1]), hi2(r[0]), hi2(r[1])};
+          const uint32_t a1[4] = {lo2(r[2]), lo2(r[3]), hi2(r[2]), hi2(r[3])};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t b0 = e4m3x2_to<T>(r[i] & 0xffffu), b1 = e4m3x2_to<T>(r[i] >> 16);
-            mma_16816<T>(acc[dp + i], ahi, b0, b1);
-            mma_16816<T>(acc[dp + i], alo, b0, b1);
+          for (int n = 0; n < NH; ++n) {
+            mma_16816<T>(sc[mt][n], a0, qb[2 * kp][n][0], qb[2 * kp][n][1]);
+            mma_16816<T>(sc[mt][n], a1, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
           }
         }
       } else {
 #pragma unroll
-        for (int dp = 0; dp < DT; dp += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(vb + v_lane_off + dp * 8 * (BS * kElem) + kk * 32, b0, b1, b2, b3);
-          mma_16816<T>(acc[dp], ahi, b0, b1);
-          mma_16816<T>(acc[dp + 1], ahi, b2, b3);
-          mma_16816<T>(acc[dp], alo, b0, b1);
-          mma_16816<T>(acc[dp + 1], alo, b2, b3);
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(kb + k_lane_off + (2 * ks * BS + 16 * mt) * 16, a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int n = 0; n < NH; ++n) mma_16816<T>(sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
+        }
+      }
+    }
+    // Online softmax update per head (column), log2 domain; tokens past the sequence get -inf.
+    float mx[NH][2];
+#pragma unroll
+    for (int n = 0; n < NH; ++n) mx[n][0] = mx[n][1] = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < NH; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int tok = 16 * mt + ((c >> 1) ? tok1 : tok0);
+          const float v = sc[mt][n][c] * scale_log2;
+          sc[mt][n][c] = tok < rem ? v : -INFINITY;
+          mx[n][c & 1] = fmaxf(mx[n][c & 1], sc[mt][n][c]);
+        }
+    float corr[NH][2], ps[NH][2];
+#pragma unroll
+    for (int n = 0; n < NH; ++n)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v = mx[n][h];
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        const float mn = fmaxf(m_[n][h], v);
+        corr[n][h] = exp2f(m_[n][h] - mn);
+        m_[n][h] = mn;
+        ps[n][h] = 0.f;
+      }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < NH; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          sc[mt][n][c] = exp2f(sc[mt][n][c] - m_[n][c & 1]);
+          ps[n][c & 1] += sc[mt][n][c];
+        }
+#pragma unroll
+    for (int n = 0; n < NH; ++n) {
+      l_[n][0] = l_[n][0] * corr[n][0] + ps[n][0];
+      l_[n][1] = l_[n][1] * corr[n][1] + ps[n][1];
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int n = 0; n < NH; ++n) {
+        acc[ks][n][0] *= corr[n][0];
+        acc[ks][n][1] *= corr[n][1];
+        acc[ks][n][2] *= corr[n][0];
+        acc[ks][n][3] *= corr[n][1];
+      }
+    // O^T += V^T P^T, one 16-token k-step per 16-token tile of S^T.
+#pragma unroll
+    for (int kk = 0; kk < MT; ++kk) {
+      uint32_t bh[NH][2], bl[NH][2];
+#pragma unroll
+      for (int n = 0; n < NH; ++n)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {  // S^T rows 0-7, then rows 8-15
+          const float x = sc[kk][n][2 * r], y = sc[kk][n][2 * r + 1];
+          const uint32_t hi = pack2<T>(x, y);
+          const float2 back = unpack2<T>(hi);
+          bh[n][r] = movmatrix_trans(hi);
+          bl[n][r] = movmatrix_trans(pack2<T>(x - back.x, y - back.y));
+        }
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int dp = 0; dp < KS / 2; ++dp) {
+          uint32_t r[4];  // dims 32dp + 0-7, 8-15, 16-23, 24-31; tokens 16kk .. 16kk+15
+          ldsm_x4(vb + v_lane_off + 32 * dp * BS + 16 * kk, r[0], r[1], r[2], r[3]);
+          const uint32_t a0[4] = {lo2(r[0]), lo2(r[1]), hi2(r[0]), hi2(r[1])};
+          const uint32_t a1[4] = {lo2(r[2]), lo2(r[3]), hi2(r[2]), hi2(r[3])};
+#pragma unroll
+          for (int n = 0; n < NH; ++n) {
+            mma_16816<T>(acc[2 * dp][n], a0, bh[n][0], bh[n][1]);
+            mma_16816<T>(acc[2 * dp + 1][n], a1, bh[n][0], bh[n][1]);
+            mma_16816<T>(acc[2 * dp][n], a0, bl[n][0], bl[n][1]);
+            mma_16816<T>(acc[2 * dp + 1][n], a1, bl[n][0], bl[n][1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int dm = 0; dm < KS; ++dm) {
+          uint32_t a[4];
+          ldsm_x4(vb + v_lane_off + dm * 16 * (BS * 2) + kk * 32, a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int n = 0; n < NH; ++n) {
+            mma_16816<T>(acc[dm][n], a, bh[n][0], bh[n][1]);
+            mma_16816<T>(acc[dm][n], a, bl[n][0], bl[n][1]);
+          }
         }
       }
     }
   }
 
-  // Complete the row sums across the four lanes of a quad.
+  // Complete the sums over the eight lanes that share a head.
   __device__ __forceinline__ void finish() {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+    for (int n = 0; n < NH; ++n)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v = l_[n][h];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        l_[n][h] = v;
+      }
   }
 
-  // out rows 0..nh-1 (row stride D) = oscale * acc / l, rounded to T.
+  // out heads 0..nh-1 (row stride D) = oscale * acc / l, rounded to T; transposed
+  // back to head-major through movmatrix so each lane stores pairs of dims.
   __device__ __forceinline__ void store_out(T* out, int nh, float oscale) const {
-    const float i0 = oscale / l0, i1 = oscale / l1;
-    const bool v0 = g < nh, v1 = g + 8 < nh;
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
-      const int d = dt * 8 + 2 * t4;
-      if (v0) *reinterpret_cast<uint32_t*>(out + g * D + d) = pack2<T>(acc[dt][0] * i0, acc[dt][1] * i0);
-      if (v1) *reinterpret_cast<uint32_t*>(out + (g + 8) * D + d) = pack2<T>(acc[dt][2] * i1, acc[dt][3] * i1);
+    for (int n = 0; n < NH; ++n) {
+      const float i0 = oscale / l_[n][0], i1 = oscale / l_[n][1];
+      const int h = 8 * n + g;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t x0 = movmatrix_trans(pack2<T>(acc[ks][n][0] * i0, acc[ks][n][1] * i1));
+        const uint32_t x1 = movmatrix_trans(pack2<T>(acc[ks][n][2] * i0, acc[ks][n][3] * i1));
+        if (h < nh) {
+          *reinterpret_cast<uint32_t*>(out + h * D + ks * 16 + 2 * t4) = x0;
+          *reinterpret_cast<uint32_t*>(out + h * D + ks * 16 + 8 + 2 * t4) = x1;
+        }
+      }
     }
   }
 
-  // Partial result of rows 0..nh-1: o = oscale * acc / l (fp32, row stride D), (m, l).
+  // Partial result of heads 0..nh-1: o = oscale * acc / l (fp32, row stride D), (m, l).
   __device__ __forceinline__ void store_partial(float* po, float* pml, int nh, float oscale) const {
-    const float i0 = oscale / l0, i1 = oscale / l1;
-    const bool v0 = g < nh, v1 = g + 8 < nh;
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
-      const int d = dt * 8 + 2 * t4;
-      if (v0) *reinterpret_cast<float2*>(po + g * D + d) = make_float2(acc[dt][0] * i0, acc[dt][1] * i0);
-      if (v1) *reinterpret_cast<float2*>(po + (g + 8) * D + d) = make_float2(acc[dt][2] * i1, acc[dt][3] * i1);
-    }
-    if (t4 == 0) {
-      if (v0) *reinterpret_cast<float2*>(pml + 2 * g) = make_float2(m0, l0);
-      if (v1) *reinterpret_cast<float2*>(pml + 2 * (g + 8)) = make_float2(m1, l1);
-    }
+    for (int n = 0; n < NH; ++n)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 8 * n + 2 * t4 + hh;
+        if (h >= nh) continue;
+        const float inv = oscale / l_[n][hh];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          po[h * D + ks * 16 + g] = acc[ks][n][hh] * inv;
+          po[h * D + ks * 16 + 8 + g] = acc[ks][n][2 + hh] * inv;
+        }
+        if (g == 0) *reinterpret_cast<float2*>(pml + 2 * h) = make_float2(m_[n][hh], l_[n][hh]);
+      }
   }
 
   // Merge this partition's result (m, l, o = acc / l) into the warp's running
   // state (M, W, O) in shared memory: M' = max(M, m), O' = O 2^(M - M') + l 2^(m - M') o,
-  // W' = W 2^(M - M') + l 2^(m - M').  so: [16][D], sml: [16][2].
+  // W' = W 2^(M - M') + l 2^(m - M').  so: [8 NH][D], sml: [8 NH][2].
   __device__ __forceinline__ void fold(float* so, float* sml, bool first) const {
-    float M[2], Wt[2];
+    float M[NH][2], Wt[NH][2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      M[h] = first ? -INFINITY : sml[2 * (g + 8 * h)];
-      Wt[h] = first ? 0.f : sml[2 * (g + 8 * h) + 1];
-    }
-    __syncwarp();
-    const float mp[2] = {m0, m1}, lp[2] = {l0, l1};
-    float fo[2], fp[2];
+    for (int n = 0; n < NH; ++n)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float mn = fmaxf(M[h], mp[h]);
-      fo[h] = exp2f(M[h] - mn);
-      fp[h] = exp2f(mp[h] - mn);  // l 2^(m - M') times o = acc / l
-      if (t4 == 0) *reinterpret_cast<float2*>(sml + 2 * (g + 8 * h)) = make_float2(mn, Wt[h] * fo[h] + lp[h] * exp2f(mp[h] - mn));
-    }
-#pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
-      const int d = dt * 8 + 2 * t4;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float2* o = reinterpret_cast<float2*>(so + (g + 8 * h) * D + d);
-        const float2 old = first ? make_float2(0.f, 0.f) : *o;
-        *o = make_float2(old.x * fo[h] + fp[h] * acc[dt][2 * h], old.y * fo[h] + fp[h] * acc[dt][2 * h + 1]);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 8 * n + 2 * t4 + hh;
+        M[n][hh] = first ? -INFINITY : sml[2 * h];
+        Wt[n][hh] = first ? 0.f : sml[2 * h + 1];
       }
-    }
+    __syncwarp();
+#pragma unroll
+    for (int n = 0; n < NH; ++n)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 8 * n + 2 * t4 + hh;
+        const float mn = fmaxf(M[n][hh], m_[n][hh]);
+        const float fo = exp2f(M[n][hh] - mn), fp = exp2f(m_[n][hh] - mn);  // l 2^(m - M') times o = acc / l
+        if (g == 0) *reinterpret_cast<float2*>(sml + 2 * h) = make_float2(mn, Wt[n][hh] * fo + l_[n][hh] * fp);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            float* o = so + h * D + ks * 16 + 8 * r + g;
+            *o = (first ? 0.f : *o) * fo + fp * acc[ks][n][2 * r + hh];
+          }
+      }
     __syncwarp();
   }
 
   // Take the running state as this piece's (m, l, acc): acc = O, l = W.
   __device__ __forceinline__ void load_state(const float* so, const float* sml) {
-    m0 = sml[2 * g];
-    l0 = sml[2 * g + 1];
-    m1 = sml[2 * (g + 8)];
-    l1 = sml[2 * (g + 8) + 1];
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
-      const int d = dt * 8 + 2 * t4;
-      const float2 a = *reinterpret_cast<const float2*>(so + g * D + d);
-      const float2 b = *reinterpret_cast<const float2*>(so + (g + 8) * D + d);
-      acc[dt][0] = a.x;
-      acc[dt][1] = a.y;
-      acc[dt][2] = b.x;
-      acc[dt][3] = b.y;
-    }
+    for (int n = 0; n < NH; ++n)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 8 * n + 2 * t4 + hh;
+        m_[n][hh] = sml[2 * h];
+        l_[n][hh] = sml[2 * h + 1];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) acc[ks][n][2 * r + hh] = so[h * D + ks * 16 + 8 * r + g];
+      }
     __syncwarp();
   }
 };
@@ -535,12 +590,14 @@ __device__ __forceinline__ void locate(long long g, const int* pre, int S, int U
 }
 
 // grid = resident CTAs (persistent); kDecodeWarps independent warps per CTA.
-template <typename T, typename TC, int D, int BS, bool kMma>
-__global__ void __launch_bounds__(DecodeShape<TC, D, BS>::kWarps * 32)
+// kMode: 0 = CUDA-core math, 1 or 2 = tensor-core math over 8 or 16 query heads per unit.
+template <typename T, typename TC, int D, int BS, int kMode>
+__global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32)
     decode_kernel(const DecodeParams p) {
-  using Sh = DecodeShape<TC, D, BS>;
+  using Sh = DecodeShape<TC, D, BS, kMode>;
   constexpr int kDecodeWarps = Sh::kWarps;
-  using Math = std::conditional_t<kMma, MmaMath<T, TC, D, BS>, SimtMath<T, TC, D, BS>>;
+  constexpr bool kMma = kMode != 0;
+  using Math = std::conditional_t<kMma, MmaMath<T, TC, D, BS, (kMode > 0 ? kMode : 1)>, SimtMath<T, TC, D, BS>>;
   constexpr int TILE = Sh::kTile, STAGES = Sh::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -552,7 +609,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS>::kWarps * 32)
   int* s_wsum = s_pre + kMaxSeqsPerLaunch + 1;             // [warps]
   float* pw = reinterpret_cast<float*>(smem + Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes) + warp * BS;
   // running state of this warp's piece across caller partitions (see fold)
-  constexpr int kRows = kMma ? 16 : 1;
+  constexpr int kRows = kMma ? 8 * kMode : 1;
   float* st_o = reinterpret_cast<float*>(smem + Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes) +
                 kDecodeWarps * BS + warp * kRows * (D + 2);
   float* st_ml = st_o + kRows * D;
@@ -843,47 +900,47 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
 
 // --- host-side launch helpers (instantiated per dtype) ------------------------------------------
 
-template <typename TC, int D, int BS, bool kMma>
+template <typename TC, int D, int BS, int kMode>
 constexpr int decode_smem_bytes() {
-  using Sh = DecodeShape<TC, D, BS>;
+  using Sh = DecodeShape<TC, D, BS, kMode>;
   return Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes + Sh::kWarps * BS * 4 +
-         Sh::kWarps * (kMma ? 16 : 1) * (D + 2) * 4;
+         Sh::kWarps * (kMode ? 8 * kMode : 1) * (D + 2) * 4;
 }
 
-template <typename T, typename TC, int D, int BS, bool kMma>
+template <typename T, typename TC, int D, int BS, int kMode>
 cudaError_t ensure_smem_attr() {
   static unsigned done = 0;  // bit d: set on device d
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 32 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1u)) return cudaSuccess;
-  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&decode_kernel<T, TC, D, BS, kMma>),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<TC, D, BS, kMma>());
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&decode_kernel<T, TC, D, BS, kMode>),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<TC, D, BS, kMode>());
   if (e == cudaSuccess && dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
   return e;
 }
 
-template <typename T, typename TC, int D, int BS, bool kMma>
+template <typename T, typename TC, int D, int BS, int kMode>
 int decode_ctas_per_sm_t() {
-  if (ensure_smem_attr<T, TC, D, BS, kMma>() != cudaSuccess) return 0;
+  if (ensure_smem_attr<T, TC, D, BS, kMode>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<T, TC, D, BS, kMma>,
-                                                    DecodeShape<TC, D, BS>::kWarps * 32,
-                                                    decode_smem_bytes<TC, D, BS, kMma>()) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, &decode_kernel<T, TC, D, BS, kMode>,
+                                                    DecodeShape<TC, D, BS, kMode>::kWarps * 32,
+                                                    decode_smem_bytes<TC, D, BS, kMode>()) != cudaSuccess)
     return 0;
   return n;
 }
 
-template <typename T, typename TC, int D, int BS, bool kMma>
+template <typename T, typename TC, int D, int BS, int kMode>
 cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream, int* launches) {
   *launches = 0;
-  cudaError_t e = ensure_smem_attr<T, TC, D, BS, kMma>();
+  cudaError_t e = ensure_smem_attr<T, TC, D, BS, kMode>();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_kernel<T, TC, D, BS, kMma>, dim3(grid), dim3(DecodeShape<TC, D, BS>::kWarps * 32),
-                 decode_smem_bytes<TC, D, BS, kMma>(), stream, p);
+  e = launch_pdl(decode_kernel<T, TC, D, BS, kMode>, dim3(grid), dim3(DecodeShape<TC, D, BS, kMode>::kWarps * 32),
+                 decode_smem_bytes<TC, D, BS, kMode>(), stream, p);
   if (e != cudaSuccess) return e;
   *launches = 1;
-  e = launch_pdl(decode_merge_kernel<T, D, kMma>, dim3(p.num_seqs * p.units), dim3(kMergeWarps * 32), 0, stream, p);
+  e = launch_pdl(decode_merge_kernel<T, D, (kMode != 0)>, dim3(p.num_seqs * p.units), dim3(kMergeWarps * 32), 0, stream, p);
   if (e != cudaSuccess) return e;
   *launches = 2;
   return cudaSuccess;
@@ -893,20 +950,26 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream
 template <typename T, typename TC, int D, int BS>
 int ctas_for(DecodeKind kind) {
   if constexpr (sizeof(T) == 4) {
-    return decode_ctas_per_sm_t<T, TC, D, BS, false>();
+    return decode_ctas_per_sm_t<T, TC, D, BS, 0>();
   } else {
-    return kind == DecodeKind::kMma ? decode_ctas_per_sm_t<T, TC, D, BS, true>()
-                                    : decode_ctas_per_sm_t<T, TC, D, BS, false>();
+    switch (kind) {
+      case DecodeKind::kMma8: return decode_ctas_per_sm_t<T, TC, D, BS, 1>();
+      case DecodeKind::kMma16: return decode_ctas_per_sm_t<T, TC, D, BS, 2>();
+      default: return decode_ctas_per_sm_t<T, TC, D, BS, 0>();
+    }
   }
 }
 
 template <typename T, typename TC, int D, int BS>
 cudaError_t launch_for(const DecodeParams& p, DecodeKind kind, int grid, cudaStream_t s, int* n) {
   if constexpr (sizeof(T) == 4) {
-    return launch_decode_t<T, TC, D, BS, false>(p, grid, s, n);
+    return launch_decode_t<T, TC, D, BS, 0>(p, grid, s, n);
   } else {
-    return kind == DecodeKind::kMma ? launch_decode_t<T, TC, D, BS, true>(p, grid, s, n)
-                                    : launch_decode_t<T, TC, D, BS, false>(p, grid, s, n);
+    switch (kind) {
+      case DecodeKind::kMma8: return launch_decode_t<T, TC, D, BS, 1>(p, grid, s, n);
+      case DecodeKind::kMma16: return launch_decode_t<T, TC, D, BS, 2>(p, grid, s, n);
+      default: return launch_decode_t<T, TC, D, BS, 0>(p, grid, s, n);
+    }
   }
 }
 

@@ -14,18 +14,22 @@ constexpr int kMaxSeqsPerLaunch = 1024;
 // Shape of the decode CTA.  One CTA per SM; every warp is an independent worker
 // with a ring of stages, one stage = the K tile and the V tile of one block.
 // Measured on GB300: about 128 KiB of copies in flight per SM streams the pool
-// fastest (more in flight queues up in the memory system, less leaves it idle),
-// with 8 warps to hide the math.  The largest tiles (32 KiB stages) use 4 warps.
+// fastest (more in flight queues up in the memory system, less leaves it idle).
+// The math decides how many warps share those bytes.  The tensor-core kernel over
+// one 8-head tile (mode 1) with stages of at most 4 KiB (FP8 tiles, or head size
+// 64) runs 16 warps of two or more stages, four warps per scheduler to hide its
+// latencies (its widening of FP8 codes makes it ALU-bound otherwise); with larger
+// stages 16 warps would leave each warp a single stage, and 8 warps with two
+// stages each measured faster.  The other kernels run 8 warps (4 for 32 KiB
+// stages).
 constexpr int kInFlightBytes = 128 * 1024;
-__host__ __device__ constexpr int decode_warps(int stage_bytes) { return stage_bytes <= 16384 ? 8 : 4; }
-__host__ __device__ constexpr int decode_stages(int stage_bytes) {
-  return kInFlightBytes / (decode_warps(stage_bytes) * stage_bytes) > 1
-             ? kInFlightBytes / (decode_warps(stage_bytes) * stage_bytes)
-             : 1;
+__host__ __device__ constexpr int decode_warps(int stage_bytes, int mode) {
+  return (mode == 1 && stage_bytes <= 4096) ? 16 : (stage_bytes <= 16384 ? 8 : 4);
 }
-// Warps per decode CTA for a cache dtype size, head size and block size.
-inline int decode_warps_for(int elem_bytes, int head_size, int block_size) {
-  return decode_warps(2 * head_size * block_size * elem_bytes);
+__host__ __device__ constexpr int decode_stages(int stage_bytes, int mode) {
+  return kInFlightBytes / (decode_warps(stage_bytes, mode) * stage_bytes) > 1
+             ? kInFlightBytes / (decode_warps(stage_bytes, mode) * stage_bytes)
+             : 1;
 }
 
 // Everything a decode launch needs; passed to the kernels by value.
@@ -58,22 +62,31 @@ struct DecodeParams {
   float out_scale;              // v_scale: a quantised cache's V reads back as code * v_scale
 };
 
-enum class DecodeKind { kSimt = 0, kMma = 1 };
+// CUDA cores, or tensor cores with one (up to 8 query heads per kv head) or two
+// 8-head tiles per head unit.
+enum class DecodeKind { kSimt = 0, kMma8 = 1, kMma16 = 2 };
 
 // Kernel choice for a shape: tensor cores when a kv head serves >= 2 query
-// heads of a 16-bit cache, CUDA cores otherwise.
+// heads of a 16-bit or FP8 cache, CUDA cores otherwise.
 inline DecodeKind decode_kind(int dtype, int group) {
-  return (dtype != 0 && group >= 2) ? DecodeKind::kMma : DecodeKind::kSimt;
+  if (dtype == 0 || group < 2) return DecodeKind::kSimt;
+  return group <= 8 ? DecodeKind::kMma8 : DecodeKind::kMma16;
 }
 
-// Head units per sequence and query rows per unit for a kernel kind.
+// Head units per sequence and query rows per unit for a kernel kind: tensor-core
+// units are one kv head's query heads, 16 at a time.
 inline int decode_units(DecodeKind k, int num_heads, int num_kv_heads) {
   const int g = num_heads / num_kv_heads;
-  return k == DecodeKind::kMma ? num_kv_heads * ((g + 15) / 16) : num_heads;
+  return k != DecodeKind::kSimt ? num_kv_heads * ((g + 15) / 16) : num_heads;
 }
 inline int decode_rows(DecodeKind k, int num_heads, int num_kv_heads) {
   const int g = num_heads / num_kv_heads;
-  return k == DecodeKind::kMma ? (g < 16 ? g : 16) : 1;
+  return k != DecodeKind::kSimt ? (g < 16 ? g : 16) : 1;
+}
+
+// Warps per decode CTA for a cache dtype size, head size, block size and kind.
+inline int decode_warps_for(int elem_bytes, int head_size, int block_size, DecodeKind kind) {
+  return decode_warps(2 * head_size * block_size * elem_bytes, static_cast<int>(kind));
 }
 
 // Resident CTAs per SM of the main decode kernel for (dtype, D, BS, kind); 0 if unsupported.
