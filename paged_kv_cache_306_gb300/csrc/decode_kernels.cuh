@@ -791,19 +791,27 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32)
 
 // --- merge of pieces --------------------------------------------------------------------------------
 //
-// One CTA per segment (sequence, head unit).  Each query row of the segment gets
-// g = 8 / rows warps (at least one); the warps of a row split its pieces 32 at a
-// time: lanes take pieces for the maximum and the weights, then every lane owns
-// D/32 head dims and sums the weighted partial outputs, with the loads of
-// consecutive pieces in flight together.  The g warps of a row combine through
-// shared memory.
-constexpr int kMergeWarps = 8;
+// One CTA per segment (sequence, head unit).  The segment's pieces are cut into
+// items of (query row, chunk of kMergeChunk consecutive pieces); each warp takes
+// one item per round and issues every load of it at once (the pieces' tags,
+// (m, l) and partial outputs, each lane owning D/32 consecutive head dims), so a
+// round costs one trip to L2.  The item's pieces are combined in registers,
+//     m_c = max m_p,  l_c = sum l_p 2^(m_p - m_c),  o_c = sum l_p 2^(m_p - m_c) o_p,
+// and left in shared memory; then warp r folds the items of row r into its
+// running (M, L, O) with the same formula and finally writes O / L.  Slots whose
+// tag is not (segment, this launch's epoch) weigh nothing and are never read
+// into a sum: when the grid has more warps than blocks of work, a warp with an
+// empty range leaves its slot inside a segment's range unwritten.
+constexpr int kMergeWarps = 16;
+constexpr int kMergeChunk = 8;
 
 template <typename T, int D, bool kMma>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
   constexpr int CPL = D / 32;  // head dims per lane
+  using Vec = std::conditional_t<CPL == 4, float4, float2>;
+  __shared__ __align__(16) float s_o[kMergeWarps][D];
   __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
-  __shared__ float s_o[kMergeWarps][D];
+  __shared__ int s_row[kMergeWarps];
   griddep_wait();
   griddep_launch_dependents();
   const int seg = blockIdx.x;
@@ -814,87 +822,83 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   unit_heads<kMma>(p, u, kvh, h0, nh);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = last - first + 1, ep = static_cast<int>(p.epoch);
-  const int g = nh >= kMergeWarps ? 1 : kMergeWarps / nh;  // warps per row
-  const int per_round = kMergeWarps / g;                     // rows per round
-  const int j = warp % g, lead = warp - j;
+  const int chunks = (K + kMergeChunk - 1) / kMergeChunk;
+  const int items = nh * chunks;
 
-  for (int r0 = 0; r0 < nh; r0 += per_round) {
-    const int r = r0 + warp / g;
-    const bool active = warp < per_round * g && r < nh;
-    // the maximum over the row's valid pieces
-    float M = -INFINITY;
-    if (active) {
-      for (int i = j * 32 + lane; i < K; i += g * 32) {
-        const long long sl = first + i;
+  float RM = -INFINITY, RL = 0.f, RO[CPL];  // row `warp`'s running state (warps < nh)
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) RO[c] = 0.f;
+
+  for (int i0 = 0; i0 < items; i0 += kMergeWarps) {
+    const int it = i0 + warp;
+    if (it < items) {
+      const int r = it / chunks, p0 = (it - r * chunks) * kMergeChunk;
+      const int n = min(kMergeChunk, K - p0);
+      float m = -INFINITY, l = 0.f;
+      if (lane < n) {
+        const long long sl = first + p0 + lane;
         const int2 tag = p.part_tag[sl];
-        const float m = p.part_ml[(sl * p.rows + r) * 2];
-        if (tag.x == seg && tag.y == ep) M = fmaxf(M, m);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (g > 1) {
-      if (lane == 0) s_m[warp] = M;
-      __syncthreads();
-      for (int jj = 0; jj < g; ++jj) M = fmaxf(M, s_m[lead + jj]);
-    }
-    // weights (lane i holds piece c0 + i) and the weighted sum of the partial outputs
-    float lsum = 0.f, acc[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-    if (active) {
-      for (int c0 = j * 32; c0 < K; c0 += g * 32) {
-        float wgt = 0.f;
-        if (c0 + lane < K) {
-          const long long sl = first + c0 + lane;
-          const int2 tag = p.part_tag[sl];
-          const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (sl * p.rows + r) * 2);
-          if (tag.x == seg && tag.y == ep) wgt = ml.y * exp2f(ml.x - M);
-        }
-        lsum += wgt;
-        const int n = min(32, K - c0);
-#pragma unroll 8
-        for (int i = 0; i < n; ++i) {
-          const float wi = __shfl_sync(0xffffffffu, wgt, i);
-          if (wi != 0.f) {  // slots of other launches or segments have weight 0 and are never read
-            const float* po = p.part_o + ((long long)(first + c0 + i) * p.rows + r) * D + lane * CPL;
-            if constexpr (CPL == 4) {
-              const float4 v = *reinterpret_cast<const float4*>(po);
-              acc[0] = fmaf(wi, v.x, acc[0]);
-              acc[1] = fmaf(wi, v.y, acc[1]);
-              acc[2] = fmaf(wi, v.z, acc[2]);
-              acc[3] = fmaf(wi, v.w, acc[3]);
-            } else {
-              const float2 v = *reinterpret_cast<const float2*>(po);
-              acc[0] = fmaf(wi, v.x, acc[0]);
-              acc[1] = fmaf(wi, v.y, acc[1]);
-            }
-          }
+        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (sl * p.rows + r) * 2);
+        if (tag.x == seg && tag.y == ep) {
+          m = ml.x;
+          l = ml.y;
         }
       }
-    }
+      Vec ov[kMergeChunk];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    if (g > 1) {
-      if (lane == 0) s_l[warp] = lsum;
+      for (int i = 0; i < kMergeChunk; ++i)
+        if (i < n)
+          ov[i] = *reinterpret_cast<const Vec*>(p.part_o + ((long long)(first + p0 + i) * p.rows + r) * D + CPL * lane);
+      // chunk maximum and weights over lanes 0..n-1
+      float mc = m;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) s_o[warp][lane * CPL + c] = acc[c];
-      __syncthreads();
-      if (j == 0) {
-        for (int jj = 1; jj < g; ++jj) {
-          lsum += s_l[lead + jj];
+      for (int o = 1; o < kMergeChunk; o <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+      mc = __shfl_sync(0xffffffffu, mc, 0);
+      const float w = m == -INFINITY ? 0.f : l * exp2f(m - mc);
+      float lc = w;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) acc[c] += s_o[lead + jj][lane * CPL + c];
+      for (int o = 1; o < kMergeChunk; o <<= 1) lc += __shfl_xor_sync(0xffffffffu, lc, o);
+      lc = __shfl_sync(0xffffffffu, lc, 0);
+      float oc[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) oc[c] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMergeChunk; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, i);
+        if (i < n && wi > 0.f) {  // a slot no piece wrote in this launch holds anything (NaN too)
+          const float* v = reinterpret_cast<const float*>(&ov[i]);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) oc[c] = fmaf(wi, v[c], oc[c]);
         }
       }
+      *reinterpret_cast<Vec*>(&s_o[warp][CPL * lane]) = *reinterpret_cast<const Vec*>(oc);
+      if (lane == 0) {
+        s_m[warp] = mc;
+        s_l[warp] = lc;
+        s_row[warp] = r;
+      }
+    } else if (lane == 0) {
+      s_row[warp] = -1;
     }
-    if (active && j == 0) {
-      const float il = 1.f / lsum;
-      T* out = static_cast<T*>(p.out) + ((long long)s * p.num_heads + h0 + r) * D + lane * CPL;
+    __syncthreads();
+    if (warp < nh) {
+      for (int j = 0; j < kMergeWarps; ++j) {
+        if (s_row[j] != warp || !(s_l[j] > 0.f)) continue;
+        const float mn = fmaxf(RM, s_m[j]);
+        const float fa = exp2f(RM - mn), fb = exp2f(s_m[j] - mn);
+        RL = RL * fa + s_l[j] * fb;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) out[c] = DType<T>::from_f32(acc[c] * il);
+        for (int c = 0; c < CPL; ++c) RO[c] = RO[c] * fa + fb * s_o[j][CPL * lane + c];
+        RM = mn;
+      }
     }
     __syncthreads();  // the shared arrays are reused by the next round
+  }
+  if (warp < nh) {
+    const float il = 1.f / RL;
+    T* out = static_cast<T*>(p.out) + ((long long)s * p.num_heads + h0 + warp) * D + CPL * lane;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) out[c] = DType<T>::from_f32(RO[c] * il);
   }
 }
 

@@ -242,3 +242,25 @@ def test_launch_count_counts_kernels():
     n0 = pa.pa_launch_count()
     gpu_step(wl, t=t)
     assert pa.pa_launch_count() - n0 == 3        # write, decode, merge
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("G", [1, 4, 7])
+def test_workspace_full_of_nan_bytes_does_not_leak_into_outputs(dtype, G):
+    """A small batch leaves warps with no blocks, so some partial slots inside a
+    segment's range are never written; whatever they hold must weigh nothing."""
+    import paged_kv_cache_306_gb300 as pa
+    wl = W.make_private("nanws", dtype, [1, 15, 17, 53, 200, 333, 90], 2 * G, 2, 128, 16, seed=61,
+                        partition_size=32)
+    t = upload(wl)
+    code = pa.PA_F16 if dtype == "f16" else pa.PA_BF16
+    need = pa.pa_decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size, wl.max_seq_len,
+                                       wl.block_size, 32, code)
+    ws = torch.full((max(need, 16),), 0xFF, dtype=torch.uint8, device="cuda")   # NaN floats, tags -1
+    pa.pa_reshape_and_cache(t["key"], t["value"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+    out = torch.empty_like(t["q"])
+    pa.pa_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"], wl.scale,
+                 wl.max_seq_len, 32, ws)
+    assert pa.pa_get_device_error() == 0
+    k, v = oracle_pools(wl)
+    assert_close(as_f64(out), oracle_out(wl, k, v), dtype, with_rounding=True)
