@@ -114,11 +114,18 @@ __device__ __forceinline__ void zero_tail_v(unsigned char* vtile, int rem, int l
 // are permuted to match within each 16-dim k-step, and the token rows of K are
 // loaded in the order perm(), so that S^T's rows line up with the permuted token
 // columns of V^T.
-template <typename T, typename TC, int D, int BS, int NH>
+//
+// kEarly (16-bit caches): block() is preceded by fetch(), which reads every K and
+// V fragment of the block out of the stage into registers, so the kernel can
+// refill the stage before the math instead of after it.
+template <typename T, typename TC, int D, int BS, int NH, bool kEarly>
 struct MmaMath {
   static constexpr int MT = BS / 16;  // 16-token tiles of a block
   static constexpr int KS = D / 16;   // 16-dim k-steps of S^T, and 16-dim row tiles of O^T
   static constexpr bool kFp8 = sizeof(TC) == 1;
+  static_assert(!(kEarly && kFp8), "early release is for 16-bit caches");
+  static constexpr bool kFetch = kEarly;
+  static constexpr int FM = kEarly ? MT : 1, FK = kEarly ? KS : 1;
 
   // Token (within a 16-token tile) of row r of S^T, which is also k-index r of P^T.
   __device__ __forceinline__ static int perm(int r) {
@@ -127,6 +134,7 @@ struct MmaMath {
 
   uint32_t qb[KS][NH][2];  // Q^T B fragments
   float acc[KS][NH][4];    // O^T accumulators
+  uint32_t kf[FM][FK][4], vf[FM][FK][4];  // the block's K and V^T A fragments (kEarly)
   float m_[NH][2], l_[NH][2];  // running max (log2 units) and lane-partial sum of heads 8n + 2t4 + {0, 1}
   uint32_t k_lane_off, v_lane_off;
   int g, t4, tok0, tok1;   // tok0 / tok1: tokens of this lane's S^T rows g and g + 8
@@ -177,6 +185,25 @@ struct MmaMath {
     }
   }
 
+  // Read the block's K and V^T fragments out of the stage (kEarly only).
+  __device__ __forceinline__ void fetch(unsigned char* stage, int tile_bytes) {
+    if constexpr (kEarly) {
+      const uint32_t kb = smem_addr(stage), vb = kb + tile_bytes;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+          ldsm_x4(kb + k_lane_off + (2 * ks * BS + 16 * mt) * 16, kf[mt][ks][0], kf[mt][ks][1], kf[mt][ks][2],
+                  kf[mt][ks][3]);
+#pragma unroll
+      for (int kk = 0; kk < MT; ++kk)
+#pragma unroll
+        for (int dm = 0; dm < KS; ++dm)
+          ldsm_x4(vb + v_lane_off + dm * 16 * (BS * 2) + kk * 32, vf[kk][dm][0], vf[kk][dm][1], vf[kk][dm][2],
+                  vf[kk][dm][3]);
+    }
+  }
+
   // Four E4M3 codes of an ldmatrix register as the low (codes 0, 1) and high pair.
   __device__ __forceinline__ static uint32_t lo2(uint32_t r) { return e4m3x2_to<T>(r & 0xffffu); }
   __device__ __forceinline__ static uint32_t hi2(uint32_t r) { return e4m3x2_to<T>(r >> 16); }
@@ -208,7 +235,12 @@ struct MmaMath {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t a[4];
-          ldsm_x4(kb + k_lane_off + (2 * ks * BS + 16 * mt) * 16, a[0], a[1], a[2], a[3]);
+          if constexpr (kEarly) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = kf[kEarly ? mt : 0][kEarly ? ks : 0][i];
+          } else {
+            ldsm_x4(kb + k_lane_off + (2 * ks * BS + 16 * mt) * 16, a[0], a[1], a[2], a[3]);
+          }
 #pragma unroll
           for (int n = 0; n < NH; ++n) mma_16816<T>(sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
         }
@@ -299,7 +331,12 @@ struct MmaMath {
 #pragma unroll
         for (int dm = 0; dm < KS; ++dm) {
           uint32_t a[4];
-          ldsm_x4(vb + v_lane_off + dm * 16 * (BS * 2) + kk * 32, a[0], a[1], a[2], a[3]);
+          if constexpr (kEarly) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = vf[kEarly ? kk : 0][kEarly ? dm : 0][i];
+          } else {
+            ldsm_x4(vb + v_lane_off + dm * 16 * (BS * 2) + kk * 32, a[0], a[1], a[2], a[3]);
+          }
 #pragma unroll
           for (int n = 0; n < NH; ++n) {
             mma_16816<T>(acc[dm][n], a, bh[n][0], bh[n][1]);
@@ -424,6 +461,9 @@ struct SimtMath {
   static constexpr int CH = BS * kElem / 16;   // 16-byte chunks per V row
   static constexpr int RPW = 32 / CH;          // V rows per warp pass
   static constexpr int VP = D / RPW;           // V rows per lane
+
+  static constexpr bool kFetch = false;
+  __device__ __forceinline__ void fetch(unsigned char*, int) {}
 
   float qv[NGH * X];
   float acc[VP];
@@ -597,7 +637,10 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32)
   using Sh = DecodeShape<TC, D, BS, kMode>;
   constexpr int kDecodeWarps = Sh::kWarps;
   constexpr bool kMma = kMode != 0;
-  using Math = std::conditional_t<kMma, MmaMath<T, TC, D, BS, (kMode > 0 ? kMode : 1)>, SimtMath<T, TC, D, BS>>;
+  // Early stage release: 16-bit caches in 8-warp CTAs whose fragments of a block fit in 64 registers.
+  constexpr bool kEarly = kMma && sizeof(TC) == 2 && kDecodeWarps == 8 && D * BS <= 128 * 16;
+  using Math = std::conditional_t<kMma, MmaMath<T, TC, D, BS, (kMode > 0 ? kMode : 1), kEarly>,
+                                  SimtMath<T, TC, D, BS>>;
   constexpr int TILE = Sh::kTile, STAGES = Sh::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -741,6 +784,14 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32)
     unsigned char* stage = ring + (k % STAGES) * 2 * TILE;
     const int rem = L - cj * BS;  // valid tokens in this block (>= 1)
     if (rem < BS) zero_tail_v<TC, D, BS>(stage + TILE, rem, lane);
+    if constexpr (Math::kFetch) {  // the block's fragments are in registers: refill the stage now
+      math.fetch(stage, TILE);
+      __syncwarp();
+      if (k + STAGES < len) {
+        fence_proxy_async_smem();
+        issue(k + STAGES);
+      }
+    }
     math.block(stage, TILE, rem, p.scale_log2);
     ++cj;
     const bool seg_end = cj == nblk, last = k + 1 == len;
@@ -781,10 +832,12 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32)
       folded = true;
       math.reset();
     }
-    __syncwarp();
-    if (k + STAGES < len) {
-      fence_proxy_async_smem();
-      issue(k + STAGES);
+    if constexpr (!Math::kFetch) {
+      __syncwarp();
+      if (k + STAGES < len) {
+        fence_proxy_async_smem();
+        issue(k + STAGES);
+      }
     }
   }
 }
