@@ -2,6 +2,8 @@
 // partition planner and launch dispatch.  No call allocates device memory or
 // synchronizes, except pa_get_device_error.
 #include <atomic>
+#include <chrono>
+#include <random>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -146,10 +148,13 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   return PA_OK;
 }
 
-// A fresh tag for every launch, so a launch never mistakes an earlier launch's
-// partial slot for its own.  Zero is never used.
+// A fresh tag for every launch, so a launch never mistakes a partial slot left by
+// an earlier launch for its own.  The sequence starts at a random point, so tags
+// left in a reused buffer by another process are as unlikely to match.  Zero is
+// never used.
 unsigned next_epoch() {
-  static std::atomic<unsigned> epoch{0};
+  static std::atomic<unsigned> epoch{static_cast<unsigned>(std::random_device{}()) ^
+                                     static_cast<unsigned>(std::chrono::steady_clock::now().time_since_epoch().count())};
   unsigned e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
   if (e == 0) e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
   return e;

@@ -107,13 +107,17 @@ __device__ __forceinline__ void zero_tail_v(unsigned char* vtile, int rem, int l
 // into a rounded 16-bit high part and the rounded remainder, so that P V keeps
 // ~16 significant bits.
 //
-// T is the query / output type and the operand type; TC is the cache element
-// type: T itself, or FP8 E4M3 (widened to T in registers).  For an FP8 cache a
-// 16-byte ldmatrix row holds 16 codes and each thread receives 4 consecutive ones,
-// which must become the (k, k+1) and (k+8, k+9) operand pairs: the dims of Q^T
-// are permuted to match within each 16-dim k-step, and the token rows of K are
-// loaded in the order perm(), so that S^T's rows line up with the permuted token
-// columns of V^T.
+// T is the query / output type; TC is the cache element type: T itself (the
+// operands are then T), or FP8 E4M3.  An FP8 cache is widened in registers to
+// fp16 operands (every E4M3 value is an fp16 number; the hardware converts two
+// codes per instruction), whatever T is: bf16 queries are brought to fp16 with a
+// power-of-two scale per head, chosen from the head's largest |q| so that every
+// element keeps its 8 significant bits, and the scale is taken back out of that
+// head's scores.  A 16-byte ldmatrix row holds 16 codes and each thread receives
+// 4 consecutive ones, which must become the (k, k+1) and (k+8, k+9) operand
+// pairs: the dims of Q^T are permuted to match within each 16-dim k-step, and
+// the token rows of K are loaded in the order perm(), so that S^T's rows line up
+// with the permuted token columns of V^T.
 //
 // kEarly (16-bit caches): block() is preceded by fetch(), which reads every K and
 // V fragment of the block out of the stage into registers, so the kernel can
@@ -123,6 +127,8 @@ struct MmaMath {
   static constexpr int MT = BS / 16;  // 16-token tiles of a block
   static constexpr int KS = D / 16;   // 16-dim k-steps of S^T, and 16-dim row tiles of O^T
   static constexpr bool kFp8 = sizeof(TC) == 1;
+  using OT = std::conditional_t<kFp8, __half, T>;  // tensor-core operand type
+  static constexpr bool kRescaleQ = kFp8 && !std::is_same<T, __half>::value;
   static_assert(!(kEarly && kFp8), "early release is for 16-bit caches");
   static constexpr bool kFetch = kEarly;
   static constexpr int FM = kEarly ? MT : 1, FK = kEarly ? KS : 1;
@@ -136,6 +142,7 @@ struct MmaMath {
   float acc[KS][NH][4];    // O^T accumulators
   uint32_t kf[FM][FK][4], vf[FM][FK][4];  // the block's K and V^T A fragments (kEarly)
   float m_[NH][2], l_[NH][2];  // running max (log2 units) and lane-partial sum of heads 8n + 2t4 + {0, 1}
+  float hs_[NH][2];            // score factor (scale * log2 e, over the q scale) of heads 8n + 2t4 + {0, 1}
   uint32_t k_lane_off, v_lane_off;
   int g, t4, tok0, tok1;   // tok0 / tok1: tokens of this lane's S^T rows g and g + 8
 
@@ -168,8 +175,9 @@ struct MmaMath {
     }
   }
 
-  // B fragments of heads 0..nh-1 of q (row stride D), zero past nh.
-  __device__ __forceinline__ void load_q(const T* q, int nh) {
+  // B fragments of heads 0..nh-1 of q (row stride D), zero past nh, and the
+  // heads' score factors.
+  __device__ __forceinline__ void load_q(const T* q, int nh, float scale_log2) {
 #pragma unroll
     for (int n = 0; n < NH; ++n) {
       const int h = 8 * n + g;
@@ -181,6 +189,41 @@ struct MmaMath {
         const int d1 = kFp8 ? d0 + 2 : d0 + 8;
         qb[ks][n][0] = h < nh ? __ldg(reinterpret_cast<const unsigned int*>(qh + d0)) : 0u;
         qb[ks][n][1] = h < nh ? __ldg(reinterpret_cast<const unsigned int*>(qh + d1)) : 0u;
+      }
+      hs_[n][0] = hs_[n][1] = scale_log2;
+      if constexpr (kRescaleQ) {
+        // head g's largest |q| over the four lanes that hold its dims
+        float mx = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float2 v = unpack2<T>(qb[ks][n][i]);
+            mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // 2^e with mx * 2^e in [2^13, 2^14): far from fp16's overflow, and any
+        // element within 2^-27 of the largest stays a normal fp16 number
+        int e = 0;
+        if (mx > 0.f) {
+          int ex;
+          frexpf(mx, &ex);  // mx = f 2^ex, f in [0.5, 1)
+          e = 14 - ex;
+        }
+        e = e > 120 ? 120 : e < -120 ? -120 : e;
+        const float up = ldexpf(1.f, e);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float2 v = unpack2<T>(qb[ks][n][i]);
+            qb[ks][n][i] = pack2<__half>(v.x * up, v.y * up);
+          }
+        // the factors of heads 2t4 and 2t4 + 1 of this tile (held by lanes 8 t4 and 8 t4 + 4)
+        const float down = scale_log2 * ldexpf(1.f, -e);
+        hs_[n][0] = __shfl_sync(0xffffffffu, down, 8 * t4);
+        hs_[n][1] = __shfl_sync(0xffffffffu, down, 8 * t4 + 4);
       }
     }
   }
@@ -204,9 +247,14 @@ struct MmaMath {
     }
   }
 
-  // Four E4M3 codes of an ldmatrix register as the low (codes 0, 1) and high pair.
-  __device__ __forceinline__ static uint32_t lo2(uint32_t r) { return e4m3x2_to<T>(r & 0xffffu); }
-  __device__ __forceinline__ static uint32_t hi2(uint32_t r) { return e4m3x2_to<T>(r >> 16); }
+  // Operand fragments of two k-steps from four ldmatrix registers of E4M3 codes:
+  // registers 0, 1 (rows 0-7, 8-15 of the first k-step) and 2, 3 (the second).
+  __device__ __forceinline__ static void widen(const uint32_t (&r)[4], uint32_t (&a0)[4], uint32_t (&a1)[4]) {
+    e4m3x4_to_f16x2(r[0], a0[0], a0[2]);
+    e4m3x4_to_f16x2(r[1], a0[1], a0[3]);
+    e4m3x4_to_f16x2(r[2], a1[0], a1[2]);
+    e4m3x4_to_f16x2(r[3], a1[1], a1[3]);
+  }
 
   __device__ __forceinline__ void block(unsigned char* stage, int tile_bytes, int rem, float scale_log2) {
     const uint32_t kb = smem_addr(stage), vb = kb + tile_bytes;
@@ -223,12 +271,12 @@ struct MmaMath {
         for (int kp = 0; kp < KS / 2; ++kp) {
           uint32_t r[4];  // (chunk 2kp, rows 0-7), (2kp, rows 8-15), (2kp+1, rows 0-7), (2kp+1, rows 8-15)
           ldsm_x4(kb + k_lane_off + (2 * kp * BS + 16 * mt) * 16, r[0], r[1], r[2], r[3]);
-          const uint32_t a0[4] = {lo2(r[0]), lo2(r[1]), hi2(r[0]), hi2(r[1])};
-          const uint32_t a1[4] = {lo2(r[2]), lo2(r[3]), hi2(r[2]), hi2(r[3])};
+          uint32_t a0[4], a1[4];
+          widen(r, a0, a1);
 #pragma unroll
           for (int n = 0; n < NH; ++n) {
-            mma_16816<T>(sc[mt][n], a0, qb[2 * kp][n][0], qb[2 * kp][n][1]);
-            mma_16816<T>(sc[mt][n], a1, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
+            mma_16816<OT>(sc[mt][n], a0, qb[2 * kp][n][0], qb[2 * kp][n][1]);
+            mma_16816<OT>(sc[mt][n], a1, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
           }
         }
       } else {
@@ -242,7 +290,7 @@ struct MmaMath {
             ldsm_x4(kb + k_lane_off + (2 * ks * BS + 16 * mt) * 16, a[0], a[1], a[2], a[3]);
           }
 #pragma unroll
-          for (int n = 0; n < NH; ++n) mma_16816<T>(sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
+          for (int n = 0; n < NH; ++n) mma_16816<OT>(sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
         }
       }
     }
@@ -257,7 +305,7 @@ struct MmaMath {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int tok = 16 * mt + ((c >> 1) ? tok1 : tok0);
-          const float v = sc[mt][n][c] * scale_log2;
+          const float v = sc[mt][n][c] * hs_[n][c & 1];
           sc[mt][n][c] = tok < rem ? v : -INFINITY;
           mx[n][c & 1] = fmaxf(mx[n][c & 1], sc[mt][n][c]);
         }
@@ -307,24 +355,24 @@ struct MmaMath {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {  // S^T rows 0-7, then rows 8-15
           const float x = sc[kk][n][2 * r], y = sc[kk][n][2 * r + 1];
-          const uint32_t hi = pack2<T>(x, y);
-          const float2 back = unpack2<T>(hi);
+          const uint32_t hi = pack2<OT>(x, y);
+          const float2 back = unpack2<OT>(hi);
           bh[n][r] = movmatrix_trans(hi);
-          bl[n][r] = movmatrix_trans(pack2<T>(x - back.x, y - back.y));
+          bl[n][r] = movmatrix_trans(pack2<OT>(x - back.x, y - back.y));
         }
       if constexpr (kFp8) {
 #pragma unroll
         for (int dp = 0; dp < KS / 2; ++dp) {
           uint32_t r[4];  // dims 32dp + 0-7, 8-15, 16-23, 24-31; tokens 16kk .. 16kk+15
           ldsm_x4(vb + v_lane_off + 32 * dp * BS + 16 * kk, r[0], r[1], r[2], r[3]);
-          const uint32_t a0[4] = {lo2(r[0]), lo2(r[1]), hi2(r[0]), hi2(r[1])};
-          const uint32_t a1[4] = {lo2(r[2]), lo2(r[3]), hi2(r[2]), hi2(r[3])};
+          uint32_t a0[4], a1[4];
+          widen(r, a0, a1);
 #pragma unroll
           for (int n = 0; n < NH; ++n) {
-            mma_16816<T>(acc[2 * dp][n], a0, bh[n][0], bh[n][1]);
-            mma_16816<T>(acc[2 * dp + 1][n], a1, bh[n][0], bh[n][1]);
-            mma_16816<T>(acc[2 * dp][n], a0, bl[n][0], bl[n][1]);
-            mma_16816<T>(acc[2 * dp + 1][n], a1, bl[n][0], bl[n][1]);
+            mma_16816<OT>(acc[2 * dp][n], a0, bh[n][0], bh[n][1]);
+            mma_16816<OT>(acc[2 * dp + 1][n], a1, bh[n][0], bh[n][1]);
+            mma_16816<OT>(acc[2 * dp][n], a0, bl[n][0], bl[n][1]);
+            mma_16816<OT>(acc[2 * dp + 1][n], a1, bl[n][0], bl[n][1]);
           }
         }
       } else {
@@ -339,8 +387,8 @@ struct MmaMath {
           }
 #pragma unroll
           for (int n = 0; n < NH; ++n) {
-            mma_16816<T>(acc[dm][n], a, bh[n][0], bh[n][1]);
-            mma_16816<T>(acc[dm][n], a, bl[n][0], bl[n][1]);
+            mma_16816<OT>(acc[dm][n], a, bh[n][0], bh[n][1]);
+            mma_16816<OT>(acc[dm][n], a, bl[n][0], bl[n][1]);
           }
         }
       }
@@ -487,7 +535,7 @@ struct SimtMath {
     lpart = 0.f;
   }
 
-  __device__ __forceinline__ void load_q(const T* q, int) {
+  __device__ __forceinline__ void load_q(const T* q, int, float) {
     const T* qh = q + half * NGH * X;
 #pragma unroll
     for (int k = 0; k < NGH * X; ++k) qv[k] = DType<T>::to_f32(qh[k]);
@@ -632,7 +680,7 @@ __device__ __forceinline__ void locate(long long g, const int* pre, int S, int U
 // grid = resident CTAs (persistent); kDecodeWarps independent warps per CTA.
 // kMode: 0 = CUDA-core math, 1 or 2 = tensor-core math over 8 or 16 query heads per unit.
 template <typename T, typename TC, int D, int BS, int kMode>
-__global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32)
+__global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
     decode_kernel(const DecodeParams p) {
   using Sh = DecodeShape<TC, D, BS, kMode>;
   constexpr int kDecodeWarps = Sh::kWarps;
@@ -775,7 +823,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32)
     unit_heads<kMma>(p, cu, kvh, h0, nh);
     seg = cs * U + cu;
     math.reset();
-    math.load_q(static_cast<const T*>(p.q) + ((long long)cs * p.num_heads + h0) * D, nh);
+    math.load_q(static_cast<const T*>(p.q) + ((long long)cs * p.num_heads + h0) * D, nh, p.scale_log2);
   };
   enter();
 

@@ -78,19 +78,16 @@ template <> struct DType<__nv_fp8_e4m3> {
   __device__ __forceinline__ static __nv_fp8_e4m3 from_f32(float v) { return __nv_fp8_e4m3(v); }
 };
 
-// Two E4M3 codes (low byte = first element) as a packed pair of 16-bit floats of
-// type T; exact, since every E4M3 value is a normal fp16 and bf16 number.
-template <typename T> __device__ __forceinline__ uint32_t e4m3x2_to(uint32_t two_codes);
-template <> __device__ __forceinline__ uint32_t e4m3x2_to<__half>(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
-template <> __device__ __forceinline__ uint32_t e4m3x2_to<__nv_bfloat16>(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
-  __half2 hh;
-  *reinterpret_cast<__half2_raw*>(&hh) = h;
-  const __nv_bfloat162 b = __floats2bfloat162_rn(__low2float(hh), __high2float(hh));
-  return *reinterpret_cast<const uint32_t*>(&b);
+// Four E4M3 codes (byte i = element i) as two packed fp16 pairs: lo = elements
+// 0, 1 and hi = elements 2, 3; exact.  The register is split into its 16-bit
+// halves in PTX so that no shift or mask is needed before the conversions.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
 }
 
 // Two fp32 values rounded to a packed pair of 16-bit floats (low half = a).

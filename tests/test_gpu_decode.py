@@ -264,3 +264,30 @@ def test_workspace_full_of_nan_bytes_does_not_leak_into_outputs(dtype, G):
     assert pa.pa_get_device_error() == 0
     k, v = oracle_pools(wl)
     assert_close(as_f64(out), oracle_out(wl, k, v), dtype, with_rounding=True)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_repeated_calls_on_one_workspace_agree_bit_exactly(dtype):
+    """The per-segment counters and slot tags of one call must never be taken for
+    the next call's: the same workspace, reused, gives the same bits every time,
+    also when it starts out full of random bytes."""
+    import paged_kv_cache_306_gb300 as pa
+    rng = np.random.default_rng(62)
+    L = rng.integers(1, 6000, size=40)
+    wl = W.make_private("reuse", dtype, L, 28, 4, 128, 16, seed=63, partition_size=-1)
+    t = upload(wl)
+    code = pa.PA_F16 if dtype == "f16" else pa.PA_BF16
+    need = pa.pa_decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size, wl.max_seq_len,
+                                       wl.block_size, 0, code)
+    ws = torch.randint(0, 256, (max(need, 16),), dtype=torch.uint8, device="cuda")
+    pa.pa_reshape_and_cache(t["key"], t["value"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(t["q"])
+        pa.pa_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"], wl.scale,
+                     wl.max_seq_len, 0, ws)
+        outs.append(out)
+    assert pa.pa_get_device_error() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    k, v = oracle_pools(wl)
+    assert_close(as_f64(outs[0]), oracle_out(wl, k, v), dtype, with_rounding=True)

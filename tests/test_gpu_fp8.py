@@ -188,3 +188,20 @@ def test_fp8_layer_workload_step(cfg, seqs):
     ref = oracle_out(wl, k, v, idx)
     err, excess = max_violation(as_f64(out)[idx], ref, "fp8", with_rounding=False)
     assert excess <= 0.0, f"config {cfg} fp8: max abs err {err:.3e} > {TOL['fp8']}"
+
+
+@pytest.mark.parametrize("G", [1, 4, 16])
+def test_fp8_bf16_queries_far_from_unit_scale(G):
+    """bf16 queries whose heads span many orders of magnitude (the FP8 path widens
+    the cache to fp16 operands and rescales each query head by a power of two)."""
+    wl = W.make_private("bigq8", "fp8", [1, 40, 300, 1029], 2 * G, 2, 128, 16, seed=39, partition_size=-1,
+                        q_dtype="bf16")
+    rng = np.random.default_rng(40)
+    q = rng.standard_normal((wl.num_seqs, wl.num_heads, wl.head_size)).astype(np.float32)
+    factors = np.float32(2.0) ** rng.choice([-20, -5, 0, 6, 12, 30], size=(wl.num_seqs, wl.num_heads, 1))
+    q *= factors
+    q[0, 0, :] = 0.0                                  # an all-zero head: uniform attention
+    wl.q = W.cast(q, "bf16")
+    out, _ = gpu_step(wl)
+    k, v = oracle_pools(wl)
+    assert_close(as_f64(out), oracle_out(wl, k, v), "fp8", with_rounding=True, out_dtype="bf16")
