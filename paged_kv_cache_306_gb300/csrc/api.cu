@@ -220,6 +220,7 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   if (num_tokens < 0 || num_tokens > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_tokens %lld", (long long)num_tokens);
   if (num_kv_heads < 1 || head_size < 1 || block_size < 1 || num_blocks < 1)
     return fail(PA_ERR_INVALID_ARG, "num_kv_heads, head_size, block_size and num_blocks must be positive");
+  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads %d > 65535", num_kv_heads);
   if (head_size % (16 / e)) return fail(PA_ERR_INVALID_ARG, "head_size %d not a multiple of x = %d", head_size, 16 / e);
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "null pointer");
@@ -255,6 +256,7 @@ pa_status pa_reshape_and_cache_scaled(const void* key, const void* value, void* 
   if (num_tokens < 0 || num_tokens > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_tokens %lld", (long long)num_tokens);
   if (num_kv_heads < 1 || head_size < 1 || block_size < 1 || num_blocks < 1)
     return fail(PA_ERR_INVALID_ARG, "num_kv_heads, head_size, block_size and num_blocks must be positive");
+  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads %d > 65535", num_kv_heads);
   if (head_size % 16) return fail(PA_ERR_INVALID_ARG, "head_size %d not a multiple of 16", head_size);
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "null pointer");
@@ -280,6 +282,7 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, i
   if (num_pairs < 0 || num_pairs > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_pairs %lld", (long long)num_pairs);
   if (num_kv_heads < 1 || head_size < 1 || block_size < 1 || num_blocks < 1)
     return fail(PA_ERR_INVALID_ARG, "num_kv_heads, head_size, block_size and num_blocks must be positive");
+  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads %d > 65535", num_kv_heads);
   const long long block_bytes = (long long)num_kv_heads * head_size * block_size * e;
   if (block_bytes % 16) return fail(PA_ERR_INVALID_ARG, "a block of %lld bytes is not a multiple of 16", block_bytes);
   if (num_pairs == 0) return PA_OK;

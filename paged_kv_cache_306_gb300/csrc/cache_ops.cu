@@ -22,9 +22,13 @@ template <> struct Word<1> { using type = uint8_t; };
 template <> struct Word<2> { using type = uint16_t; };
 template <> struct Word<4> { using type = uint32_t; };
 
-// One CTA per token.
+// One warp per (token, kv head), kWriteWarps heads per CTA: grid = (tokens, head
+// groups).  Each lane issues all of its loads before its stores, so a head's row
+// costs one round trip to memory.
+constexpr int kWriteWarps = 4;
+
 template <int E>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kWriteWarps * 32)
     reshape_and_cache_kernel(const unsigned char* __restrict__ key, const unsigned char* __restrict__ value,
                              unsigned char* __restrict__ k_cache, unsigned char* __restrict__ v_cache,
                              const int64_t* __restrict__ slot_mapping, int num_kv_heads, int head_size,
@@ -34,29 +38,42 @@ __global__ void __launch_bounds__(128)
   griddep_wait();
   griddep_launch_dependents();
   const long long t = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kWriteWarps + (threadIdx.x >> 5);
+  if (h >= num_kv_heads) return;
   const long long slot = slot_mapping[t];
   if (slot < 0) return;  // padding token
   if (slot >= num_blocks * block_size) {
-    if (threadIdx.x == 0) set_error(err, kErrSlot);
+    if (h == 0 && lane == 0) set_error(err, kErrSlot);
     return;
   }
   const long long blk = slot / block_size;
   const int off = static_cast<int>(slot - blk * block_size);
-  const int groups_per_head = head_size / X;
-  const long long row = t * num_kv_heads * head_size;  // first element of token t's rows
+  const int groups = head_size / X;
+  const long long row = (t * num_kv_heads + h) * head_size;  // first element of the token's row for head h
 
-  // K: 16-byte group g of head h -> k_cache[blk, h, g, off, :]
-  for (int c = threadIdx.x; c < num_kv_heads * groups_per_head; c += blockDim.x) {
-    const int h = c / groups_per_head, g = c - h * groups_per_head;
-    const uint4 v = *reinterpret_cast<const uint4*>(key + (row + (long long)c * X) * E);
-    const long long dst = (((blk * num_kv_heads + h) * groups_per_head + g) * block_size + off) * X;
-    *reinterpret_cast<uint4*>(k_cache + dst * E) = v;
+  // K: 16-byte group g -> k_cache[blk, h, g, off, :]
+  const long long kbase = (blk * num_kv_heads + h) * groups * block_size + off;  // in 16-byte groups
+  for (int g0 = lane; g0 < groups; g0 += 64) {
+    uint4 v[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (g0 + 32 * j < groups) v[j] = *reinterpret_cast<const uint4*>(key + (row + (long long)(g0 + 32 * j) * X) * E);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (g0 + 32 * j < groups)
+        *reinterpret_cast<uint4*>(k_cache + (kbase + (long long)(g0 + 32 * j) * block_size) * 16) = v[j];
   }
-  // V: element (h, d) -> v_cache[blk, h, d, off]
-  for (int i = threadIdx.x; i < num_kv_heads * head_size; i += blockDim.x) {
-    const int h = i / head_size, d = i - h * head_size;
-    const W v = reinterpret_cast<const W*>(value)[row + i];
-    reinterpret_cast<W*>(v_cache)[((blk * num_kv_heads + h) * head_size + d) * block_size + off] = v;
+  // V: element d -> v_cache[blk, h, d, off]
+  const long long vbase = (blk * num_kv_heads + h) * head_size * block_size + off;
+  for (int d0 = lane; d0 < head_size; d0 += 128) {
+    W v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (d0 + 32 * j < head_size) v[j] = reinterpret_cast<const W*>(value)[row + d0 + 32 * j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (d0 + 32 * j < head_size) reinterpret_cast<W*>(v_cache)[vbase + (long long)(d0 + 32 * j) * block_size] = v[j];
   }
 }
 
@@ -64,30 +81,36 @@ __global__ void __launch_bounds__(128)
 // arguments of the write, "Reading vLLM's PagedAttention kernel" §3.2): element x
 // of the key (value) row is stored as the E4M3 code of x / k_scale (x / v_scale),
 // the division correctly rounded in fp32, the code rounded to nearest (ties to
-// even) and clamped to +-448.  One CTA per token; in the K pool a 16-element group
-// of a head is 16 contiguous codes, written with one 16-byte store.
+// even) and clamped to +-448.  One warp per (token, kv head) as above; in the K
+// pool a 16-element group of a head is 16 contiguous codes, one 16-byte store.
 template <typename TS>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kWriteWarps * 32)
     reshape_and_cache_e4m3_kernel(const TS* __restrict__ key, const TS* __restrict__ value,
                                   unsigned char* __restrict__ k_cache, unsigned char* __restrict__ v_cache,
                                   const int64_t* __restrict__ slot_mapping, int num_kv_heads, int head_size,
                                   int block_size, long long num_blocks, float k_scale, float v_scale, unsigned* err) {
+  constexpr int NV = sizeof(TS);  // 16-byte loads per 16-element group
   griddep_wait();
   griddep_launch_dependents();
   const long long t = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kWriteWarps + (threadIdx.x >> 5);
+  if (h >= num_kv_heads) return;
   const long long slot = slot_mapping[t];
   if (slot < 0) return;  // padding token
   if (slot >= num_blocks * block_size) {
-    if (threadIdx.x == 0) set_error(err, kErrSlot);
+    if (h == 0 && lane == 0) set_error(err, kErrSlot);
     return;
   }
   const long long blk = slot / block_size;
   const int off = static_cast<int>(slot - blk * block_size);
   const int groups = head_size / 16;
-  const long long row = t * num_kv_heads * head_size;
-  for (int c = threadIdx.x; c < num_kv_heads * groups; c += blockDim.x) {
-    const int h = c / groups, g = c - h * groups;
-    const TS* src = key + row + (long long)c * 16;
+  const long long row = (t * num_kv_heads + h) * head_size;
+  for (int g = lane; g < groups; g += 32) {
+    uint4 raw[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) raw[i] = reinterpret_cast<const uint4*>(key + row + (long long)g * 16)[i];
+    const TS* src = reinterpret_cast<const TS*>(raw);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -104,11 +127,19 @@ __global__ void __launch_bounds__(128)
     *reinterpret_cast<uint4*>(k_cache + (((blk * num_kv_heads + h) * groups + g) * block_size + off) * 16) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
-  for (int i = threadIdx.x; i < num_kv_heads * head_size; i += blockDim.x) {
-    const int h = i / head_size, d = i - h * head_size;
-    const float x = __fdiv_rn(DType<TS>::to_f32(value[row + i]), v_scale);
-    v_cache[((blk * num_kv_heads + h) * head_size + d) * block_size + off] =
-        static_cast<unsigned char>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+  const long long vbase = (blk * num_kv_heads + h) * head_size * block_size + off;
+  for (int d0 = lane; d0 < head_size; d0 += 128) {
+    TS v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (d0 + 32 * j < head_size) v[j] = value[row + d0 + 32 * j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (d0 + 32 * j < head_size) {
+        const float x = __fdiv_rn(DType<TS>::to_f32(v[j]), v_scale);
+        v_cache[vbase + (long long)(d0 + 32 * j) * block_size] =
+            static_cast<unsigned char>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+      }
   }
 }
 
@@ -142,13 +173,14 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
   const auto* vp = static_cast<const unsigned char*>(value);
   auto* kc = static_cast<unsigned char*>(k_cache);
   auto* vc = static_cast<unsigned char*>(v_cache);
-  const dim3 grid(static_cast<unsigned>(num_tokens));
+  const dim3 grid(static_cast<unsigned>(num_tokens), (num_kv_heads + kWriteWarps - 1) / kWriteWarps);
+  const dim3 block(kWriteWarps * 32);
   const cudaError_t e =
-      elem_bytes == 4   ? launch_pdl(reshape_and_cache_kernel<4>, grid, dim3(128), 0, stream, kp, vp, kc, vc,
+      elem_bytes == 4   ? launch_pdl(reshape_and_cache_kernel<4>, grid, block, 0, stream, kp, vp, kc, vc,
                                      slot_mapping, num_kv_heads, head_size, block_size, (long long)num_blocks, err)
-      : elem_bytes == 2 ? launch_pdl(reshape_and_cache_kernel<2>, grid, dim3(128), 0, stream, kp, vp, kc, vc,
+      : elem_bytes == 2 ? launch_pdl(reshape_and_cache_kernel<2>, grid, block, 0, stream, kp, vp, kc, vc,
                                      slot_mapping, num_kv_heads, head_size, block_size, (long long)num_blocks, err)
-                        : launch_pdl(reshape_and_cache_kernel<1>, grid, dim3(128), 0, stream, kp, vp, kc, vc,
+                        : launch_pdl(reshape_and_cache_kernel<1>, grid, block, 0, stream, kp, vp, kc, vc,
                                      slot_mapping, num_kv_heads, head_size, block_size, (long long)num_blocks, err);
   if (e == cudaSuccess) *launches = 1;
   return e;
@@ -163,19 +195,20 @@ cudaError_t launch_reshape_and_cache_e4m3(const void* key, const void* value, vo
   if (num_tokens == 0) return cudaSuccess;
   auto* kc = static_cast<unsigned char*>(k_cache);
   auto* vc = static_cast<unsigned char*>(v_cache);
-  const dim3 grid(static_cast<unsigned>(num_tokens));
+  const dim3 grid(static_cast<unsigned>(num_tokens), (num_kv_heads + kWriteWarps - 1) / kWriteWarps);
+  const dim3 block(kWriteWarps * 32);
   const long long nb = num_blocks;
   cudaError_t e;
   if (key_dtype == 0)
-    e = launch_pdl(reshape_and_cache_e4m3_kernel<float>, grid, dim3(128), 0, stream, static_cast<const float*>(key),
+    e = launch_pdl(reshape_and_cache_e4m3_kernel<float>, grid, block, 0, stream, static_cast<const float*>(key),
                    static_cast<const float*>(value), kc, vc, slot_mapping, num_kv_heads, head_size, block_size, nb,
                    k_scale, v_scale, err);
   else if (key_dtype == 1)
-    e = launch_pdl(reshape_and_cache_e4m3_kernel<__half>, grid, dim3(128), 0, stream,
+    e = launch_pdl(reshape_and_cache_e4m3_kernel<__half>, grid, block, 0, stream,
                    static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc, slot_mapping,
                    num_kv_heads, head_size, block_size, nb, k_scale, v_scale, err);
   else
-    e = launch_pdl(reshape_and_cache_e4m3_kernel<__nv_bfloat16>, grid, dim3(128), 0, stream,
+    e = launch_pdl(reshape_and_cache_e4m3_kernel<__nv_bfloat16>, grid, block, 0, stream,
                    static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc, vc,
                    slot_mapping, num_kv_heads, head_size, block_size, nb, k_scale, v_scale, err);
   if (e == cudaSuccess) *launches = 1;
