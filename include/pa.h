@@ -69,7 +69,8 @@ typedef enum {
   PA_ERR_UNSUPPORTED = 2,  /* valid, but outside what the kernels are built for */
   PA_ERR_ALIGNMENT = 3,    /* a pointer breaks the alignment rule above */
   PA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
-  PA_ERR_CUDA = 5          /* a CUDA runtime call failed (see pa_last_error_message) */
+  PA_ERR_CUDA = 5,         /* a CUDA runtime call failed (see pa_last_error_message) */
+  PA_ERR_OUT_OF_BLOCKS = 6 /* the block manager's pool cannot serve the request (pa_block_manager.h) */
 } pa_status;
 
 typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;

@@ -12,7 +12,8 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libpa.so")
 
-PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_ALIGNMENT, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(6)
+(PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_ALIGNMENT, PA_ERR_WORKSPACE, PA_ERR_CUDA,
+ PA_ERR_OUT_OF_BLOCKS) = range(7)
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PARTITION_NONE = 0
 PARTITION_AUTO = -1
@@ -59,6 +60,22 @@ def load():
     lib.pa_launch_count.argtypes = []
     lib.pa_launch_count.restype = ctypes.c_uint64
     for f in (lib.pa_reshape_and_cache, lib.pa_copy_blocks, lib.pa_decode, lib.pa_get_device_error):
+        f.restype = i32
+    # host-side block manager (include/pa_block_manager.h)
+    lib.pa_bm_create.argtypes = [i64, i32, ctypes.POINTER(P)]
+    lib.pa_bm_destroy.argtypes = [P]
+    lib.pa_bm_destroy.restype = None
+    lib.pa_bm_num_free_blocks.argtypes = [P]
+    lib.pa_bm_num_free_blocks.restype = i64
+    lib.pa_bm_add_sequence.argtypes = [P, i64, i64, P]
+    lib.pa_bm_fork.argtypes = [P, i64, i64]
+    lib.pa_bm_free_sequence.argtypes = [P, i64]
+    lib.pa_bm_append_tokens.argtypes = [P, P, i32, P, P, i64, ctypes.POINTER(i64)]
+    lib.pa_bm_seq_len.argtypes = [P, i64, ctypes.POINTER(i64)]
+    lib.pa_bm_block_tables.argtypes = [P, P, i32, P, i32, P]
+    lib.pa_bm_refcount.argtypes = [P, i64, ctypes.POINTER(i32)]
+    for f in (lib.pa_bm_create, lib.pa_bm_add_sequence, lib.pa_bm_fork, lib.pa_bm_free_sequence,
+              lib.pa_bm_append_tokens, lib.pa_bm_seq_len, lib.pa_bm_block_tables, lib.pa_bm_refcount):
         f.restype = i32
     _lib = lib
     return lib
@@ -219,3 +236,80 @@ def pa_get_device_error(stream=None):
 
 def pa_launch_count():
     return load().pa_launch_count()
+
+
+class BlockManager:
+    """The library's host-side block manager (include/pa_block_manager.h): free list,
+    reference counts, per-sequence block lists, fork and copy-on-write.  Arrays in
+    and out are numpy (host memory); nothing here touches the GPU."""
+
+    def __init__(self, num_blocks, block_size):
+        import numpy  # noqa: F401  (arrays below)
+        self._lib = load()
+        h = ctypes.c_void_p()
+        check(self._lib.pa_bm_create(int(num_blocks), int(block_size), ctypes.byref(h)))
+        self._h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free_blocks(self):
+        return self._lib.pa_bm_num_free_blocks(self._h)
+
+    def add_sequence(self, seq_id, num_tokens):
+        """A new sequence of num_tokens tokens; returns their slots (int64)."""
+        import numpy as np
+        slots = np.empty(int(num_tokens), np.int64)
+        check(self._lib.pa_bm_add_sequence(self._h, int(seq_id), int(num_tokens),
+                                           slots.ctypes.data if num_tokens else None))
+        return slots
+
+    def fork(self, parent_id, child_id):
+        check(self._lib.pa_bm_fork(self._h, int(parent_id), int(child_id)))
+
+    def free_sequence(self, seq_id):
+        check(self._lib.pa_bm_free_sequence(self._h, int(seq_id)))
+
+    def append_tokens(self, seq_ids):
+        """One new token per listed sequence: returns (slot_mapping int64 [n], copies int64 [k, 2])."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, np.int64)
+        n = len(ids)
+        slots = np.empty(n, np.int64)
+        copies = np.empty((max(n, 1), 2), np.int64)
+        nc = ctypes.c_int64(0)
+        check(self._lib.pa_bm_append_tokens(self._h, ids.ctypes.data if n else None, n,
+                                            slots.ctypes.data if n else None, copies.ctypes.data, max(n, 1),
+                                            ctypes.byref(nc)))
+        return slots, copies[:nc.value].copy()
+
+    def seq_len(self, seq_id):
+        n = ctypes.c_int64(0)
+        check(self._lib.pa_bm_seq_len(self._h, int(seq_id), ctypes.byref(n)))
+        return n.value
+
+    def block_tables(self, seq_ids, max_blocks_per_seq):
+        """(block_tables int32 [n, max_blocks_per_seq] with -1 past the end, seq_lens int32 [n])."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, np.int64)
+        n = len(ids)
+        bt = np.empty((max(n, 1), int(max_blocks_per_seq)), np.int32)
+        sl = np.empty(max(n, 1), np.int32)
+        check(self._lib.pa_bm_block_tables(self._h, ids.ctypes.data if n else None, n, bt.ctypes.data,
+                                           int(max_blocks_per_seq), sl.ctypes.data))
+        return bt[:n].copy(), sl[:n].copy()
+
+    def refcount(self, block):
+        r = ctypes.c_int(0)
+        check(self._lib.pa_bm_refcount(self._h, int(block), ctypes.byref(r)))
+        return r.value

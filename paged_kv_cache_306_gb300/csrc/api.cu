@@ -204,6 +204,7 @@ const char* pa_status_string(pa_status s) {
     case PA_ERR_ALIGNMENT: return "PA_ERR_ALIGNMENT";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_OUT_OF_BLOCKS: return "PA_ERR_OUT_OF_BLOCKS";
     default: return "PA_ERR_UNKNOWN";
   }
 }
