@@ -51,9 +51,11 @@ def _load():
         lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i64, i32]
         lib.oracle_copy_blocks.argtypes = [P, P, P, i64, i32, i32, i32, i64, i32]
         lib.oracle_widen.argtypes = [P, P, i64, i32]
+        lib.oracle_prefill.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i64, f64, i32]
         for f in (lib.oracle_decode, lib.oracle_reshape_and_cache, lib.oracle_copy_blocks,
                   lib.oracle_widen, lib.oracle_num_threads, lib.oracle_elem_bytes, lib.oracle_pack_x,
-                  lib.oracle_decode_scaled, lib.oracle_reshape_and_cache_scaled, lib.oracle_encode_e4m3):
+                  lib.oracle_decode_scaled, lib.oracle_reshape_and_cache_scaled, lib.oracle_encode_e4m3,
+                  lib.oracle_prefill):
             f.restype = ctypes.c_int
         lib.oracle_elem_bytes.argtypes = [i32]
         lib.oracle_pack_x.argtypes = [i32]
@@ -123,6 +125,24 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, dtype, num_kv_hea
                                       code, float(k_scale), float(v_scale))
     _check(st)
     return (out, w) if return_weights else out
+
+
+def prefill(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, dtype):
+    """Chunked prefill (see pa_oracle.c): query token i of sequence s, at position
+    seq_lens[s] - n_s + i, attends causally to positions 0..itself; fp64 out [T_q, H, D]."""
+    code = _code(dtype)
+    T, H, D = q.shape
+    NB, Hkv = k_cache.shape[0], k_cache.shape[1]
+    bs = v_cache.shape[3]
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    if qsl[-1] != T:
+        raise ValueError("query_start_loc does not end at the number of query tokens")
+    out = np.zeros((T, H, D), dtype=np.float64)
+    _check(_load().oracle_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), bt.shape[1], _ptr(sl),
+                                  _ptr(qsl), len(sl), H, Hkv, D, bs, NB, float(scale), code))
+    return out
 
 
 def encode_e4m3(x):

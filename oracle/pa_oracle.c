@@ -380,6 +380,82 @@ int oracle_decode_scaled(double* out, double* weights, int64_t w_stride, const v
 }
 
 /*
+ * Chunked prefill over the paged pool: the step before decode ([BHHXX] §2.3: a
+ * prompt is processed, its K/V enter the cache, then tokens are generated one
+ * at a time), read as causal attention of a chunk of new query tokens over the
+ * sequence's cached history and the chunk itself.  For sequence s the cache
+ * holds L = seq_lens[s] tokens after the chunk's write, the chunk is the
+ * n = query_start_loc[s+1] - query_start_loc[s] tokens at positions L-n .. L-1,
+ * and query token i (row query_start_loc[s] + i) at position p = L - n + i
+ * attends to positions 0..p:
+ *     z_t = scale * <q[row,h,:], K_s[t,:]>      t <= p
+ *     out[row,h,:] = sum_t softmax(z)_t V_s[t,:]
+ * q and out are [num_query_tokens, num_heads, head_size]; K_s, V_s as in decode.
+ */
+int oracle_prefill(double* out, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                   const int32_t* query_start_loc, int num_seqs, int num_heads, int num_kv_heads,
+                   int head_size, int block_size, int64_t num_blocks, double scale, int dtype) {
+  if (!elem_bytes(dtype) || num_seqs < 0 || num_kv_heads < 1 || num_heads % num_kv_heads || block_size < 1 ||
+      head_size % pack_x(dtype) || query_start_loc[0] != 0)
+    return OR_ERR_ARG;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int n = query_start_loc[s + 1] - query_start_loc[s];
+    if (n < 0 || n > seq_lens[s] || seq_lens[s] < 1 ||
+        (int64_t)seq_lens[s] > (int64_t)max_blocks_per_seq * block_size)
+      return OR_ERR_SEQ_LEN;
+  }
+  const int G = num_heads / num_kv_heads;
+  const int D = head_size;
+  int status = OR_OK;
+  const int64_t n_pairs = (int64_t)num_seqs * num_heads;
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t sh = 0; sh < n_pairs; ++sh) {
+    const int s = (int)(sh / num_heads), h = (int)(sh % num_heads);
+    const int L = seq_lens[s], n = query_start_loc[s + 1] - query_start_loc[s];
+    if (n == 0) continue;
+    double* K = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* V = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* z = (double*)malloc(sizeof(double) * (size_t)L);
+    if (!K || !V || !z) {
+#pragma omp critical
+      status = OR_ERR_NOMEM;
+      free(K); free(V); free(z);
+      continue;
+    }
+    int st = gather_seq(K, V, k_cache, v_cache, block_tables + (int64_t)s * max_blocks_per_seq, L, h / G,
+                        num_kv_heads, D, block_size, num_blocks, dtype, 1.0, 1.0);
+    if (st != OR_OK) {
+#pragma omp critical
+      status = st;
+      free(K); free(V); free(z);
+      continue;
+    }
+    for (int i = 0; i < n; ++i) {
+      const int p = L - n + i;  /* position of query token i */
+      const int64_t qo = ((int64_t)(query_start_loc[s] + i) * num_heads + h) * D;
+      for (int t = 0; t <= p; ++t) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += load(q, qo + d, dtype) * K[(int64_t)t * D + d];
+        z[t] = scale * acc;
+      }
+      double m = z[0];
+      for (int t = 1; t <= p; ++t) if (z[t] > m) m = z[t];
+      double Z = 0.0;
+      for (int t = 0; t <= p; ++t) { z[t] = exp(z[t] - m); Z += z[t]; }
+      for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int t = 0; t <= p; ++t) acc += z[t] * V[(int64_t)t * D + d];
+        out[qo + d] = acc / Z;
+      }
+    }
+    free(K); free(V); free(z);
+  }
+  return status;
+}
+
+/*
  * The decode definition above for a cache in the query's own dtype (no scales).
  */
 int oracle_decode(double* out, double* weights, int64_t w_stride, const void* q,

@@ -44,6 +44,10 @@ MUTANTS = {
     "k-scale-dropped": ("k_scale * load(k_cache", "load(k_cache"),
     "v-scale-dropped": ("v_scale * load(v_cache", "load(v_cache"),
     "quantise-multiplies": ("(float)load(value, src, key_dtype) / vs", "(float)load(value, src, key_dtype) * vs"),
+    "prefill-position-off-by-one": ("const int p = L - n + i;", "const int p = L - n + i - 1 + (i == 0);"),
+    "prefill-ignores-history": ("const int p = L - n + i;", "const int p = i;"),
+    "prefill-wrong-query-row": ("(int64_t)(query_start_loc[s] + i) * num_heads", "(int64_t)(s + i) * num_heads"),
+    "prefill-not-normalised": ("out[qo + d] = acc / Z;", "out[qo + d] = acc;"),
 }
 
 
@@ -62,4 +66,5 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
-    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+    # exit code 1: a pin failed (2 would be a collection error, which catches nothing)
+    assert r.returncode == 1, f"mutant {name} survived the pins (exit {r.returncode}):\n{r.stdout[-2000:]}"

@@ -458,3 +458,70 @@ def test_value_scale_scales_the_output_and_key_scale_acts_like_query_scale():
     c = oracle.decode(q, k8, v8, bt, L, 0.025, "fp8", q_dtype="f32", k_scale=1.0, v_scale=0.5)
     assert np.max(np.abs(a - 0.5 * b)) < 1e-14
     assert np.max(np.abs(a - c)) < 1e-12
+
+
+# --- chunked prefill (the step before decode) ---------------------------------------------------
+
+def prefill_case(rng, S, H, Hkv, D, bs, NB, max_len):
+    """A tiny paged pool and, per sequence, a chunk of n_s <= L_s new query tokens."""
+    q1, Kl, Vl, bt, L = tiny_case(rng, S, H, Hkv, D, bs, NB, max_len)
+    n = np.array([rng.integers(0, l + 1) for l in L], np.int32)
+    n[0] = L[0]                                     # one pure prefill (no cached history)
+    qsl = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = rng.standard_normal((int(qsl[-1]), H, D))
+    return q, Kl, Vl, bt, L, qsl
+
+
+@pytest.mark.parametrize("D,bs,G", [(4, 1, 1), (8, 4, 2), (4, 16, 3), (16, 2, 1)])
+def test_prefill_matches_brute_force_walk_up_to_each_position(D, bs, G):
+    """Row i of sequence s equals the pages' per-token walk over the first p + 1
+    tokens, p = L_s - n_s + i (the causal reading of a chunk after its history)."""
+    rng = np.random.default_rng(70 + D + bs + G)
+    Hkv = 2
+    q, Kl, Vl, bt, L, qsl = prefill_case(rng, 4, Hkv * G, Hkv, D, bs, 64, 24)
+    k, v = pools_from_logical(Kl, Vl, 2)
+    got = oracle.prefill(q, k, v, bt, L, qsl, 0.37, "f64")
+    for s in range(len(L)):
+        n = qsl[s + 1] - qsl[s]
+        for i in range(n):
+            p = L[s] - n + i
+            for h in range(Hkv * G):
+                kvh = h // G
+                kb = {int(b): Kl[b, kvh].tolist() for b in bt[s] if b >= 0}
+                vb = {int(b): Vl[b, kvh].tolist() for b in bt[s] if b >= 0}
+                ref = brute.paged_decode_one(q[qsl[s] + i, h].tolist(), [int(b) for b in bt[s] if b >= 0], kb, vb,
+                                             int(p + 1), bs, 0.37)
+                assert np.max(np.abs(got[qsl[s] + i, h] - ref)) < 1e-12
+
+
+def test_prefill_of_one_token_per_sequence_is_decode():
+    rng = np.random.default_rng(74)
+    q, Kl, Vl, bt, L = tiny_case(rng, 5, 6, 3, 8, 4, 64, 30)
+    k, v = pools_from_logical(Kl, Vl, 2)
+    qsl = np.arange(6, dtype=np.int32)
+    got = oracle.prefill(q, k, v, bt, L, qsl, 0.3, "f64")
+    assert np.max(np.abs(got - oracle.decode(q, k, v, bt, L, 0.3, "f64"))) < 1e-13
+
+
+def test_a_chunk_gives_the_rows_of_the_whole_prompt():
+    """Prefill of tokens a..L-1 after a cached history of a tokens gives exactly the
+    rows a..L-1 of the prefill of the whole prompt."""
+    rng = np.random.default_rng(75)
+    q, Kl, Vl, bt, L = tiny_case(rng, 1, 4, 2, 8, 4, 32, 30)
+    L = np.array([29], np.int32)
+    bt = rng.permutation(32)[:8].reshape(1, 8).astype(np.int32)
+    k, v = pools_from_logical(Kl, Vl, 2)
+    qa = rng.standard_normal((29, 4, 8))
+    full = oracle.prefill(qa, k, v, bt, L, np.array([0, 29], np.int32), 0.5, "f64")
+    for a in (0, 1, 7, 16, 28):
+        part = oracle.prefill(qa[a:], k, v, bt, L, np.array([0, 29 - a], np.int32), 0.5, "f64")
+        assert np.array_equal(part, full[a:])
+
+
+def test_prefill_rejects_a_chunk_longer_than_its_sequence():
+    rng = np.random.default_rng(76)
+    q, Kl, Vl, bt, L = tiny_case(rng, 2, 2, 2, 8, 4, 32, 10)
+    k, v = pools_from_logical(Kl, Vl, 2)
+    qsl = np.array([0, int(L[0]) + 1, int(L[0]) + 2], np.int32)
+    with pytest.raises(Exception):
+        oracle.prefill(np.zeros((int(qsl[-1]), 2, 8)), k, v, bt, L, qsl, 0.5, "f64")
