@@ -213,6 +213,34 @@ PA_API pa_status pa_get_device_error(int* code, void* stream);
 PA_API uint64_t pa_launch_count(void);
 
 /*
+ * Chunked prefill: causal attention of a chunk of new query tokens per sequence
+ * over the paged pool -- the step before decode ("vLLM's PagedAttention: why the
+ * KV cache is paged", §2.3: a prompt is processed and its K/V enter the cache,
+ * then tokens are generated one at a time).  The chunk's own K/V must already be
+ * in the cache (pa_reshape_and_cache with the chunk's slots).  For sequence s,
+ * seq_lens[s] = L counts every cached token, the chunk included; the chunk is
+ * the n = query_start_loc[s+1] - query_start_loc[s] tokens at positions
+ * L - n .. L - 1, its queries are rows query_start_loc[s] .. of q, and query
+ * token i (position p = L - n + i) attends to positions 0..p:
+ *     out[row, h, :] = softmax(scale * q[row, h, :] . K_s[0..p]^T) V_s[0..p]
+ * query head h reading kv head h / (num_heads / num_kv_heads).
+ *
+ * q, out          [num_query_tokens, num_heads, head_size], the cache dtype
+ * query_start_loc int32 [num_seqs + 1], query_start_loc[0] = 0, non-decreasing,
+ *                 query_start_loc[num_seqs] = num_query_tokens
+ * dtype           PA_F16 or PA_BF16; head_size 64 or 128; block_size 16 or 32
+ *
+ * No workspace.  A sequence whose length lies outside [1, max_seq_len] or whose
+ * chunk is longer than itself is recorded as PA_DEVERR_SEQ_LEN and its rows of
+ * out are unspecified.  Asynchronous on `stream`.
+ */
+PA_API pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, int num_seqs, int num_query_tokens, int max_seq_len,
+                            int num_heads, int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                            float scale, pa_dtype dtype, void* stream);
+
+/*
  * Decode with no allocation anywhere: the same computation, arguments and
  * results as pa_decode, but the per-partition scratch lives in a fixed array
  * inside the library instead of a caller-provided workspace.  This serves

@@ -34,6 +34,7 @@ from ._binding import (  # noqa: F401
     pa_decode_plan_partition,
     pa_decode_workspace_size,
     pa_get_device_error,
+    pa_prefill,
     pa_launch_count,
     pa_reshape_and_cache,
     pa_reshape_and_cache_scaled,

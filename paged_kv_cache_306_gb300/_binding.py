@@ -61,6 +61,8 @@ def load():
     lib.pa_launch_count.restype = ctypes.c_uint64
     for f in (lib.pa_reshape_and_cache, lib.pa_copy_blocks, lib.pa_decode, lib.pa_get_device_error):
         f.restype = i32
+    lib.pa_prefill.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32, i32, P]
+    lib.pa_prefill.restype = i32
     # host-side block manager (include/pa_block_manager.h)
     lib.pa_bm_create.argtypes = [i64, i32, ctypes.POINTER(P)]
     lib.pa_bm_destroy.argtypes = [P]
@@ -225,6 +227,29 @@ def pa_decode_scaled(out, q, k_cache, v_cache, block_tables, seq_lens, scale, ma
                                partition_size, _ptr(workspace), ws_bytes, dtype_code(dt), cc, float(k_scale),
                                float(v_scale), _stream(stream)))
     return workspace
+
+
+def pa_prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, max_seq_len, stream=None):
+    """Chunked prefill: query rows query_start_loc[s] .. query_start_loc[s+1]-1 are the last
+    tokens of sequence s (seq_lens[s] tokens in the cache, theirs included) and attend
+    causally; writes out [num_query_tokens, H, D]."""
+    import torch
+    dt = q.dtype
+    _need_cuda("q", q, dt, 3)
+    _need_cuda("out", out, dt, 3)
+    _need_cuda("k_cache", k_cache, dt, 5)
+    _need_cuda("v_cache", v_cache, dt, 4)
+    _need_cuda("block_tables", block_tables, torch.int32, 2)
+    _need_cuda("seq_lens", seq_lens, torch.int32, 1)
+    _need_cuda("query_start_loc", query_start_loc, torch.int32, 1)
+    T, H, D = q.shape
+    nb, hkv, _, bs = v_cache.shape
+    S = seq_lens.numel()
+    if query_start_loc.numel() != S + 1:
+        raise PAError(PA_ERR_INVALID_ARG, "query_start_loc must have num_seqs + 1 entries")
+    check(load().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                            block_tables.shape[1], _ptr(seq_lens), _ptr(query_start_loc), S, T, max_seq_len, H, hkv,
+                            D, bs, nb, float(scale), dtype_code(dt), _stream(stream)))
 
 
 def pa_get_device_error(stream=None):

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libpa.so")
 SOURCES = ["api.cu", "cache_ops.cu", "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu", "decode_fp8.cu", "decode_noalloc.cu",
-           "block_manager.cpp"]
+           "prefill.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -426,6 +426,55 @@ pa_status pa_decode_scaled(void* out, const void* q, const void* k_cache, const 
                      workspace_bytes, q_dtype, cache_dtype, k_scale, v_scale, stream);
 }
 
+pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                     const int32_t* query_start_loc, int num_seqs, int num_query_tokens, int max_seq_len,
+                     int num_heads, int num_kv_heads, int head_size, int block_size, int64_t num_blocks, float scale,
+                     pa_dtype dtype, void* stream) {
+  pa_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
+  if (st != PA_OK) return st;
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "prefill runs on fp16 and bf16 caches");
+  if (num_query_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_query_tokens %d < 0", num_query_tokens);
+  if (max_blocks_per_seq < 1 || (long long)max_seq_len > (long long)max_blocks_per_seq * block_size)
+    return fail(PA_ERR_INVALID_ARG, "max_seq_len %d exceeds max_blocks_per_seq %d * block_size %d", max_seq_len,
+                max_blocks_per_seq, block_size);
+  if (num_blocks < 1) return fail(PA_ERR_INVALID_ARG, "num_blocks %lld < 1", (long long)num_blocks);
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+  if (num_seqs == 0 || num_query_tokens == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+    return fail(PA_ERR_ALIGNMENT, "q/out/caches need 16-byte, tables and lengths 4-byte alignment");
+  pa::PrefillParams p{};
+  st = device_error_ptr(&p.err);
+  if (st != PA_OK) return st;
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_query_tokens = num_query_tokens;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  for (int c0 = 0; c0 < num_seqs; c0 += pa::kMaxSeqsPerLaunch) {
+    p.num_seqs = num_seqs - c0 < pa::kMaxSeqsPerLaunch ? num_seqs - c0 : pa::kMaxSeqsPerLaunch;
+    p.block_tables = block_tables + (size_t)c0 * max_blocks_per_seq;
+    p.seq_lens = seq_lens + c0;
+    p.query_start_loc = query_start_loc + c0;  // offsets stay absolute rows of q and out
+    int n = 0;
+    const cudaError_t ce = pa::launch_prefill(static_cast<int>(dtype), head_size, block_size, p,
+                                              static_cast<cudaStream_t>(stream), &n);
+    g_launches.fetch_add(n, std::memory_order_relaxed);
+    if (ce != cudaSuccess) return cuda_fail(ce, "prefill launch");
+  }
+  return PA_OK;
+}
+
 pa_status pa_get_device_error(int* code, void* stream) {
   if (!code) return fail(PA_ERR_INVALID_ARG, "null code pointer");
   unsigned* err = nullptr;

@@ -115,6 +115,30 @@ int decode_ctas_per_sm_fp8(bool q_is_bf16, int head_size, int block_size, Decode
 cudaError_t launch_decode_fp8(bool q_is_bf16, int head_size, int block_size, const DecodeParams& p, DecodeKind kind,
                               int grid, cudaStream_t s, int* n);
 
+// Chunked prefill (prefill.cu): causal attention of a chunk of new query tokens
+// per sequence over the paged pool; 16-bit caches.
+struct PrefillParams {
+  void* out;                       // [num_query_tokens, H, D]
+  const void* q;                   // [num_query_tokens, H, D]
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;     // [S, max_blocks_per_seq]
+  const int32_t* seq_lens;         // [S]: tokens in the cache, the chunk's included
+  const int32_t* query_start_loc;  // [S + 1]: the chunk of sequence s is rows qsl[s] .. qsl[s+1]-1
+  unsigned* err;
+  long long num_blocks;
+  int max_blocks_per_seq;
+  int num_seqs;                    // <= kMaxSeqsPerLaunch
+  int num_query_tokens;
+  int num_heads;
+  int num_kv_heads;
+  int group;
+  int max_seq_len;
+  float scale_log2;
+};
+cudaError_t launch_prefill(int dtype, int head_size, int block_size, const PrefillParams& p, cudaStream_t stream,
+                           int* launches);
+
 // Write path (cache_ops.cu).
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                      const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,

@@ -176,3 +176,20 @@ def test_scaled_write_rejects_bad_arguments_on_the_host(lib):
     assert w(cache_dt=F16, ks=0.5) == B.PA_ERR_INVALID_ARG   # a 16-bit cache takes no scales
     assert w(cache_dt=F16, key_dt=B.PA_BF16, ks=1.0, vs=1.0) == B.PA_ERR_INVALID_ARG
     assert w(T=0) == B.PA_OK
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+
+    def pf(dt=B.PA_F16, D=128, bs=16, T=8, q=8192, S=2, msl=64, mb=4, H=8, Hkv=2):
+        return lib.pa_prefill(P(8192), P(q), P(8192), P(8192), P(8192), mb, P(8192), P(8192), S, T, msl, H, Hkv, D,
+                              bs, 64, 0.1, dt, None)
+    assert pf(dt=B.PA_F32) == B.PA_ERR_UNSUPPORTED       # tensor-core prefill: 16-bit caches
+    assert pf(dt=B.PA_FP8_E4M3) == B.PA_ERR_UNSUPPORTED
+    assert pf(D=96) == B.PA_ERR_UNSUPPORTED
+    assert pf(bs=8) == B.PA_ERR_UNSUPPORTED
+    assert pf(T=-1) == B.PA_ERR_INVALID_ARG
+    assert pf(msl=65) == B.PA_ERR_INVALID_ARG
+    assert pf(H=6, Hkv=4) == B.PA_ERR_INVALID_ARG
+    assert pf(q=8200) == B.PA_ERR_ALIGNMENT
+    assert pf(T=0) == B.PA_OK and pf(S=0) == B.PA_OK

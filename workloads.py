@@ -98,6 +98,7 @@ class Workload:
     unique_tokens: int = 0       # valid tokens summed over distinct physical blocks
     meta: dict = field(default_factory=dict)
     q_dtype: str = None          # dtype of q, key, value and out (defaults to the cache dtype)
+    query_start_loc: np.ndarray = None  # prefill: int32 [S + 1], the chunk of sequence s is rows qsl[s]..qsl[s+1]-1
     k_scale: float = 1.0         # an FP8 pool reads back as code * scale
     v_scale: float = 1.0
 
@@ -227,6 +228,68 @@ def make_private(name, dtype, seq_lens, num_heads, num_kv_heads, head_size, bloc
     return _finish(name, dtype, S, num_heads, num_kv_heads, head_size, block_size, nb, tables, seq_lens,
                    k, v, rng, partition_size, q_std=q_std, kv_std=kv_std, poison=poison, q_dtype=q_dtype,
                    kv_scale=kv_scale)
+
+
+def make_prefill(name, dtype, context_lens, query_lens, num_heads, num_kv_heads, head_size, block_size, *,
+                 seed, pool_factor=1.25, poison=True):
+    """Chunked prefill: sequence s has context_lens[s] cached tokens and a chunk of
+    query_lens[s] new tokens (positions context .. context + n - 1), whose K/V rows
+    (`key`, `value`, `slot_mapping`, one row per new token in sequence order) the
+    step writes before the prefill; `q` holds one query row per new token.
+    Physical blocks are a random permutation of the pool's ids; slots not yet
+    written (the chunk's and those past the sequence) are poisoned.
+    """
+    rng = np.random.default_rng(seed)
+    ctx = [int(x) for x in context_lens]
+    qn = [int(x) for x in query_lens]
+    S = len(ctx)
+    L = [c + n for c, n in zip(ctx, qn)]
+    bs = block_size
+    nblk = [-(-l // bs) for l in L]
+    need = sum(nblk)
+    nb = max(1, math.ceil(pool_factor * need))
+    ids = rng.permutation(nb)[:need]
+    tables, c = [], 0
+    for n in nblk:
+        tables.append(ids[c:c + n].astype(np.int32))
+        c += n
+    k, v = _empty_pools(nb, num_kv_heads, head_size, bs, dtype, poison)
+    _fill_blocks(rng, k, v, ids, dtype, 1.0)
+    fv = fill_value(dtype, poison)
+    slots = []
+    for s in range(S):
+        if L[s] % bs:
+            _poison_tail(k, v, int(tables[s][-1]), L[s] % bs, dtype, poison)
+        for pos in range(ctx[s], L[s]):          # the chunk: written by the step itself
+            phys, off = int(tables[s][pos // bs]), pos % bs
+            slots.append(phys * bs + off)
+            k[phys, :, :, off, :] = fv
+            v[phys, :, :, off] = fv
+    mb = max(nblk) if S else 1
+    bt = np.full((S, mb), -1, dtype=np.int32)
+    for s, t in enumerate(tables):
+        bt[s, :len(t)] = t
+    T = sum(qn)
+    qsl = np.concatenate([[0], np.cumsum(qn)]).astype(np.int32)
+    q = randn(rng, (T, num_heads, head_size), dtype)
+    key = randn(rng, (T, num_kv_heads, head_size), dtype)
+    value = randn(rng, (T, num_kv_heads, head_size), dtype)
+    return Workload(name=name, dtype=dtype, num_seqs=S, num_heads=num_heads, num_kv_heads=num_kv_heads,
+                    head_size=head_size, block_size=bs, num_blocks=nb, scale=1.0 / math.sqrt(head_size),
+                    partition_size=0, q=q, key=key, value=value, slot_mapping=np.asarray(slots, np.int64),
+                    k_cache=k, v_cache=v, block_tables=bt, seq_lens=np.asarray(L, np.int32),
+                    unique_tokens=int(sum(L)), meta={"context_lens": ctx, "query_lens": qn},
+                    query_start_loc=qsl)
+
+
+def prefill_config(*, poison=True, seed=None):
+    """Chunked prefill of a Qwen2.5-7B-shaped layer (fp16, 28/4 heads, D 128, bs 16):
+    16 sequences, each a chunk of 512 new tokens after U{0..3584} cached ones."""
+    sd = 406 if seed is None else seed
+    rng = np.random.default_rng(sd)
+    ctx = rng.integers(0, 3585, size=16)
+    return make_prefill("qwen2.5-7b-prefill-chunk512-f16", "f16", ctx, [512] * 16, 28, 4, 128, 16, seed=sd + 1000,
+                        poison=poison)
 
 
 def make_prefix_shared(name, dtype, num_groups, group_size, num_heads, num_kv_heads, head_size,
