@@ -12,6 +12,12 @@ copies rotated so K/V always come from HBM); `e2e` is the same metric through
 the Python API with the step's inputs copied from pinned host memory and the
 output copied back inside the timed region.  Rank 0 prints one JSON line.
 
+--mode prefill times chunked prefill instead (16 sequences of a Qwen2.5-7B-shaped
+layer, a chunk of 512 new tokens each after 0..3584 cached ones): a step is the
+chunk's reshape_and_cache and the prefill; the metric is attention TFLOP/s
+(4 * head_size * keys attended, summed over query rows and heads) against the
+measured dense bf16 tensor peak.
+
 --kv-dtype fp8 keeps the workload's shapes and query dtype but stores the pool
 as FP8 E4M3 codes (quantising write, dequantising decode); bytes are counted at
 one byte per cached element.
@@ -39,6 +45,8 @@ METRIC = "paged-decode KV read GB/s (% of GB300 HBM peak) and decode tokens/s pe
 WORKLOADS = {"tiny": 1, "qwen": 2, "llama": 3, "long": 4, "mixed": 5}
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_METRIC = "paged chunked-prefill attention TFLOP/s (% of GB300 dense bf16 tensor peak)"
 
 
 # --- byte accounting ------------------------------------------------------------------------
@@ -63,13 +71,25 @@ def write_bytes(wl):
     return tok + len(wl.cow) * blk * 2 + len(wl.cow) * 16
 
 
-def measured_peaks():
+def measured_peaks(key="hbm_gbs"):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d[key]), "measured"
+    return (FALLBACK_HBM_GBS if key == "hbm_gbs" else FALLBACK_BF16_TFLOPS), "fallback"
+
+
+def prefill_flops(wl):
+    """Useful flops of one prefill: query token i of a chunk of n (sequence of L tokens)
+    sees L - n + i + 1 keys; QK^T and PV take 2 * head_size flops per key each."""
+    total = 0
+    for s in range(wl.num_seqs):
+        L = int(wl.seq_lens[s])
+        n = int(wl.query_start_loc[s + 1] - wl.query_start_loc[s])
+        keys = n * (L - n + 1) + n * (n - 1) // 2
+        total += 4 * wl.head_size * wl.num_heads * keys
+    return total
 
 
 # --- clocks --------------------------------------------------------------------------------
@@ -466,6 +486,156 @@ def run_reference(args, wl, cfg, world_size, rank):
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_prefill(args, world_size, rank, local_rank):
+    """Chunked prefill of the Qwen2.5-7B-shaped layer: write the chunk, then prefill."""
+    import torch
+    import paged_kv_cache_306_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    wl = W.prefill_config(poison=False)
+    pool_bytes = wl.num_blocks * wl.num_kv_heads * wl.head_size * wl.block_size * 2 * 2
+    copies = max(2, math.ceil(4 * L2_BYTES / pool_bytes))
+    sets = [{"q": W.to_torch(wl.q, wl.dtype, dev), "key": W.to_torch(wl.key, wl.dtype, dev),
+             "value": W.to_torch(wl.value, wl.dtype, dev), "k": W.to_torch(wl.k_cache, wl.dtype, dev),
+             "v": W.to_torch(wl.v_cache, wl.dtype, dev), "out": torch.empty(wl.q.shape, dtype=torch.float16, device=dev)}
+            for _ in range(copies)]
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    qsl = torch.from_numpy(wl.query_start_loc).to(dev)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+
+    def step(i, ev=None):
+        s = sets[i % copies]
+        pa.pa_reshape_and_cache(s["key"], s["value"], s["k"], s["v"], slots, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.pa_prefill(s["out"], s["q"], s["k"], s["v"], bt, sl, qsl, wl.scale, wl.max_seq_len, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if pa.pa_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world_size, dev)
+    torch.cuda.synchronize(dev)
+    launches0 = pa.pa_launch_count()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    launches = pa.pa_launch_count() - launches0
+    barrier(world_size, dev)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    if pa.pa_get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    ms_step = max_over_ranks(start.elapsed_time(stop), world_size, dev) / args.steps
+    kn = min(args.steps, 500)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kn)]
+    for i in range(kn):
+        step(i, evs[i])
+    torch.cuda.synchronize(dev)
+    pre_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    # end to end: q, key, value, tables, lengths and slots from pinned host memory, out back
+    s0 = sets[0]
+    parts = {"q": W.to_torch(wl.q, wl.dtype, "cpu"), "key": W.to_torch(wl.key, wl.dtype, "cpu"),
+             "value": W.to_torch(wl.value, wl.dtype, "cpu"), "bt": torch.from_numpy(wl.block_tables),
+             "sl": torch.from_numpy(wl.seq_lens), "qsl": torch.from_numpy(wl.query_start_loc),
+             "slots": torch.from_numpy(wl.slot_mapping)}
+    offs, off = {}, 0
+    for k_, t_ in parts.items():
+        offs[k_] = off
+        off += (t_.numel() * t_.element_size() + 255) // 256 * 256
+    h_stage = torch.empty(off, dtype=torch.uint8).pin_memory()
+    d_stage = torch.empty(off, dtype=torch.uint8, device=dev)
+    devt = {}
+    for k_, t_ in parts.items():
+        nb_ = t_.numel() * t_.element_size()
+        h_stage[offs[k_]:offs[k_] + nb_].copy_(t_.contiguous().view(-1).view(torch.uint8))
+        devt[k_] = d_stage[offs[k_]:offs[k_] + nb_].view(t_.dtype).view(t_.shape)
+    out_host = torch.empty(wl.q.shape, dtype=torch.float16).pin_memory()
+
+    def e2e_step():
+        d_stage.copy_(h_stage, non_blocking=True)
+        pa.pa_reshape_and_cache(devt["key"], devt["value"], s0["k"], s0["v"], devt["slots"], stream=stream)
+        pa.pa_prefill(s0["out"], devt["q"], s0["k"], s0["v"], devt["bt"], devt["sl"], devt["qsl"], wl.scale,
+                      wl.max_seq_len, stream=stream)
+        out_host.copy_(s0["out"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ne = min(args.steps, 500)
+    a.record(stream)
+    for _ in range(ne):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / ne
+
+    flops = prefill_flops(wl)
+    peak, kind = measured_peaks("bf16_tflops")
+    achieved = flops / (pre_ms * 1e-3) / 1e12
+    L = wl.seq_lens
+    cfg = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
+           "head_size": wl.head_size, "block_size": wl.block_size, "query_tokens": int(wl.query_start_loc[-1]),
+           "chunk": 512, "seq_lens": {"min": int(L.min()), "max": int(L.max()), "total": int(L.sum())},
+           "num_blocks": wl.num_blocks, "seed": 406, "flops_per_step": int(flops),
+           "prefill_us": round(pre_ms * 1e3, 2), "pool_copies_rotated": copies,
+           "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e6:.0f} MB rotated",
+           "parallelism": f"replicas x{world_size}"}
+    line = {"metric": PREFILL_METRIC, "value": round(world_size * flops / (ms_step * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfg,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel",
+                         "flops_per_launch": int(flops), "launch_us": round(pre_ms * 1e3, 2),
+                         "peak_source": f"{kind} bf16_tflops (fp16 runs at the bf16 rate)"},
+            "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "ms_per_step": round(e2e_ms, 5), "steps": ne, "h2d_bytes_per_step": int(off),
+                    "d2h_bytes_per_step": int(out_host.numel() * 2), "copies_per_step": 2},
+            "gpu_launches": int(launches), "clocks": clocks}
+    return line, wl
+
+
+def prefill_cpu_baseline(wl, seconds=12.0):
+    """The oracle on the host cores over a bounded sample: the first rows of one sequence."""
+    import oracle
+    k, v = wl.clone_pools()
+    oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, wl.dtype)
+    s = int(np.argmin(wl.seq_lens))
+    n = int(wl.query_start_loc[s + 1] - wl.query_start_loc[s])
+    rows, done_flops, t0 = 8, 0, time.perf_counter()
+    while True:
+        r = min(rows, n)
+        # the sample: the chunk's last r tokens as a chunk of their own (positions L - r ..)
+        q = np.ascontiguousarray(wl.q[wl.query_start_loc[s + 1] - r:wl.query_start_loc[s + 1]])
+        oracle.prefill(q, k, v, wl.block_tables[[s]], wl.seq_lens[[s]], np.array([0, r], np.int32), wl.scale,
+                       wl.dtype)
+        L = int(wl.seq_lens[s])
+        done_flops += 4 * wl.head_size * wl.num_heads * (r * (L - r + 1) + r * (r - 1) // 2)
+        dt = time.perf_counter() - t0
+        if dt > seconds / 4 or r == n:
+            break
+        rows *= 2
+    return {"value": round(done_flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"the last {r} query tokens of sequence {s} ({L} tokens), all heads, "
+                                        f"{dt:.1f} s, fp64 C oracle"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -475,6 +645,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen")
     ap.add_argument("--block-size", type=int, default=None, help="mixed workload only: 16 or 32")
     ap.add_argument("--partition", type=int, default=None, help="override the workload's partition size")
+    ap.add_argument("--mode", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--kv-dtype", choices=["fp8"], default=None,
                     help="store the pool as FP8 E4M3 codes (not for the fp32 tiny workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -485,6 +656,34 @@ def main(argv=None):
 
     world_size, rank, local_rank = dist_env()
     cfg = WORKLOADS[args.workload]
+
+    if args.mode == "prefill":
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+            wl = W.prefill_config(poison=False)
+            cb = prefill_cpu_baseline(wl, seconds=min(120.0, 4.0 * (args.steps + args.warmup)))
+            print(json.dumps({"metric": PREFILL_METRIC, "value": cb["value"], "unit": "TFLOP/s", "n_gpus": world_size,
+                              "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+                              "impl": "reference", "config": {"workload": wl.name}, "cpu_baseline": cb,
+                              "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+            return 0
+        if world_size > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        line, wl = run_prefill(args, world_size, rank, local_rank)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                line["cpu_baseline"] = prefill_cpu_baseline(wl, args.cpu_seconds)
+            print(json.dumps(line), flush=True)
+        if world_size > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
 
     if args.impl == "reference":
         if rank != 0:

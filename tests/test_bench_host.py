@@ -92,3 +92,9 @@ def test_reference_arm_with_an_fp8_pool():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["config"]["kv_cache_dtype"] == "fp8_e4m3" and line["value"] > 0
     assert line["dtype"].startswith("fp8_e4m3")
+
+
+def test_prefill_flops_count_every_key_each_query_row_sees():
+    wl = W.make_prefill("f", "f16", [0, 5, 40], [3, 17, 1], 8, 2, 64, 16, seed=1, poison=False)
+    keys = sum(c + i + 1 for c, n in zip([0, 5, 40], [3, 17, 1]) for i in range(n))
+    assert bench.prefill_flops(wl) == 4 * 64 * 8 * keys
