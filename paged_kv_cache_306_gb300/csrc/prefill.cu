@@ -27,8 +27,11 @@
 //   * Units are dealt to warps round-robin over the grid (unit = warp + k * W).
 #include <math.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_launch.h"
+#include "prefill_tc.cuh"
 
 namespace pa {
 
@@ -356,12 +359,45 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream, int* l
   return e;
 }
 
+// The tcgen05 kernel (prefill_tc.cuh): one CTA per tile of 128 query rows.
+template <typename T, int D, int BS>
+cudaError_t launch_prefill_tc_t(const PrefillParams& p, cudaStream_t stream, int* launches) {
+  using Sh = tc::Shape<T, D, BS>;
+  *launches = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static unsigned done = 0;
+  if (dev >= 32 || !(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & (1u << dev))) {
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&tc::prefill_tc_kernel<T, D, BS>),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
+  }
+  // at most Hkv * (T G / 128 + S) tiles; CTAs past the real ones exit at once
+  const long long tiles = (long long)p.num_kv_heads *
+                          (((long long)p.num_query_tokens * p.group + tc::kRows - 1) / tc::kRows + p.num_seqs);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  e = launch_pdl(tc::prefill_tc_kernel<T, D, BS>, dim3(static_cast<unsigned>(tiles)), dim3(tc::kThreads), Sh::kSmem,
+                 stream, p);
+  if (e == cudaSuccess) *launches = 1;
+  return e;
+}
+
+// tcgen05 (tensor memory) kernel, or the warp-level one above
+constexpr bool kPrefillTensorMemory = true;
+
+template <typename T, int D, int BS>
+cudaError_t launch_prefill_pick(const PrefillParams& p, cudaStream_t s, int* n) {
+  return kPrefillTensorMemory ? launch_prefill_tc_t<T, D, BS>(p, s, n) : launch_prefill_t<T, D, BS>(p, s, n);
+}
+
 template <typename T>
 cudaError_t launch_prefill_dispatch(int head_size, int block_size, const PrefillParams& p, cudaStream_t s, int* n) {
-  if (head_size == 64 && block_size == 16) return launch_prefill_t<T, 64, 16>(p, s, n);
-  if (head_size == 64 && block_size == 32) return launch_prefill_t<T, 64, 32>(p, s, n);
-  if (head_size == 128 && block_size == 16) return launch_prefill_t<T, 128, 16>(p, s, n);
-  if (head_size == 128 && block_size == 32) return launch_prefill_t<T, 128, 32>(p, s, n);
+  if (head_size == 64 && block_size == 16) return launch_prefill_pick<T, 64, 16>(p, s, n);
+  if (head_size == 64 && block_size == 32) return launch_prefill_pick<T, 64, 32>(p, s, n);
+  if (head_size == 128 && block_size == 16) return launch_prefill_pick<T, 128, 16>(p, s, n);
+  if (head_size == 128 && block_size == 32) return launch_prefill_pick<T, 128, 32>(p, s, n);
   return cudaErrorInvalidValue;
 }
 
