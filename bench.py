@@ -601,7 +601,7 @@ def run_prefill(args, world_size, rank, local_rank):
             "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfg,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel",
+                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_tc_kernel",
                          "flops_per_launch": int(flops), "launch_us": round(pre_ms * 1e3, 2),
                          "peak_source": f"{kind} bf16_tflops (fp16 runs at the bf16 rate)"},
             "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",

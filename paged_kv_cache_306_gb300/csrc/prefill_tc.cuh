@@ -1,12 +1,15 @@
 // prefill_tc.cuh -- chunked prefill on the 5th-generation tensor cores (tcgen05, TMEM).
 //
-// Same result as the warp-level prefill in prefill.cu (causal attention of each
-// sequence's chunk of new query tokens over its paged cache), restructured for
-// sm_103a's tcgen05 MMA, whose accumulators live in tensor memory (TMEM):
+// Causal attention of each sequence's chunk of new query tokens over its paged
+// cache (what is computed: see prefill.cu), on sm_103a's tcgen05 MMA, whose
+// accumulators live in tensor memory (TMEM):
 //
-//   * A CTA of 4 warps owns a tile of 128 query rows -- (token, query head) pairs
-//     of one kv head, head fastest -- and TMEM lanes 0..127 are those rows: thread
-//     t of the CTA owns row t through the softmax and the epilogue.
+//   * A CTA of 8 warps owns a tile of 128 query rows -- (token, query head) pairs
+//     of one kv head, head fastest -- and TMEM lanes 0..127 are those rows.  Two
+//     threads share a row, one from each group of 4 warps (a warp reaches TMEM
+//     lanes 32 (warp % 4) ..): each takes half of a chunk's keys in the softmax
+//     and half of the head dims in the epilogue; the row maximum and sum are
+//     combined through shared memory.
 //   * Keys are taken 64 at a time (4 blocks of 16 or 2 of 32).  Their K and V
 //     tiles arrive by 1-D bulk copies (TMA unit) into a 2-stage ring, prefetched
 //     two chunks ahead.  A pool K tile [D/8][bs][8] is already the K-major
@@ -34,7 +37,7 @@ namespace pa {
 namespace tc {
 
 constexpr int kRows = 128;     // query rows per CTA (= TMEM lanes)
-constexpr int kThreads = 128;  // 4 warps
+constexpr int kThreads = 256;  // 8 warps: two threads per row
 constexpr int kKeys = 64;      // keys per chunk
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -113,12 +116,13 @@ struct Shape {
   static constexpr int kOffStage = kQBytes;
   static constexpr int kOffV2 = kOffStage + 2 * kStageBytes;
   static constexpr int kOffP = kOffV2 + kV2Bytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffRed = kOffP + 2 * kPBytes;   // [2][128] floats: per-half row maxima / sums
+  static constexpr int kOffBar = kOffRed + 2 * kRows * 4;
   static constexpr int kSmem = kOffBar + 8 * 8 + 16;
   static constexpr int kTmemCols = 256;  // S: 64 columns, O: D columns at 64
 };
 
-// grid: one CTA per tile of 128 rows; p.units_hint CTAs beyond the real tiles exit
+// grid: one CTA per tile of 128 rows (an upper bound on the tiles; the CTAs past the real ones exit)
 template <typename T, int D, int BS>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
   using Sh = Shape<T, D, BS>;
@@ -127,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   unsigned char* sStage = smem + Sh::kOffStage;
   unsigned char* sV2 = smem + Sh::kOffV2;
   unsigned char* sP = smem + Sh::kOffP;
+  float* s_red = reinterpret_cast<float*>(smem + Sh::kOffRed);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);  // [2]
   uint64_t* s_done = full + 2;
   uint64_t* o_done = full + 3;
@@ -187,15 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  // ---- this thread's row; Q into shared memory (core matrices: 8 rows x 16 bytes)
-  const int r = tid, row = row_lo + r;
+  // ---- this thread's row and half; Q into shared memory (core matrices: 8 rows x 16 bytes)
+  const int r = tid & (kRows - 1), half = tid >> 7, row = row_lo + r;
   const bool valid = row < row_hi;
   const int pos = valid ? ctx + row / G : p_max;  // a padding row behaves as the last real one
   {
     const T* q = static_cast<const T*>(p.q) +
                  ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) * D;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
+    for (int c = half * (D / 16); c < (half + 1) * (D / 16); ++c) {
       const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(q) + c) : make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(sQ + (r / 8) * (D / 8) * 128 + c * 128 + (r % 8) * 16) = v;
     }
@@ -239,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   fence_after();
   const uint32_t tmem = *s_tmem;
   const uint32_t t_s = tmem, t_o = tmem + kKeys;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  constexpr int kHalfKeys = kKeys / 2, kHalfD = D / 2;
 
   constexpr uint32_t kIdS = idesc<T>(kRows, BS), kIdO = idesc<T>(kRows, D);
   const float sl2 = p.scale_log2;
@@ -301,24 +307,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       fence_proxy_async_smem();
       issue(c + 2);
     }
-    // ---- softmax of this thread's row over the chunk's 64 keys
-    float sv[kKeys];
-    {
-      float a[32];
-      ld32(t_s + lane_base, a);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sv[j] = a[j];
-      ld32(t_s + lane_base + 32, a);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sv[32 + j] = a[j];
-    }
-    const int lim = pos - c * kKeys;  // keys 0..lim of this chunk are visible to the row
+    // ---- softmax of this thread's half of the chunk's keys for its row
+    float sv[kHalfKeys];
+    ld32(t_s + lane_base + half * kHalfKeys, sv);
+    const int lim = pos - c * kKeys - half * kHalfKeys;  // keys 0..lim of this half are visible to the row
     float mx = -INFINITY;
+    if (lim >= kHalfKeys - 1) {  // all visible (every chunk but the last ones of a row)
 #pragma unroll
-    for (int j = 0; j < kKeys; ++j) {
-      sv[j] = j <= lim ? sv[j] * sl2 : -INFINITY;
-      mx = fmaxf(mx, sv[j]);
+      for (int j = 0; j < kHalfKeys; ++j) {
+        sv[j] *= sl2;
+        mx = fmaxf(mx, sv[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kHalfKeys; ++j) {
+        sv[j] = j <= lim ? sv[j] * sl2 : -INFINITY;
+        mx = fmaxf(mx, sv[j]);
+      }
     }
+    s_red[half * kRows + r] = mx;
+    __syncthreads();
+    mx = fmaxf(s_red[r], s_red[kRows + r]);
     // move the running maximum only when it grows by more than 2^8 (P stays <= 256)
     float corr = 1.f;
     const bool move = mx > m + 8.f;
@@ -329,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     }
     float ps = 0.f;
 #pragma unroll
-    for (int kg = 0; kg < kKeys / 8; ++kg) {
+    for (int kg = 0; kg < kHalfKeys / 8; ++kg) {
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
         const float2 back = unpack2<T>(hi[j]);
         lo[j] = pack2<T>(x - back.x, y - back.y);
       }
-      const int off = (r / 8) * (kKeys / 8) * 128 + kg * 128 + (r % 8) * 16;
+      const int off = (r / 8) * (kKeys / 8) * 128 + (half * (kHalfKeys / 8) + kg) * 128 + (r % 8) * 16;
       *reinterpret_cast<uint4*>(sP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(sP + Sh::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     // rescale O (idle: the previous P V is done, this one is not issued) where the maximum moved
     if (c > 0 && __any_sync(0xffffffffu, move && corr != 1.f)) {
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = half * kHalfD; c0 < (half + 1) * kHalfD; c0 += 32) {
         float o[32];
         ld32(t_o + lane_base + c0, o);
 #pragma unroll
@@ -380,12 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   }
   if (ok) {
     fence_after();
-    // epilogue: out = O / l, rounded to T
-    const float inv = 1.f / l;
+    // epilogue: out = O / l, rounded to T; l is the sum of the two halves' sums
+    s_red[half * kRows + r] = l;
+    __syncthreads();
+    const float inv = 1.f / (s_red[r] + s_red[kRows + r]);
     T* out = static_cast<T*>(p.out) +
              ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) * D;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = half * kHalfD; c0 < (half + 1) * kHalfD; c0 += 32) {
       float o[32];
       ld32(t_o + lane_base + c0, o);
       if (valid) {
