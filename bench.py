@@ -2,11 +2,14 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload qwen|llama|long|mixed|tiny] [--block-size 16|32]
-                    [--kv-dtype fp8]
+                    [--kv-dtype fp8] [--step fused|separate]
 
 A step is the whole hot path on one batch: copy-on-write block copies (the
-mixed workload only), reshape_and_cache of every sequence's new token, and
-decode attention (plus the partition merge when the planner splits).
+mixed workload only), the write of every sequence's new token, and decode
+attention (plus the partition merge when the planner splits).  By default the
+step is one pa_decode_step call, which does all three in the decode kernel;
+--step separate times pa_copy_blocks + pa_reshape_and_cache + pa_decode
+instead (always so for an FP8 cache, whose write quantises).
 `value` is algorithmic bytes per step / step time (inputs resident in HBM, pool
 copies rotated so K/V always come from HBM); `e2e` is the same metric through
 the Python API with the step's inputs copied from pinned host memory and the
@@ -255,6 +258,7 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     ps = wl.partition_size if args.partition is None else args.partition
     code = {"f32": pa.PA_F32, "f16": pa.PA_F16, "bf16": pa.PA_BF16, "fp8": pa.PA_FP8_E4M3}[wl.dtype]
     write, decode = api_calls(wl)
+    fused = uses_fused_step(args, wl)
     resolved = pa.pa_decode_plan_partition(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
                                            wl.max_seq_len, wl.block_size, code) if ps == -1 else ps
     ws_bytes = pa.pa_decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
@@ -263,6 +267,14 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
 
     def step(i, ev=None):
         s = sets[i % copies]
+        if fused:
+            if ev is not None:
+                ev[0].record(stream)
+            pa.pa_decode_step(s["out"], s["q"], s["key"], s["value"], s["k"], s["v"], cow if len(wl.cow) else None,
+                              bt, sl, wl.scale, wl.max_seq_len, resolved, ws, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         if len(wl.cow):
             pa.pa_copy_blocks(s["k"], s["v"], cow, stream=stream)
         write(s["key"], s["value"], s["k"], s["v"], slots, stream=stream)
@@ -301,7 +313,8 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     ms_total = max_over_ranks(start.elapsed_time(stop), world_size, dev)
     ms_step = ms_total / args.steps
 
-    # the decode call alone: events on the launching stream around every call
+    # the decode call alone (the fused call: it also copies and writes): events on
+    # the launching stream around every call
     kn = min(args.steps, 2000)
     dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kn)]
     for i in range(kn):
@@ -310,17 +323,20 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_events]))
 
     # end to end through the API: pinned host inputs in, result out, every step
-    e2e = run_e2e(args, wl, dev, stream, sets[0], bt, sl, resolved, ws)
+    e2e = run_e2e(args, wl, dev, stream, sets[0], bt, sl, resolved, ws, fused)
 
     step_bytes = decode_bytes(wl) + write_bytes(wl)
     dbytes = decode_bytes(wl)
     peak, peak_kind = measured_peaks()
     # DRAM-level bytes: a physical block shared by several sequences is read once
-    rbytes = decode_bytes(wl, unique=True)
+    rbytes = decode_bytes(wl, unique=True) + (write_bytes(wl) if fused else 0)
     achieved = rbytes / (dec_ms * 1e-3) / 1e9
     traffic = load_traffic(wl)
     cfgd = describe(wl, cfg)
     cfgd.update({"partition_size": int(resolved), "pool_copies_rotated": copies,
+                 "step": ("fused: one pa_decode_step call (block copies, new tokens and decode in the decode "
+                          "kernel) + merge" if fused else
+                          "separate: pa_copy_blocks + pa_reshape_and_cache + pa_decode"),
                  "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e6:.0f} MB rotated",
                  "decode_bytes": int(dbytes), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
                  "step_bytes": int(step_bytes), "decode_us": round(dec_ms * 1e3, 2),
@@ -334,7 +350,8 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
         "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfgd,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_decode call: decode_kernel + decode_merge_kernel",
+                     "kernel": ("pa_decode_step call: decode_kernel (copies, new tokens, decode) + decode_merge_kernel"
+                                if fused else "pa_decode call: decode_kernel + decode_merge_kernel"),
                      "bytes_per_launch": int(rbytes), "launch_us": round(dec_ms * 1e3, 2),
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
@@ -342,12 +359,17 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     return line
 
 
+def uses_fused_step(args, wl):
+    """The fused step takes fp32 and 16-bit caches; an FP8 cache's write quantises."""
+    return args.step == "fused" and wl.dtype != "fp8"
+
+
 def pa_dtype(wl):
     import torch
     return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.q_dtype]
 
 
-def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws):
+def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws, fused):
     """Same step through the Python API, with the step's inputs copied from pinned
     host memory and the output copied back, every step.  The inputs are packed in
     one pinned staging buffer (one host-to-device copy per step)."""
@@ -362,6 +384,8 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws):
         "slots": torch.from_numpy(wl.slot_mapping),
         "cow": torch.from_numpy(np.ascontiguousarray(wl.cow)),
     }
+    if fused:  # the fused step finds each new token's slot through the block table
+        del parts["slots"]
     offs, off = {}, 0
     for k, t in parts.items():
         offs[k] = off
@@ -381,6 +405,12 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws):
 
     def step():
         d_stage.copy_(h_stage, non_blocking=True)
+        if fused:
+            pa.pa_decode_step(s["out"], devt["q"], devt["key"], devt["value"], s["k"], s["v"],
+                              devt["cow"] if len(wl.cow) else None, devt["bt"], devt["sl"], wl.scale,
+                              wl.max_seq_len, resolved, ws, stream=stream)
+            out_host.copy_(s["out"], non_blocking=True)
+            return
         if len(wl.cow):
             pa.pa_copy_blocks(s["k"], s["v"], devt["cow"], stream=stream)
         write(devt["key"], devt["value"], s["k"], s["v"], devt["slots"], stream=stream)
@@ -648,6 +678,8 @@ def main(argv=None):
     ap.add_argument("--mode", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--kv-dtype", choices=["fp8"], default=None,
                     help="store the pool as FP8 E4M3 codes (not for the fp32 tiny workload)")
+    ap.add_argument("--step", choices=["fused", "separate"], default="fused",
+                    help="one pa_decode_step call, or copy_blocks + reshape_and_cache + decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

@@ -204,6 +204,44 @@ PA_API pa_status pa_decode_scaled(void* out, const void* q, const void* k_cache,
                                   float k_scale, float v_scale, void* stream);
 
 /*
+ * One generation step in one call: the copy-on-write copies, then the write of
+ * each sequence's new token fused into decode ("vLLM's
+ * PagedAttention: why the KV cache is paged", §4.2: a shared block about to be
+ * written is copied first, then written; "Reading vLLM's PagedAttention kernel",
+ * §3.2 write path and §2 decode).  The result equals, byte for byte in the pools
+ * and bit for bit in out, the three calls
+ *     pa_copy_blocks(k_cache, v_cache, src_dst, num_pairs, ...);
+ *     pa_reshape_and_cache(key, value, k_cache, v_cache, slots, num_seqs, ...);
+ *     pa_decode(out, q, k_cache, v_cache, block_tables, ..., seq_lens, ...);
+ * where slots[s] is the position seq_lens[s] - 1 of sequence s under its block
+ * table: the new token of a sequence is the last one it attends to.
+ *
+ * key, value  [num_seqs, num_kv_heads, head_size], the cache dtype: one new token
+ *             per sequence (a sequence with seq_lens[s] outside [1, max_seq_len]
+ *             writes nothing and is reported as in pa_decode)
+ * src_dst     int64 [num_pairs, 2] (may be NULL when num_pairs is 0), as in
+ *             pa_copy_blocks; the copies complete before any token is written
+ * everything else as in pa_decode, with the same workspace size.
+ *
+ * dtype is PA_F32, PA_F16 or PA_BF16 (an FP8 cache is written by
+ * pa_reshape_and_cache_scaled, not here).  No two sequences of the call may
+ * write the same slot, and no sequence may read a slot another one writes
+ * (the block manager's copy-on-write guarantees both).
+ *
+ * Kernels: the decode kernel writes each new token and decodes (the token
+ * reaches the stage of its sequence's last block with that block's TMA copy,
+ * so decode never waits for the write), then the merge kernel.  With
+ * num_pairs > 0 the copy kernel of pa_copy_blocks runs first.  Asynchronous on
+ * `stream`.
+ */
+PA_API pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                                void* v_cache, const int64_t* src_dst, int64_t num_pairs,
+                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
+                                int block_size, int64_t num_blocks, float scale, int partition_size,
+                                void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
  * Read and clear the first device-side error recorded on the current device
  * (PA_DEVERR_*; 0 if none).  Synchronizes `stream` first.
  */

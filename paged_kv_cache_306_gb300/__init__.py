@@ -4,8 +4,9 @@ A small C-ABI library (``_build/libpa.so``, sources in ``csrc/``, interface in
 ``include/pa.h``) with hand-written sm_103a kernels for the two directions of a
 paged KV cache: the write path (``pa_reshape_and_cache``, ``pa_copy_blocks``)
 and decode attention over the block pool (``pa_decode``), with an FP8 E4M3
-cache variant of both (``pa_reshape_and_cache_scaled``, ``pa_decode_scaled``), and
-the host-side block manager that produces block tables, slots and copy-on-write
+cache variant of both (``pa_reshape_and_cache_scaled``, ``pa_decode_scaled``), the
+three fused into one generation step (``pa_decode_step``), chunked prefill
+(``pa_prefill``) and the host-side block manager that produces block tables, slots and copy-on-write
 pairs (``BlockManager``, ``include/pa_block_manager.h``).  This package is the
 thin Python binding; PyTorch supplies device memory and streams only.
 """
@@ -31,6 +32,7 @@ from ._binding import (  # noqa: F401
     pa_copy_blocks,
     pa_decode,
     pa_decode_scaled,
+    pa_decode_step,
     pa_decode_plan_partition,
     pa_decode_workspace_size,
     pa_get_device_error,

@@ -327,7 +327,9 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
                              int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
                              int block_size, int64_t num_blocks, float scale, int partition_size, void* workspace,
                              size_t workspace_bytes, pa_dtype q_dtype, pa_dtype dtype, float k_scale, float v_scale,
-                             void* stream) {
+                             void* stream, const void* new_key = nullptr, const void* new_value = nullptr,
+                             const int64_t* copy_pairs = nullptr, int64_t num_copies = 0) {
+  // new_key != nullptr: the fused step (pa_decode_step), already validated there.
   // `dtype` is the cache dtype from here on; q and out have q_dtype.
   pa_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
   if (st != PA_OK) return st;
@@ -368,6 +370,7 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.seg_first = reinterpret_cast<int*>(ws + pl.off_first);
   p.seg_last = reinterpret_cast<int*>(ws + pl.off_last);
+  p.fused = new_key != nullptr;
   st = device_error_ptr(&p.err);
   if (st != PA_OK) return st;
   p.k_cache = k_cache;
@@ -385,6 +388,15 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * k_scale * 1.4426950408889634);
   p.out_scale = v_scale;
 
+  if (p.fused && num_copies > 0) {  // the copy-on-write copies: their own kernel, before any token lands
+    int n = 0;
+    const long long block_bytes = (long long)num_kv_heads * head_size * block_size * elem_bytes(dtype);
+    const cudaError_t ce = pa::launch_copy_blocks(const_cast<void*>(k_cache), const_cast<void*>(v_cache), copy_pairs,
+                                                  num_copies, block_bytes, num_blocks, p.err,
+                                                  static_cast<cudaStream_t>(stream), &n);
+    g_launches.fetch_add(n, std::memory_order_relaxed);
+    if (ce != cudaSuccess) return cuda_fail(ce, "copy_blocks launch");
+  }
   const size_t row_bytes = (size_t)num_heads * head_size * elem_bytes(q_dtype);
   const int launch_dtype = dtype == PA_FP8_E4M3 ? 16 + static_cast<int>(q_dtype) : static_cast<int>(dtype);
   for (int c0 = 0; c0 < num_seqs; c0 += pl.chunk) {
@@ -393,6 +405,11 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     p.out = static_cast<char*>(out) + (size_t)c0 * row_bytes;
     p.block_tables = block_tables + (size_t)c0 * max_blocks_per_seq;
     p.seq_lens = seq_lens + c0;
+    if (p.fused) {
+      const size_t kv_row_bytes = (size_t)num_kv_heads * head_size * elem_bytes(dtype);
+      p.new_key = static_cast<const char*>(new_key) + (size_t)c0 * kv_row_bytes;
+      p.new_value = static_cast<const char*>(new_value) + (size_t)c0 * kv_row_bytes;
+    }
     p.epoch = next_epoch();
     int n = 0;
     const cudaError_t ce = pa::launch_decode(launch_dtype, head_size, block_size, p, pl.kind, pl.grid,
@@ -424,6 +441,29 @@ pa_status pa_decode_scaled(void* out, const void* q, const void* k_cache, const 
   return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                      num_heads, num_kv_heads, head_size, block_size, num_blocks, scale, partition_size, workspace,
                      workspace_bytes, q_dtype, cache_dtype, k_scale, v_scale, stream);
+}
+
+pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* src_dst, int64_t num_pairs, const int32_t* block_tables,
+                         int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                         int num_heads, int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                         float scale, int partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                         void* stream) {
+  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "the fused step runs on fp32, fp16 and bf16 caches");
+  if (num_pairs < 0 || num_pairs > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_pairs %lld", (long long)num_pairs);
+  if (num_pairs > 0 && (!src_dst || !aligned(src_dst, 8)))
+    return fail(num_pairs > 0 && src_dst ? PA_ERR_ALIGNMENT : PA_ERR_INVALID_ARG,
+                "src_dst must be a non-null, 8-byte aligned int64 array");
+  if (num_seqs > 0 && (!key || !value)) return fail(PA_ERR_INVALID_ARG, "null key or value");
+  if (num_seqs > 0 && (!aligned(key, 16) || !aligned(value, 16)))
+    return fail(PA_ERR_ALIGNMENT, "key/value need 16-byte alignment");
+  if (num_seqs == 0 && num_pairs > 0)  // nothing to decode: the copies alone
+    return pa_copy_blocks(k_cache, v_cache, src_dst, num_pairs, num_kv_heads, head_size, block_size, num_blocks,
+                          dtype, stream);
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                     num_heads, num_kv_heads, head_size, block_size, num_blocks, scale, partition_size, workspace,
+                     workspace_bytes, dtype, dtype, 1.f, 1.f, stream, key, value, src_dst, num_pairs);
 }
 
 pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,

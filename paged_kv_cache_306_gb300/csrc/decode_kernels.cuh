@@ -36,6 +36,13 @@
 //     tensor-core work.  K and V come straight from the stage with ldmatrix; P
 //     stays in registers, split into a rounded 16-bit high part and the rounded
 //     remainder so P V keeps ~16 significant bits.
+//   * The fused step (pa_decode_step) writes each sequence's new token as part of
+//     decode.  Every warp stores its share of the tokens to the pool while its
+//     first stages are in flight, and nothing waits for those stores: the token's
+//     K and V rows also ride along with the TMA copy of the sequence's last block
+//     into a side buffer beside the stage, and the warp that waits on that stage
+//     puts the token into its slot of the stage, whatever the copy saw of the slot
+//     in the pool.  The write costs no kernel of its own.
 //   * CUDA-core math (fp32 caches, or one query head per kv head): half-warps split
 //     the head dims of the scores, lanes split V rows and token chunks for P V, and
 //     the reductions are warp shuffles.
@@ -66,6 +73,13 @@ struct DecodeShape {
   static constexpr int kBarBytes = kWarps * kStages * 8;
   // per-sequence tables: lengths, block prefix, warp sums
   static constexpr int kTableBytes = (kMaxSeqsPerLaunch + (kMaxSeqsPerLaunch + 1) + kWarps + 3) * 4;
+  // score row and running state per warp
+  static constexpr int kRows = kMode ? 8 * kMode : 1;
+  static constexpr int kStateBytes = kWarps * BS * 4 + kWarps * kRows * (D + 2) * 4;
+  // the fused step: a sequence's new K and V rows land beside the stage of its last block
+  static constexpr int kSideOffset = (kRingBytes + kBarBytes + kTableBytes + kStateBytes + 127) / 128 * 128;
+  static constexpr int kSideStage = 2 * D * kElem;
+  static constexpr int kSmemBytes = kSideOffset + kWarps * kStages * kSideStage;
 };
 
 // Wait for block i's stage.  On timeout record the error and drain the copies
@@ -643,6 +657,29 @@ struct SimtMath {
   }
 };
 
+// --- the fused step: the new token ---------------------------------------------------------------
+
+// The fused step's new token of a (sequence, kv head) -- its K and V rows, copied
+// by TMA into `side` with the stage of the sequence's last block -- into that
+// stage at slot `off` (K tile [D/X][BS][X]: 16 bytes per X-group, D/X <= 32 of
+// them; V tile [D][BS]: one element per dim).
+template <typename TC, int D, int BS>
+__device__ __forceinline__ void inject_token(unsigned char* stage, int tile_bytes, const unsigned char* side, int off,
+                                             int lane) {
+  constexpr int X = 16 / static_cast<int>(sizeof(TC)), VPL = D / 32;
+  const TC* sv = reinterpret_cast<const TC*>(side + D * sizeof(TC));
+  TC* v = reinterpret_cast<TC*>(stage + tile_bytes);
+  uint4 g;
+  TC e[VPL];
+  if (lane < D / X) g = reinterpret_cast<const uint4*>(side)[lane];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) e[i] = sv[lane + 32 * i];
+  if (lane < D / X) *reinterpret_cast<uint4*>(stage + (lane * BS + off) * 16) = g;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) v[(lane + 32 * i) * BS + off] = e[i];
+  __syncwarp();
+}
+
 // --- the schedule ---------------------------------------------------------------------------------
 
 // Head unit u of a sequence: its kv head, first query head and query-row count.
@@ -694,6 +731,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char* ring = smem + warp * STAGES * 2 * TILE;
+  unsigned char* side = smem + Sh::kSideOffset + warp * STAGES * Sh::kSideStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kRingBytes) + warp * STAGES;
   int* s_len = reinterpret_cast<int*>(smem + Sh::kRingBytes + Sh::kBarBytes);
   int* s_pre = s_len + kMaxSeqsPerLaunch;                 // [S + 1] block prefix per unit
@@ -760,17 +798,66 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
     }
   }
 
-  // This warp's range of the T blocks of work.
-  const long long T_all = (long long)s_pre[S] * U;
   const int W = gridDim.x * kDecodeWarps;
   const int w = blockIdx.x * kDecodeWarps + warp;
+
+  // The fused step's pool writes: item i = (sequence, kv head) of the launch goes
+  // to warp i mod W.  A batch of items is loaded before any of it is stored (the
+  // stores may alias the loads as far as the compiler knows).  Nothing in this
+  // launch reads these slots from the pool afterwards: decode takes the tokens
+  // from the side buffers (see issue), so the stores need no ordering.
+  auto write_tokens = [&]() {
+    constexpr int X = 16 / static_cast<int>(sizeof(TC)), VPL = D / 32, kBatch = 4;
+    const long long tile_bytes = (long long)D * BS * sizeof(TC);
+    unsigned char* kc = static_cast<unsigned char*>(const_cast<void*>(p.k_cache));
+    unsigned char* vc = static_cast<unsigned char*>(const_cast<void*>(p.v_cache));
+    const int items = S * p.num_kv_heads;
+    for (int i0 = w; i0 < items; i0 += kBatch * W) {
+      uint4 kv[kBatch];
+      TC vv[kBatch][VPL];
+      long long tile[kBatch];
+      int off[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = i0 + b * W;
+        tile[b] = -1;
+        if (i >= items) continue;
+        const int s2 = i / p.num_kv_heads, h = i - s2 * p.num_kv_heads, L2 = s_len[s2];
+        if (L2 == 0) continue;
+        const int blk = __ldg(p.block_tables + (long long)s2 * p.max_blocks_per_seq + (L2 - 1) / BS);
+        if (blk < 0 || blk >= p.num_blocks) continue;  // recorded when decode reads the block
+        tile[b] = (long long)blk * p.num_kv_heads + h;
+        off[b] = (L2 - 1) % BS;
+        const TC* key = static_cast<const TC*>(p.new_key) + (long long)i * D;
+        const TC* value = static_cast<const TC*>(p.new_value) + (long long)i * D;
+        if (lane < D / X) kv[b] = __ldg(reinterpret_cast<const uint4*>(key) + lane);
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) vv[b][e] = value[lane + 32 * e];
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (tile[b] < 0) continue;
+        if (lane < D / X) *reinterpret_cast<uint4*>(kc + tile[b] * tile_bytes + (lane * BS + off[b]) * 16) = kv[b];
+        TC* vt = reinterpret_cast<TC*>(vc + tile[b] * tile_bytes);
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) vt[(lane + 32 * e) * BS + off[b]] = vv[b][e];
+      }
+    }
+  };
+
+  // This warp's range of the T blocks of work.
+  const long long T_all = (long long)s_pre[S] * U;
   const long long qt = T_all / W, rt = T_all % W;
   const long long start = w * qt + (w * rt) / W;
   const long long end = (w + 1) * qt + ((w + 1) * rt) / W;
   const int len = static_cast<int>(end - start);
-  if (len <= 0) return;
+  if (len <= 0) {
+    if (p.fused) write_tokens();
+    return;
+  }
 
-  // Table lookups: lane i resolves work position start + 32 * group + i.
+  // Table lookups: lane i resolves work position start + 32 * group + i: the
+  // physical block, and kvh | sequence << 16 | (last block of the sequence) << 30.
   const int32_t* __restrict__ bt = p.block_tables;
   auto fetch = [&](int group, int& phys, int& kvh) {
     const long long gpos = start + 32LL * group + lane;
@@ -781,6 +868,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       locate(gpos, s_pre, S, U, s, u, j);
       unit_heads<kMma>(p, u, kvh, h0, nh);
       phys = __ldg(bt + (long long)s * p.max_blocks_per_seq + j);
+      kvh |= (s << 16) | ((j == s_pre[s + 1] - s_pre[s] - 1) << 30);
     }
   };
   int phys_cur, kvh_cur, phys_nxt, kvh_nxt, group_cur = 0;
@@ -794,7 +882,8 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       fetch(group_cur + 1, phys_nxt, kvh_nxt);
     }
     int phys = __shfl_sync(0xffffffffu, phys_cur, k & 31);
-    const int kvh = __shfl_sync(0xffffffffu, kvh_cur, k & 31);
+    const int tag = __shfl_sync(0xffffffffu, kvh_cur, k & 31);
+    const int kvh = tag & 0xffff;
     if (phys < 0 || phys >= p.num_blocks) {  // out-of-pool entry: record it, read block 0 instead
       if (lane == 0) set_error(p.err, kErrBlockId);
       phys = 0;
@@ -803,12 +892,21 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       const int st = k % STAGES;
       unsigned char* dst = ring + st * 2 * TILE;
       const long long tile = (long long)phys * p.num_kv_heads + kvh;
-      mbar_arrive_expect_tx(&bars[st], 2 * TILE);
+      const bool with_token = p.fused && (tag >> 30);
+      mbar_arrive_expect_tx(&bars[st], 2 * TILE + (with_token ? Sh::kSideStage : 0));
       bulk_copy_g2s(dst, static_cast<const unsigned char*>(p.k_cache) + tile * TILE, TILE, &bars[st]);
       bulk_copy_g2s(dst + TILE, static_cast<const unsigned char*>(p.v_cache) + tile * TILE, TILE, &bars[st]);
+      if (with_token) {  // the new token's K and V rows of (sequence, kv head)
+        const long long row = ((long long)((tag >> 16) & 0x3fff) * p.num_kv_heads + kvh) * (D * sizeof(TC));
+        unsigned char* sd = side + st * Sh::kSideStage;
+        bulk_copy_g2s(sd, static_cast<const unsigned char*>(p.new_key) + row, D * sizeof(TC), &bars[st]);
+        bulk_copy_g2s(sd + D * sizeof(TC), static_cast<const unsigned char*>(p.new_value) + row, D * sizeof(TC),
+                      &bars[st]);
+      }
     }
   };
   for (int k = 0; k < STAGES && k < len; ++k) issue(k);
+  if (p.fused) write_tokens();  // while the first stages are in flight
 
   // The compute cursor walks the same positions in order.
   Math math;
@@ -831,6 +929,8 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
     if (!wait_stage<STAGES>(bars, k, len, p.err, lane)) break;
     unsigned char* stage = ring + (k % STAGES) * 2 * TILE;
     const int rem = L - cj * BS;  // valid tokens in this block (>= 1)
+    if (p.fused && cj == nblk - 1)  // the sequence's new token: from the step's input, not the pool
+      inject_token<TC, D, BS>(stage, TILE, side + (k % STAGES) * Sh::kSideStage, (L - 1) % BS, lane);
     if (rem < BS) zero_tail_v<TC, D, BS>(stage + TILE, rem, lane);
     if constexpr (Math::kFetch) {  // the block's fragments are in registers: refill the stage now
       math.fetch(stage, TILE);
@@ -1007,9 +1107,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
 
 template <typename TC, int D, int BS, int kMode>
 constexpr int decode_smem_bytes() {
-  using Sh = DecodeShape<TC, D, BS, kMode>;
-  return Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes + Sh::kWarps * BS * 4 +
-         Sh::kWarps * (kMode ? 8 * kMode : 1) * (D + 2) * 4;
+  return DecodeShape<TC, D, BS, kMode>::kSmemBytes;
 }
 
 template <typename T, typename TC, int D, int BS, int kMode>

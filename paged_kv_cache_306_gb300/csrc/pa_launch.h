@@ -60,6 +60,12 @@ struct DecodeParams {
   unsigned epoch;               // distinguishes this launch's partial slots from stale ones
   float scale_log2;             // scale * k_scale * log2(e)
   float out_scale;              // v_scale: a quantised cache's V reads back as code * v_scale
+  // The fused step (pa_decode_step): the new token of each sequence s (rows s of
+  // new_key and new_value, [S, Hkv, D] in the cache dtype) goes into position
+  // seq_lens[s] - 1 as part of decode; fused == 0 for plain decode.
+  const void* new_key;
+  const void* new_value;
+  int fused;
 };
 
 // CUDA cores, or tensor cores with one (up to 8 query heads per kv head) or two

@@ -103,3 +103,25 @@ def assert_close(got, ref, dtype, with_rounding=True, what="", out_dtype=None):
     err, worst = max_violation(got, ref, dtype, with_rounding, out_dtype)
     assert worst <= 0.0, f"{what}: max abs err {err:.3e} exceeds tolerance (excess {worst:.3e})"
     return err
+
+
+def fused_step(wl, partition_size=None, t=None, workspace=None, check_error=True):
+    """The same step as gpu_step in one call (pa_decode_step); returns (out, tensors)."""
+    import torch
+    import paged_kv_cache_306_gb300 as pa
+    t = upload(wl) if t is None else t
+    out = torch.empty_like(t["q"])
+    ps = wl.partition_size if partition_size is None else partition_size
+    pa.pa_decode_step(out, t["q"], t["key"], t["value"], t["k_cache"], t["v_cache"],
+                      t["cow"] if len(wl.cow) else None, t["block_tables"], t["seq_lens"], wl.scale, wl.max_seq_len,
+                      ps, workspace)
+    if check_error:
+        code = pa.pa_get_device_error()
+        assert code == 0, f"device error {code}: {pa.DEVICE_ERRORS.get(code)}"
+    return out, t
+
+
+def same_bytes(a, b):
+    """Bitwise equality of two CUDA tensors of one dtype and shape."""
+    import torch
+    return a.shape == b.shape and torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))

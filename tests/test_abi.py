@@ -193,3 +193,23 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert pf(H=6, Hkv=4) == B.PA_ERR_INVALID_ARG
     assert pf(q=8200) == B.PA_ERR_ALIGNMENT
     assert pf(T=0) == B.PA_OK and pf(S=0) == B.PA_OK
+
+
+def test_fused_step_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+
+    def st(dt=B.PA_F16, key=8192, value=8192, sd=8192, npairs=1, S=1, D=128, bs=16, msl=16, q=8192):
+        return lib.pa_decode_step(P(8192), P(q), P(key), P(value), P(8192), P(8192), P(sd), npairs, P(8192), 4,
+                                  P(8192), S, msl, 4, 4, D, bs, 8, 0.1, 0, None, 0, dt, None)
+    assert st(dt=B.PA_FP8_E4M3) == B.PA_ERR_UNSUPPORTED   # an FP8 cache is written by the scaled write
+    assert st(dt=7) == B.PA_ERR_UNSUPPORTED
+    assert st(npairs=-1) == B.PA_ERR_INVALID_ARG
+    assert st(sd=0) == B.PA_ERR_INVALID_ARG                # pairs without an array
+    assert st(sd=8196) == B.PA_ERR_ALIGNMENT
+    assert st(key=0) == B.PA_ERR_INVALID_ARG
+    assert st(value=8200) == B.PA_ERR_ALIGNMENT
+    assert st(D=96) == B.PA_ERR_UNSUPPORTED                # the decode checks follow
+    assert st(msl=65) == B.PA_ERR_INVALID_ARG
+    assert st(q=8200) == B.PA_ERR_ALIGNMENT
+    assert st(S=0, npairs=0, key=0, value=0, q=0) == B.PA_OK
+    assert lib.pa_last_error_message()

@@ -136,3 +136,25 @@ def test_fp8_config_keeps_the_shapes_of_its_16_bit_workload():
     assert np.array_equal(a.block_tables, b.block_tables)
     with pytest.raises(ValueError):
         W.config(1, kv_dtype="fp8")
+
+
+@pytest.mark.parametrize("bs,seed", [(16, 1), (16, 20), (32, 8), (32, 9)])
+def test_no_poison_reaches_a_read_slot_when_sharers_of_a_block_differ_in_length(bs, seed):
+    """Short prefixes make sequences of one group end inside the same shared block
+    with different lengths; the last sharer then writes in place into the block
+    the others copy.  Before the step that slot holds a prefix token, which the
+    copies carry; no poison may be read by any sequence after the step."""
+    wl = W.make_prefix_shared("short", "f32", 4, 5, 4, 2, 64, bs, seed=seed, len_range=(4, 200),
+                              prefix_range=(5, 120), partition_size=0)
+    src = set(wl.cow[:, 0].tolist())
+    k, v = wl.clone_pools()
+    oracle.copy_blocks(k, v, wl.cow, "f32")
+    oracle.reshape_and_cache(wl.key, wl.value, k, v, wl.slot_mapping, "f32")
+    for s in range(wl.num_seqs):
+        L = int(wl.seq_lens[s])
+        for j in range(-(-L // bs)):
+            n = min(bs, L - j * bs)
+            b = int(wl.block_tables[s, j])
+            assert np.all(np.isfinite(k[b, :, :, :n, :])) and np.all(np.isfinite(v[b, :, :, :n])), (s, j)
+    assert np.all(np.isfinite(oracle.decode(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale, "f32")))
+    assert any(int(wl.slot_mapping[s]) // bs in src for s in range(wl.num_seqs)), "no in-place writer to test"

@@ -401,6 +401,9 @@ def make_prefix_shared(name, dtype, num_groups, group_size, num_heads, num_kv_he
             tables[i] = tables[i].copy()
             tables[i][j] = dst
     cow = np.asarray(cow, dtype=np.int64).reshape(-1, 2)
+    # the last sharer of a copied block writes its new token there in place, after
+    # the copies: until then the slot holds the prefix token the copies take along
+    src_before = {int(b): (k[b].copy(), v[b].copy()) for b in set(cow[:, 0].tolist())}
 
     # distinct physical blocks and their valid-token counts (for byte accounting)
     valid = {}
@@ -414,8 +417,11 @@ def make_prefix_shared(name, dtype, num_groups, group_size, num_heads, num_kv_he
                  meta={"prefix_lens": P.tolist(), "group_size": group_size}, q_dtype=q_dtype, kv_scale=kv_scale)
     # _finish poisons the new-token slot of the (post-copy) target block; a
     # copy-on-write destination is still unwritten before the step, so the
-    # poison there is what the copy must overwrite.  The source block keeps the
-    # prefix token at that offset, which the siblings still read.
+    # poison there is what the copy must overwrite.  A copy's source keeps its
+    # tokens, the slot of an in-place writer included, which the copies carry.
+    for b, (kb, vb) in src_before.items():
+        wl.k_cache[b] = kb
+        wl.v_cache[b] = vb
     wl.cow = cow
     return wl
 
