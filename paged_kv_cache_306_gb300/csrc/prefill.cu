@@ -21,12 +21,13 @@
 #include "pa_device.cuh"
 #include "pa_launch.h"
 #include "prefill_tc.cuh"
+#include "prefill_ws.cuh"
 
 namespace pa {
 
 // ---- host side ------------------------------------------------------------------------------
 
-// The tcgen05 kernel (prefill_tc.cuh): one CTA per tile of 128 query rows.
+// The tcgen05 kernel (prefill_tc.cuh): one CTA per tile of 128 query rows, two per SM.
 template <typename T, int D, int BS>
 cudaError_t launch_prefill_tc_t(const PrefillParams& p, cudaStream_t stream, int* launches) {
   using Sh = tc::Shape<T, D, BS>;
@@ -38,6 +39,10 @@ cudaError_t launch_prefill_tc_t(const PrefillParams& p, cudaStream_t stream, int
   if (dev >= 32 || !(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & (1u << dev))) {
     e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&tc::prefill_tc_kernel<T, D, BS>),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    // all of the SM's unified memory as shared memory: two CTAs of ~113 KiB each
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&tc::prefill_tc_kernel<T, D, BS>),
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     if (dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
   }
@@ -51,12 +56,101 @@ cudaError_t launch_prefill_tc_t(const PrefillParams& p, cudaStream_t stream, int
   return e;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time libcuda)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The K pool [NB][Hkv][D/8][bs][8] seen as rows of 16 keys x 8 dims (128 16-bit
+// elements, 256 bytes); a box is one row (tile::gather4 takes four of them).
+template <int D, int BS>
+cudaError_t encode_k_map(const PrefillParams& p, CUtensorMap* map) {
+  const EncodeTiledFn enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const unsigned long long rows = (unsigned long long)p.num_blocks * p.num_kv_heads * (D / 8) * (BS / 16);
+  if (rows > 0x7fffffffULL) return cudaErrorInvalidValue;  // rows are addressed with int32 coordinates
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {128, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(p.k_cache), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The V pool [NB][Hkv][D][bs] seen as NB * Hkv * D rows of bs 16-bit elements; a box is
+// [D rows][8 elements]: one 8-key group of one (block, kv head) tile, landing as [D][8].
+template <int D, int BS>
+cudaError_t encode_v_map(const PrefillParams& p, CUtensorMap* map) {
+  const EncodeTiledFn enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const unsigned long long rows = (unsigned long long)p.num_blocks * p.num_kv_heads * D;
+  if (rows > 0x7fffffffULL) return cudaErrorInvalidValue;  // box rows are addressed with int32 coordinates
+  const cuuint64_t dims[2] = {(cuuint64_t)BS, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)BS * 2};
+  const cuuint32_t box[2] = {8, (cuuint32_t)D};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(p.v_cache), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The warp-specialised tcgen05 kernel (prefill_ws.cuh): one CTA per tile of 128 query rows, two per SM.
+template <typename T, int D, int BS>
+cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int* launches) {
+  using Sh = ws::Shape<T, D, BS>;
+  *launches = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static unsigned done = 0;
+  if (dev >= 32 || !(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & (1u << dev))) {
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&ws::prefill_ws_kernel<T, D, BS>),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&ws::prefill_ws_kernel<T, D, BS>),
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    if (dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
+  }
+  CUtensorMap kmap, vmap;
+  e = encode_k_map<D, BS>(p, &kmap);
+  if (e != cudaSuccess) return e;
+  e = encode_v_map<D, BS>(p, &vmap);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)p.num_kv_heads *
+                          (((long long)p.num_query_tokens * p.group + ws::kRows - 1) / ws::kRows + p.num_seqs);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  e = launch_pdl(ws::prefill_ws_kernel<T, D, BS>, dim3(static_cast<unsigned>(tiles)), dim3(ws::kThreads), Sh::kSmem,
+                 stream, p, kmap, vmap);
+  if (e == cudaSuccess) *launches = 1;
+  return e;
+}
+
+template <typename T, int D, int BS>
+cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t s, int* n) {
+  return launch_prefill_ws_t<T, D, BS>(p, s, n);
+}
+
 template <typename T>
 cudaError_t launch_prefill_dispatch(int head_size, int block_size, const PrefillParams& p, cudaStream_t s, int* n) {
-  if (head_size == 64 && block_size == 16) return launch_prefill_tc_t<T, 64, 16>(p, s, n);
-  if (head_size == 64 && block_size == 32) return launch_prefill_tc_t<T, 64, 32>(p, s, n);
-  if (head_size == 128 && block_size == 16) return launch_prefill_tc_t<T, 128, 16>(p, s, n);
-  if (head_size == 128 && block_size == 32) return launch_prefill_tc_t<T, 128, 32>(p, s, n);
+  if (head_size == 64 && block_size == 16) return launch_prefill_t<T, 64, 16>(p, s, n);
+  if (head_size == 64 && block_size == 32) return launch_prefill_t<T, 64, 32>(p, s, n);
+  if (head_size == 128 && block_size == 16) return launch_prefill_t<T, 128, 16>(p, s, n);
+  if (head_size == 128 && block_size == 32) return launch_prefill_t<T, 128, 32>(p, s, n);
   return cudaErrorInvalidValue;
 }
 

@@ -11,8 +11,10 @@
 //     and half of the head dims in the epilogue; the row maximum and sum are
 //     combined through shared memory.
 //   * Keys are taken 64 at a time (4 blocks of 16 or 2 of 32).  Their K and V
-//     tiles arrive by 1-D bulk copies (TMA unit) into a 2-stage ring, prefetched
-//     two chunks ahead.  A pool K tile [D/8][bs][8] is already the K-major
+//     tiles arrive by 1-D bulk copies (TMA unit) into one stage; the next chunk's
+//     copies start as soon as the S MMAs have read K and V has been re-laid out,
+//     so they run under the softmax and P V.  At under 113 KiB of shared memory
+//     two CTAs share an SM, and each one's serial phases fill the other's gaps.  A pool K tile [D/8][bs][8] is already the K-major
 //     core-matrix layout the MMA reads (8 keys x 16 bytes per core matrix), so
 //     S = Q K^T is issued straight from the stage: one MMA of M=128, N=bs, K=16
 //     per block and 16-dim step, into TMEM columns 0..63.
@@ -114,29 +116,27 @@ struct Shape {
   static constexpr int kV2Bytes = kKeys * D * 2;           // V re-laid out [key/8][D][8]
   static constexpr int kPBytes = kRows * kKeys * 2;        // P high (then P low)
   static constexpr int kOffStage = kQBytes;
-  static constexpr int kOffV2 = kOffStage + 2 * kStageBytes;
+  static constexpr int kOffV2 = kOffStage + kStageBytes;
   static constexpr int kOffP = kOffV2 + kV2Bytes;
-  static constexpr int kOffRed = kOffP + 2 * kPBytes;   // [2][128] floats: per-half row maxima / sums
-  static constexpr int kOffBar = kOffRed + 2 * kRows * 4;
-  static constexpr int kSmem = kOffBar + 8 * 8 + 16;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kSmem = kOffBar + 8 * 8 + 16;  // <= 113 KiB: two CTAs per SM
   static constexpr int kTmemCols = 256;  // S: 64 columns, O: D columns at 64
 };
 
 // grid: one CTA per tile of 128 rows (an upper bound on the tiles; the CTAs past the real ones exit)
 template <typename T, int D, int BS>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillParams p) {
   using Sh = Shape<T, D, BS>;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* sQ = smem;
   unsigned char* sStage = smem + Sh::kOffStage;
   unsigned char* sV2 = smem + Sh::kOffV2;
   unsigned char* sP = smem + Sh::kOffP;
-  float* s_red = reinterpret_cast<float*>(smem + Sh::kOffRed);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);  // [2]
-  uint64_t* s_done = full + 2;
-  uint64_t* o_done = full + 3;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 4);
-  int* s_tile = reinterpret_cast<int*>(full + 5);  // sequence, kv head, tile (or -1)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);
+  uint64_t* s_done = full + 1;
+  uint64_t* o_done = full + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 3);
+  int* s_tile = reinterpret_cast<int*>(full + 4);  // sequence, kv head, tile (or -1)
   const int tid = threadIdx.x, warp = tid >> 5;
 
   griddep_launch_dependents();
@@ -167,8 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     s_tile[0] = found;
     s_tile[1] = fk;
     s_tile[2] = fj;
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    mbar_init(full, 1);
     mbar_init(s_done, 1);
     mbar_init(o_done, 1);
     fence_barrier_init();
@@ -206,19 +205,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     }
   }
 
-  // ---- producer: blocks of chunk c into stage c & 1 (thread 0)
+  // ---- producer: blocks of chunk c into the stage (thread 0)
   const int32_t* bt = p.block_tables + (long long)s * p.max_blocks_per_seq;
-  auto issue = [&](int c) {
-    unsigned char* st = sStage + (c & 1) * Sh::kStageBytes;
-    int phys[Sh::kBlocks];
-    int nv = 0;
+  // the table entries of the next chunk to issue, loaded one chunk ahead (thread 0)
+  int phys[Sh::kBlocks];
+  auto load_table = [&](int c) {
 #pragma unroll
     for (int b = 0; b < Sh::kBlocks; ++b) {
       const int gb = c * Sh::kBlocks + b;
       phys[b] = gb < nblk ? __ldg(bt + gb) : -1;
-      if (gb < nblk) ++nv;
     }
-    mbar_arrive_expect_tx(&full[c & 1], 2 * nv * Sh::kTile);
+  };
+  auto issue = [&](int c) {
+    unsigned char* st = sStage;
+    int nv = 0;
+#pragma unroll
+    for (int b = 0; b < Sh::kBlocks; ++b)
+      if (c * Sh::kBlocks + b < nblk) ++nv;
+    mbar_arrive_expect_tx(full, 2 * nv * Sh::kTile);
 #pragma unroll
     for (int b = 0; b < Sh::kBlocks; ++b) {
       if (c * Sh::kBlocks + b >= nblk) continue;
@@ -229,15 +233,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       }
       const long long tl = (long long)ph * p.num_kv_heads + kvh;
       bulk_copy_g2s(st + b * Sh::kTile, static_cast<const unsigned char*>(p.k_cache) + tl * Sh::kTile, Sh::kTile,
-                    &full[c & 1]);
+                    full);
       bulk_copy_g2s(st + (Sh::kBlocks + b) * Sh::kTile, static_cast<const unsigned char*>(p.v_cache) + tl * Sh::kTile,
-                    Sh::kTile, &full[c & 1]);
+                    Sh::kTile, full);
     }
+    load_table(c + 1);  // lands while this chunk is processed
   };
   if (tid == 0) {
+    load_table(0);
     issue(0);
-    if (nchunks > 1) issue(1);
   }
+  // chunk whose copies, S MMAs or P V MMAs are in flight and not yet waited for (-1: none); every
+  // thread tracks them alike, so that a CTA that gives up waits for exactly these before it exits
+  int pend_full = 0, pend_s = -1, pend_o = -1;
   fence_proxy_async_smem();  // Q's generic stores before the MMAs read it
   fence_before();
   __syncthreads();
@@ -246,6 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   const uint32_t t_s = tmem, t_o = tmem + kKeys;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   constexpr int kHalfKeys = kKeys / 2, kHalfD = D / 2;
+  // P's shared-memory piece (16 bytes) of row rr, half hh, key group kg (K-major core matrices)
+  auto p_off = [&](int rr, int hh, int kg) {
+    return (rr / 8) * (kKeys / 8) * 128 + (hh * (kHalfKeys / 8) + kg) * 128 + (rr % 8) * 16;
+  };
+  // The two threads of a row exchange their half's maximum (and at the end their
+  // sums) through shared memory: each writes into the first P piece its partner
+  // will write, and only the partner reads it -- before overwriting it with P.
+  float* x_mine = reinterpret_cast<float*>(sP + p_off(r, half ^ 1, 0));
+  const float* x_partner = reinterpret_cast<const float*>(sP + p_off(r, half, 0));
 
   constexpr uint32_t kIdS = idesc<T>(kRows, BS), kIdO = idesc<T>(kRows, D);
   const float sl2 = p.scale_log2;
@@ -253,14 +270,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   bool ok = true;
 
   for (int c = 0; c < nchunks && ok; ++c) {
-    unsigned char* st = sStage + (c & 1) * Sh::kStageBytes;
-    // K and V of this chunk landed; the previous P V is done with V2 and P
-    ok = mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, kWaitNs);
-    if (ok && c > 0) ok = mbar_wait_bounded(o_done, (c - 1) & 1, kWaitNs);
+    unsigned char* st = sStage;
+    // K and V of this chunk landed
+    ok = mbar_wait_bounded(full, c & 1, kWaitNs);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
+    pend_full = -1;
+    // S = Q K^T for the chunk's blocks (thread 0), at once: the S columns of TMEM were read
+    // by the previous chunk's softmax, and the MMAs run in issue order after its P V
+    if (tid == 0) {
+      fence_after();
+#pragma unroll
+      for (int b = 0; b < Sh::kBlocks; ++b) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t da = sdesc(smem_addr(sQ) + ks * 256, 128, (D / 8) * 128);
+          const uint64_t db = sdesc(smem_addr(st) + b * Sh::kTile + ks * 2 * (BS * 16), BS * 16, 128);
+          mma(t_s + b * BS, da, db, kIdS, ks > 0);
+        }
+      }
+      commit(s_done);
+    }
+    pend_s = c;
+    // the previous P V is done with V2, P and O before they are touched again
+    if (c > 0) ok = mbar_wait_bounded(o_done, (c - 1) & 1, kWaitNs);
     fence_after();
     // V re-layout: piece (key group kg of 8, dim d) -> V2 + kg * (D * 16) + d * 16; keys past the sequence are zero
     for (int i = tid; i < (kKeys / 8) * D; i += kThreads) {
@@ -280,32 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       *reinterpret_cast<uint4*>(sV2 + kg * (D * 16) + d * 16) = v;
     }
     fence_proxy_async_smem();
-    fence_before();
-    __syncthreads();
-    // S = Q K^T for the chunk's blocks (thread 0), then the stage's K is consumed
-    if (tid == 0) {
-      fence_after();
-#pragma unroll
-      for (int b = 0; b < Sh::kBlocks; ++b) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t da = sdesc(smem_addr(sQ) + ks * 256, 128, (D / 8) * 128);
-          const uint64_t db = sdesc(smem_addr(st) + b * Sh::kTile + ks * 2 * (BS * 16), BS * 16, 128);
-          mma(t_s + b * BS, da, db, kIdS, ks > 0);
-        }
-      }
-      commit(s_done);
-    }
-    ok = mbar_wait_bounded(s_done, c & 1, kWaitNs);
+    if (ok) ok = mbar_wait_bounded(s_done, c & 1, kWaitNs);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
+    pend_s = pend_o = -1;
     fence_after();
-    // the stage is free (K read by the S MMAs, V copied out): prefetch chunk c + 2 into it
-    if (tid == 0 && c + 2 < nchunks) {
-      fence_proxy_async_smem();
-      issue(c + 2);
+    // the stage is free (K read by the S MMAs, V copied out): prefetch chunk c + 1 into it
+    if (c + 1 < nchunks) {
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        issue(c + 1);
+      }
+      pend_full = c + 1;
     }
     // ---- softmax of this thread's half of the chunk's keys for its row
     float sv[kHalfKeys];
@@ -325,9 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
         mx = fmaxf(mx, sv[j]);
       }
     }
-    s_red[half * kRows + r] = mx;
-    __syncthreads();
-    mx = fmaxf(s_red[r], s_red[kRows + r]);
+    *x_mine = mx;
+    // the two warps of these rows (warp and warp ^ 4) meet; the others go on
+    switch (warp & 3) {  // literal barrier ids (1..4; 0 is __syncthreads)
+      case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+      case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+      case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+      default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+    }
+    mx = fmaxf(mx, *x_partner);
     // move the running maximum only when it grows by more than 2^8 (P stays <= 256)
     float corr = 1.f;
     const bool move = mx > m + 8.f;
@@ -348,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
         const float2 back = unpack2<T>(hi[j]);
         lo[j] = pack2<T>(x - back.x, y - back.y);
       }
-      const int off = (r / 8) * (kKeys / 8) * 128 + (half * (kHalfKeys / 8) + kg) * 128 + (r % 8) * 16;
+      const int off = p_off(r, half, kg);
       *reinterpret_cast<uint4*>(sP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(sP + Sh::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
@@ -381,18 +410,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       }
       commit(o_done);
     }
+    pend_o = c;
   }
 
   if (ok) {
     ok = mbar_wait_bounded(o_done, (nchunks - 1) & 1, kWaitNs);
     ok = __syncthreads_and(ok);
+    if (ok) pend_o = -1;
   }
   if (ok) {
     fence_after();
     // epilogue: out = O / l, rounded to T; l is the sum of the two halves' sums
-    s_red[half * kRows + r] = l;
+    *x_mine = l;  // P is no longer read
     __syncthreads();
-    const float inv = 1.f / (s_red[r] + s_red[kRows + r]);
+    const float inv = 1.f / (l + *x_partner);
     T* out = static_cast<T*>(p.out) +
              ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) * D;
 #pragma unroll
@@ -414,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   } else {
     if (tid == 0) set_error(p.err, kErrTimeout);
     // let copies and MMAs in flight finish (bounded) before the memory they target goes away
-    mbar_wait_bounded(o_done, 0, kWaitNs / 8);
-    mbar_wait_bounded(&full[0], 0, kWaitNs / 8);
-    mbar_wait_bounded(&full[1], 0, kWaitNs / 8);
+    if (pend_full >= 0) mbar_wait_bounded(full, pend_full & 1, kWaitNs / 8);
+    if (pend_s >= 0) mbar_wait_bounded(s_done, pend_s & 1, kWaitNs / 8);
+    if (pend_o >= 0) mbar_wait_bounded(o_done, pend_o & 1, kWaitNs / 8);
   }
   fence_before();
   __syncthreads();

@@ -1,0 +1,457 @@
+// prefill_ws.cuh -- chunked prefill on tcgen05 with warp specialisation.
+//
+// The same computation as prefill_tc.cuh (causal attention of each sequence's
+// chunk of new query tokens over its paged cache; see prefill.cu).  A CTA owns a
+// tile of 128 query rows -- (token, query head) pairs of one kv head, head
+// fastest -- which are TMEM lanes 0..127, and takes keys 64 at a time.  The
+// phases of a chunk run in different warps that hand over through mbarriers, so
+// the copies, the MMAs and the softmax of neighbouring chunks overlap:
+//
+//   * warp 4, one thread: the TMA copies of chunk c into stage c % 2 once P V of
+//     chunk c - 2 has read the stage, through two tensor maps.  K: the pool seen
+//     as rows of 16 keys x 8 dims (one 256-byte run of a K tile [D/8][bs][8]); one
+//     tile::gather4 load per 8-dim chunk fetches the rows of the chunk's 64 keys
+//     (from up to four blocks anywhere in the pool) and lands them as [64][8]:
+//     the K operand of S = Q K^T becomes [D/8][64 keys][8], core matrices with one
+//     uniform stride, so S is one MMA of N = 64 per 16 dims (a block-by-block S
+//     of N = bs took four times the MMAs and was the largest cost).  V: the pool
+//     seen as rows of bs keys (one dim of a V tile [D][bs]); each [D rows x 8 keys]
+//     box lands as [D][8], one 8-key group of the [key/8][D][8] layout the P V MMA
+//     reads.  No re-layout pass.
+//   * warp 5, one thread: S(c) = Q K^T into TMEM columns S[c % 2] (once chunk c
+//     has landed and P V(c - 2), which read P from those columns, is done), then
+//     O += P V(c - 1) with P read from TMEM; each group is committed to mbarriers.
+//   * warps 0..3, one thread per row: the softmax of S(c) while the tensor cores
+//     run P V(c - 1) and S(c + 1).  P = exp2(s - m) goes back into the row's own S
+//     columns as rounded 16-bit high and low parts (two per 32-bit column).  The
+//     running maximum moves only when it grows by more than 2^8; then the row's O
+//     is rescaled in TMEM after P V(c - 1) has finished (rare).  In the last chunk
+//     the V of keys past the sequence (or past the blocks loaded) is zeroed in
+//     shared memory first: P is 0 there, but 0 * NaN would poison O.
+//
+// At under 113 KiB of shared memory and 256 TMEM columns, two CTAs share an SM.
+// Every wait is bounded (1 s of %globaltimer); a thread that gives up records
+// PA_DEVERR_TIMEOUT and raises a CTA-wide abort flag that makes every other wait
+// give up at once; the threads that issued copies or MMAs then wait (bounded)
+// for them before TMEM is freed.
+#pragma once
+
+#include <cuda.h>
+
+#include "pa_device.cuh"
+#include "pa_launch.h"
+#include "prefill_tc.cuh"
+
+namespace pa {
+namespace ws {
+
+using tc::commit;
+using tc::fence_after;
+using tc::fence_before;
+using tc::idesc;
+using tc::ld32;
+using tc::mma;
+using tc::sdesc;
+using tc::st32;
+
+constexpr int kRows = 128;  // query rows per CTA (= TMEM lanes)
+constexpr int kKeys = 64;   // keys per chunk
+constexpr int kSoftmaxThreads = 128;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// tcgen05 MMA with the A operand in TMEM (row i in lane i, two 16-bit K elements per column)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"((uint32_t)accumulate));
+}
+
+// 2-D tensor-map copy global -> shared (box at element coordinates x, y)
+__device__ __forceinline__ void tma_2d_g2s(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// tile::gather4 tensor-map copy: four rows (element row indices rows[0..3]) of a 2-D
+// map whose box is one row high, landing one after another in shared memory
+__device__ __forceinline__ void tma_gather4_g2s(void* dst, const CUtensorMap* map, const int (&rows)[4], uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3]), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// A bounded wait that also gives up at once when another thread of the CTA has
+// given up (*abort set); a thread that times out sets *abort and records the error.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitNs) {
+      *abort = 1;
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+template <typename T, int D, int BS>
+struct Shape {
+  static constexpr int kTile = D * BS * 2;                 // one block's K (or V) tile
+  static constexpr int kBlocks = kKeys / BS;               // blocks per chunk
+  static constexpr int kQBytes = kRows * D * 2;            // Q, core-matrix layout
+  static constexpr int kStageBytes = 2 * kKeys * D * 2;    // K as [D/8][64][8], then V as [key/8][D][8]
+  static constexpr int kKBytes = kKeys * D * 2;
+  static constexpr int kOffStage = kQBytes;
+  static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
+  static constexpr int kNumBars = 8;
+  static constexpr int kSmem = kOffBar + kNumBars * 8 + 32;  // <= 113 KiB: two CTAs per SM
+  static constexpr int kTmemCols = 256;  // S/P[0]: 0..63, S/P[1]: 64..127, O: 128..128+D
+};
+
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_ws_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
+  using Sh = Shape<T, D, BS>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* sQ = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);
+  uint64_t* full = bars;        // [2] stage landed (TMA bytes)
+  uint64_t* sfull = bars + 2;   // [2] S in TMEM (commit)
+  uint64_t* pfull = bars + 4;   // [2] P in TMEM, O rescaled and V tail zeroed where needed (128 arrivals)
+  uint64_t* pvdone = bars + 6;  // [2] P V done: P's columns, the stage and O are free (commit)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
+  int* s_tile = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, tile (or -1)
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tile + 3);  // a thread gave up
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // ---- which tile (tiles of a sequence are taken last first, so the longest start early)
+  if (tid == 0) {
+    const int G = p.group, Hkv = p.num_kv_heads;
+    long long t = blockIdx.x;
+    int found = -1, fk = 0, fj = 0;
+    for (int s = 0; s < p.num_seqs && found < 0; ++s) {
+      const int L = p.seq_lens[s], a = p.query_start_loc[s], b = p.query_start_loc[s + 1];
+      const int n = b - a;
+      if (L < 1 || L > p.max_seq_len || a < 0 || b > p.num_query_tokens || n < 0 || n > L) {
+        if (blockIdx.x == 0) set_error(p.err, kErrSeqLen);
+        continue;
+      }
+      const long long tiles = (long long)((n * G + kRows - 1) / kRows);
+      if (t < tiles * Hkv) {
+        found = s;
+        fk = static_cast<int>(t / tiles);
+        fj = static_cast<int>(tiles - 1 - t % tiles);
+      } else {
+        t -= tiles * Hkv;
+      }
+    }
+    s_tile[0] = found;
+    s_tile[1] = fk;
+    s_tile[2] = fj;
+    *s_abort = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&sfull[i], 1);
+      mbar_init(&pfull[i], kSoftmaxThreads);
+      mbar_init(&pvdone[i], 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int s = s_tile[0];
+  if (s < 0) return;  // no tile for this CTA (before any TMEM is taken)
+  const int kvh = s_tile[1], tile = s_tile[2];
+  const int G = p.group;
+  const int L = p.seq_lens[s], tok0 = p.query_start_loc[s], n = p.query_start_loc[s + 1] - tok0;
+  const int rows = n * G, row_lo = tile * kRows, row_hi = min(rows, row_lo + kRows);
+  const int ctx = L - n;
+  const int p_max = ctx + (row_hi - 1) / G;  // last position any row of the tile has
+  const int nblk = p_max / BS + 1;            // blocks holding keys 0..p_max
+  const int nchunks = (p_max + kKeys) / kKeys;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(s_tmem)),
+                 "r"(Sh::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // the softmax threads' rows; Q into shared memory (core matrices: 8 rows x 16 bytes)
+  const int r = tid & (kRows - 1), row = row_lo + r;
+  const bool valid = row < row_hi;
+  if (tid < kSoftmaxThreads) {
+    const T* q = static_cast<const T*>(p.q) +
+                 ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) * D;
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(q) + c) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sQ + (r / 8) * (D / 8) * 128 + c * 128 + (r % 8) * 16) = v;
+    }
+  }
+  fence_proxy_async_smem();  // Q's generic stores before the MMAs read it
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t t_o = tmem + 2 * kKeys;
+  auto wait = [&](uint64_t* bar, int parity) { return wait_or_abort(bar, parity, s_abort, p.err); };
+
+  if (warp < 4) {
+    // ================= softmax: row r, all keys of each chunk =================
+    const int pos = valid ? ctx + row / G : p_max;  // a padding row behaves as the last real one
+    const int kz = min(L, nblk * BS);               // first key whose V must read as zero
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int sb = c & 1;
+      if (!wait(&sfull[sb], (c >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      const uint32_t t_s = tmem + lane_base + sb * kKeys;
+      float sv[kKeys];
+      {
+        float a[32];
+        ld32(t_s, a);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = a[j];
+        ld32(t_s + 32, a);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[32 + j] = a[j];
+      }
+      const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
+      float mx = -INFINITY;
+      if (lim >= kKeys - 1) {
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) {
+          sv[j] *= sl2;
+          mx = fmaxf(mx, sv[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) {
+          sv[j] = j <= lim ? sv[j] * sl2 : -INFINITY;
+          mx = fmaxf(mx, sv[j]);
+        }
+      }
+      float corr = 1.f;
+      const bool move = mx > m + 8.f;
+      if (move) {
+        corr = m == -INFINITY ? 0.f : exp2f(m - mx);
+        m = mx;
+        l *= corr;
+      }
+      // O holds P V up to chunk c - 1 once that group is done: rescale the row if the maximum moved
+      if (c > 0 && move && corr != 1.f) {
+        if (!wait(&pvdone[(c - 1) & 1], ((c - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          ld32(t_o + lane_base + c0, o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] *= corr;
+          st32(t_o + lane_base + c0, o);
+        }
+      }
+      // P into the row's S columns: high parts in 0..31, low parts in 32..63
+      {
+        float hi[32], lo[32];
+        float ps = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x0 = exp2f(sv[2 * j] - m), x1 = exp2f(sv[2 * j + 1] - m);
+          ps += x0 + x1;
+          const uint32_t h = pack2<T>(x0, x1);
+          const float2 back = unpack2<T>(h);
+          hi[j] = __uint_as_float(h);
+          lo[j] = __uint_as_float(pack2<T>(x0 - back.x, x1 - back.y));
+        }
+        st32(t_s, hi);
+        st32(t_s + 32, lo);
+        l += ps;
+      }
+      // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as zero
+      if (c == nchunks - 1 && kz < (c + 1) * kKeys) {
+        unsigned char* vbase = smem + Sh::kOffStage + sb * Sh::kStageBytes + Sh::kKBytes;
+        const int k0 = kz - c * kKeys, cnt = (kKeys - k0) * D;
+        for (int i = tid; i < cnt; i += kSoftmaxThreads) {
+          const int kk = k0 + i / D, d = i % D;
+          *reinterpret_cast<T*>(vbase + (kk / 8) * (D * 16) + d * 16 + (kk % 8) * 2) = DType<T>::from_f32(0.f);
+        }
+        fence_proxy_async_smem();
+      }
+      fence_before();
+      mbar_arrive(&pfull[sb]);
+    }
+    if (ok && wait(&pvdone[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1)) {
+      fence_after();
+      const float inv = 1.f / l;
+      T* out = static_cast<T*>(p.out) +
+               ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) *
+                   D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float o[32];
+        ld32(t_o + lane_base + c0, o);
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 w;
+            w.x = pack2<T>(o[j] * inv, o[j + 1] * inv);
+            w.y = pack2<T>(o[j + 2] * inv, o[j + 3] * inv);
+            w.z = pack2<T>(o[j + 4] * inv, o[j + 5] * inv);
+            w.w = pack2<T>(o[j + 6] * inv, o[j + 7] * inv);
+            *reinterpret_cast<uint4*>(out + c0 + j) = w;
+          }
+        }
+      }
+    }
+  } else if (warp == kProducerWarp) {
+    // ================= TMA copies of chunk c into stage c % 2 =================
+    if (lane == 0) {
+      const int32_t* bt = p.block_tables + (long long)s * p.max_blocks_per_seq;
+      int phys[Sh::kBlocks];
+      auto load_table = [&](int c) {
+#pragma unroll
+        for (int b = 0; b < Sh::kBlocks; ++b) {
+          const int gb = c * Sh::kBlocks + b;
+          phys[b] = gb < nblk ? __ldg(bt + gb) : -1;
+        }
+      };
+      load_table(0);
+      int issued = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunks; ++c) {
+        const int sb = c & 1;
+        if (c >= 2 && !wait(&pvdone[sb], ((c - 2) >> 1) & 1)) {  // S(c-2) and P V(c-2) are done with the stage
+          ok = false;
+          break;
+        }
+        unsigned char* st = smem + Sh::kOffStage + sb * Sh::kStageBytes;
+        int nv = 0;
+        long long tl[Sh::kBlocks];
+#pragma unroll
+        for (int b = 0; b < Sh::kBlocks; ++b) {
+          int ph = phys[b];
+          if (c * Sh::kBlocks + b < nblk) {
+            ++nv;
+            if (ph < 0 || ph >= p.num_blocks) {
+              set_error(p.err, kErrBlockId);
+              ph = 0;
+            }
+          } else {
+            ph = phys[0] < 0 || phys[0] >= p.num_blocks ? 0 : phys[0];  // a block past the keys: any rows do
+          }
+          tl[b] = (long long)ph * p.num_kv_heads + kvh;
+        }
+        mbar_arrive_expect_tx(&full[sb], Sh::kKBytes + nv * Sh::kTile);
+        // K: per 8-dim chunk dc, the rows (16 keys each) of the chunk's 64 keys
+#pragma unroll
+        for (int dc = 0; dc < D / 8; ++dc) {
+          int rw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int b = (16 * q) / BS, h = (16 * q) % BS / 16;
+            rw[q] = static_cast<int>((tl[b] * (D / 8) + dc) * (BS / 16) + h);
+          }
+          tma_gather4_g2s(st + dc * (kKeys * 16), &tmap_k, rw, &full[sb]);
+        }
+        // V: per block and 8-key group, [D][8]
+#pragma unroll
+        for (int b = 0; b < Sh::kBlocks; ++b) {
+          if (c * Sh::kBlocks + b >= nblk) continue;
+#pragma unroll
+          for (int g = 0; g < BS / 8; ++g)  // V rows tl*D .. tl*D+D-1, keys 8g .. 8g+7 of the block
+            tma_2d_g2s(st + Sh::kKBytes + ((b * BS) / 8 + g) * (D * 16), &tmap_v, g * 8, static_cast<int>(tl[b] * D),
+                       &full[sb]);
+        }
+        issued = c + 1;
+        load_table(c + 1);  // lands while this chunk is in flight
+      }
+      if (!ok) {  // the copies of the last two chunks issued may still be landing
+        for (int c = issued - 2; c < issued; ++c)
+          if (c >= 0) mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, kWaitNs / 8);
+      }
+    }
+  } else {
+    // ================= MMA issue: S(c), then O += P V(c - 1) =================
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc<T>(kRows, kKeys), kIdO = idesc<T>(kRows, D);
+      bool ok = true;
+      int last_s = -1, last_pv = -1;  // last groups committed
+      for (int c = 0; c <= nchunks && ok; ++c) {
+        if (c < nchunks) {
+          const int sb = c & 1;
+          ok = wait(&full[sb], (c >> 1) & 1);
+          if (ok && c >= 2) ok = wait(&pvdone[sb], ((c - 2) >> 1) & 1);  // P(c-2) read from S[sb]
+          if (!ok) break;
+          fence_after();
+          const unsigned char* st = smem + Sh::kOffStage + sb * Sh::kStageBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t da = sdesc(smem_addr(sQ) + ks * 256, 128, (D / 8) * 128);
+            const uint64_t db = sdesc(smem_addr(st) + ks * 2 * (kKeys * 16), kKeys * 16, 128);
+            mma(tmem + sb * kKeys, da, db, kIdS, ks > 0);
+          }
+          commit(&sfull[sb]);
+          last_s = c;
+        }
+        if (c >= 1) {
+          const int c1 = c - 1, sb = c1 & 1;
+          if (!(ok = wait(&pfull[sb], (c1 >> 1) & 1))) break;
+          fence_after();
+          const uint32_t sV = smem_addr(smem + Sh::kOffStage + sb * Sh::kStageBytes + Sh::kKBytes);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk) {
+              const uint64_t db = sdesc(sV + kk * 2 * (D * 16), D * 16, 128);
+              mma_ts(t_o, tmem + sb * kKeys + part * 32 + kk * 8, db, kIdO, c1 > 0 || part > 0 || kk > 0);
+            }
+          }
+          commit(&pvdone[sb]);
+          last_pv = c1;
+        }
+      }
+      if (!ok) {  // MMAs committed but maybe not finished: wait (bounded) for the last of each kind
+        if (last_s >= 0) mbar_wait_bounded(&sfull[last_s & 1], (last_s >> 1) & 1, kWaitNs / 8);
+        if (last_pv >= 0) mbar_wait_bounded(&pvdone[last_pv & 1], (last_pv >> 1) & 1, kWaitNs / 8);
+      }
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Sh::kTmemCols));
+  }
+}
+
+}  // namespace ws
+}  // namespace pa
