@@ -110,6 +110,113 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
+// The tile of rank `rank` (0-based) in the order of decreasing length -- the chunks of
+// keys it reads -- ties by sequence, kv head and tile index; so the longest tiles of
+// the whole launch start first and the short ones fill the tail.  Every thread of
+// the CTA takes part (thread t owns sequences t * kPer ..); tile j of sequence s
+// covers rows 128 j .. of its n * G rows and reads chunks 0 .. (ctx + (row_hi - 1) / G) / 64,
+// which is non-decreasing in j, so the tiles of s reading >= x chunks are a suffix
+// in j counted in closed form, and the rank-th tile is found by a binary search on x.
+// Writes (sequence, kv head, tile) to out; returns false when rank is past the tiles.
+__device__ bool pick_tile(const PrefillParams& p, int rank, int* red, int* out) {
+  constexpr int kPer = (kMaxSeqsPerLaunch + kThreads - 1) / kThreads;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.group, Hkv = p.num_kv_heads;
+  int ctx[kPer], rows[kPer], nt[kPer];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int s = tid * kPer + i;
+    ctx[i] = rows[i] = nt[i] = 0;
+    if (s < p.num_seqs) {
+      const int L = __ldg(p.seq_lens + s), a = __ldg(p.query_start_loc + s), b = __ldg(p.query_start_loc + s + 1);
+      const int n = b - a;
+      if (L < 1 || L > p.max_seq_len || a < 0 || b > p.num_query_tokens || n < 0 || n > L) {
+        bad = true;
+      } else {
+        ctx[i] = L - n;
+        rows[i] = n * G;
+        nt[i] = (rows[i] + kRows - 1) / kRows;
+      }
+    }
+  }
+  if (bad && blockIdx.x == 0) set_error(p.err, kErrSeqLen);
+  // tiles of owned sequence i that read >= x chunks
+  auto cnt = [&](int i, int x) -> int {
+    const long long need = (long long)G * (64LL * (x - 1) - ctx[i]) + 1;  // rows the tile must reach
+    if (nt[i] == 0 || need > rows[i]) return 0;
+    if (need <= 1) return nt[i];
+    return nt[i] - static_cast<int>((need + kRows - 1) / kRows - 1);
+  };
+  int buf = 0;
+  auto reduce = [&](int v, bool take_max) -> int {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const int u = __shfl_xor_sync(0xffffffffu, v, o);
+      v = take_max ? max(v, u) : v + u;
+    }
+    buf ^= 1;
+    if (lane == 0) red[buf * 8 + warp] = v;
+    __syncthreads();
+    int t = take_max ? 0 : 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) t = take_max ? max(t, red[buf * 8 + w]) : t + red[buf * 8 + w];
+    return t;
+  };
+  int local = 0, longest = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    local += nt[i];
+    if (nt[i]) longest = max(longest, (ctx[i] + (rows[i] - 1) / G) / 64 + 1);
+  }
+  if ((long long)Hkv * reduce(local, false) <= rank) return false;
+  int lo = 1, hi = reduce(longest, true);  // C(lo) > rank
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    local = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) local += cnt(i, mid);
+    if ((long long)Hkv * reduce(local, false) > rank) lo = mid;
+    else hi = mid - 1;
+  }
+  // rank among the tiles of exactly lo chunks, ordered by (sequence, kv head, tile)
+  local = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) local += cnt(i, lo + 1);
+  const long long r = rank - (long long)Hkv * reduce(local, false);
+  int e[kPer], mine = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    e[i] = cnt(i, lo) - cnt(i, lo + 1);
+    mine += e[i];
+  }
+  int incl = mine;  // inclusive scan over threads (sequence order)
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  buf ^= 1;
+  if (lane == 31) red[buf * 8 + warp] = incl;
+  __syncthreads();
+  long long before = incl - mine;
+  for (int w = 0; w < warp; ++w) before += red[buf * 8 + w];
+  before *= Hkv;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const long long span = (long long)Hkv * e[i];
+    if (r >= before && r < before + span) {
+      const int q = static_cast<int>(r - before);
+      out[0] = tid * kPer + i;
+      out[1] = q / e[i];
+      out[2] = nt[i] - cnt(i, lo) + q % e[i];
+    }
+    before += span;
+  }
+  __syncthreads();
+  return true;
+}
+
 template <typename T, int D, int BS>
 struct Shape {
   static constexpr int kTile = D * BS * 2;                 // one block's K (or V) tile
@@ -120,7 +227,8 @@ struct Shape {
   static constexpr int kOffStage = kQBytes;
   static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
   static constexpr int kNumBars = 8;
-  static constexpr int kSmem = kOffBar + kNumBars * 8 + 32;  // <= 113 KiB: two CTAs per SM
+  static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][8] ints: block reductions
+  static constexpr int kSmem = kOffRed + 2 * 8 * 4;            // <= 113 KiB: two CTAs per SM
   static constexpr int kTmemCols = 256;  // S/P[0]: 0..63, S/P[1]: 64..127, O: 128..128+D
 };
 
@@ -144,30 +252,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   griddep_launch_dependents();
   griddep_wait();
 
-  // ---- which tile (tiles of a sequence are taken last first, so the longest start early)
+  // ---- which tile: the longest first over the whole launch
+  const bool has_tile = pick_tile(p, static_cast<int>(blockIdx.x), reinterpret_cast<int*>(smem + Sh::kOffRed), s_tile);
   if (tid == 0) {
-    const int G = p.group, Hkv = p.num_kv_heads;
-    long long t = blockIdx.x;
-    int found = -1, fk = 0, fj = 0;
-    for (int s = 0; s < p.num_seqs && found < 0; ++s) {
-      const int L = p.seq_lens[s], a = p.query_start_loc[s], b = p.query_start_loc[s + 1];
-      const int n = b - a;
-      if (L < 1 || L > p.max_seq_len || a < 0 || b > p.num_query_tokens || n < 0 || n > L) {
-        if (blockIdx.x == 0) set_error(p.err, kErrSeqLen);
-        continue;
-      }
-      const long long tiles = (long long)((n * G + kRows - 1) / kRows);
-      if (t < tiles * Hkv) {
-        found = s;
-        fk = static_cast<int>(t / tiles);
-        fj = static_cast<int>(tiles - 1 - t % tiles);
-      } else {
-        t -= tiles * Hkv;
-      }
-    }
-    s_tile[0] = found;
-    s_tile[1] = fk;
-    s_tile[2] = fj;
+    if (!has_tile) s_tile[0] = -1;
     *s_abort = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&full[i], 1);
