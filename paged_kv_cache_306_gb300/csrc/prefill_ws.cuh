@@ -7,8 +7,9 @@
 // phases of a chunk run in different warps that hand over through mbarriers, so
 // the copies, the MMAs and the softmax of neighbouring chunks overlap:
 //
-//   * warp 4, one thread: the TMA copies of chunk c into stage c % 2 once P V of
-//     chunk c - 2 has read the stage, through two tensor maps.  K: the pool seen
+//   * warp 4, one thread: the TMA copies of chunk c into stage c % 2, K once S of
+//     chunk c - 2 has read the stage's K and V once P V of chunk c - 2 has read its
+//     V (each on its own mbarrier: S waits only for K), through two tensor maps.  K: the pool seen
 //     as rows of 16 keys x 8 dims (one 256-byte run of a K tile [D/8][bs][8]); one
 //     tile::gather4 load per 8-dim chunk fetches the rows of the chunk's 64 keys
 //     (from up to four blocks anywhere in the pool) and lands them as [64][8]:
@@ -71,6 +72,36 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(id), "r"((uint32_t)accumulate));
+}
+
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait
+__device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2^x by the hardware's approximate exponential (|relative error| below 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // 2-D tensor-map copy global -> shared (box at element coordinates x, y)
@@ -226,7 +257,7 @@ struct Shape {
   static constexpr int kKBytes = kKeys * D * 2;
   static constexpr int kOffStage = kQBytes;
   static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
-  static constexpr int kNumBars = 8;
+  static constexpr int kNumBars = 10;
   static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][8] ints: block reductions
   static constexpr int kSmem = kOffRed + 2 * 8 * 4;            // <= 113 KiB: two CTAs per SM
   static constexpr int kTmemCols = 256;  // S/P[0]: 0..63, S/P[1]: 64..127, O: 128..128+D
@@ -240,10 +271,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* sQ = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);
-  uint64_t* full = bars;        // [2] stage landed (TMA bytes)
-  uint64_t* sfull = bars + 2;   // [2] S in TMEM (commit)
-  uint64_t* pfull = bars + 4;   // [2] P in TMEM, O rescaled and V tail zeroed where needed (128 arrivals)
-  uint64_t* pvdone = bars + 6;  // [2] P V done: P's columns, the stage and O are free (commit)
+  uint64_t* fullk = bars;       // [2] the stage's K landed (TMA bytes)
+  uint64_t* fullv = bars + 2;   // [2] the stage's V landed (TMA bytes)
+  uint64_t* sfull = bars + 4;   // [2] S in TMEM, the stage's K read (commit)
+  uint64_t* pfull = bars + 6;   // [2] P in TMEM, O rescaled and V tail zeroed where needed (128 arrivals)
+  uint64_t* pvdone = bars + 8;  // [2] P V done: P's columns, the stage's V and O are free (commit)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
   int* s_tile = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, tile (or -1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tile + 3);  // a thread gave up
@@ -258,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!has_tile) s_tile[0] = -1;
     *s_abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&fullk[i], 1);
+      mbar_init(&fullv[i], 1);
       mbar_init(&sfull[i], 1);
       mbar_init(&pfull[i], kSoftmaxThreads);
       mbar_init(&pvdone[i], 1);
@@ -319,15 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       fence_after();
       const uint32_t t_s = tmem + lane_base + sb * kKeys;
       float sv[kKeys];
-      {
-        float a[32];
-        ld32(t_s, a);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = a[j];
-        ld32(t_s + 32, a);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 + j] = a[j];
-      }
+      ld64(t_s, sv);
       const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
       float mx = -INFINITY;
       if (lim >= kKeys - 1) {
@@ -372,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float ps = 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float x0 = exp2f(sv[2 * j] - m), x1 = exp2f(sv[2 * j + 1] - m);
+          const float x0 = ex2(sv[2 * j] - m), x1 = ex2(sv[2 * j + 1] - m);
           ps += x0 + x1;
           const uint32_t h = pack2<T>(x0, x1);
           const float2 back = unpack2<T>(h);
@@ -385,6 +410,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as zero
       if (c == nchunks - 1 && kz < (c + 1) * kKeys) {
+        if (!wait(&fullv[sb], (c >> 1) & 1)) {
+          ok = false;
+          break;
+        }
         unsigned char* vbase = smem + Sh::kOffStage + sb * Sh::kStageBytes + Sh::kKBytes;
         const int k0 = kz - c * kKeys, cnt = (kKeys - k0) * D;
         for (int i = tid; i < cnt; i += kSoftmaxThreads) {
@@ -432,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       };
       load_table(0);
-      int issued = 0;
+      int issued_k = 0, issued_v = 0;
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
         const int sb = c & 1;
-        if (c >= 2 && !wait(&pvdone[sb], ((c - 2) >> 1) & 1)) {  // S(c-2) and P V(c-2) are done with the stage
+        if (c >= 2 && !wait(&sfull[sb], ((c - 2) >> 1) & 1)) {  // S(c-2) is done with the stage's K
           ok = false;
           break;
         }
@@ -457,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           tl[b] = (long long)ph * p.num_kv_heads + kvh;
         }
-        mbar_arrive_expect_tx(&full[sb], Sh::kKBytes + nv * Sh::kTile);
+        mbar_arrive_expect_tx(&fullk[sb], Sh::kKBytes);
         // K: per 8-dim chunk dc, the rows (16 keys each) of the chunk's 64 keys
 #pragma unroll
         for (int dc = 0; dc < D / 8; ++dc) {
@@ -467,8 +496,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int b = (16 * q) / BS, h = (16 * q) % BS / 16;
             rw[q] = static_cast<int>((tl[b] * (D / 8) + dc) * (BS / 16) + h);
           }
-          tma_gather4_g2s(st + dc * (kKeys * 16), &tmap_k, rw, &full[sb]);
+          tma_gather4_g2s(st + dc * (kKeys * 16), &tmap_k, rw, &fullk[sb]);
         }
+        issued_k = c + 1;
+        if (c >= 2 && !wait(&pvdone[sb], ((c - 2) >> 1) & 1)) {  // P V(c-2) is done with the stage's V
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&fullv[sb], nv * Sh::kTile);
         // V: per block and 8-key group, [D][8]
 #pragma unroll
         for (int b = 0; b < Sh::kBlocks; ++b) {
@@ -476,14 +511,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int g = 0; g < BS / 8; ++g)  // V rows tl*D .. tl*D+D-1, keys 8g .. 8g+7 of the block
             tma_2d_g2s(st + Sh::kKBytes + ((b * BS) / 8 + g) * (D * 16), &tmap_v, g * 8, static_cast<int>(tl[b] * D),
-                       &full[sb]);
+                       &fullv[sb]);
         }
-        issued = c + 1;
+        issued_v = c + 1;
         load_table(c + 1);  // lands while this chunk is in flight
       }
       if (!ok) {  // the copies of the last two chunks issued may still be landing
-        for (int c = issued - 2; c < issued; ++c)
-          if (c >= 0) mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, kWaitNs / 8);
+        for (int c = issued_k - 2; c < issued_k; ++c)
+          if (c >= 0) mbar_wait_bounded(&fullk[c & 1], (c >> 1) & 1, kWaitNs / 8);
+        for (int c = issued_v - 2; c < issued_v; ++c)
+          if (c >= 0) mbar_wait_bounded(&fullv[c & 1], (c >> 1) & 1, kWaitNs / 8);
       }
     }
   } else {
@@ -495,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int c = 0; c <= nchunks && ok; ++c) {
         if (c < nchunks) {
           const int sb = c & 1;
-          ok = wait(&full[sb], (c >> 1) & 1);
+          ok = wait(&fullk[sb], (c >> 1) & 1);
           if (ok && c >= 2) ok = wait(&pvdone[sb], ((c - 2) >> 1) & 1);  // P(c-2) read from S[sb]
           if (!ok) break;
           fence_after();
@@ -511,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (c >= 1) {
           const int c1 = c - 1, sb = c1 & 1;
-          if (!(ok = wait(&pfull[sb], (c1 >> 1) & 1))) break;
+          if (!(ok = wait(&pfull[sb], (c1 >> 1) & 1) && wait(&fullv[sb], (c1 >> 1) & 1))) break;
           fence_after();
           const uint32_t sV = smem_addr(smem + Sh::kOffStage + sb * Sh::kStageBytes + Sh::kKBytes);
 #pragma unroll
