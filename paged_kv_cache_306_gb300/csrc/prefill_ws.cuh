@@ -7,9 +7,10 @@
 // phases of a chunk run in different warps that hand over through mbarriers, so
 // the copies, the MMAs and the softmax of neighbouring chunks overlap:
 //
-//   * warp 4, one thread: the TMA copies of chunk c into stage c % 2, K once S of
-//     chunk c - 2 has read the stage's K and V once P V of chunk c - 2 has read its
-//     V (each on its own mbarrier: S waits only for K), through two tensor maps.  K: the pool seen
+//   * warp 4, one thread: the TMA copies of chunk c, through two tensor maps: K
+//     into K buffer c % 2 once S of chunk c - 2 has read it, V into V buffer c % 3
+//     once P V of chunk c - 3 has read it (V is needed last), each on its own
+//     mbarrier, so S waits only for K and the V copies are well ahead.  K: the pool seen
 //     as rows of 16 keys x 8 dims (one 256-byte run of a K tile [D/8][bs][8]); one
 //     tile::gather4 load per 8-dim chunk fetches the rows of the chunk's 64 keys
 //     (from up to four blocks anywhere in the pool) and lands them as [64][8]:
@@ -60,6 +61,7 @@ constexpr int kKeys = 64;   // keys per chunk
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
+constexpr int kVStages = 3;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -253,11 +255,12 @@ struct Shape {
   static constexpr int kTile = D * BS * 2;                 // one block's K (or V) tile
   static constexpr int kBlocks = kKeys / BS;               // blocks per chunk
   static constexpr int kQBytes = kRows * D * 2;            // Q, core-matrix layout
-  static constexpr int kStageBytes = 2 * kKeys * D * 2;    // K as [D/8][64][8], then V as [key/8][D][8]
-  static constexpr int kKBytes = kKeys * D * 2;
-  static constexpr int kOffStage = kQBytes;
-  static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
-  static constexpr int kNumBars = 10;
+  static constexpr int kKBytes = kKeys * D * 2;  // a chunk's K as [D/8][64][8]
+  static constexpr int kVBytes = kKeys * D * 2;  // a chunk's V as [key/8][D][8]
+  static constexpr int kOffK = kQBytes;          // K ring: 2 buffers
+  static constexpr int kOffV = kOffK + 2 * kKBytes;  // V ring: 3 buffers (V is read last)
+  static constexpr int kOffBar = kOffV + kVStages * kVBytes;
+  static constexpr int kNumBars = 2 + kVStages + 2 + 2 + 2 + kVStages;
   static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][8] ints: block reductions
   static constexpr int kSmem = kOffRed + 2 * 8 * 4;            // <= 113 KiB: two CTAs per SM
   static constexpr int kTmemCols = 256;  // S/P[0]: 0..63, S/P[1]: 64..127, O: 128..128+D
@@ -271,11 +274,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* sQ = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);
-  uint64_t* fullk = bars;       // [2] the stage's K landed (TMA bytes)
-  uint64_t* fullv = bars + 2;   // [2] the stage's V landed (TMA bytes)
-  uint64_t* sfull = bars + 4;   // [2] S in TMEM, the stage's K read (commit)
-  uint64_t* pfull = bars + 6;   // [2] P in TMEM, O rescaled and V tail zeroed where needed (128 arrivals)
-  uint64_t* pvdone = bars + 8;  // [2] P V done: P's columns, the stage's V and O are free (commit)
+  uint64_t* fullk = bars;                   // [2] K buffer landed (TMA bytes)
+  uint64_t* fullv = fullk + 2;              // [kVStages] V buffer landed (TMA bytes)
+  uint64_t* sfull = fullv + kVStages;       // [2] S in TMEM, the K buffer read (commit)
+  uint64_t* pfull = sfull + 2;              // [2] P in TMEM, O rescaled and V tail zeroed where needed (128 arrivals)
+  uint64_t* pvdone = pfull + 2;             // [2] P V done: P's columns and O are free (commit)
+  uint64_t* vfree = pvdone + 2;             // [kVStages] P V done with the V buffer (commit)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
   int* s_tile = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, tile (or -1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tile + 3);  // a thread gave up
@@ -291,10 +295,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     *s_abort = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&fullk[i], 1);
-      mbar_init(&fullv[i], 1);
       mbar_init(&sfull[i], 1);
       mbar_init(&pfull[i], kSoftmaxThreads);
       mbar_init(&pvdone[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&fullv[i], 1);
+      mbar_init(&vfree[i], 1);
     }
     fence_barrier_init();
   }
@@ -410,11 +417,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as zero
       if (c == nchunks - 1 && kz < (c + 1) * kKeys) {
-        if (!wait(&fullv[sb], (c >> 1) & 1)) {
+        if (!wait(&fullv[c % kVStages], (c / kVStages) & 1)) {
           ok = false;
           break;
         }
-        unsigned char* vbase = smem + Sh::kOffStage + sb * Sh::kStageBytes + Sh::kKBytes;
+        unsigned char* vbase = smem + Sh::kOffV + (c % kVStages) * Sh::kVBytes;
         const int k0 = kz - c * kKeys, cnt = (kKeys - k0) * D;
         for (int i = tid; i < cnt; i += kSoftmaxThreads) {
           const int kk = k0 + i / D, d = i % D;
@@ -469,7 +476,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           ok = false;
           break;
         }
-        unsigned char* st = smem + Sh::kOffStage + sb * Sh::kStageBytes;
+        unsigned char* sk = smem + Sh::kOffK + sb * Sh::kKBytes;
+        const int vb = c % kVStages;
+        unsigned char* sv_ = smem + Sh::kOffV + vb * Sh::kVBytes;
         int nv = 0;
         long long tl[Sh::kBlocks];
 #pragma unroll
@@ -496,22 +505,22 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int b = (16 * q) / BS, h = (16 * q) % BS / 16;
             rw[q] = static_cast<int>((tl[b] * (D / 8) + dc) * (BS / 16) + h);
           }
-          tma_gather4_g2s(st + dc * (kKeys * 16), &tmap_k, rw, &fullk[sb]);
+          tma_gather4_g2s(sk + dc * (kKeys * 16), &tmap_k, rw, &fullk[sb]);
         }
         issued_k = c + 1;
-        if (c >= 2 && !wait(&pvdone[sb], ((c - 2) >> 1) & 1)) {  // P V(c-2) is done with the stage's V
+        if (c >= kVStages && !wait(&vfree[vb], ((c - kVStages) / kVStages) & 1)) {  // P V(c-3) read the buffer
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&fullv[sb], nv * Sh::kTile);
+        mbar_arrive_expect_tx(&fullv[vb], nv * Sh::kTile);
         // V: per block and 8-key group, [D][8]
 #pragma unroll
         for (int b = 0; b < Sh::kBlocks; ++b) {
           if (c * Sh::kBlocks + b >= nblk) continue;
 #pragma unroll
           for (int g = 0; g < BS / 8; ++g)  // V rows tl*D .. tl*D+D-1, keys 8g .. 8g+7 of the block
-            tma_2d_g2s(st + Sh::kKBytes + ((b * BS) / 8 + g) * (D * 16), &tmap_v, g * 8, static_cast<int>(tl[b] * D),
-                       &fullv[sb]);
+            tma_2d_g2s(sv_ + ((b * BS) / 8 + g) * (D * 16), &tmap_v, g * 8, static_cast<int>(tl[b] * D),
+                       &fullv[vb]);
         }
         issued_v = c + 1;
         load_table(c + 1);  // lands while this chunk is in flight
@@ -519,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!ok) {  // the copies of the last two chunks issued may still be landing
         for (int c = issued_k - 2; c < issued_k; ++c)
           if (c >= 0) mbar_wait_bounded(&fullk[c & 1], (c >> 1) & 1, kWaitNs / 8);
-        for (int c = issued_v - 2; c < issued_v; ++c)
-          if (c >= 0) mbar_wait_bounded(&fullv[c & 1], (c >> 1) & 1, kWaitNs / 8);
+        for (int c = issued_v - kVStages; c < issued_v; ++c)
+          if (c >= 0) mbar_wait_bounded(&fullv[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
       }
     }
   } else {
@@ -536,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (ok && c >= 2) ok = wait(&pvdone[sb], ((c - 2) >> 1) & 1);  // P(c-2) read from S[sb]
           if (!ok) break;
           fence_after();
-          const unsigned char* st = smem + Sh::kOffStage + sb * Sh::kStageBytes;
+          const unsigned char* st = smem + Sh::kOffK + sb * Sh::kKBytes;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint64_t da = sdesc(smem_addr(sQ) + ks * 256, 128, (D / 8) * 128);
@@ -548,9 +557,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (c >= 1) {
           const int c1 = c - 1, sb = c1 & 1;
-          if (!(ok = wait(&pfull[sb], (c1 >> 1) & 1) && wait(&fullv[sb], (c1 >> 1) & 1))) break;
+          const int vb = c1 % kVStages;
+          if (!(ok = wait(&pfull[sb], (c1 >> 1) & 1) && wait(&fullv[vb], (c1 / kVStages) & 1))) break;
           fence_after();
-          const uint32_t sV = smem_addr(smem + Sh::kOffStage + sb * Sh::kStageBytes + Sh::kKBytes);
+          const uint32_t sV = smem_addr(smem + Sh::kOffV + vb * Sh::kVBytes);
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -560,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
           }
           commit(&pvdone[sb]);
+          commit(&vfree[vb]);
           last_pv = c1;
         }
       }
