@@ -361,19 +361,20 @@ __global__ void __launch_bounds__(kThreads, 2)
       float sv[kKeys];
       ld64(t_s, sv);
       const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
-      float mx = -INFINITY;
-      if (lim >= kKeys - 1) {
+      if (lim < kKeys - 1) {           // the diagonal chunk (or past it): hide the later keys
 #pragma unroll
-        for (int j = 0; j < kKeys; ++j) {
-          sv[j] *= sl2;
-          mx = fmaxf(mx, sv[j]);
-        }
-      } else {
+        for (int j = 0; j < kKeys; ++j)
+          if (j > lim) sv[j] = -INFINITY;
+      }
+      // the row maximum of the raw scores, as a tree (scale > 0 keeps the order)
+      float mx;
+      {
+        float t[8];
 #pragma unroll
-        for (int j = 0; j < kKeys; ++j) {
-          sv[j] = j <= lim ? sv[j] * sl2 : -INFINITY;
-          mx = fmaxf(mx, sv[j]);
-        }
+        for (int i = 0; i < 8; ++i) t[i] = sv[i];
+#pragma unroll
+        for (int j = 8; j < kKeys; ++j) t[j & 7] = fmaxf(t[j & 7], sv[j]);
+        mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7]))) * sl2;
       }
       float corr = 1.f;
       const bool move = mx > m + 8.f;
@@ -401,11 +402,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       // P into the row's S columns: high parts in 0..31, low parts in 32..63
       {
         float hi[32], lo[32];
-        float ps = 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x0 = ex2(sv[2 * j] - m), x1 = ex2(sv[2 * j + 1] - m);
-          ps += x0 + x1;
+        for (int j = 0; j < 32; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
+          const float x0 = ex2(fmaf(sv[2 * j], sl2, -m)), x1 = ex2(fmaf(sv[2 * j + 1], sl2, -m));
+          ps[j & 3] += x0 + x1;
           const uint32_t h = pack2<T>(x0, x1);
           const float2 back = unpack2<T>(h);
           hi[j] = __uint_as_float(h);
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         st32(t_s, hi);
         st32(t_s + 32, lo);
-        l += ps;
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       }
       // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as zero
       if (c == nchunks - 1 && kz < (c + 1) * kKeys) {
