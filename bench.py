@@ -331,7 +331,7 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     # DRAM-level bytes: a physical block shared by several sequences is read once
     rbytes = decode_bytes(wl, unique=True) + (write_bytes(wl) if fused else 0)
     achieved = rbytes / (dec_ms * 1e-3) / 1e9
-    traffic = load_traffic(wl)
+    traffic = load_traffic(wl, fused)
     cfgd = describe(wl, cfg)
     cfgd.update({"partition_size": int(resolved), "pool_copies_rotated": copies,
                  "step": ("fused: one pa_decode_step call (block copies, new tokens and decode in the decode "
@@ -433,11 +433,12 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws, fused):
             "d2h_bytes_per_step": int(d2h), "copies_per_step": 2}
 
 
-def load_traffic(wl):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
-    on the current kernel source; otherwise null."""
+def load_traffic(wl, fused):
+    """DRAM bytes per timed call from the committed ncu summary, if it was taken on the
+    current kernel source and on the same call (the fused step for 16-bit and fp32
+    pools, pa_decode_scaled for FP8 pools); otherwise null."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or fused != (wl.dtype != "fp8"):
         return None
     try:
         import hashlib
@@ -631,7 +632,7 @@ def run_prefill(args, world_size, rank, local_rank):
             "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfg,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_tc_kernel",
+                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_ws_kernel",
                          "flops_per_launch": int(flops), "launch_us": round(pre_ms * 1e3, 2),
                          "peak_source": f"{kind} bf16_tflops (fp16 runs at the bf16 rate)"},
             "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",

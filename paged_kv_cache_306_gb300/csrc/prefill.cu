@@ -9,52 +9,21 @@
 //     out = softmax(scale * q K^T) V
 // over K, V gathered through the block table, as decode does for one token.
 //
-// The kernel is in prefill_tc.cuh (tcgen05 MMAs with accumulators in tensor
-// memory); this file holds its host-side launch and dispatch.  A warp-level
-// version (mma.sync m16n8k16, one warp per 16 query rows, the same TMA ring as
-// decode) was built first and measured 154 TFLOP/s on the Qwen-shaped chunked
-// prefill; the tcgen05 kernel replaced it.
+// The kernel is in prefill_ws.cuh (tcgen05 MMAs with accumulators in tensor
+// memory, warp-specialised); this file holds its host-side launch: the two
+// tensor maps its TMA copies read the pools through, and the dispatch over
+// dtype, head size and block size.
 #include <math.h>
 
 #include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
-#include "prefill_tc.cuh"
 #include "prefill_ws.cuh"
 
 namespace pa {
 
 // ---- host side ------------------------------------------------------------------------------
-
-// The tcgen05 kernel (prefill_tc.cuh): one CTA per tile of 128 query rows, two per SM.
-template <typename T, int D, int BS>
-cudaError_t launch_prefill_tc_t(const PrefillParams& p, cudaStream_t stream, int* launches) {
-  using Sh = tc::Shape<T, D, BS>;
-  *launches = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  static unsigned done = 0;
-  if (dev >= 32 || !(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & (1u << dev))) {
-    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&tc::prefill_tc_kernel<T, D, BS>),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
-    if (e != cudaSuccess) return e;
-    // all of the SM's unified memory as shared memory: two CTAs of ~113 KiB each
-    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&tc::prefill_tc_kernel<T, D, BS>),
-                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    if (dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
-  }
-  // at most Hkv * (T G / 128 + S) tiles; CTAs past the real ones exit at once
-  const long long tiles = (long long)p.num_kv_heads *
-                          (((long long)p.num_query_tokens * p.group + tc::kRows - 1) / tc::kRows + p.num_seqs);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  e = launch_pdl(tc::prefill_tc_kernel<T, D, BS>, dim3(static_cast<unsigned>(tiles)), dim3(tc::kThreads), Sh::kSmem,
-                 stream, p);
-  if (e == cudaSuccess) *launches = 1;
-  return e;
-}
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link-time libcuda)
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -1,7 +1,8 @@
 // prefill_ws.cuh -- chunked prefill on tcgen05 with warp specialisation.
 //
-// The same computation as prefill_tc.cuh (causal attention of each sequence's
-// chunk of new query tokens over its paged cache; see prefill.cu).  A CTA owns a
+// Causal attention of each sequence's chunk of new query tokens over its paged
+// cache (what is computed: see prefill.cu), on sm_103a's tcgen05 MMAs with the
+// accumulators in tensor memory (TMEM).  A CTA owns a
 // tile of 128 query rows -- (token, query head) pairs of one kv head, head
 // fastest -- which are TMEM lanes 0..127, and takes keys 64 at a time.  The
 // phases of a chunk run in different warps that hand over through mbarriers, so
@@ -42,7 +43,7 @@
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
-#include "prefill_tc.cuh"
+#include "tc_ops.cuh"
 
 namespace pa {
 namespace ws {
