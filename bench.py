@@ -455,23 +455,34 @@ def load_traffic(wl, fused):
 # --- the CPU oracle (reference arm and cpu_baseline) ------------------------------------------
 
 def cpu_baseline(wl, seconds=12.0):
-    """The oracle on the host cores over a bounded sample: whole sequences, all heads."""
+    """The oracle on the host cores over a bounded sample: whole sequences, all heads.
+    Also a shorter single-thread pass over the same sequences, for the ratio."""
     import oracle
     # the oracle sees the pool after the step's write (as the GPU does)
     k, v = oracle_pools_after_write(wl)
-    done, nbytes, t0 = 0, 0, time.perf_counter()
     order = np.argsort(wl.seq_lens)             # shortest first keeps the sample bounded
     e = W.ELEM_BYTES[wl.dtype]
-    while time.perf_counter() - t0 < seconds and done < wl.num_seqs:
-        s = int(order[done])
-        sub = W.subset(wl, [s])
-        oracle_decode(wl, sub.q, k, v, sub)
-        nbytes += int(wl.seq_lens[s]) * wl.num_kv_heads * wl.head_size * e * 2
-        done += 1
-    dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": f"{done} of {wl.num_seqs} sequences (shortest first), all heads, "
-                                        f"{dt:.1f} s, fp64 C oracle"}
+
+    def run(budget):
+        done, nbytes, t0 = 0, 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget and done < wl.num_seqs:
+            s = int(order[done])
+            sub = W.subset(wl, [s])
+            oracle_decode(wl, sub.q, k, v, sub)
+            nbytes += int(wl.seq_lens[s]) * wl.num_kv_heads * wl.head_size * e * 2
+            done += 1
+        return done, nbytes, time.perf_counter() - t0
+
+    cores = oracle.num_threads()
+    done, nbytes, dt = run(seconds)
+    oracle.set_num_threads(1)
+    done1, nbytes1, dt1 = run(seconds / 4)
+    oracle.set_num_threads(cores)
+    all_core, one_core = nbytes / dt / 1e9, nbytes1 / dt1 / 1e9
+    return {"value": round(all_core, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_core_value": round(one_core, 4), "all_vs_single": round(all_core / one_core, 2),
+            "sample": f"{done} of {wl.num_seqs} sequences (shortest first), all heads, {dt:.1f} s on {cores} "
+                      f"threads; single thread: {done1} sequences, {dt1:.1f} s; fp64 C oracle"}
 
 
 def run_reference(args, wl, cfg, world_size, rank):

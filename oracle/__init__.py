@@ -57,6 +57,8 @@ def _load():
                   lib.oracle_decode_scaled, lib.oracle_reshape_and_cache_scaled, lib.oracle_encode_e4m3,
                   lib.oracle_prefill):
             f.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [i32]
+        lib.oracle_set_num_threads.restype = None
         lib.oracle_elem_bytes.argtypes = [i32]
         lib.oracle_pack_x.argtypes = [i32]
         _lib = lib
@@ -82,6 +84,11 @@ def _code(dtype):
 
 def num_threads():
     return _load().oracle_num_threads()
+
+
+def set_num_threads(n):
+    """Threads the oracle's parallel loops use from now on."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def pack_x(dtype):

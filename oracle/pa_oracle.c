@@ -148,6 +148,15 @@ static int64_t v_index(int64_t b, int h, int d, int t, int Hkv, int D, int bs) {
 int oracle_elem_bytes(int dtype) { return elem_bytes(dtype); }
 int oracle_pack_x(int dtype) { return elem_bytes(dtype) ? pack_x(dtype) : 0; }
 
+/* Threads the parallel loops use from now on (n >= 1); for timing one core against all. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
