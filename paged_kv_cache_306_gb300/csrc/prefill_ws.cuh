@@ -353,7 +353,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
       const int sb = c & 1;
-      if (!wait(&sfull[sb], (c >> 1) & 1)) {
+      // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them
+      // is taken by the whole warp, so each wait's outcome is agreed across the warp
+      if (!__all_sync(0xffffffffu, wait(&sfull[sb], (c >> 1) & 1))) {
         ok = false;
         break;
       }
@@ -385,18 +387,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         l *= corr;
       }
       // O holds P V up to chunk c - 1 once that group is done: rescale the row if the maximum moved
-      if (c > 0 && move && corr != 1.f) {
-        if (!wait(&pvdone[(c - 1) & 1], ((c - 1) >> 1) & 1)) {
+      // (the whole warp takes the branch when one of its rows needs it; the others scale by 1)
+      const bool rescale = c > 0 && move && corr != 1.f;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!__all_sync(0xffffffffu, wait(&pvdone[(c - 1) & 1], ((c - 1) >> 1) & 1))) {
           ok = false;
           break;
         }
         fence_after();
+        const float f = rescale ? corr : 1.f;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
           ld32(t_o + lane_base + c0, o);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] *= corr;
+          for (int j = 0; j < 32; ++j) o[j] *= f;
           st32(t_o + lane_base + c0, o);
         }
       }
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as zero
       if (c == nchunks - 1 && kz < (c + 1) * kKeys) {
-        if (!wait(&fullv[c % kVStages], (c / kVStages) & 1)) {
+        if (!__all_sync(0xffffffffu, wait(&fullv[c % kVStages], (c / kVStages) & 1))) {
           ok = false;
           break;
         }
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       fence_before();
       mbar_arrive(&pfull[sb]);
     }
-    if (ok && wait(&pvdone[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1)) {
+    if (__all_sync(0xffffffffu, ok && wait(&pvdone[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1))) {
       fence_after();
       const float inv = 1.f / l;
       T* out = static_cast<T*>(p.out) +

@@ -111,3 +111,57 @@ def test_full_size_chunked_prefill_sampled():
     ref = oracle.prefill(np.ascontiguousarray(wl.q[rows]), k, v, wl.block_tables[keep], wl.seq_lens[keep],
                          sub_qsl.astype(np.int32), wl.scale, wl.dtype)
     assert_close(as_f64(out)[rows], ref, "f16", with_rounding=False, what="full-size prefill")
+
+
+def ramp_scores(wl):
+    """Keys t/8 and queries 8 along dim 0 (all else 0), so the score of key t is t:
+    every 64-key chunk raises the row maximum by more than 2^8 after scaling, and
+    the running maximum moves (O is rescaled in tensor memory) at every chunk."""
+    bs, D = wl.block_size, wl.head_size
+    k32 = np.zeros(wl.k_cache.shape, np.float32)
+    ctx = wl.meta["context_lens"]
+    for s, c in enumerate(ctx):
+        for t in range(c):
+            k32[int(wl.block_tables[s][t // bs]), :, 0, t % bs, 0] = t / 8.0
+    keep = wl.k_cache.copy()  # poisoned slots stay poisoned
+    kc = W.cast(k32, wl.dtype)
+    for s, c in enumerate(ctx):  # only the context slots take the ramp
+        for t in range(c):
+            blk, off = int(wl.block_tables[s][t // bs]), t % bs
+            keep[blk, :, :, off, :] = kc[blk, :, :, off, :]
+    wl.k_cache = keep
+    q = np.zeros((wl.q.shape[0], wl.num_heads, D), np.float32)
+    q[:, :, 0] = 8.0
+    wl.q = W.cast(q, wl.dtype)
+    key = np.zeros((wl.key.shape[0], wl.num_kv_heads, D), np.float32)
+    for s, c in enumerate(ctx):
+        for i in range(int(wl.query_start_loc[s + 1] - wl.query_start_loc[s])):
+            key[int(wl.query_start_loc[s]) + i, :, 0] = (c + i) / 8.0
+    wl.key = W.cast(key, wl.dtype)
+    return wl
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,G", [(128, 7), (64, 4)])
+def test_running_maximum_moving_every_chunk(dtype, D, G):
+    wl = W.make_prefill("ramp", dtype, [0, 300, 1000], [200, 70, 129], 2 * G, 2, D, 16, seed=41)
+    ramp_scores(wl)
+    out, _ = run_prefill(wl)
+    assert_close(as_f64(out), oracle_prefill(wl), dtype, with_rounding=True, what=f"{dtype} D{D} G{G}")
+
+
+def test_more_sequences_than_one_launch_holds():
+    rng = np.random.default_rng(43)
+    ctx, qn = rng.integers(0, 40, size=1100), rng.integers(1, 6, size=1100)
+    wl = W.make_prefill("many", "f16", ctx, qn, 8, 2, 64, 16, seed=44)
+    out, _ = run_prefill(wl)
+    assert_close(as_f64(out), oracle_prefill(wl), "f16", with_rounding=True)
+
+
+def test_sequences_with_no_new_tokens_are_skipped():
+    """A sequence whose chunk is empty has no query rows and no tiles; the others are
+    unaffected (the tile order is computed over all sequences)."""
+    wl = W.make_prefill("empty", "bf16", [50, 0, 700, 33, 10], [0, 90, 0, 17, 1], 8, 2, 128, 32, seed=45)
+    assert wl.q.shape[0] == 108
+    out, _ = run_prefill(wl)
+    assert_close(as_f64(out), oracle_prefill(wl), "bf16", with_rounding=True)
