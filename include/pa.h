@@ -270,7 +270,8 @@ PA_API uint64_t pa_launch_count(void);
  *
  * No workspace.  A sequence whose length lies outside [1, max_seq_len] or whose
  * chunk is longer than itself is recorded as PA_DEVERR_SEQ_LEN and its rows of
- * out are unspecified.  Asynchronous on `stream`.
+ * out are unspecified.  num_blocks * num_kv_heads * head_size must stay below
+ * 2^31 (PA_ERR_UNSUPPORTED otherwise).  Asynchronous on `stream`.
  */
 PA_API pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,

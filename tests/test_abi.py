@@ -193,6 +193,9 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert pf(H=6, Hkv=4) == B.PA_ERR_INVALID_ARG
     assert pf(q=8200) == B.PA_ERR_ALIGNMENT
     assert pf(T=0) == B.PA_OK and pf(S=0) == B.PA_OK
+    big = lib.pa_prefill(P(8192), P(8192), P(8192), P(8192), P(8192), 4, P(8192), P(8192), 2, 8, 64, 8, 2, 128, 16,
+                         1 << 24, 0.1, B.PA_F16, None)
+    assert big == B.PA_ERR_UNSUPPORTED     # 2^24 blocks x 2 kv heads x 128 dims: past the tensor maps' rows
 
 
 def test_fused_step_rejects_bad_arguments_on_the_host(lib):
