@@ -98,3 +98,31 @@ def test_prefill_flops_count_every_key_each_query_row_sees():
     wl = W.make_prefill("f", "f16", [0, 5, 40], [3, 17, 1], 8, 2, 64, 16, seed=1, poison=False)
     keys = sum(c + i + 1 for c, n in zip([0, 5, 40], [3, 17, 1]) for i in range(n))
     assert bench.prefill_flops(wl) == 4 * 64 * 8 * keys
+
+
+def test_fused_step_is_the_default_except_for_fp8_pools():
+    import argparse
+    fused = argparse.Namespace(step="fused")
+    separate = argparse.Namespace(step="separate")
+    assert bench.uses_fused_step(fused, W.config(1, poison=False))
+    assert not bench.uses_fused_step(separate, W.config(1, poison=False))
+    wl8 = W.make_private("fp8", "fp8", [20, 40], 8, 2, 128, 16, seed=1, q_dtype="f16")
+    assert not bench.uses_fused_step(fused, wl8)
+    # the ncu traffic in profiles/ was taken on the fused call; a separate step reports none
+    wl = W.config(1, poison=False)
+    assert bench.load_traffic(wl, False) is None
+
+
+def test_write_bytes_count_tokens_and_copies():
+    wl = W.config(5, poison=False, block_size=16)
+    e = 2
+    tok = wl.num_seqs * wl.num_kv_heads * wl.head_size * (e + e) * 2 + wl.num_seqs * 8
+    blk = wl.num_kv_heads * wl.head_size * wl.block_size * e * 2
+    assert bench.write_bytes(wl) == tok + len(wl.cow) * (2 * blk + 16)
+
+
+def test_cpu_baseline_reports_all_threads_and_one():
+    wl = W.config(1, poison=False)
+    cb = bench.cpu_baseline(wl, seconds=0.5)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["single_core_value"] > 0
+    assert cb["cores"] >= 1 and cb["all_vs_single"] > 0
