@@ -308,7 +308,7 @@ def test_slot_mapping_round_trip(dtype):
     key = rng.standard_normal((T, Hkv, D)).astype(st)
     val = rng.standard_normal((T, Hkv, D)).astype(st)
     slots = rng.permutation(NB * bs)[:T].astype(np.int64)
-    slots[3] = -1                                       # a padding token is skipped
+    slots[3] = slots[T - 1] = -1                        # padding tokens are skipped (one after every real one)
     oracle.reshape_and_cache(key, val, k, v, slots, dtype)
     Kl, Vl = logical_from_pools(k, v)
     K0, V0 = logical_from_pools(k0, v0)
