@@ -223,8 +223,8 @@ PA_API pa_status pa_decode_scaled(void* out, const void* q, const void* k_cache,
  *             pa_copy_blocks; the copies complete before any token is written
  * everything else as in pa_decode, with the same workspace size.
  *
- * dtype is PA_F32, PA_F16 or PA_BF16 (an FP8 cache is written by
- * pa_reshape_and_cache_scaled, not here).  No two sequences of the call may
+ * dtype is PA_F32, PA_F16 or PA_BF16; an FP8 cache takes pa_decode_step_scaled
+ * below.  No two sequences of the call may
  * write the same slot, and no sequence may read a slot another one writes
  * (the block manager's copy-on-write guarantees both).
  *
@@ -240,6 +240,25 @@ PA_API pa_status pa_decode_step(void* out, const void* q, const void* key, const
                                 int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
                                 int block_size, int64_t num_blocks, float scale, int partition_size,
                                 void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_decode_step over a cache whose dtype differs from the query's: with
+ * cache_dtype PA_FP8_E4M3 and q_dtype PA_F16 or PA_BF16, key and value come in
+ * q_dtype and are stored as pa_reshape_and_cache_scaled stores them (the E4M3
+ * code of x / k_scale, x / v_scale), then decode reads the pool as
+ * pa_decode_scaled does.  Equal, byte for byte in the pools and bit for bit in
+ * out, to pa_copy_blocks + pa_reshape_and_cache_scaled + pa_decode_scaled.  For
+ * any other cache_dtype, q_dtype must equal it and both scales be 1 (then it is
+ * pa_decode_step).
+ */
+PA_API pa_status pa_decode_step_scaled(void* out, const void* q, const void* key, const void* value,
+                                       void* k_cache, void* v_cache, const int64_t* src_dst, int64_t num_pairs,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* seq_lens, int num_seqs, int max_seq_len, int num_heads,
+                                       int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                                       float scale, int partition_size, void* workspace, size_t workspace_bytes,
+                                       pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale, float v_scale,
+                                       void* stream);
 
 /*
  * Read and clear the first device-side error recorded on the current device

@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     pa_decode,
     pa_decode_scaled,
     pa_decode_step,
+    pa_decode_step_scaled,
     pa_decode_plan_partition,
     pa_decode_workspace_size,
     pa_get_device_error,

@@ -66,6 +66,9 @@ def load():
     lib.pa_decode_step.argtypes = [P, P, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, i32,
                                    P, sz, i32, P]
     lib.pa_decode_step.restype = i32
+    lib.pa_decode_step_scaled.argtypes = [P, P, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
+                                          f32, i32, P, sz, i32, i32, f32, f32, P]
+    lib.pa_decode_step_scaled.restype = i32
     # host-side block manager (include/pa_block_manager.h)
     lib.pa_bm_create.argtypes = [i64, i32, ctypes.POINTER(P)]
     lib.pa_bm_destroy.argtypes = [P]
@@ -265,6 +268,43 @@ def pa_decode_step(out, q, key, value, k_cache, v_cache, src_dst, block_tables, 
                              _ptr(src_dst) if npairs else None, npairs, _ptr(block_tables), block_tables.shape[1],
                              _ptr(seq_lens), S, max_seq_len, H, hkv, D, bs, nb, float(scale), partition_size,
                              _ptr(workspace), ws_bytes, code, _stream(stream)))
+    return workspace
+
+
+def pa_decode_step_scaled(out, q, key, value, k_cache, v_cache, src_dst, block_tables, seq_lens, scale,
+                          max_seq_len, k_scale, v_scale, partition_size=PARTITION_AUTO, workspace=None, stream=None):
+    """pa_decode_step over a cache whose dtype differs from q's: an FP8 E4M3 pool takes the
+    new key/value rows in q's dtype, stores their codes of x / scale and decodes as
+    pa_decode_scaled does."""
+    import torch
+    dt = q.dtype
+    _need_cuda("q", q, dt, 3)
+    _need_cuda("out", out, dt, 3)
+    _need_cuda("key", key, dt, 3)
+    _need_cuda("value", value, dt, 3)
+    _need_cuda("k_cache", k_cache, None, 5)
+    _need_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _need_cuda("block_tables", block_tables, torch.int32, 2)
+    _need_cuda("seq_lens", seq_lens, torch.int32, 1)
+    npairs = 0
+    if src_dst is not None:
+        _need_cuda("src_dst", src_dst, torch.int64)
+        npairs = src_dst.numel() // 2
+    S, H, D = q.shape
+    nb, hkv, _, bs = v_cache.shape
+    if key.shape != (S, hkv, D) or value.shape != (S, hkv, D):
+        raise ValueError(f"key/value must be [{S}, {hkv}, {D}]")
+    cc = dtype_code(k_cache.dtype)
+    lib = load()
+    need = lib.pa_decode_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, cc)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib.pa_decode_step_scaled(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(src_dst) if npairs else None, npairs, _ptr(block_tables),
+                                    block_tables.shape[1], _ptr(seq_lens), S, max_seq_len, H, hkv, D, bs, nb,
+                                    float(scale), partition_size, _ptr(workspace), ws_bytes, dtype_code(dt), cc,
+                                    float(k_scale), float(v_scale), _stream(stream)))
     return workspace
 
 

@@ -371,6 +371,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   p.seg_first = reinterpret_cast<int*>(ws + pl.off_first);
   p.seg_last = reinterpret_cast<int*>(ws + pl.off_last);
   p.fused = new_key != nullptr;
+  p.write_k_scale = k_scale;
+  p.write_v_scale = v_scale;
   st = device_error_ptr(&p.err);
   if (st != PA_OK) return st;
   p.k_cache = k_cache;
@@ -443,14 +445,16 @@ pa_status pa_decode_scaled(void* out, const void* q, const void* k_cache, const 
                      workspace_bytes, q_dtype, cache_dtype, k_scale, v_scale, stream);
 }
 
-pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value, void* k_cache, void* v_cache,
-                         const int64_t* src_dst, int64_t num_pairs, const int32_t* block_tables,
-                         int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int max_seq_len,
-                         int num_heads, int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
-                         float scale, int partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype,
-                         void* stream) {
-  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "the fused step runs on fp32, fp16 and bf16 caches");
+pa_status pa_decode_step_scaled(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                                void* v_cache, const int64_t* src_dst, int64_t num_pairs,
+                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_size,
+                                int block_size, int64_t num_blocks, float scale, int partition_size,
+                                void* workspace, size_t workspace_bytes, pa_dtype q_dtype, pa_dtype cache_dtype,
+                                float k_scale, float v_scale, void* stream) {
+  if (cache_dtype != PA_F32 && cache_dtype != PA_F16 && cache_dtype != PA_BF16 && cache_dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "unknown cache dtype %d", static_cast<int>(cache_dtype));
+  if (!elem_bytes(q_dtype)) return fail(PA_ERR_INVALID_ARG, "unknown query dtype %d", static_cast<int>(q_dtype));
   if (num_pairs < 0 || num_pairs > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_pairs %lld", (long long)num_pairs);
   if (num_pairs > 0 && (!src_dst || !aligned(src_dst, 8)))
     return fail(num_pairs > 0 && src_dst ? PA_ERR_ALIGNMENT : PA_ERR_INVALID_ARG,
@@ -460,10 +464,24 @@ pa_status pa_decode_step(void* out, const void* q, const void* key, const void* 
     return fail(PA_ERR_ALIGNMENT, "key/value need 16-byte alignment");
   if (num_seqs == 0 && num_pairs > 0)  // nothing to decode: the copies alone
     return pa_copy_blocks(k_cache, v_cache, src_dst, num_pairs, num_kv_heads, head_size, block_size, num_blocks,
-                          dtype, stream);
+                          cache_dtype, stream);
   return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                      num_heads, num_kv_heads, head_size, block_size, num_blocks, scale, partition_size, workspace,
-                     workspace_bytes, dtype, dtype, 1.f, 1.f, stream, key, value, src_dst, num_pairs);
+                     workspace_bytes, q_dtype, cache_dtype, k_scale, v_scale, stream, key, value, src_dst, num_pairs);
+}
+
+pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* src_dst, int64_t num_pairs, const int32_t* block_tables,
+                         int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                         int num_heads, int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                         float scale, int partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                         void* stream) {
+  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "the fused step on an FP8 cache is pa_decode_step_scaled (query dtype, scales)");
+  return pa_decode_step_scaled(out, q, key, value, k_cache, v_cache, src_dst, num_pairs, block_tables,
+                               max_blocks_per_seq, seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads, head_size,
+                               block_size, num_blocks, scale, partition_size, workspace, workspace_bytes, dtype, dtype,
+                               1.f, 1.f, stream);
 }
 
 pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,

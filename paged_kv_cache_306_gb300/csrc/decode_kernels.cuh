@@ -78,8 +78,10 @@ struct DecodeShape {
   static constexpr int kStateBytes = kWarps * BS * 4 + kWarps * kRows * (D + 2) * 4;
   // the fused step: a sequence's new K and V rows land beside the stage of its last block
   static constexpr int kSideOffset = (kRingBytes + kBarBytes + kTableBytes + kStateBytes + 127) / 128 * 128;
-  static constexpr int kSideStage = 2 * D * kElem;
+  // (the rows come in the query's dtype: 16-bit for an FP8 pool, the pool's own otherwise)
+  static constexpr int kSideStage = 2 * D * (kElem < 2 ? 2 : kElem);
   static constexpr int kSmemBytes = kSideOffset + kWarps * kStages * kSideStage;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 // Wait for block i's stage.  On timeout record the error and drain the copies
@@ -659,6 +661,51 @@ struct SimtMath {
 
 // --- the fused step: the new token ---------------------------------------------------------------
 
+// The E4M3 codes of x / scale, the division correctly rounded in fp32, the
+// conversion round-to-nearest-even and saturating -- the write path's conversion,
+// so the fused step stores and decodes the very codes the separate write stores.
+template <typename TS>
+__device__ __forceinline__ uint4 e4m3_codes16(const TS* src, float scale) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float a = __fdiv_rn(DType<TS>::to_f32(src[4 * i + 2 * j]), scale);
+      const float b = __fdiv_rn(DType<TS>::to_f32(src[4 * i + 2 * j + 1]), scale);
+      packed |= (__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3) & 0xffffu) << (16 * j);
+    }
+    w[i] = packed;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <typename TS>
+__device__ __forceinline__ unsigned char e4m3_code(TS x, float scale) {
+  return static_cast<unsigned char>(
+      __nv_cvt_float_to_fp8(__fdiv_rn(DType<TS>::to_f32(x), scale), __NV_SATFINITE, __NV_E4M3));
+}
+
+// The fused step's new token into an FP8 stage: the side buffer holds the K and V rows
+// in the query dtype T; they are quantised as the write path quantises them.
+template <typename T, int D, int BS>
+__device__ __forceinline__ void inject_token_e4m3(unsigned char* stage, int tile_bytes, const unsigned char* side,
+                                                  int off, float k_scale, float v_scale, int lane) {
+  constexpr int VPL = D / 32;
+  const T* sk = reinterpret_cast<const T*>(side);
+  const T* sv = sk + D;
+  unsigned char* v = stage + tile_bytes;
+  if (lane < D / 16) {
+    T e[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) e[i] = sk[lane * 16 + i];
+    *reinterpret_cast<uint4*>(stage + (lane * BS + off) * 16) = e4m3_codes16<T>(e, k_scale);
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) v[(lane + 32 * i) * BS + off] = e4m3_code<T>(sv[lane + 32 * i], v_scale);
+  __syncwarp();
+}
+
 // The fused step's new token of a (sequence, kv head) -- its K and V rows, copied
 // by TMA into `side` with the stage of the sequence's last block -- into that
 // stage at slot `off` (K tile [D/X][BS][X]: 16 bytes per X-group, D/X <= 32 of
@@ -806,7 +853,40 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   // stores may alias the loads as far as the compiler knows).  Nothing in this
   // launch reads these slots from the pool afterwards: decode takes the tokens
   // from the side buffers (see issue), so the stores need no ordering.
+  auto write_tokens_e4m3 = [&]() {  // an FP8 pool: rows in T, quantised as the write path does
+    constexpr int VPL = D / 32;
+    const long long tile_bytes = (long long)D * BS;
+    unsigned char* kc = static_cast<unsigned char*>(const_cast<void*>(p.k_cache));
+    unsigned char* vc = static_cast<unsigned char*>(const_cast<void*>(p.v_cache));
+    const int items = S * p.num_kv_heads;
+    for (int i = w; i < items; i += W) {
+      const int s2 = i / p.num_kv_heads, h = i - s2 * p.num_kv_heads, L2 = s_len[s2];
+      if (L2 == 0) continue;
+      const int blk = __ldg(p.block_tables + (long long)s2 * p.max_blocks_per_seq + (L2 - 1) / BS);
+      if (blk < 0 || blk >= p.num_blocks) continue;  // recorded when decode reads the block
+      const long long tile = (long long)blk * p.num_kv_heads + h;
+      const int off = (L2 - 1) % BS;
+      const T* key = static_cast<const T*>(p.new_key) + (long long)i * D;
+      const T* value = static_cast<const T*>(p.new_value) + (long long)i * D;
+      T e[16], vv[VPL];
+      if (lane < D / 16) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) e[j] = key[lane * 16 + j];
+      }
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) vv[j] = value[lane + 32 * j];
+      if (lane < D / 16)
+        *reinterpret_cast<uint4*>(kc + tile * tile_bytes + (lane * BS + off) * 16) = e4m3_codes16<T>(e, p.write_k_scale);
+#pragma unroll
+      for (int j = 0; j < VPL; ++j)
+        vc[tile * tile_bytes + (long long)(lane + 32 * j) * BS + off] = e4m3_code<T>(vv[j], p.write_v_scale);
+    }
+  };
   auto write_tokens = [&]() {
+    if constexpr (sizeof(TC) == 1) {
+      write_tokens_e4m3();
+      return;
+    }
     constexpr int X = 16 / static_cast<int>(sizeof(TC)), VPL = D / 32, kBatch = 4;
     const long long tile_bytes = (long long)D * BS * sizeof(TC);
     unsigned char* kc = static_cast<unsigned char*>(const_cast<void*>(p.k_cache));
@@ -893,15 +973,16 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       unsigned char* dst = ring + st * 2 * TILE;
       const long long tile = (long long)phys * p.num_kv_heads + kvh;
       const bool with_token = p.fused && (tag >> 30);
-      mbar_arrive_expect_tx(&bars[st], 2 * TILE + (with_token ? Sh::kSideStage : 0));
+      mbar_arrive_expect_tx(
+          &bars[st], 2 * TILE + (with_token ? 2 * D * static_cast<int>(sizeof(TC) == 1 ? sizeof(T) : sizeof(TC)) : 0));
       bulk_copy_g2s(dst, static_cast<const unsigned char*>(p.k_cache) + tile * TILE, TILE, &bars[st]);
       bulk_copy_g2s(dst + TILE, static_cast<const unsigned char*>(p.v_cache) + tile * TILE, TILE, &bars[st]);
       if (with_token) {  // the new token's K and V rows of (sequence, kv head)
-        const long long row = ((long long)((tag >> 16) & 0x3fff) * p.num_kv_heads + kvh) * (D * sizeof(TC));
+        constexpr int kRowBytes = D * static_cast<int>(sizeof(TC) == 1 ? sizeof(T) : sizeof(TC));
+        const long long row = ((long long)((tag >> 16) & 0x3fff) * p.num_kv_heads + kvh) * kRowBytes;
         unsigned char* sd = side + st * Sh::kSideStage;
-        bulk_copy_g2s(sd, static_cast<const unsigned char*>(p.new_key) + row, D * sizeof(TC), &bars[st]);
-        bulk_copy_g2s(sd + D * sizeof(TC), static_cast<const unsigned char*>(p.new_value) + row, D * sizeof(TC),
-                      &bars[st]);
+        bulk_copy_g2s(sd, static_cast<const unsigned char*>(p.new_key) + row, kRowBytes, &bars[st]);
+        bulk_copy_g2s(sd + kRowBytes, static_cast<const unsigned char*>(p.new_value) + row, kRowBytes, &bars[st]);
       }
     }
   };
@@ -930,7 +1011,13 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
     unsigned char* stage = ring + (k % STAGES) * 2 * TILE;
     const int rem = L - cj * BS;  // valid tokens in this block (>= 1)
     if (p.fused && cj == nblk - 1)  // the sequence's new token: from the step's input, not the pool
-      inject_token<TC, D, BS>(stage, TILE, side + (k % STAGES) * Sh::kSideStage, (L - 1) % BS, lane);
+    {
+      if constexpr (sizeof(TC) == 1)
+        inject_token_e4m3<T, D, BS>(stage, TILE, side + (k % STAGES) * Sh::kSideStage, (L - 1) % BS,
+                                    p.write_k_scale, p.write_v_scale, lane);
+      else
+        inject_token<TC, D, BS>(stage, TILE, side + (k % STAGES) * Sh::kSideStage, (L - 1) % BS, lane);
+    }
     if (rem < BS) zero_tail_v<TC, D, BS>(stage + TILE, rem, lane);
     if constexpr (Math::kFetch) {  // the block's fragments are in registers: refill the stage now
       math.fetch(stage, TILE);

@@ -63,8 +63,9 @@ struct DecodeParams {
   // The fused step (pa_decode_step): the new token of each sequence s (rows s of
   // new_key and new_value, [S, Hkv, D] in the cache dtype) goes into position
   // seq_lens[s] - 1 as part of decode; fused == 0 for plain decode.
-  const void* new_key;
+  const void* new_key;            // the query dtype for an FP8 pool (quantised with the scales below)
   const void* new_value;
+  float write_k_scale, write_v_scale;  // FP8 pool: stored code = E4M3(x / scale)
   int fused;
 };
 

@@ -112,9 +112,14 @@ def fused_step(wl, partition_size=None, t=None, workspace=None, check_error=True
     t = upload(wl) if t is None else t
     out = torch.empty_like(t["q"])
     ps = wl.partition_size if partition_size is None else partition_size
-    pa.pa_decode_step(out, t["q"], t["key"], t["value"], t["k_cache"], t["v_cache"],
-                      t["cow"] if len(wl.cow) else None, t["block_tables"], t["seq_lens"], wl.scale, wl.max_seq_len,
-                      ps, workspace)
+    if wl.dtype == "fp8":
+        pa.pa_decode_step_scaled(out, t["q"], t["key"], t["value"], t["k_cache"], t["v_cache"],
+                                 t["cow"] if len(wl.cow) else None, t["block_tables"], t["seq_lens"], wl.scale,
+                                 wl.max_seq_len, wl.k_scale, wl.v_scale, ps, workspace)
+    else:
+        pa.pa_decode_step(out, t["q"], t["key"], t["value"], t["k_cache"], t["v_cache"],
+                          t["cow"] if len(wl.cow) else None, t["block_tables"], t["seq_lens"], wl.scale,
+                          wl.max_seq_len, ps, workspace)
     if check_error:
         code = pa.pa_get_device_error()
         assert code == 0, f"device error {code}: {pa.DEVICE_ERRORS.get(code)}"

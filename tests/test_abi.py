@@ -216,3 +216,19 @@ def test_fused_step_rejects_bad_arguments_on_the_host(lib):
     assert st(q=8200) == B.PA_ERR_ALIGNMENT
     assert st(S=0, npairs=0, key=0, value=0, q=0) == B.PA_OK
     assert lib.pa_last_error_message()
+
+
+def test_scaled_fused_step_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+
+    def st(qdt=B.PA_F16, cdt=B.PA_FP8_E4M3, ks=0.5, vs=0.5, key=8192, S=1):
+        return lib.pa_decode_step_scaled(P(8192), P(8192), P(key), P(8192), P(8192), P(8192), None, 0, P(8192), 4,
+                                         P(8192), S, 16, 4, 4, 128, 16, 8, 0.1, 0, None, 0, qdt, cdt, ks, vs, None)
+    assert st(qdt=B.PA_F32) == B.PA_ERR_UNSUPPORTED       # an FP8 pool is read by fp16 or bf16 queries
+    assert st(ks=0.0) == B.PA_ERR_INVALID_ARG
+    assert st(vs=float("inf")) == B.PA_ERR_INVALID_ARG
+    assert st(cdt=B.PA_F16, ks=1.0, vs=1.0, qdt=B.PA_BF16) == B.PA_ERR_INVALID_ARG  # 16-bit pool: the query's dtype
+    assert st(cdt=B.PA_F16, ks=0.5, vs=1.0) == B.PA_ERR_INVALID_ARG                 # and scales 1
+    assert st(cdt=9) == B.PA_ERR_UNSUPPORTED
+    assert st(key=8200) == B.PA_ERR_ALIGNMENT
+    assert st(S=0, key=0) == B.PA_OK

@@ -218,3 +218,38 @@ def test_serving_loop_on_the_fused_step(dtype, bs):
         assert_close(as_f64(out), ref, dtype, with_rounding=True, what=f"step {step}")
     assert copies_seen > 0
     bm.close()
+
+
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,bs,G", [(128, 16, 7), (128, 32, 1), (64, 16, 4), (128, 16, 16)])
+def test_fused_step_on_an_fp8_pool(q_dtype, D, bs, G):
+    """The new token quantised where it is written and where it enters the stage, with
+    the write path's conversion: bit-identical with the three separate calls."""
+    rng = np.random.default_rng(zlib.crc32(repr(("fp8step", q_dtype, D, bs, G)).encode()))
+    L = [1, bs - 1, bs, bs + 1, 3 * bs + 5] + list(rng.integers(2, 500, size=3))
+    wl = W.make_private("fp8step", "fp8", L, 2 * G, 2, D, bs, seed=int(rng.integers(1 << 30)), partition_size=-1,
+                        q_dtype=q_dtype)
+    out, t = check_against_separate_calls(wl)
+    k, v = oracle_pools(wl)
+    assert np.array_equal(W.from_torch(t["k_cache"], "fp8").view(np.uint8), k.view(np.uint8))
+    assert np.array_equal(W.from_torch(t["v_cache"], "fp8").view(np.uint8), v.view(np.uint8))
+    assert_close(as_f64(out), oracle_out(wl, k, v), "fp8", with_rounding=True, out_dtype=q_dtype)
+
+
+def test_fused_step_on_an_fp8_pool_with_copy_on_write():
+    wl = W.make_prefix_shared("fp8cow", "fp8", 3, 4, 8, 2, 128, 16, seed=99, len_range=(8, 700),
+                              prefix_range=(10, 300), partition_size=-1, q_dtype="f16")
+    assert len(wl.cow) > 0
+    out, t = check_against_separate_calls(wl)
+    k, v = oracle_pools(wl)
+    assert np.array_equal(W.from_torch(t["k_cache"], "fp8").view(np.uint8), k.view(np.uint8))
+    assert_close(as_f64(out), oracle_out(wl, k, v), "fp8", with_rounding=True, out_dtype="f16")
+
+
+@pytest.mark.parametrize("cfg", [2, 5])
+def test_full_size_fp8_workloads_match_separate_calls(cfg):
+    wl = W.config(cfg, kv_dtype="fp8")
+    out, t = check_against_separate_calls(wl)
+    seqs = list(np.random.default_rng(cfg).choice(wl.num_seqs, 3, replace=False))
+    k, v = oracle_pools(wl)
+    assert_close(as_f64(out)[seqs], oracle_out(wl, k, v, seqs), "fp8", with_rounding=True, out_dtype=wl.q_dtype)
