@@ -290,7 +290,10 @@ PA_API uint64_t pa_launch_count(void);
  * No workspace.  A sequence whose length lies outside [1, max_seq_len] or whose
  * chunk is longer than itself is recorded as PA_DEVERR_SEQ_LEN and its rows of
  * out are unspecified.  num_blocks * num_kv_heads * head_size must stay below
- * 2^31 (PA_ERR_UNSUPPORTED otherwise).  Asynchronous on `stream`.
+ * 2^31 (PA_ERR_UNSUPPORTED otherwise).  The kernel reads the pools through TMA
+ * tensor maps encoded on the host at every call (cuTensorMapEncodeTiled, found
+ * through the CUDA runtime; PA_ERR_CUDA if the driver does not provide it).
+ * Asynchronous on `stream`.
  */
 PA_API pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
