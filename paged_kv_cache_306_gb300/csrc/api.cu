@@ -407,8 +407,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     p.out = static_cast<char*>(out) + (size_t)c0 * row_bytes;
     p.block_tables = block_tables + (size_t)c0 * max_blocks_per_seq;
     p.seq_lens = seq_lens + c0;
-    if (p.fused) {
-      const size_t kv_row_bytes = (size_t)num_kv_heads * head_size * elem_bytes(dtype);
+    if (p.fused) {  // the new rows come in the query dtype (an FP8 pool quantises them itself)
+      const size_t kv_row_bytes = (size_t)num_kv_heads * head_size * elem_bytes(q_dtype);
       p.new_key = static_cast<const char*>(new_key) + (size_t)c0 * kv_row_bytes;
       p.new_value = static_cast<const char*>(new_value) + (size_t)c0 * kv_row_bytes;
     }
