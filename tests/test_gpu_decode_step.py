@@ -253,3 +253,14 @@ def test_full_size_fp8_workloads_match_separate_calls(cfg):
     seqs = list(np.random.default_rng(cfg).choice(wl.num_seqs, 3, replace=False))
     k, v = oracle_pools(wl)
     assert_close(as_f64(out)[seqs], oracle_out(wl, k, v, seqs), "fp8", with_rounding=True, out_dtype=wl.q_dtype)
+
+
+def test_fp8_fused_step_over_more_sequences_than_one_launch_holds():
+    """Later launches start at their sequences' rows of the 16-bit key/value input."""
+    rng = np.random.default_rng(101)
+    wl = W.make_private("manyfp8", "fp8", rng.integers(1, 60, size=1100), 8, 2, 64, 16, seed=102,
+                        partition_size=-1, q_dtype="bf16")
+    out, t = check_against_separate_calls(wl)
+    k, v = oracle_pools(wl)
+    assert np.array_equal(W.from_torch(t["k_cache"], "fp8").view(np.uint8), k.view(np.uint8))
+    assert_close(as_f64(out), oracle_out(wl, k, v), "fp8", with_rounding=True, out_dtype="bf16")
