@@ -1,19 +1,27 @@
 """Benchmark of one decode step of one attention layer over a paged KV pool.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload qwen|llama|long|mixed|tiny] [--block-size 16|32]
-                    [--kv-dtype fp8] [--step fused|separate]
+                    [--workload long|qwen|llama|mixed|tiny] [--block-size 16|32]
+                    [--kv-dtype fp8] [--step fused|separate] [--calls C] [--configs all|none|LIST]
 
+The headline workload is the long-context split-KV layer (4 sequences of 32K to
+128K tokens, 32 query / 8 kv heads, head size 128, bf16, PARTITION_SIZE 512).
 A step is the whole hot path on one batch: copy-on-write block copies (the
 mixed workload only), the write of every sequence's new token, and decode
-attention (plus the partition merge when the planner splits).  By default the
-step is one pa_decode_step call, which does all three in the decode kernel;
---step separate times pa_copy_blocks + pa_reshape_and_cache + pa_decode
-instead (always so for an FP8 cache, whose write quantises).
-`value` is algorithmic bytes per step / step time (inputs resident in HBM, pool
-copies rotated so K/V always come from HBM); `e2e` is the same metric through
-the Python API with the step's inputs copied from pinned host memory and the
-output copied back inside the timed region.  Rank 0 prints one JSON line.
+attention with its partition merge.  By default the step is one pa_decode_step
+(pa_decode_step_scaled for an FP8 pool) call, which does all three;
+--step separate times pa_copy_blocks + the write + decode instead.
+
+`value` is algorithmic bytes per step / step time over exactly K back-to-back
+steps (inputs resident in HBM, pool copies rotated so K/V always come from HBM).
+A physical block referenced by several sequences counts once (its bytes leave
+DRAM once).  `roofline` times C single calls (default 200, whatever K is), each
+between CUDA events on the launching stream, and reports the median, p10 and
+p90.  `e2e` is the same step through the Python API with the step's inputs
+copied from pinned host memory and the output copied back inside the timed
+region.  `configs` repeats the call and step measurements for every other
+workload (the other decode layers, both block sizes of the mixed batch, and the
+FP8 pools).  Rank 0 prints one JSON line.
 
 --mode prefill times chunked prefill instead (16 sequences of a Qwen2.5-7B-shaped
 layer, a chunk of 512 new tokens each after 0..3584 cached ones): a step is the
@@ -50,6 +58,12 @@ L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged chunked-prefill attention TFLOP/s (% of GB300 dense bf16 tensor peak)"
+# the workloads measured beside the headline: (key, workload, block size, kv dtype)
+SUBRECORDS = [
+    ("qwen", 2, None, None), ("llama", 3, None, None), ("mixed-bs16", 5, 16, None), ("mixed-bs32", 5, 32, None),
+    ("tiny", 1, None, None), ("long-fp8", 4, None, "fp8"), ("qwen-fp8", 2, None, "fp8"),
+    ("llama-fp8", 3, None, "fp8"), ("mixed-bs16-fp8", 5, 16, "fp8"),
+]
 
 
 # --- byte accounting ------------------------------------------------------------------------
@@ -74,6 +88,17 @@ def write_bytes(wl):
     return tok + len(wl.cow) * blk * 2 + len(wl.cow) * 16
 
 
+def step_bytes(wl):
+    """Algorithmic bytes of one whole step (write and copies, then decode), shared
+    physical blocks counted once: the numerator of `value`."""
+    return decode_bytes(wl, unique=True) + write_bytes(wl)
+
+
+def call_bytes(wl, fused):
+    """Algorithmic bytes of the single timed call: the fused step also writes."""
+    return decode_bytes(wl, unique=True) + (write_bytes(wl) if fused else 0)
+
+
 def measured_peaks(key="hbm_gbs"):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -95,18 +120,28 @@ def prefill_flops(wl):
     return total
 
 
+def spread(ms):
+    """Median, p10 and p90 of per-call times (ms) in microseconds."""
+    a = np.asarray(ms, dtype=np.float64) * 1e3
+    return {"median": round(float(np.median(a)), 3), "p10": round(float(np.percentile(a, 10)), 3),
+            "p90": round(float(np.percentile(a, 90)), 3)}
+
+
 # --- clocks --------------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU work runs;
+    summaries are taken afterwards over the time window of each timed region."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.rows = []
 
     def start(self):
         try:
@@ -119,16 +154,15 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self, t0, t1):
+    def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return
         time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
@@ -137,15 +171,23 @@ class ClockSampler:
                 try:
                     ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                     ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                    self.rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
                 except (ValueError, IndexError):
                     continue
         os.unlink(self.path)
-        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+
+    def window(self, t0, t1):
+        """Median SM clock, its maximum and the throttle reasons seen within [t0, t1]
+        (the nearest samples when the window is shorter than the sampling period)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for r in self.rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        if not inside and self.rows:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.rows, key=lambda r: abs(r[0] - mid))]
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        reasons = sorted({self.NAMES[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
                 "reasons": reasons, "samples": len(inside)}
 
@@ -179,7 +221,17 @@ def barrier(world_size, device=None):
             dist.barrier()
 
 
-# --- our arm ---------------------------------------------------------------------------------
+# --- the workload description (identical in both arms) ---------------------------------------
+
+def pool_bytes(wl):
+    return wl.num_blocks * wl.num_kv_heads * wl.head_size * wl.block_size * W.ELEM_BYTES[wl.dtype] * 2
+
+
+def pool_copies(wl):
+    """Copies of the pool rotated between steps so that >= 4x L2 of K/V lies between
+    two uses of one copy."""
+    return max(2, math.ceil(4 * L2_BYTES / pool_bytes(wl)))
+
 
 def describe(wl, cfg):
     L = wl.seq_lens
@@ -193,16 +245,44 @@ def describe(wl, cfg):
     return d
 
 
+def config_dict(args, wl, cfg):
+    """The workload as both arms state it: shapes, seed, split, step and the L2 rule."""
+    ps = wl.partition_size if args.partition is None else args.partition
+    d = describe(wl, cfg)
+    d.update({"partition_size": "auto" if ps == -1 else int(ps),
+              "step": ("fused: one pa_decode_step call (block copies, new tokens and decode) + merge"
+                       if uses_fused_step(args, wl) else
+                       "separate: pa_copy_blocks + reshape_and_cache + decode"),
+              "l2": f"inputs larger than L2: {pool_copies(wl)} pool copies of {pool_bytes(wl) / 1e6:.0f} MB "
+                    f"rotated between steps",
+              "bytes": "shared physical blocks counted once"})
+    return d
+
+
 def dtype_label(wl):
     """The arithmetic type of the path: an FP8 pool is widened to the query dtype."""
     return wl.dtype if wl.dtype != "fp8" else f"fp8_e4m3 cache, {wl.q_dtype} compute"
 
 
+def uses_fused_step(args, wl):
+    """One pa_decode_step(_scaled) call per step unless --step separate."""
+    return args.step == "fused"
+
+
+def pa_dtype(wl):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.q_dtype]
+
+
+# --- our arm ---------------------------------------------------------------------------------
+
 def api_calls(wl):
-    """(write, decode) through the public API for the workload's cache dtype."""
+    """(write, decode, step) through the public API for the workload's cache dtype."""
     import paged_kv_cache_306_gb300 as pa
     if wl.dtype != "fp8":
-        return pa.pa_reshape_and_cache, pa.pa_decode
+        def fused(out, q, key, value, k, v, cow, bt, sl, scale, msl, ps, ws, stream=None):
+            return pa.pa_decode_step(out, q, key, value, k, v, cow, bt, sl, scale, msl, ps, ws, stream=stream)
+        return pa.pa_reshape_and_cache, pa.pa_decode, fused
 
     def write(key, value, k, v, slots, stream=None):
         pa.pa_reshape_and_cache_scaled(key, value, k, v, slots, wl.k_scale, wl.v_scale, stream=stream)
@@ -210,7 +290,11 @@ def api_calls(wl):
     def decode(out, q, k, v, bt, sl, scale, max_seq_len, partition_size, ws, stream=None):
         return pa.pa_decode_scaled(out, q, k, v, bt, sl, scale, max_seq_len, wl.k_scale, wl.v_scale,
                                    partition_size, ws, stream=stream)
-    return write, decode
+
+    def fused(out, q, key, value, k, v, cow, bt, sl, scale, msl, ps, ws, stream=None):
+        return pa.pa_decode_step_scaled(out, q, key, value, k, v, cow, bt, sl, scale, msl, wl.k_scale, wl.v_scale,
+                                        ps, ws, stream=stream)
+    return write, decode, fused
 
 
 def oracle_pools_after_write(wl):
@@ -232,6 +316,111 @@ def oracle_decode(wl, q, k, v, sub):
                          k_scale=wl.k_scale, v_scale=wl.v_scale)
 
 
+class Runner:
+    """A workload resident on the GPU (rotated pool copies, tables, workspace) and its step."""
+
+    def __init__(self, args, wl, dev, stream):
+        import torch
+        import paged_kv_cache_306_gb300 as pa
+        self.wl, self.dev, self.stream = wl, dev, stream
+        self.copies = pool_copies(wl)
+        free = torch.cuda.mem_get_info(dev)[0]
+        self.copies = max(1, min(self.copies, int(0.6 * free // pool_bytes(wl))))
+        self.sets = []
+        for _ in range(self.copies):
+            self.sets.append({
+                "q": W.to_torch(wl.q, wl.q_dtype, dev), "key": W.to_torch(wl.key, wl.q_dtype, dev),
+                "value": W.to_torch(wl.value, wl.q_dtype, dev), "k": W.to_torch(wl.k_cache, wl.dtype, dev),
+                "v": W.to_torch(wl.v_cache, wl.dtype, dev),
+                "out": torch.empty(wl.q.shape, dtype=pa_dtype(wl), device=dev)})
+        self.bt = torch.from_numpy(wl.block_tables).to(dev)
+        self.sl = torch.from_numpy(wl.seq_lens).to(dev)
+        self.slots = torch.from_numpy(wl.slot_mapping).to(dev)
+        self.cow = torch.from_numpy(np.ascontiguousarray(wl.cow)).to(dev)
+        self.ps = wl.partition_size if args.partition is None else args.partition
+        code = {"f32": pa.PA_F32, "f16": pa.PA_F16, "bf16": pa.PA_BF16, "fp8": pa.PA_FP8_E4M3}[wl.dtype]
+        self.resolved = pa.pa_decode_plan_partition(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
+                                                    wl.max_seq_len, wl.block_size, code) if self.ps == -1 else self.ps
+        need = pa.pa_decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
+                                           wl.max_seq_len, wl.block_size, self.resolved, code)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.write, self.decode, self.fused_call = api_calls(wl)
+        self.fused = uses_fused_step(args, wl)
+
+    def step(self, i, ev=None):
+        """Step i on pool copy i mod copies; with `ev`, events around the timed call."""
+        wl, s, st = self.wl, self.sets[i % self.copies], self.stream
+        cow = self.cow if len(wl.cow) else None
+        if self.fused:
+            if ev is not None:
+                ev[0].record(st)
+            self.fused_call(s["out"], s["q"], s["key"], s["value"], s["k"], s["v"], cow, self.bt, self.sl, wl.scale,
+                            wl.max_seq_len, self.resolved, self.ws, stream=st)
+            if ev is not None:
+                ev[1].record(st)
+            return
+        import paged_kv_cache_306_gb300 as pa
+        if cow is not None:
+            pa.pa_copy_blocks(s["k"], s["v"], cow, stream=st)
+        self.write(s["key"], s["value"], s["k"], s["v"], self.slots, stream=st)
+        if ev is not None:
+            ev[0].record(st)
+        self.decode(s["out"], s["q"], s["k"], s["v"], self.bt, self.sl, wl.scale, wl.max_seq_len, self.resolved,
+                    self.ws, stream=st)
+        if ev is not None:
+            ev[1].record(st)
+
+    def timed_steps(self, steps, world_size=1):
+        """Exactly `steps` steps back to back between events; returns (ms, launches, t0, t1)."""
+        import torch
+        import paged_kv_cache_306_gb300 as pa
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world_size, self.dev)
+        torch.cuda.synchronize(self.dev)
+        launches0 = pa.pa_launch_count()
+        t0 = time.time()
+        start.record(self.stream)
+        for i in range(steps):
+            self.step(i)
+        stop.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        t1 = time.time()
+        launches = pa.pa_launch_count() - launches0
+        barrier(world_size, self.dev)
+        return start.elapsed_time(stop), launches, t0, t1
+
+    def timed_calls(self, calls):
+        """`calls` single calls, each between events on the launching stream; per-call ms."""
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+        torch.cuda.synchronize(self.dev)
+        t0 = time.time()
+        for i in range(calls):
+            self.step(i, evs[i])
+        torch.cuda.synchronize(self.dev)
+        t1 = time.time()
+        return [a.elapsed_time(b) for a, b in evs], t0, t1
+
+
+def device_error_check(where):
+    import paged_kv_cache_306_gb300 as pa
+    code = pa.pa_get_device_error()
+    if code != 0:
+        raise RuntimeError(f"device error {code} ({pa.DEVICE_ERRORS.get(code)}) {where}")
+
+
+def roofline_of(wl, fused, call_ms, peak, peak_kind):
+    nbytes = call_bytes(wl, fused)
+    med = float(np.median(call_ms))
+    achieved = nbytes / (med * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": load_traffic(wl, fused),
+            "kernel": ("pa_decode_step call: decode_kernel (copies, new tokens, decode) + decode_merge_kernel"
+                       if fused else "pa_decode call: decode_kernel + decode_merge_kernel"),
+            "bytes_per_launch": int(nbytes), "launch_us": spread(call_ms), "calls": len(call_ms),
+            "peak_source": f"{peak_kind} hbm_gbs (of {peak_kind})"}
+
+
 def run_ours(args, wl, cfg, world_size, rank, local_rank):
     import torch
     import paged_kv_cache_306_gb300 as pa
@@ -239,142 +428,103 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    e = W.ELEM_BYTES[wl.dtype]
-    pool_bytes = wl.num_blocks * wl.num_kv_heads * wl.head_size * wl.block_size * e * 2
-    copies = max(2, math.ceil(4 * L2_BYTES / pool_bytes))
-    copies = min(copies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // pool_bytes)))
-
-    sets = []
-    for _ in range(copies):
-        sets.append({
-            "q": W.to_torch(wl.q, wl.q_dtype, dev), "key": W.to_torch(wl.key, wl.q_dtype, dev),
-            "value": W.to_torch(wl.value, wl.q_dtype, dev), "k": W.to_torch(wl.k_cache, wl.dtype, dev),
-            "v": W.to_torch(wl.v_cache, wl.dtype, dev), "out": torch.empty(wl.q.shape, dtype=pa_dtype(wl), device=dev),
-        })
-    bt = torch.from_numpy(wl.block_tables).to(dev)
-    sl = torch.from_numpy(wl.seq_lens).to(dev)
-    slots = torch.from_numpy(wl.slot_mapping).to(dev)
-    cow = torch.from_numpy(np.ascontiguousarray(wl.cow)).to(dev)
-    ps = wl.partition_size if args.partition is None else args.partition
-    code = {"f32": pa.PA_F32, "f16": pa.PA_F16, "bf16": pa.PA_BF16, "fp8": pa.PA_FP8_E4M3}[wl.dtype]
-    write, decode = api_calls(wl)
-    fused = uses_fused_step(args, wl)
-    resolved = pa.pa_decode_plan_partition(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
-                                           wl.max_seq_len, wl.block_size, code) if ps == -1 else ps
-    ws_bytes = pa.pa_decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
-                                           wl.max_seq_len, wl.block_size, resolved, code)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-
-    def step(i, ev=None):
-        s = sets[i % copies]
-        if fused:
-            if ev is not None:
-                ev[0].record(stream)
-            pa.pa_decode_step(s["out"], s["q"], s["key"], s["value"], s["k"], s["v"], cow if len(wl.cow) else None,
-                              bt, sl, wl.scale, wl.max_seq_len, resolved, ws, stream=stream)
-            if ev is not None:
-                ev[1].record(stream)
-            return
-        if len(wl.cow):
-            pa.pa_copy_blocks(s["k"], s["v"], cow, stream=stream)
-        write(s["key"], s["value"], s["k"], s["v"], slots, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        decode(s["out"], s["q"], s["k"], s["v"], bt, sl, wl.scale, wl.max_seq_len, resolved, ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-
+    r = Runner(args, wl, dev, stream)
     for i in range(args.warmup):
-        step(i)
+        r.step(i)
     torch.cuda.synchronize(dev)
-    if pa.pa_get_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+    device_error_check("during warm-up")
 
-    # timed region: K steps back to back, events around the whole loop only
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
-    barrier(world_size, dev)
-    torch.cuda.synchronize(dev)
-    launches0 = pa.pa_launch_count()
-    t0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    stop.record(stream)
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    launches = pa.pa_launch_count() - launches0
-    barrier(world_size, dev)
-    clocks = sampler.stop(t0, t1) if sampler else None
-    if pa.pa_get_device_error() != 0:
-        raise RuntimeError("device error in the timed region")
-    ms_total = max_over_ranks(start.elapsed_time(stop), world_size, dev)
+    ms_total, launches, t0, t1 = r.timed_steps(args.steps, world_size)
+    device_error_check("in the timed region")
+    ms_total = max_over_ranks(ms_total, world_size, dev)
     ms_step = ms_total / args.steps
 
-    # the decode call alone (the fused call: it also copies and writes): events on
-    # the launching stream around every call
-    kn = min(args.steps, 2000)
-    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kn)]
-    for i in range(kn):
-        step(i, dec_events[i])
-    torch.cuda.synchronize(dev)
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_events]))
-
-    # end to end through the API: pinned host inputs in, result out, every step
-    e2e = run_e2e(args, wl, dev, stream, sets[0], bt, sl, resolved, ws, fused)
-
-    step_bytes = decode_bytes(wl) + write_bytes(wl)
-    dbytes = decode_bytes(wl)
+    # single calls between events on the launching stream: a fixed count, whatever --steps is
+    call_ms, c0, c1 = r.timed_calls(args.calls)
+    device_error_check("in the per-call pass")
+    e2e = run_e2e(args, r)
     peak, peak_kind = measured_peaks()
-    # DRAM-level bytes: a physical block shared by several sequences is read once
-    rbytes = decode_bytes(wl, unique=True) + (write_bytes(wl) if fused else 0)
-    achieved = rbytes / (dec_ms * 1e-3) / 1e9
-    traffic = load_traffic(wl, fused)
-    cfgd = describe(wl, cfg)
-    cfgd.update({"partition_size": int(resolved), "pool_copies_rotated": copies,
-                 "step": ("fused: one pa_decode_step call (block copies, new tokens and decode in the decode "
-                          "kernel) + merge" if fused else
-                          "separate: pa_copy_blocks + pa_reshape_and_cache + pa_decode"),
-                 "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e6:.0f} MB rotated",
-                 "decode_bytes": int(dbytes), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
-                 "step_bytes": int(step_bytes), "decode_us": round(dec_ms * 1e3, 2),
-                 "tokens_per_s_per_layer": round(world_size * wl.num_seqs / (ms_step * 1e-3), 1),
-                 "pct_of_hbm_peak_step": round(100 * step_bytes / (ms_step * 1e-3) / 1e9 / peak, 2),
-                 "peak_gbs": peak, "peak_kind": peak_kind, "parallelism": f"replicas x{world_size}"})
+    sbytes = step_bytes(wl)
     line = {
-        "metric": METRIC, "value": round(world_size * step_bytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "metric": METRIC, "value": round(world_size * sbytes / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(wl),
-        "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfgd,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("pa_decode_step call: decode_kernel (copies, new tokens, decode) + decode_merge_kernel"
-                                if fused else "pa_decode call: decode_kernel + decode_merge_kernel"),
-                     "bytes_per_launch": int(rbytes), "launch_us": round(dec_ms * 1e3, 2),
-                     "peak_source": f"{peak_kind} hbm_gbs"},
-        "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
+        "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": config_dict(args, wl, cfg),
+        "roofline": roofline_of(wl, r.fused, call_ms, peak, peak_kind),
+        "tokens_per_s_per_layer": round(world_size * wl.num_seqs / (ms_step * 1e-3), 1),
+        "detail": {"decode_bytes": int(decode_bytes(wl)), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
+                   "write_bytes": int(write_bytes(wl)), "step_bytes": int(sbytes),
+                   "pct_of_hbm_peak_step": round(100 * sbytes / (ms_step * 1e-3) / 1e9 / peak, 2),
+                   "partition_size_resolved": int(r.resolved), "pool_copies_rotated": r.copies,
+                   "parallelism": f"replicas x{world_size}", "peak_gbs": peak, "peak_kind": peak_kind},
+        "e2e": e2e, "gpu_launches": int(launches),
     }
+    del r
+    torch.cuda.empty_cache()
+    subs = []
+    windows = []
+    if args.configs != "none" and world_size == 1:
+        keys = [k for k, *_ in SUBRECORDS] if args.configs == "all" else args.configs.split(",")
+        for key in keys:
+            rec, win = run_subrecord(args, key, dev, stream, peak, peak_kind)
+            subs.append(rec)
+            windows.append(win)
+    if sampler:
+        sampler.stop()
+        line["clocks"] = sampler.window(t0, t1)
+        line["clocks_calls"] = sampler.window(c0, c1)
+        for rec, win in zip(subs, windows):
+            rec["clocks"] = sampler.window(*win)
+    if subs:
+        line["configs"] = subs
     return line
 
 
-def uses_fused_step(args, wl):
-    """The fused step takes fp32 and 16-bit caches; an FP8 cache's write quantises."""
-    return args.step == "fused" and wl.dtype != "fp8"
-
-
-def pa_dtype(wl):
+def run_subrecord(args, key, dev, stream, peak, peak_kind):
+    """Call and step measurements of one other workload, as for the headline."""
     import torch
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.q_dtype]
+    spec = {k: (c, bs, kd) for k, c, bs, kd in SUBRECORDS}
+    if key not in spec:
+        raise SystemExit(f"unknown --configs entry {key!r}")
+    cfg, bs, kd = spec[key]
+    wl = W.config(cfg, poison=False, block_size=bs, kv_dtype=kd)
+    sub_args = argparse.Namespace(**{**vars(args), "partition": None})
+    r = Runner(sub_args, wl, dev, stream)
+    for i in range(max(3, args.warmup)):
+        r.step(i)
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps, 20)
+    ms, _, t0, _ = r.timed_steps(steps)
+    call_ms, _, t1 = r.timed_calls(args.calls)
+    device_error_check(f"in sub-record {key}")
+    ms_step = ms / steps
+    sbytes = step_bytes(wl)
+    roof = roofline_of(wl, r.fused, call_ms, peak, peak_kind)
+    rec = {"workload": wl.name, "dtype": dtype_label(wl), "partition_size": "auto" if r.ps == -1 else int(r.ps),
+           "call_us": roof["launch_us"], "calls": len(call_ms), "bytes_per_call": roof["bytes_per_launch"],
+           "call_gbs": roof["achieved"], "frac": roof["frac"], "traffic": roof["traffic"],
+           "step_us": round(ms_step * 1e3, 3), "steps": steps,
+           "value_gbs": round(sbytes / (ms_step * 1e-3) / 1e9, 2),
+           "pct_of_hbm_peak_step": round(100 * sbytes / (ms_step * 1e-3) / 1e9 / peak, 2),
+           "tokens_per_s_per_layer": round(wl.num_seqs / (ms_step * 1e-3), 1),
+           "decode_bytes": int(decode_bytes(wl)), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
+           "step": "fused" if r.fused else "separate", "pool_copies_rotated": r.copies}
+    if cfg == 1:
+        rec["note"] = "latency-bound batch (4 short sequences): no roofline claim"
+    del r
+    torch.cuda.empty_cache()
+    return rec, (t0, t1)
 
 
-def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws, fused):
+def run_e2e(args, r):
     """Same step through the Python API, with the step's inputs copied from pinned
     host memory and the output copied back, every step.  The inputs are packed in
     one pinned staging buffer (one host-to-device copy per step)."""
     import torch
-    import paged_kv_cache_306_gb300 as pa
+    wl, dev, stream, s = r.wl, r.dev, r.stream, r.sets[0]
     parts = {
         "q": W.to_torch(wl.q, wl.q_dtype, "cpu"),
         "key": W.to_torch(wl.key, wl.q_dtype, "cpu"),
@@ -384,7 +534,7 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws, fused):
         "slots": torch.from_numpy(wl.slot_mapping),
         "cow": torch.from_numpy(np.ascontiguousarray(wl.cow)),
     }
-    if fused:  # the fused step finds each new token's slot through the block table
+    if r.fused:  # the fused step finds each new token's slot through the block table
         del parts["slots"]
     offs, off = {}, 0
     for k, t in parts.items():
@@ -401,21 +551,20 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws, fused):
     h2d = off
     d2h = out_host.numel() * out_host.element_size()
     steps = min(args.steps, 2000)
-    write, decode = api_calls(wl)
+    cow = devt["cow"] if len(wl.cow) else None
+    import paged_kv_cache_306_gb300 as pa
 
     def step():
         d_stage.copy_(h_stage, non_blocking=True)
-        if fused:
-            pa.pa_decode_step(s["out"], devt["q"], devt["key"], devt["value"], s["k"], s["v"],
-                              devt["cow"] if len(wl.cow) else None, devt["bt"], devt["sl"], wl.scale,
-                              wl.max_seq_len, resolved, ws, stream=stream)
-            out_host.copy_(s["out"], non_blocking=True)
-            return
-        if len(wl.cow):
-            pa.pa_copy_blocks(s["k"], s["v"], devt["cow"], stream=stream)
-        write(devt["key"], devt["value"], s["k"], s["v"], devt["slots"], stream=stream)
-        decode(s["out"], devt["q"], s["k"], s["v"], devt["bt"], devt["sl"], wl.scale, wl.max_seq_len,
-               resolved, ws, stream=stream)
+        if r.fused:
+            r.fused_call(s["out"], devt["q"], devt["key"], devt["value"], s["k"], s["v"], cow, devt["bt"],
+                         devt["sl"], wl.scale, wl.max_seq_len, r.resolved, r.ws, stream=stream)
+        else:
+            if cow is not None:
+                pa.pa_copy_blocks(s["k"], s["v"], cow, stream=stream)
+            r.write(devt["key"], devt["value"], s["k"], s["v"], devt["slots"], stream=stream)
+            r.decode(s["out"], devt["q"], s["k"], s["v"], devt["bt"], devt["sl"], wl.scale, wl.max_seq_len,
+                     r.resolved, r.ws, stream=stream)
         out_host.copy_(s["out"], non_blocking=True)
 
     for _ in range(3):
@@ -428,17 +577,16 @@ def run_e2e(args, wl, dev, stream, s, bt_dev, sl_dev, resolved, ws, fused):
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
-    return {"value": round((decode_bytes(wl) + write_bytes(wl)) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(step_bytes(wl) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 5), "steps": steps, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "copies_per_step": 2}
 
 
 def load_traffic(wl, fused):
     """DRAM bytes per timed call from the committed ncu summary, if it was taken on the
-    current kernel source and on the same call (the fused step for 16-bit and fp32
-    pools, pa_decode_scaled for FP8 pools); otherwise null."""
+    current kernel source and on the same kind of call; otherwise null."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    if not os.path.exists(p) or fused != (wl.dtype != "fp8"):
+    if not os.path.exists(p):
         return None
     try:
         import hashlib
@@ -447,7 +595,9 @@ def load_traffic(wl, fused):
         if d.get("kernel_sha256") != hashlib.sha256(src).hexdigest():
             return None
         ent = d.get("workloads", {}).get(wl.name)
-        return ent.get("dram_bytes_per_launch") if ent else None
+        if not ent or ent.get("fused", True) != fused:
+            return None
+        return ent.get("dram_bytes_per_launch")
     except (OSError, ValueError, KeyError):
         return None
 
@@ -522,7 +672,7 @@ def run_reference(args, wl, cfg, world_size, rank):
     return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world_size, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(wl), "data": "synthetic", "impl": "reference",
-            "config": describe(wl, cfg),
+            "config": config_dict(args, wl, cfg),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -537,8 +687,8 @@ def run_prefill(args, world_size, rank, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     wl = W.prefill_config(poison=False)
-    pool_bytes = wl.num_blocks * wl.num_kv_heads * wl.head_size * wl.block_size * 2 * 2
-    copies = max(2, math.ceil(4 * L2_BYTES / pool_bytes))
+    pbytes = wl.num_blocks * wl.num_kv_heads * wl.head_size * wl.block_size * 2 * 2
+    copies = max(2, math.ceil(4 * L2_BYTES / pbytes))
     sets = [{"q": W.to_torch(wl.q, wl.dtype, dev), "key": W.to_torch(wl.key, wl.dtype, dev),
              "value": W.to_torch(wl.value, wl.dtype, dev), "k": W.to_torch(wl.k_cache, wl.dtype, dev),
              "v": W.to_torch(wl.v_cache, wl.dtype, dev), "out": torch.empty(wl.q.shape, dtype=torch.float16, device=dev)}
@@ -560,8 +710,7 @@ def run_prefill(args, world_size, rank, local_rank):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
-    if pa.pa_get_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+    device_error_check("during warm-up")
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
@@ -578,16 +727,16 @@ def run_prefill(args, world_size, rank, local_rank):
     t1 = time.time()
     launches = pa.pa_launch_count() - launches0
     barrier(world_size, dev)
-    clocks = sampler.stop(t0, t1) if sampler else None
-    if pa.pa_get_device_error() != 0:
-        raise RuntimeError("device error in the timed region")
+    device_error_check("in the timed region")
     ms_step = max_over_ranks(start.elapsed_time(stop), world_size, dev) / args.steps
-    kn = min(args.steps, 500)
+    kn = args.calls
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kn)]
+    c0 = time.time()
     for i in range(kn):
         step(i, evs[i])
     torch.cuda.synchronize(dev)
-    pre_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    c1 = time.time()
+    pre_ms = [a.elapsed_time(b) for a, b in evs]
 
     # end to end: q, key, value, tables, lengths and slots from pinned host memory, out back
     s0 = sets[0]
@@ -626,30 +775,35 @@ def run_prefill(args, world_size, rank, local_rank):
     b.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = a.elapsed_time(b) / ne
+    if sampler:
+        sampler.stop()
 
     flops = prefill_flops(wl)
     peak, kind = measured_peaks("bf16_tflops")
-    achieved = flops / (pre_ms * 1e-3) / 1e12
+    med = float(np.median(pre_ms))
+    achieved = flops / (med * 1e-3) / 1e12
     L = wl.seq_lens
     cfg = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
            "head_size": wl.head_size, "block_size": wl.block_size, "query_tokens": int(wl.query_start_loc[-1]),
            "chunk": 512, "seq_lens": {"min": int(L.min()), "max": int(L.max()), "total": int(L.sum())},
-           "num_blocks": wl.num_blocks, "seed": 406, "flops_per_step": int(flops),
-           "prefill_us": round(pre_ms * 1e3, 2), "pool_copies_rotated": copies,
-           "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e6:.0f} MB rotated",
-           "parallelism": f"replicas x{world_size}"}
+           "num_blocks": wl.num_blocks, "seed": 406,
+           "l2": f"inputs larger than L2: {copies} pool copies of {pbytes / 1e6:.0f} MB rotated"}
     line = {"metric": PREFILL_METRIC, "value": round(world_size * flops / (ms_step * 1e-3) / 1e12, 2),
             "unit": "TFLOP/s", "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfg,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_ws_kernel",
-                         "flops_per_launch": int(flops), "launch_us": round(pre_ms * 1e3, 2),
-                         "peak_source": f"{kind} bf16_tflops (fp16 runs at the bf16 rate)"},
+                         "flops_per_launch": int(flops), "launch_us": spread(pre_ms), "calls": kn,
+                         "peak_source": f"{kind} bf16_tflops (of {kind}; fp16 runs at the bf16 rate)"},
+            "detail": {"flops_per_step": int(flops), "parallelism": f"replicas x{world_size}"},
             "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                     "ms_per_step": round(e2e_ms, 5), "steps": ne, "h2d_bytes_per_step": int(off),
                     "d2h_bytes_per_step": int(out_host.numel() * 2), "copies_per_step": 2},
-            "gpu_launches": int(launches), "clocks": clocks}
+            "gpu_launches": int(launches)}
+    if sampler:
+        line["clocks"] = sampler.window(t0, t1)
+        line["clocks_calls"] = sampler.window(c0, c1)
     return line, wl
 
 
@@ -678,13 +832,14 @@ def prefill_cpu_baseline(wl, seconds=12.0):
                                         f"{dt:.1f} s, fp64 C oracle"}
 
 
-def main(argv=None):
+def parser():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--calls", type=int, default=200, help="single calls timed between events (median, p10, p90)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long")
     ap.add_argument("--block-size", type=int, default=None, help="mixed workload only: 16 or 32")
     ap.add_argument("--partition", type=int, default=None, help="override the workload's partition size")
     ap.add_argument("--mode", choices=["decode", "prefill"], default="decode")
@@ -692,11 +847,21 @@ def main(argv=None):
                     help="store the pool as FP8 E4M3 codes (not for the fp32 tiny workload)")
     ap.add_argument("--step", choices=["fused", "separate"], default="fused",
                     help="one pa_decode_step call, or copy_blocks + reshape_and_cache + decode")
+    ap.add_argument("--configs", default="all",
+                    help="other workloads measured beside the headline: all, none, or a comma list of "
+                         + ",".join(k for k, *_ in SUBRECORDS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap
+
+
+def main(argv=None):
+    ap = parser()
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.calls < 50:
+        ap.error("--calls must be at least 50")
 
     world_size, rank, local_rank = dist_env()
     cfg = WORKLOADS[args.workload]

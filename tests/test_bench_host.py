@@ -71,6 +71,7 @@ def test_reference_arm_prints_one_json_line():
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
+    assert line["config"]["workload"] == "tiny-f32" and line["config"]["bytes"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["steps"] == 3
 
@@ -100,17 +101,50 @@ def test_prefill_flops_count_every_key_each_query_row_sees():
     assert bench.prefill_flops(wl) == 4 * 64 * 8 * keys
 
 
-def test_fused_step_is_the_default_except_for_fp8_pools():
+def test_fused_step_is_the_default_for_every_pool():
     import argparse
     fused = argparse.Namespace(step="fused")
     separate = argparse.Namespace(step="separate")
     assert bench.uses_fused_step(fused, W.config(1, poison=False))
     assert not bench.uses_fused_step(separate, W.config(1, poison=False))
     wl8 = W.make_private("fp8", "fp8", [20, 40], 8, 2, 128, 16, seed=1, q_dtype="f16")
-    assert not bench.uses_fused_step(fused, wl8)
-    # the ncu traffic in profiles/ was taken on the fused call; a separate step reports none
+    assert bench.uses_fused_step(fused, wl8)
+
+
+def test_value_counts_shared_blocks_once():
+    wl = W.config(5, poison=False, block_size=16)
+    assert bench.step_bytes(wl) == bench.decode_bytes(wl, unique=True) + bench.write_bytes(wl)
+    assert bench.step_bytes(wl) < bench.decode_bytes(wl) + bench.write_bytes(wl)
+    assert bench.call_bytes(wl, True) == bench.step_bytes(wl)
+    assert bench.call_bytes(wl, False) == bench.decode_bytes(wl, unique=True)
+
+
+def test_call_spread_is_median_and_percentiles():
+    ms = [0.2] * 80 + [0.1] * 10 + [0.3] * 10 + [5.0]
+    s = bench.spread(ms)
+    assert s["median"] == 200.0 and s["p10"] <= 200.0 <= s["p90"]
+    assert s["p90"] <= 300.0
+
+
+def test_both_arms_state_the_same_config():
+    import argparse
+    args = argparse.Namespace(step="fused", partition=None)
+    wl = W.config(4, poison=False)
+    d = bench.config_dict(args, wl, 4)
+    assert d["workload"] == "long-context-bf16" and d["partition_size"] == 512
+    assert d == bench.config_dict(args, W.config(4, poison=False), 4)
+
+
+def test_headline_defaults_to_the_long_context_layer():
+    a = bench.parser().parse_args([])
+    assert a.workload == "long" and a.gpus == 1 and a.calls >= 200 and a.configs == "all"
+    assert bench.WORKLOADS[a.workload] == 4
+
+
+def test_traffic_record_needs_the_current_kernel_source(tmp_path, monkeypatch):
     wl = W.config(1, poison=False)
-    assert bench.load_traffic(wl, False) is None
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic(wl, True) is None
 
 
 def test_write_bytes_count_tokens_and_copies():
