@@ -59,6 +59,8 @@ def load():
     lib.pa_get_device_error.argtypes = [ctypes.POINTER(i32), P]
     lib.pa_launch_count.argtypes = []
     lib.pa_launch_count.restype = ctypes.c_uint64
+    lib.pa_set_test_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.pa_set_test_wait_limit.restype = None
     for f in (lib.pa_reshape_and_cache, lib.pa_copy_blocks, lib.pa_decode, lib.pa_get_device_error):
         f.restype = i32
     lib.pa_prefill.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32, i32, P]
@@ -126,6 +128,20 @@ def _need_cuda(name, t, dtype=None, dims=None):
         raise PAError(PA_ERR_INVALID_ARG, f"{name} has dtype {t.dtype}, expected {dtype}")
     if dims is not None and t.dim() != dims:
         raise PAError(PA_ERR_INVALID_ARG, f"{name} must have {dims} dims")
+
+
+def _workspace(need, workspace, device, stream):
+    """The caller's workspace when it is large enough, else a fresh one from torch's
+    allocator.  A fresh one used on a stream other than the current one is recorded
+    on that stream, so the allocator does not hand its memory out again before the
+    kernels that use it have finished there."""
+    import torch
+    if not need or (workspace is not None and workspace.numel() * workspace.element_size() >= need):
+        return workspace
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    if stream is not None and stream != torch.cuda.current_stream(device):
+        ws.record_stream(stream)
+    return ws
 
 
 def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
@@ -200,8 +216,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_l
     code = dtype_code(dt)
     lib = load()
     need = lib.pa_decode_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, code)
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    workspace = _workspace(need, workspace, q.device, stream)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(lib.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                         block_tables.shape[1], _ptr(seq_lens), S, max_seq_len, H, hkv, D, bs, nb, float(scale),
@@ -225,8 +240,7 @@ def pa_decode_scaled(out, q, k_cache, v_cache, block_tables, seq_lens, scale, ma
     cc = dtype_code(k_cache.dtype)
     lib = load()
     need = lib.pa_decode_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, cc)
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    workspace = _workspace(need, workspace, q.device, stream)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(lib.pa_decode_scaled(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                block_tables.shape[1], _ptr(seq_lens), S, max_seq_len, H, hkv, D, bs, nb, float(scale),
@@ -261,8 +275,7 @@ def pa_decode_step(out, q, key, value, k_cache, v_cache, src_dst, block_tables, 
     code = dtype_code(dt)
     lib = load()
     need = lib.pa_decode_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, code)
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    workspace = _workspace(need, workspace, q.device, stream)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(lib.pa_decode_step(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
                              _ptr(src_dst) if npairs else None, npairs, _ptr(block_tables), block_tables.shape[1],
@@ -297,8 +310,7 @@ def pa_decode_step_scaled(out, q, key, value, k_cache, v_cache, src_dst, block_t
     cc = dtype_code(k_cache.dtype)
     lib = load()
     need = lib.pa_decode_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, cc)
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    workspace = _workspace(need, workspace, q.device, stream)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(lib.pa_decode_step_scaled(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(src_dst) if npairs else None, npairs, _ptr(block_tables),
@@ -340,6 +352,12 @@ def pa_get_device_error(stream=None):
 
 def pa_launch_count():
     return load().pa_launch_count()
+
+
+def pa_set_test_wait_limit(nanoseconds):
+    """Timeout-path test only: while > 0, the kernels' first pipeline wait runs out after
+    this many nanoseconds on a barrier nothing completes (0 restores normal operation)."""
+    load().pa_set_test_wait_limit(int(nanoseconds))
 
 
 class BlockManager:

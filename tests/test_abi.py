@@ -32,6 +32,32 @@ def lib():
     return B.load()
 
 
+# Every pointer these tests pass lies inside a buffer the test owns: 1 MiB of zeroed
+# device memory when a GPU is present, else host memory (without a device no kernel
+# can launch).  A host-side check that stopped rejecting its case would then launch
+# on memory that exists, never on a made-up address.
+_BUF = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _owned_buffer():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        t = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+        _BUF["base"], _BUF["keep"] = t.data_ptr(), t
+    else:
+        raw = (ctypes.c_ubyte * ((1 << 20) + 256))()
+        _BUF["base"], _BUF["keep"] = (ctypes.addressof(raw) + 255) // 256 * 256, raw
+    yield
+    _BUF.clear()
+
+
+def A(off):
+    """Byte `off` of the owned buffer (off 0 stands for a null pointer)."""
+    assert 0 <= off < (1 << 20)
+    return ctypes.c_void_p(_BUF["base"] + off) if off else ctypes.c_void_p(0)
+
+
 def test_header_declares_the_boundary_calls():
     names = declared_functions()
     for n in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_size",
@@ -57,9 +83,8 @@ def _decode(lib, **kw):
     a = dict(out=8192, q=8192, k=8192, v=8192, bt=8192, mb=4, sl=8192, S=1, msl=16, H=4, Hkv=4, D=128, bs=16,
              nb=8, scale=0.1, ps=0, ws=None, wsb=0, dt=B.PA_F16)
     a.update(kw)
-    P = ctypes.c_void_p
-    return lib.pa_decode(P(a["out"]), P(a["q"]), P(a["k"]), P(a["v"]), P(a["bt"]), a["mb"], P(a["sl"]), a["S"],
-                         a["msl"], a["H"], a["Hkv"], a["D"], a["bs"], a["nb"], a["scale"], a["ps"], P(a["ws"]),
+    return lib.pa_decode(A(a["out"]), A(a["q"]), A(a["k"]), A(a["v"]), A(a["bt"]), a["mb"], A(a["sl"]), a["S"],
+                         a["msl"], a["H"], a["Hkv"], a["D"], a["bs"], a["nb"], a["scale"], a["ps"], A(a["ws"] or 0),
                          a["wsb"], a["dt"], None)
 
 
@@ -101,16 +126,15 @@ def test_plan_rejects_what_decode_rejects(lib):
 
 
 def test_write_path_rejects_bad_arguments_on_the_host(lib):
-    P = ctypes.c_void_p
-    st = lib.pa_reshape_and_cache(P(16), P(16), P(16), P(16), P(16), 4, 2, 60, 16, 8, B.PA_F16, None)
+    st = lib.pa_reshape_and_cache(A(16), A(16), A(16), A(16), A(16), 4, 2, 60, 16, 8, B.PA_F16, None)
     assert st == B.PA_ERR_INVALID_ARG                   # head size not a multiple of x
-    st = lib.pa_reshape_and_cache(P(16), P(16), P(24), P(16), P(16), 4, 2, 64, 16, 8, B.PA_F16, None)
+    st = lib.pa_reshape_and_cache(A(16), A(16), A(24), A(16), A(16), 4, 2, 64, 16, 8, B.PA_F16, None)
     assert st == B.PA_ERR_ALIGNMENT
     st = lib.pa_reshape_and_cache(None, None, None, None, None, 0, 2, 64, 16, 8, B.PA_F16, None)
     assert st == B.PA_OK                                # nothing to write
-    st = lib.pa_copy_blocks(P(16), P(16), P(12), 3, 2, 64, 16, 8, B.PA_F16, None)
+    st = lib.pa_copy_blocks(A(16), A(16), A(12), 3, 2, 64, 16, 8, B.PA_F16, None)
     assert st == B.PA_ERR_ALIGNMENT
-    st = lib.pa_copy_blocks(P(16), P(16), P(16), 3, 2, 64, 16, 8, 5, None)
+    st = lib.pa_copy_blocks(A(16), A(16), A(16), 3, 2, 64, 16, 8, 5, None)
     assert st == B.PA_ERR_INVALID_ARG
 
 
@@ -127,10 +151,9 @@ def _decode_scaled(lib, **kw):
     a = dict(out=8192, q=8192, k=8192, v=8192, bt=8192, mb=4, sl=8192, S=1, msl=16, H=4, Hkv=2, D=128, bs=16,
              nb=8, scale=0.1, ps=0, ws=None, wsb=0, qdt=B.PA_F16, cdt=B.PA_FP8_E4M3, ks=0.5, vs=0.25)
     a.update(kw)
-    P = ctypes.c_void_p
-    return lib.pa_decode_scaled(P(a["out"]), P(a["q"]), P(a["k"]), P(a["v"]), P(a["bt"]), a["mb"], P(a["sl"]),
+    return lib.pa_decode_scaled(A(a["out"]), A(a["q"]), A(a["k"]), A(a["v"]), A(a["bt"]), a["mb"], A(a["sl"]),
                                 a["S"], a["msl"], a["H"], a["Hkv"], a["D"], a["bs"], a["nb"], a["scale"], a["ps"],
-                                P(a["ws"]), a["wsb"], a["qdt"], a["cdt"], a["ks"], a["vs"], None)
+                                A(a["ws"] or 0), a["wsb"], a["qdt"], a["cdt"], a["ks"], a["vs"], None)
 
 
 def test_plain_decode_refuses_an_fp8_cache(lib):
@@ -162,11 +185,10 @@ def test_scaled_decode_with_no_sequences_is_a_no_op(lib):
 
 
 def test_scaled_write_rejects_bad_arguments_on_the_host(lib):
-    P = ctypes.c_void_p
     F8, F16 = B.PA_FP8_E4M3, B.PA_F16
 
     def w(key_dt=F16, cache_dt=F8, ks=0.5, vs=0.5, D=128, key=16, T=4):
-        return lib.pa_reshape_and_cache_scaled(P(key), P(16), P(16), P(16), P(16), T, 2, D, 16, 8, key_dt, cache_dt,
+        return lib.pa_reshape_and_cache_scaled(A(key), A(16), A(16), A(16), A(16), T, 2, D, 16, 8, key_dt, cache_dt,
                                                ks, vs, None)
     assert w(key_dt=F8) == B.PA_ERR_UNSUPPORTED           # codes are not a source dtype
     assert w(ks=0.0) == B.PA_ERR_INVALID_ARG
@@ -179,10 +201,8 @@ def test_scaled_write_rejects_bad_arguments_on_the_host(lib):
 
 
 def test_prefill_rejects_bad_arguments_on_the_host(lib):
-    P = ctypes.c_void_p
-
     def pf(dt=B.PA_F16, D=128, bs=16, T=8, q=8192, S=2, msl=64, mb=4, H=8, Hkv=2):
-        return lib.pa_prefill(P(8192), P(q), P(8192), P(8192), P(8192), mb, P(8192), P(8192), S, T, msl, H, Hkv, D,
+        return lib.pa_prefill(A(8192), A(q), A(8192), A(8192), A(8192), mb, A(8192), A(8192), S, T, msl, H, Hkv, D,
                               bs, 64, 0.1, dt, None)
     assert pf(dt=B.PA_F32) == B.PA_ERR_UNSUPPORTED       # tensor-core prefill: 16-bit caches
     assert pf(dt=B.PA_FP8_E4M3) == B.PA_ERR_UNSUPPORTED
@@ -193,17 +213,16 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert pf(H=6, Hkv=4) == B.PA_ERR_INVALID_ARG
     assert pf(q=8200) == B.PA_ERR_ALIGNMENT
     assert pf(T=0) == B.PA_OK and pf(S=0) == B.PA_OK
-    big = lib.pa_prefill(P(8192), P(8192), P(8192), P(8192), P(8192), 4, P(8192), P(8192), 2, 8, 64, 8, 2, 128, 16,
-                         1 << 24, 0.1, B.PA_F16, None)
+    # null pointers: the row-count check comes first, and without it the null check would refuse
+    big = lib.pa_prefill(None, None, None, None, None, 4, None, None, 2, 8, 64, 8, 2, 128, 16, 1 << 24, 0.1,
+                         B.PA_F16, None)
     assert big == B.PA_ERR_UNSUPPORTED     # 2^24 blocks x 2 kv heads x 128 dims: past the tensor maps' rows
 
 
 def test_fused_step_rejects_bad_arguments_on_the_host(lib):
-    P = ctypes.c_void_p
-
     def st(dt=B.PA_F16, key=8192, value=8192, sd=8192, npairs=1, S=1, D=128, bs=16, msl=16, q=8192):
-        return lib.pa_decode_step(P(8192), P(q), P(key), P(value), P(8192), P(8192), P(sd), npairs, P(8192), 4,
-                                  P(8192), S, msl, 4, 4, D, bs, 8, 0.1, 0, None, 0, dt, None)
+        return lib.pa_decode_step(A(8192), A(q), A(key), A(value), A(8192), A(8192), A(sd), npairs, A(8192), 4,
+                                  A(8192), S, msl, 4, 4, D, bs, 8, 0.1, 0, None, 0, dt, None)
     assert st(dt=B.PA_FP8_E4M3) == B.PA_ERR_UNSUPPORTED   # an FP8 cache is written by the scaled write
     assert st(dt=7) == B.PA_ERR_UNSUPPORTED
     assert st(npairs=-1) == B.PA_ERR_INVALID_ARG
@@ -219,11 +238,9 @@ def test_fused_step_rejects_bad_arguments_on_the_host(lib):
 
 
 def test_scaled_fused_step_rejects_bad_arguments_on_the_host(lib):
-    P = ctypes.c_void_p
-
     def st(qdt=B.PA_F16, cdt=B.PA_FP8_E4M3, ks=0.5, vs=0.5, key=8192, S=1):
-        return lib.pa_decode_step_scaled(P(8192), P(8192), P(key), P(8192), P(8192), P(8192), None, 0, P(8192), 4,
-                                         P(8192), S, 16, 4, 4, 128, 16, 8, 0.1, 0, None, 0, qdt, cdt, ks, vs, None)
+        return lib.pa_decode_step_scaled(A(8192), A(8192), A(key), A(8192), A(8192), A(8192), None, 0, A(8192), 4,
+                                         A(8192), S, 16, 4, 4, 128, 16, 8, 0.1, 0, None, 0, qdt, cdt, ks, vs, None)
     assert st(qdt=B.PA_F32) == B.PA_ERR_UNSUPPORTED       # an FP8 pool is read by fp16 or bf16 queries
     assert st(ks=0.0) == B.PA_ERR_INVALID_ARG
     assert st(vs=float("inf")) == B.PA_ERR_INVALID_ARG
