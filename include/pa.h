@@ -46,6 +46,11 @@
  *     for pa_get_device_error().
  *   - Thread safety: calls may be made from several host threads; the
  *     device-error word and the launch counter are shared per process.
+ *   - The library looks up the device addresses of its own device-side objects
+ *     (the error word, the scratch of pa_decode_noalloc) once per device, on the
+ *     first call that needs them.  A cudaDeviceReset() of a device the library has
+ *     used makes those addresses stale: do not call the library on that device
+ *     again in the same process.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -75,9 +80,12 @@ typedef enum {
 
 typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
-/* partition_size values for pa_decode */
-#define PA_PARTITION_NONE 0    /* one pass over each whole sequence */
-#define PA_PARTITION_AUTO (-1) /* the planner picks from the shape and the SM count */
+/* partition_size values for pa_decode.  The kernels cut sequences wherever their
+ * load-balanced schedule needs to (every warp streams an equal share of all blocks)
+ * and merge the pieces, so no caller partition is ever needed for speed: AUTO means
+ * "no caller partitions" and is resolved to NONE (see pa_decode_plan_partition). */
+#define PA_PARTITION_NONE 0    /* no caller partitions */
+#define PA_PARTITION_AUTO (-1) /* the library's choice: currently always PA_PARTITION_NONE */
 
 /* device-side error codes returned by pa_get_device_error */
 #define PA_DEVERR_NONE 0
@@ -137,10 +145,9 @@ PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src
                          pa_dtype dtype, void* stream);
 
 /*
- * The partition size pa_decode uses for PA_PARTITION_AUTO on the current
- * device: PA_PARTITION_NONE or a positive multiple of block_size.  The choice
- * depends only on the arguments and the device's SM count.  Returns -1 for
- * arguments pa_decode would reject.
+ * The partition size pa_decode uses for PA_PARTITION_AUTO: PA_PARTITION_NONE for
+ * every shape pa_decode accepts (the schedule splits sequences by itself; see
+ * PA_PARTITION_AUTO above).  Returns -1 for arguments pa_decode would reject.
  */
 PA_API int pa_decode_plan_partition(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                              int max_seq_len, int block_size, pa_dtype dtype);
@@ -270,6 +277,19 @@ PA_API pa_status pa_get_device_error(int* code, void* stream);
 PA_API uint64_t pa_launch_count(void);
 
 /*
+ * Diagnostics, for testing the timeout path only (no counterpart in the pages).
+ * Every pipeline wait in the kernels gives up after about 1 s, records
+ * PA_DEVERR_TIMEOUT, waits (bounded) for the copies it has in flight and ends
+ * the kernel early, leaving the outputs of the call unspecified; the context
+ * stays usable.  While `nanoseconds` > 0, decode, the fused step and prefill
+ * launched afterwards make their first pipeline wait (per decode warp, per
+ * prefill CTA) on a barrier that nothing completes, for that long, so that this
+ * path runs for real.  0 (the default) restores normal operation.  The setting
+ * is process-wide and is read when a call enqueues its kernels.
+ */
+PA_API void pa_set_test_wait_limit(uint64_t nanoseconds);
+
+/*
  * Chunked prefill: causal attention of a chunk of new query tokens per sequence
  * over the paged pool -- the step before decode ("vLLM's PagedAttention: why the
  * KV cache is paged", §2.3: a prompt is processed and its K/V enter the cache,
@@ -316,8 +336,10 @@ PA_API pa_status pa_prefill(void* out, const void* q, const void* k_cache, const
  *     (see pa_decode_workspace_size) is rejected with PA_ERR_WORKSPACE before
  *     anything is enqueued; pick a larger partition_size or use pa_decode.
  *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any stream
- *     capture begins.
+ *     device, with that device current) and keeps it for the life of the process;
+ *     make that first call before any stream capture begins.  The address stays
+ *     valid until a cudaDeviceReset() of that device, after which this call must
+ *     not be used on it again.
  *   - Every call on a device shares the one array and it keeps whatever the last
  *     call left there.  Nothing in it has to start at zero: each call writes
  *     every partial result before its merge reads it.  Calls whose work overlaps

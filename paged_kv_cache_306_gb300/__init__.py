@@ -40,5 +40,6 @@ from ._binding import (  # noqa: F401
     pa_prefill,
     pa_launch_count,
     pa_reshape_and_cache,
+    pa_set_test_wait_limit,
     pa_reshape_and_cache_scaled,
 )

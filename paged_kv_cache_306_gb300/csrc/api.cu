@@ -20,6 +20,7 @@ __device__ unsigned g_device_error;
 
 thread_local char t_message[512] = "";
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_test_wait_ns{0};  // pa_set_test_wait_limit
 
 constexpr int kMaxDevices = 64;
 
@@ -213,6 +214,8 @@ const char* pa_last_error_message(void) { return t_message; }
 
 uint64_t pa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+void pa_set_test_wait_limit(uint64_t nanoseconds) { g_test_wait_ns.store(nanoseconds, std::memory_order_relaxed); }
+
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_size,
                                int block_size, int64_t num_blocks, pa_dtype dtype, void* stream) {
@@ -389,6 +392,7 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   p.num_slots = static_cast<int>(pl.slots);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * k_scale * 1.4426950408889634);
   p.out_scale = v_scale;
+  p.test_wait_ns = g_test_wait_ns.load(std::memory_order_relaxed);
 
   if (p.fused && num_copies > 0) {  // the copy-on-write copies: their own kernel, before any token lands
     int n = 0;
@@ -524,6 +528,7 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
   p.group = num_heads / num_kv_heads;
   p.max_seq_len = max_seq_len;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.test_wait_ns = g_test_wait_ns.load(std::memory_order_relaxed);
   for (int c0 = 0; c0 < num_seqs; c0 += pa::kMaxSeqsPerLaunch) {
     p.num_seqs = num_seqs - c0 < pa::kMaxSeqsPerLaunch ? num_seqs - c0 : pa::kMaxSeqsPerLaunch;
     p.block_tables = block_tables + (size_t)c0 * max_blocks_per_seq;

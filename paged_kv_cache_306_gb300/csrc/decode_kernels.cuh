@@ -70,7 +70,7 @@ struct DecodeShape {
   static constexpr int kWarps = decode_warps(2 * kTile, kMode);
   static constexpr int kStages = decode_stages(2 * kTile, kMode);
   static constexpr int kRingBytes = kWarps * kStages * 2 * kTile;
-  static constexpr int kBarBytes = kWarps * kStages * 8;
+  static constexpr int kBarBytes = (kWarps * kStages + 2) * 8;  // the ring's, then one nothing completes (+pad)
   // per-sequence tables: lengths, block prefix, warp sums
   static constexpr int kTableBytes = (kMaxSeqsPerLaunch + (kMaxSeqsPerLaunch + 1) + kWarps + 3) * 4;
   // score row and running state per warp
@@ -85,14 +85,21 @@ struct DecodeShape {
 };
 
 // Wait for block i's stage.  On timeout record the error and drain the copies
-// still in flight (each with its own bounded wait) so none lands after exit.
+// still in flight, the timed-out stage's included (each with its own bounded
+// wait), so none lands after exit.  With test_ns > 0 (the timeout-path test), the
+// warp's first wait is made on `never`, an mbarrier nothing completes, for test_ns
+// nanoseconds: it runs out as a real timeout would, while the drains keep their
+// normal limit, so every copy issued still lands before the warp stops.
 template <int STAGES>
-__device__ __forceinline__ bool wait_stage(uint64_t* bars, int i, int n, unsigned* err, int lane) {
+__device__ __forceinline__ bool wait_stage(uint64_t* bars, uint64_t* never, unsigned long long test_ns, int i, int n,
+                                           unsigned* err, int lane) {
   const int st = i % STAGES;
-  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], (i / STAGES) & 1, kWaitLimitNs));
+  const bool ok =
+      __all_sync(0xffffffffu, (test_ns && i == 0) ? mbar_wait_bounded(never, 0, test_ns)
+                                                  : mbar_wait_bounded(&bars[st], (i / STAGES) & 1, kWaitLimitNs));
   if (!ok) {
     if (lane == 0) set_error(err, kErrTimeout);
-    for (int j = i + 1; j < n && j < i + STAGES; ++j)
+    for (int j = i; j < n && j < i + STAGES; ++j)
       mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1, kWaitLimitNs / 8);
   }
   return ok;
@@ -780,6 +787,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   unsigned char* ring = smem + warp * STAGES * 2 * TILE;
   unsigned char* side = smem + Sh::kSideOffset + warp * STAGES * Sh::kSideStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kRingBytes) + warp * STAGES;
+  uint64_t* never = reinterpret_cast<uint64_t*>(smem + Sh::kRingBytes) + kDecodeWarps * STAGES;
   int* s_len = reinterpret_cast<int*>(smem + Sh::kRingBytes + Sh::kBarBytes);
   int* s_pre = s_len + kMaxSeqsPerLaunch;                 // [S + 1] block prefix per unit
   int* s_wsum = s_pre + kMaxSeqsPerLaunch + 1;             // [warps]
@@ -792,6 +800,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
 
   if (lane == 0) {
     for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
+    if (warp == 0) mbar_init(never, 1);  // visible to the other warps after the table prologue's barriers
     fence_barrier_init();
   }
   __syncwarp();
@@ -1007,7 +1016,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   enter();
 
   for (int k = 0; k < len; ++k) {
-    if (!wait_stage<STAGES>(bars, k, len, p.err, lane)) break;
+    if (!wait_stage<STAGES>(bars, never, p.test_wait_ns, k, len, p.err, lane)) break;
     unsigned char* stage = ring + (k % STAGES) * 2 * TILE;
     const int rem = L - cj * BS;  // valid tokens in this block (>= 1)
     if (p.fused && cj == nblk - 1)  // the sequence's new token: from the step's input, not the pool

@@ -67,6 +67,9 @@ struct DecodeParams {
   const void* new_value;
   float write_k_scale, write_v_scale;  // FP8 pool: stored code = E4M3(x / scale)
   int fused;
+  // > 0 only in the timeout-path test: every warp's first pipeline wait runs out
+  // after this many nanoseconds (see pa_set_test_wait_limit)
+  unsigned long long test_wait_ns;
 };
 
 // CUDA cores, or tensor cores with one (up to 8 query heads per kv head) or two
@@ -142,6 +145,7 @@ struct PrefillParams {
   int group;
   int max_seq_len;
   float scale_log2;
+  unsigned long long test_wait_ns;  // > 0 only in the timeout-path test (see pa_set_test_wait_limit)
 };
 cudaError_t launch_prefill(int dtype, int head_size, int block_size, const PrefillParams& p, cudaStream_t stream,
                            int* launches);

@@ -128,7 +128,8 @@ __device__ __forceinline__ void tma_gather4_g2s(void* dst, const CUtensorMap* ma
 
 // A bounded wait that also gives up at once when another thread of the CTA has
 // given up (*abort set); a thread that times out sets *abort and records the error.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err,
+                                              uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -136,7 +137,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       set_error(err, kErrTimeout);
       return false;
@@ -261,7 +262,7 @@ struct Shape {
   static constexpr int kOffK = kQBytes;          // K ring: 2 buffers
   static constexpr int kOffV = kOffK + 2 * kKBytes;  // V ring: 3 buffers (V is read last)
   static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-  static constexpr int kNumBars = 2 + kVStages + 2 + 2 + 2 + kVStages;
+  static constexpr int kNumBars = 2 + kVStages + 2 + 2 + 2 + kVStages + 1;  // the last: nothing completes it
   static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][8] ints: block reductions
   static constexpr int kSmem = kOffRed + 2 * 8 * 4;            // <= 113 KiB: two CTAs per SM
   static constexpr int kTmemCols = 256;  // S/P[0]: 0..63, S/P[1]: 64..127, O: 128..128+D
@@ -281,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* pfull = sfull + 2;              // [2] P in TMEM, O rescaled and V tail zeroed where needed (128 arrivals)
   uint64_t* pvdone = pfull + 2;             // [2] P V done: P's columns and O are free (commit)
   uint64_t* vfree = pvdone + 2;             // [kVStages] P V done with the V buffer (commit)
+  uint64_t* never = vfree + kVStages;       // nothing completes it: the timeout-path test waits on it
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
   int* s_tile = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, tile (or -1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tile + 3);  // a thread gave up
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&fullv[i], 1);
       mbar_init(&vfree[i], 1);
     }
+    mbar_init(never, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -342,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tmem = *s_tmem;
   const uint32_t t_o = tmem + 2 * kKeys;
   auto wait = [&](uint64_t* bar, int parity) { return wait_or_abort(bar, parity, s_abort, p.err); };
+  int issued_k = 0, issued_v = 0;  // chunks whose K (V) copies the producer issued
 
   if (warp < 4) {
     // ================= softmax: row r, all keys of each chunk =================
@@ -475,7 +479,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       };
       load_table(0);
-      int issued_k = 0, issued_v = 0;
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
         const int sb = c & 1;
@@ -532,18 +535,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         issued_v = c + 1;
         load_table(c + 1);  // lands while this chunk is in flight
       }
-      if (!ok) {  // the copies of the last two chunks issued may still be landing
-        for (int c = issued_k - 2; c < issued_k; ++c)
-          if (c >= 0) mbar_wait_bounded(&fullk[c & 1], (c >> 1) & 1, kWaitNs / 8);
-        for (int c = issued_v - kVStages; c < issued_v; ++c)
-          if (c >= 0) mbar_wait_bounded(&fullv[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
-      }
     }
   } else {
     // ================= MMA issue: S(c), then O += P V(c - 1) =================
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc<T>(kRows, kKeys), kIdO = idesc<T>(kRows, D);
-      bool ok = true;
+      // the timeout-path test: the first wait runs out on `never` (no MMA issued yet);
+      // the producer then drains its copies with the normal limit
+      bool ok = !p.test_wait_ns || wait_or_abort(never, 0, s_abort, p.err, p.test_wait_ns);
       int last_s = -1, last_pv = -1;  // last groups committed
       for (int c = 0; c <= nchunks && ok; ++c) {
         if (c < nchunks) {
@@ -590,6 +589,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   fence_before();
   __syncthreads();
+  // After an abort (whoever raised it, before or after the producer's loop ended) no
+  // consumer waits for the copies still landing: the producer waits (bounded) for the
+  // last chunks it issued, so nothing lands after the CTA exits.
+  if (*s_abort && warp == kProducerWarp && lane == 0) {
+    for (int c = issued_k - 2; c < issued_k; ++c)
+      if (c >= 0) mbar_wait_bounded(&fullk[c & 1], (c >> 1) & 1, kWaitNs / 8);
+    for (int c = issued_v - kVStages; c < issued_v; ++c)
+      if (c >= 0) mbar_wait_bounded(&fullv[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
+  }
   if (warp == 0) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Sh::kTmemCols));
