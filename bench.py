@@ -58,11 +58,13 @@ L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged chunked-prefill attention TFLOP/s (% of GB300 dense bf16 tensor peak)"
-# the workloads measured beside the headline: (key, workload, block size, kv dtype)
+# the workloads measured beside the headline: (key, workload, block size, kv dtype, plain call);
+# the prefix-sharing batch once more through the plain call shows what shared reads gain
 SUBRECORDS = [
-    ("qwen", 2, None, None), ("llama", 3, None, None), ("mixed-bs16", 5, 16, None), ("mixed-bs32", 5, 32, None),
-    ("tiny", 1, None, None), ("long-fp8", 4, None, "fp8"), ("qwen-fp8", 2, None, "fp8"),
-    ("llama-fp8", 3, None, "fp8"), ("mixed-bs16-fp8", 5, 16, "fp8"),
+    ("qwen", 2, None, None, False), ("llama", 3, None, None, False), ("mixed-bs16", 5, 16, None, False),
+    ("mixed-bs32", 5, 32, None, False), ("mixed-bs16-plain", 5, 16, None, True), ("tiny", 1, None, None, False),
+    ("long-fp8", 4, None, "fp8", False), ("qwen-fp8", 2, None, "fp8", False), ("llama-fp8", 3, None, "fp8", False),
+    ("mixed-bs16-fp8", 5, 16, "fp8", False),
 ]
 
 
@@ -249,10 +251,12 @@ def config_dict(args, wl, cfg):
     """The workload as both arms state it: shapes, seed, split, step and the L2 rule."""
     ps = wl.partition_size if args.partition is None else args.partition
     d = describe(wl, cfg)
+    call = "pa_decode_shared" if uses_shared(args, wl) else "pa_decode_step"
     d.update({"partition_size": "auto" if ps == -1 else int(ps),
-              "step": ("fused: one pa_decode_step call (block copies, new tokens and decode) + merge"
+              "step": (f"fused: one {call} call (block copies, new tokens and decode) + merge"
                        if uses_fused_step(args, wl) else
-                       "separate: pa_copy_blocks + reshape_and_cache + decode"),
+                       "separate: pa_copy_blocks + reshape_and_cache + " +
+                       ("pa_decode_shared" if uses_shared(args, wl) else "decode")),
               "l2": f"inputs larger than L2: {pool_copies(wl)} pool copies of {pool_bytes(wl) / 1e6:.0f} MB "
                     f"rotated between steps",
               "bytes": "shared physical blocks counted once"})
@@ -267,6 +271,12 @@ def dtype_label(wl):
 def uses_fused_step(args, wl):
     """One pa_decode_step(_scaled) call per step unless --step separate."""
     return args.step == "fused"
+
+
+def uses_shared(args, wl):
+    """Batches of forked sequences (the mixed workload) go through pa_decode_shared,
+    which reads each shared block once per cluster, unless --plain."""
+    return "group_size" in wl.meta and not getattr(args, "plain", False)
 
 
 def pa_dtype(wl):
@@ -346,6 +356,29 @@ class Runner:
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.write, self.decode, self.fused_call = api_calls(wl)
         self.fused = uses_fused_step(args, wl)
+        self.shared = uses_shared(args, wl)
+        if self.shared:  # the forked sequences' prefix groups, and the larger workspace of the shared call
+            grp, blk = W.prefix_groups(wl.block_tables, wl.seq_lens, wl.block_size)
+            self.grp, self.blk = torch.from_numpy(grp).to(dev), torch.from_numpy(blk).to(dev)
+            need = pa.pa_decode_shared_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
+                                                      wl.max_seq_len, wl.block_size, self.resolved, code)
+            self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            self.fused_call, self.decode = self._shared_calls()
+
+    def _shared_calls(self):
+        import paged_kv_cache_306_gb300 as pa
+        wl = self.wl
+
+        def fused(out, q, key, value, k, v, cow, bt, sl, scale, msl, ps, ws, stream=None, grp=None, blk=None):
+            return pa.pa_decode_shared(out, q, key, value, k, v, cow, bt, sl, self.grp if grp is None else grp,
+                                       self.blk if blk is None else blk, scale, msl, wl.k_scale, wl.v_scale, ps, ws,
+                                       stream=stream)
+
+        def decode(out, q, k, v, bt, sl, scale, msl, ps, ws, stream=None, grp=None, blk=None):
+            return pa.pa_decode_shared(out, q, None, None, k, v, None, bt, sl, self.grp if grp is None else grp,
+                                       self.blk if blk is None else blk, scale, msl, wl.k_scale, wl.v_scale, ps, ws,
+                                       stream=stream)
+        return fused, decode
 
     def step(self, i, ev=None):
         """Step i on pool copy i mod copies; with `ev`, events around the timed call."""
@@ -415,8 +448,8 @@ def roofline_of(wl, fused, call_ms, peak, peak_kind):
     achieved = nbytes / (med * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": load_traffic(wl, fused),
-            "kernel": ("pa_decode_step call: decode_kernel (copies, new tokens, decode) + decode_merge_kernel"
-                       if fused else "pa_decode call: decode_kernel + decode_merge_kernel"),
+            "kernel": ("fused step call: decode_kernel (copies, new tokens, decode) + decode_merge_kernel"
+                       if fused else "decode call: decode_kernel + decode_merge_kernel"),
             "bytes_per_launch": int(nbytes), "launch_us": spread(call_ms), "calls": len(call_ms),
             "peak_source": f"{peak_kind} hbm_gbs (of {peak_kind})"}
 
@@ -486,12 +519,12 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
 def run_subrecord(args, key, dev, stream, peak, peak_kind):
     """Call and step measurements of one other workload, as for the headline."""
     import torch
-    spec = {k: (c, bs, kd) for k, c, bs, kd in SUBRECORDS}
+    spec = {k: (c, bs, kd, plain) for k, c, bs, kd, plain in SUBRECORDS}
     if key not in spec:
         raise SystemExit(f"unknown --configs entry {key!r}")
-    cfg, bs, kd = spec[key]
+    cfg, bs, kd, plain = spec[key]
     wl = W.config(cfg, poison=False, block_size=bs, kv_dtype=kd)
-    sub_args = argparse.Namespace(**{**vars(args), "partition": None})
+    sub_args = argparse.Namespace(**{**vars(args), "partition": None, "plain": plain})
     r = Runner(sub_args, wl, dev, stream)
     for i in range(max(3, args.warmup)):
         r.step(i)
@@ -511,7 +544,8 @@ def run_subrecord(args, key, dev, stream, peak, peak_kind):
            "pct_of_hbm_peak_step": round(100 * sbytes / (ms_step * 1e-3) / 1e9 / peak, 2),
            "tokens_per_s_per_layer": round(wl.num_seqs / (ms_step * 1e-3), 1),
            "decode_bytes": int(decode_bytes(wl)), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
-           "step": "fused" if r.fused else "separate", "pool_copies_rotated": r.copies}
+           "step": "fused" if r.fused else "separate", "pool_copies_rotated": r.copies,
+           "call": "pa_decode_shared" if r.shared else ("pa_decode_step" if r.fused else "pa_decode")}
     if cfg == 1:
         rec["note"] = "latency-bound batch (4 short sequences): no roofline claim"
     del r
@@ -536,6 +570,8 @@ def run_e2e(args, r):
     }
     if r.fused:  # the fused step finds each new token's slot through the block table
         del parts["slots"]
+    if r.shared:  # the prefix groups travel with the step's tables
+        parts["grp"], parts["blk"] = r.grp.cpu(), r.blk.cpu()
     offs, off = {}, 0
     for k, t in parts.items():
         offs[k] = off
@@ -554,17 +590,19 @@ def run_e2e(args, r):
     cow = devt["cow"] if len(wl.cow) else None
     import paged_kv_cache_306_gb300 as pa
 
+    kw = {"grp": devt["grp"], "blk": devt["blk"]} if r.shared else {}
+
     def step():
         d_stage.copy_(h_stage, non_blocking=True)
         if r.fused:
             r.fused_call(s["out"], devt["q"], devt["key"], devt["value"], s["k"], s["v"], cow, devt["bt"],
-                         devt["sl"], wl.scale, wl.max_seq_len, r.resolved, r.ws, stream=stream)
+                         devt["sl"], wl.scale, wl.max_seq_len, r.resolved, r.ws, stream=stream, **kw)
         else:
             if cow is not None:
                 pa.pa_copy_blocks(s["k"], s["v"], cow, stream=stream)
             r.write(devt["key"], devt["value"], s["k"], s["v"], devt["slots"], stream=stream)
             r.decode(s["out"], devt["q"], s["k"], s["v"], devt["bt"], devt["sl"], wl.scale, wl.max_seq_len,
-                     r.resolved, r.ws, stream=stream)
+                     r.resolved, r.ws, stream=stream, **kw)
         out_host.copy_(s["out"], non_blocking=True)
 
     for _ in range(3):
@@ -847,6 +885,8 @@ def parser():
                     help="store the pool as FP8 E4M3 codes (not for the fp32 tiny workload)")
     ap.add_argument("--step", choices=["fused", "separate"], default="fused",
                     help="one pa_decode_step call, or copy_blocks + reshape_and_cache + decode")
+    ap.add_argument("--plain", action="store_true",
+                    help="run the prefix-sharing workload through pa_decode_step / decode, not pa_decode_shared")
     ap.add_argument("--configs", default="all",
                     help="other workloads measured beside the headline: all, none, or a comma list of "
                          + ",".join(k for k, *_ in SUBRECORDS))

@@ -94,6 +94,7 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 #define PA_DEVERR_SLOT 3       /* a slot_mapping entry >= num_blocks * block_size */
 #define PA_DEVERR_TIMEOUT 4    /* a pipeline wait in a kernel gave up after ~1 s */
 #define PA_DEVERR_COPY_ID 5    /* a copy_blocks id outside [0, num_blocks) */
+#define PA_DEVERR_SHARED 6     /* pa_decode_shared: a block declared shared differs between two tables */
 
 /* Human-readable name of a status. Never NULL. */
 PA_API const char* pa_status_string(pa_status s);
@@ -266,6 +267,58 @@ PA_API pa_status pa_decode_step_scaled(void* out, const void* q, const void* key
                                        float scale, int partition_size, void* workspace, size_t workspace_bytes,
                                        pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale, float v_scale,
                                        void* stream);
+
+/*
+ * Decode (or a whole step) over sequences that share prefix blocks, reading each
+ * shared block once for all of its sharers ("vLLM's PagedAttention: why the KV
+ * cache is paged", §4.2: the sequences of one request -- parallel samples of a
+ * common prompt -- map their first logical blocks to the same physical blocks,
+ * with reference counts, until a write forces a copy).  The result is the one the
+ * pages define for each sequence on its own: equal, up to fp32 rounding, to
+ * pa_decode_step_scaled (key != NULL) or pa_decode_scaled (key == value == NULL)
+ * with the same arguments; what changes is that a block held by several sequences
+ * of a cluster leaves DRAM once.
+ *
+ * prefix_group   int32 [num_seqs]: a group is a run of consecutive sequences with
+ *                equal values (any ids; a sequence that shares nothing can have a
+ *                value of its own).
+ * prefix_blocks  int32 [num_seqs]: sequence s holds the first prefix_blocks[s]
+ *                blocks of its group's common prefix, so that any two sequences s,
+ *                t of a group have equal block-table entries 0 .. min(prefix_blocks[s],
+ *                prefix_blocks[t]) - 1.  (Comparing every table of a group with
+ *                that of its longest sequence gives such values; so does
+ *                pa_bm_prefix_groups.)  Values beyond a sequence's blocks are
+ *                clipped.  A declared entry that differs is reported as
+ *                PA_DEVERR_SHARED and the affected outputs are unspecified.
+ *
+ * How it is used: a group is cut into clusters of C / (num_heads / num_kv_heads)
+ * consecutive sequences (C = 16 query heads for 16-bit caches, 8 for FP8 caches,
+ * whose kernel keeps more warps); the first B blocks of a cluster (B: the second largest
+ * prefix_blocks among its members) are attended once, with the query heads of all
+ * members in one tensor-core tile (a member's columns take part in the blocks it
+ * holds), and merged with each member's own blocks.  The last block of every
+ * sequence is always read as its own.  Clusters need a 16-bit cache with at most 8
+ * query heads per kv head, or an FP8 cache with at most 4; for other shapes the call runs as
+ * pa_decode_step_scaled / pa_decode_scaled.  A launch covers at most 1024
+ * sequences; a cluster never spans two launches.
+ *
+ * key, value may be NULL (both): decode only; then num_pairs must be 0.  Every
+ * other argument as in pa_decode_step_scaled, except that the workspace must hold
+ * pa_decode_shared_workspace_size() bytes.
+ */
+PA_API pa_status pa_decode_shared(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                                  void* v_cache, const int64_t* src_dst, int64_t num_pairs,
+                                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                  const int32_t* prefix_group, const int32_t* prefix_blocks, int num_seqs,
+                                  int max_seq_len, int num_heads, int num_kv_heads, int head_size, int block_size,
+                                  int64_t num_blocks, float scale, int partition_size, void* workspace,
+                                  size_t workspace_bytes, pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                                  float v_scale, void* stream);
+
+/* Workspace bytes of pa_decode_shared (0 for arguments it would reject). */
+PA_API size_t pa_decode_shared_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                              int max_seq_len, int block_size, int partition_size,
+                                              pa_dtype cache_dtype);
 
 /*
  * Read and clear the first device-side error recorded on the current device

@@ -84,6 +84,16 @@ PA_API pa_status pa_bm_seq_len(const pa_block_manager* bm, int64_t seq_id, int64
 PA_API pa_status pa_bm_block_tables(const pa_block_manager* bm, const int64_t* seq_ids, int num_seqs,
                                     int32_t* block_tables, int max_blocks_per_seq, int32_t* seq_lens);
 
+/* For pa_decode_shared: the listed sequences' prefix groups -- runs of consecutive
+ * entries whose first logical block is one physical block (sequences of one fork
+ * family that still share their prefix) -- with prefix_group[i] the index of the
+ * run's first entry, and prefix_blocks[i] the leading logical blocks sequence i
+ * holds in the same physical blocks as the run's longest sequence (0 for a run
+ * of one).  List the sequences of a fork family next to each other to let decode
+ * read their common blocks once. */
+PA_API pa_status pa_bm_prefix_groups(const pa_block_manager* bm, const int64_t* seq_ids, int num_seqs,
+                                     int32_t* prefix_group, int32_t* prefix_blocks);
+
 /* Number of sequences that reference a block (0 when it is free). */
 PA_API pa_status pa_bm_refcount(const pa_block_manager* bm, int64_t block, int* refcount);
 

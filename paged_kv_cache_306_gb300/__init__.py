@@ -32,6 +32,8 @@ from ._binding import (  # noqa: F401
     pa_copy_blocks,
     pa_decode,
     pa_decode_scaled,
+    pa_decode_shared,
+    pa_decode_shared_workspace_size,
     pa_decode_step,
     pa_decode_step_scaled,
     pa_decode_plan_partition,

@@ -18,7 +18,8 @@ PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PARTITION_NONE = 0
 PARTITION_AUTO = -1
 DEVICE_ERRORS = {0: "none", 1: "block id outside the pool", 2: "seq_len outside [1, max_seq_len]",
-                 3: "slot outside the pool", 4: "pipeline wait timed out", 5: "copy id outside the pool"}
+                 3: "slot outside the pool", 4: "pipeline wait timed out", 5: "copy id outside the pool",
+                 6: "a block declared shared differs between two tables"}
 
 _lib = None
 
@@ -61,6 +62,11 @@ def load():
     lib.pa_launch_count.restype = ctypes.c_uint64
     lib.pa_set_test_wait_limit.argtypes = [ctypes.c_uint64]
     lib.pa_set_test_wait_limit.restype = None
+    lib.pa_decode_shared.argtypes = [P, P, P, P, P, P, P, i64, P, i32, P, P, P, i32, i32, i32, i32, i32, i32, i64,
+                                     f32, i32, P, sz, i32, i32, f32, f32, P]
+    lib.pa_decode_shared.restype = i32
+    lib.pa_decode_shared_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.pa_decode_shared_workspace_size.restype = sz
     for f in (lib.pa_reshape_and_cache, lib.pa_copy_blocks, lib.pa_decode, lib.pa_get_device_error):
         f.restype = i32
     lib.pa_prefill.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32, i32, P]
@@ -84,6 +90,8 @@ def load():
     lib.pa_bm_seq_len.argtypes = [P, i64, ctypes.POINTER(i64)]
     lib.pa_bm_block_tables.argtypes = [P, P, i32, P, i32, P]
     lib.pa_bm_refcount.argtypes = [P, i64, ctypes.POINTER(i32)]
+    lib.pa_bm_prefix_groups.argtypes = [P, P, i32, P, P]
+    lib.pa_bm_prefix_groups.restype = i32
     for f in (lib.pa_bm_create, lib.pa_bm_add_sequence, lib.pa_bm_fork, lib.pa_bm_free_sequence,
               lib.pa_bm_append_tokens, lib.pa_bm_seq_len, lib.pa_bm_block_tables, lib.pa_bm_refcount):
         f.restype = i32
@@ -320,6 +328,59 @@ def pa_decode_step_scaled(out, q, key, value, k_cache, v_cache, src_dst, block_t
     return workspace
 
 
+def pa_decode_shared_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size,
+                                    partition_size, cache_dtype):
+    return load().pa_decode_shared_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len,
+                                                  block_size, partition_size,
+                                                  cache_dtype if isinstance(cache_dtype, int) else dtype_code(cache_dtype))
+
+
+def pa_decode_shared(out, q, key, value, k_cache, v_cache, src_dst, block_tables, seq_lens, prefix_group,
+                     prefix_blocks, scale, max_seq_len, k_scale=1.0, v_scale=1.0, partition_size=PARTITION_AUTO,
+                     workspace=None, stream=None):
+    """Decode (key/value given: the whole fused step) over sequences that share prefix
+    blocks: prefix_group (int32 [S], runs of equal values) and prefix_blocks (int32 [S],
+    the leading blocks each sequence holds of its group's common prefix) describe the
+    sharing; each shared block is read once per cluster of sequences that hold it.
+    Returns the workspace tensor used (or None)."""
+    import torch
+    dt = q.dtype
+    _need_cuda("q", q, dt, 3)
+    _need_cuda("out", out, dt, 3)
+    _need_cuda("k_cache", k_cache, None, 5)
+    _need_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _need_cuda("block_tables", block_tables, torch.int32, 2)
+    _need_cuda("seq_lens", seq_lens, torch.int32, 1)
+    _need_cuda("prefix_group", prefix_group, torch.int32, 1)
+    _need_cuda("prefix_blocks", prefix_blocks, torch.int32, 1)
+    S, H, D = q.shape
+    nb, hkv, _, bs = v_cache.shape
+    if prefix_group.numel() != S or prefix_blocks.numel() != S:
+        raise PAError(PA_ERR_INVALID_ARG, "prefix_group and prefix_blocks must have num_seqs entries")
+    npairs = 0
+    if key is not None:
+        _need_cuda("key", key, dt, 3)
+        _need_cuda("value", value, dt, 3)
+        if key.shape != (S, hkv, D) or value.shape != (S, hkv, D):
+            raise ValueError(f"key/value must be [{S}, {hkv}, {D}]")
+        if src_dst is not None:
+            _need_cuda("src_dst", src_dst, torch.int64)
+            npairs = src_dst.numel() // 2
+    elif src_dst is not None and src_dst.numel():
+        raise PAError(PA_ERR_INVALID_ARG, "block copies come with a step's new tokens (key, value)")
+    cc = dtype_code(k_cache.dtype)
+    lib = load()
+    need = lib.pa_decode_shared_workspace_size(S, H, hkv, D, max_seq_len, bs, partition_size, cc)
+    workspace = _workspace(need, workspace, q.device, stream)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib.pa_decode_shared(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(src_dst) if npairs else None, npairs, _ptr(block_tables), block_tables.shape[1],
+                               _ptr(seq_lens), _ptr(prefix_group), _ptr(prefix_blocks), S, max_seq_len, H, hkv, D,
+                               bs, nb, float(scale), partition_size, _ptr(workspace), ws_bytes, dtype_code(dt), cc,
+                               float(k_scale), float(v_scale), _stream(stream)))
+    return workspace
+
+
 def pa_prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, max_seq_len, stream=None):
     """Chunked prefill: query rows query_start_loc[s] .. query_start_loc[s+1]-1 are the last
     tokens of sequence s (seq_lens[s] tokens in the cache, theirs included) and attend
@@ -430,6 +491,18 @@ class BlockManager:
         check(self._lib.pa_bm_block_tables(self._h, ids.ctypes.data if n else None, n, bt.ctypes.data,
                                            int(max_blocks_per_seq), sl.ctypes.data))
         return bt[:n].copy(), sl[:n].copy()
+
+    def prefix_groups(self, seq_ids):
+        """(prefix_group, prefix_blocks), int32 [n] each: pa_decode_shared's description of
+        which listed sequences share prefix blocks (runs of one fork family)."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, np.int64)
+        n = len(ids)
+        grp = np.empty(max(n, 1), np.int32)
+        blk = np.empty(max(n, 1), np.int32)
+        check(self._lib.pa_bm_prefix_groups(self._h, ids.ctypes.data if n else None, n, grp.ctypes.data,
+                                            blk.ctypes.data))
+        return grp[:n].copy(), blk[:n].copy()
 
     def refcount(self, block):
         r = ctypes.c_int(0)

@@ -94,13 +94,27 @@ pa_status check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int 
 struct DecodePlan {
   pa::DecodeKind kind;
   int units;         // head units per sequence
-  int rows;          // query rows per unit
+  int rows;          // query rows per partial-result slot
   int part_blocks;   // caller partition in blocks (a huge value when none)
   int chunk;         // sequences per launch
   int grid;          // CTAs of the main kernel (all resident)
+  int members;       // sequences per shared-prefix cluster; 0: no shared prefixes
   long long slots;   // partial-result slots
-  size_t off_tag, off_ml, off_o, off_first, off_last, bytes;
+  size_t off_tag, off_ml, off_o, off_first, off_last, off_info, bytes;
 };
+
+// Shared prefixes pay off where the tensor-core tile has room for the query heads
+// of several sequences.  16-bit caches: clusters fill the 16 columns of two 8-head
+// tiles (at most 8 query heads per kv head).  FP8 caches: one 8-head tile, which
+// keeps their 16-warp kernel (the widening of the codes needs the warps); at most
+// 4 query heads per kv head.  Elsewhere the shared-prefix call runs the plain
+// schedule.
+int shared_members(pa_dtype dtype, int num_heads, int num_kv_heads) {
+  const int group = num_heads / num_kv_heads;
+  const int cols = dtype == PA_FP8_E4M3 ? 8 : 16;
+  if (dtype == PA_F32 || 2 * group > cols) return 0;
+  return cols / group;
+}
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -110,11 +124,15 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // kMaxSeqsPerLaunch sequences.  Partial slots: one per warp plus one per segment,
 // the most pieces a launch can leave (pieces start at warp or segment boundaries).
 pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len, int block_size,
-                    int partition_size, pa_dtype dtype, DecodePlan* pl) {
+                    int partition_size, pa_dtype dtype, DecodePlan* pl, bool shared = false) {
   const int group = num_heads / num_kv_heads;
-  pl->kind = pa::decode_kind(static_cast<int>(dtype), group);
+  pl->members = shared ? shared_members(dtype, num_heads, num_kv_heads) : 0;
+  if (pl->members && (max_seq_len + block_size - 1) / block_size >= (1 << pa::kInfoOffBits))
+    return fail(PA_ERR_UNSUPPORTED, "shared prefixes: at most %d blocks per sequence", (1 << pa::kInfoOffBits) - 1);
+  pl->kind = pl->members ? (dtype == PA_FP8_E4M3 ? pa::DecodeKind::kMma8 : pa::DecodeKind::kMma16)
+                         : pa::decode_kind(static_cast<int>(dtype), group);
   pl->units = pa::decode_units(pl->kind, num_heads, num_kv_heads);
-  pl->rows = pa::decode_rows(pl->kind, num_heads, num_kv_heads);
+  pl->rows = pl->members ? (dtype == PA_FP8_E4M3 ? 8 : 16) : pa::decode_rows(pl->kind, num_heads, num_kv_heads);
   const int nblk_max = ceil_div(max_seq_len, block_size);
   pl->part_blocks = partition_size > 0 ? partition_size / block_size : (1 << 30);
   long long chunk = num_seqs < pa::kMaxSeqsPerLaunch ? num_seqs : pa::kMaxSeqsPerLaunch;
@@ -130,7 +148,8 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   if (grid > (long long)sms * ctas) grid = (long long)sms * ctas;
   if (grid < 1) grid = 1;
   pl->grid = static_cast<int>(grid);
-  const long long segs = chunk * pl->units;
+  // segments: one per (sequence, unit); with shared prefixes two (shared part, own part)
+  const long long segs = chunk * pl->units * (pl->members ? 2 : 1);
   pl->slots = grid * warps + segs;
   if (pl->slots > 0x7fffffffLL || segs > 0x7fffffffLL)
     return fail(PA_ERR_UNSUPPORTED, "too many partial results (%lld); use a larger partition_size", pl->slots);
@@ -145,6 +164,8 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   off = align256(off + (size_t)segs * sizeof(int));
   pl->off_last = off;
   off = align256(off + (size_t)segs * sizeof(int));
+  pl->off_info = off;
+  if (pl->members) off = align256(off + (size_t)chunk * 2 * sizeof(int));
   pl->bytes = off;
   return PA_OK;
 }
@@ -331,7 +352,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
                              int block_size, int64_t num_blocks, float scale, int partition_size, void* workspace,
                              size_t workspace_bytes, pa_dtype q_dtype, pa_dtype dtype, float k_scale, float v_scale,
                              void* stream, const void* new_key = nullptr, const void* new_value = nullptr,
-                             const int64_t* copy_pairs = nullptr, int64_t num_copies = 0) {
+                             const int64_t* copy_pairs = nullptr, int64_t num_copies = 0,
+                             const int32_t* prefix_group = nullptr, const int32_t* prefix_blocks = nullptr) {
   // new_key != nullptr: the fused step (pa_decode_step), already validated there.
   // `dtype` is the cache dtype from here on; q and out have q_dtype.
   pa_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, dtype);
@@ -359,8 +381,11 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return fail(PA_ERR_ALIGNMENT, "q/out/caches need 16-byte, block_tables/seq_lens 4-byte alignment");
 
+  if (prefix_group && (!aligned(prefix_group, 4) || !aligned(prefix_blocks, 4)))
+    return fail(PA_ERR_ALIGNMENT, "prefix_group and prefix_blocks need 4-byte alignment");
   DecodePlan pl;
-  st = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, partition_size, dtype, &pl);
+  st = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, partition_size, dtype, &pl,
+                 prefix_group != nullptr);
   if (st != PA_OK) return st;
   if (!workspace || workspace_bytes < pl.bytes)
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pl.bytes, workspace ? workspace_bytes : 0);
@@ -373,6 +398,9 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.seg_first = reinterpret_cast<int*>(ws + pl.off_first);
   p.seg_last = reinterpret_cast<int*>(ws + pl.off_last);
+  p.seq_info = reinterpret_cast<int*>(ws + pl.off_info);
+  p.shared = pl.members > 0;
+  p.members = pl.members;
   p.fused = new_key != nullptr;
   p.write_k_scale = k_scale;
   p.write_v_scale = v_scale;
@@ -411,6 +439,9 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     p.out = static_cast<char*>(out) + (size_t)c0 * row_bytes;
     p.block_tables = block_tables + (size_t)c0 * max_blocks_per_seq;
     p.seq_lens = seq_lens + c0;
+    // a chunk's first sequence starts a cluster: its link to the previous chunk is not read
+    p.prefix_group = p.shared ? prefix_group + c0 : nullptr;
+    p.prefix_blocks = p.shared ? prefix_blocks + c0 : nullptr;
     if (p.fused) {  // the new rows come in the query dtype (an FP8 pool quantises them itself)
       const size_t kv_row_bytes = (size_t)num_kv_heads * head_size * elem_bytes(q_dtype);
       p.new_key = static_cast<const char*>(new_key) + (size_t)c0 * kv_row_bytes;
@@ -486,6 +517,46 @@ pa_status pa_decode_step(void* out, const void* q, const void* key, const void* 
                                max_blocks_per_seq, seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads, head_size,
                                block_size, num_blocks, scale, partition_size, workspace, workspace_bytes, dtype, dtype,
                                1.f, 1.f, stream);
+}
+
+size_t pa_decode_shared_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_seq_len,
+                                       int block_size, int partition_size, pa_dtype cache_dtype) {
+  if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, cache_dtype) != PA_OK)
+    return 0;
+  if (partition_size == PA_PARTITION_AUTO) partition_size = PA_PARTITION_NONE;
+  if (partition_size < 0 || (partition_size > 0 && partition_size % block_size) || num_seqs == 0) return 0;
+  DecodePlan pl;
+  if (make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_seq_len, block_size, partition_size, cache_dtype,
+                &pl, true) != PA_OK)
+    return 0;
+  return pl.bytes;
+}
+
+pa_status pa_decode_shared(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                           void* v_cache, const int64_t* src_dst, int64_t num_pairs, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* prefix_group,
+                           const int32_t* prefix_blocks, int num_seqs, int max_seq_len, int num_heads,
+                           int num_kv_heads, int head_size, int block_size, int64_t num_blocks, float scale,
+                           int partition_size, void* workspace, size_t workspace_bytes, pa_dtype q_dtype,
+                           pa_dtype cache_dtype, float k_scale, float v_scale, void* stream) {
+  if (cache_dtype != PA_F32 && cache_dtype != PA_F16 && cache_dtype != PA_BF16 && cache_dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "unknown cache dtype %d", static_cast<int>(cache_dtype));
+  if (!elem_bytes(q_dtype)) return fail(PA_ERR_INVALID_ARG, "unknown query dtype %d", static_cast<int>(q_dtype));
+  if (num_seqs > 0 && (!prefix_group || !prefix_blocks))
+    return fail(PA_ERR_INVALID_ARG, "null prefix_group or prefix_blocks");
+  if ((key == nullptr) != (value == nullptr)) return fail(PA_ERR_INVALID_ARG, "key and value: both or neither");
+  if (num_pairs < 0 || num_pairs > 0x7fffffffLL) return fail(PA_ERR_INVALID_ARG, "num_pairs %lld", (long long)num_pairs);
+  if (num_pairs > 0 && (!src_dst || !aligned(src_dst, 8)))
+    return fail(src_dst ? PA_ERR_ALIGNMENT : PA_ERR_INVALID_ARG, "src_dst must be a non-null, 8-byte aligned int64 array");
+  if (num_pairs > 0 && !key) return fail(PA_ERR_INVALID_ARG, "block copies come with the step's new tokens");
+  if (key && (!aligned(key, 16) || !aligned(value, 16))) return fail(PA_ERR_ALIGNMENT, "key/value need 16-byte alignment");
+  if (num_seqs == 0 && num_pairs > 0)  // nothing to decode: the copies alone
+    return pa_copy_blocks(k_cache, v_cache, src_dst, num_pairs, num_kv_heads, head_size, block_size, num_blocks,
+                          cache_dtype, stream);
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                     num_heads, num_kv_heads, head_size, block_size, num_blocks, scale, partition_size, workspace,
+                     workspace_bytes, q_dtype, cache_dtype, k_scale, v_scale, stream, key, value, src_dst, num_pairs,
+                     prefix_group, prefix_blocks);
 }
 
 pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -215,6 +215,41 @@ pa_status pa_bm_block_tables(const pa_block_manager* bm, const int64_t* seq_ids,
   return PA_OK;
 }
 
+pa_status pa_bm_prefix_groups(const pa_block_manager* bm, const int64_t* seq_ids, int num_seqs, int32_t* prefix_group,
+                              int32_t* prefix_blocks) {
+  if (!bm) return pa::record_failure(PA_ERR_INVALID_ARG, "null manager");
+  std::lock_guard<std::mutex> lock(bm->mu);
+  if (num_seqs < 0) return failf(PA_ERR_INVALID_ARG, "num_seqs %lld", static_cast<long long>(num_seqs));
+  if (num_seqs > 0 && (!seq_ids || !prefix_group || !prefix_blocks))
+    return pa::record_failure(PA_ERR_INVALID_ARG, "null pointer");
+  std::vector<const std::vector<int32_t>*> rows(static_cast<size_t>(num_seqs));
+  for (int i = 0; i < num_seqs; ++i) {
+    auto it = bm->seqs.find(seq_ids[i]);
+    if (it == bm->seqs.end()) return failf(PA_ERR_INVALID_ARG, "no sequence %lld", seq_ids[i]);
+    rows[static_cast<size_t>(i)] = &it->second.blocks;
+  }
+  // a group: consecutive sequences whose first block is one physical block (sharing is
+  // always a prefix, so two sequences that share anything share block 0); each is
+  // compared with the longest sequence of its group
+  for (int i = 0; i < num_seqs;) {
+    int j = i + 1;
+    while (j < num_seqs && !rows[i]->empty() && !rows[j]->empty() && (*rows[j])[0] == (*rows[i])[0]) ++j;
+    int ref = i;
+    for (int t = i; t < j; ++t)
+      if (rows[t]->size() > rows[ref]->size()) ref = t;
+    for (int t = i; t < j; ++t) {
+      const std::vector<int32_t>& a = *rows[t];
+      const std::vector<int32_t>& r = *rows[ref];
+      size_t n = 0;
+      while (n < a.size() && n < r.size() && a[n] == r[n]) ++n;
+      prefix_group[t] = i;
+      prefix_blocks[t] = j - i > 1 ? static_cast<int32_t>(n) : 0;
+    }
+    i = j;
+  }
+  return PA_OK;
+}
+
 pa_status pa_bm_refcount(const pa_block_manager* bm, int64_t block, int* refcount) {
   if (!bm || !refcount) return pa::record_failure(PA_ERR_INVALID_ARG, "null pointer");
   std::lock_guard<std::mutex> lock(bm->mu);

@@ -72,7 +72,14 @@ struct DecodeShape {
   static constexpr int kRingBytes = kWarps * kStages * 2 * kTile;
   static constexpr int kBarBytes = (kWarps * kStages + 2) * 8;  // the ring's, then one nothing completes (+pad)
   // per-sequence tables: lengths, block prefix, warp sums
-  static constexpr int kTableBytes = (kMaxSeqsPerLaunch + (kMaxSeqsPerLaunch + 1) + kWarps + 3) * 4;
+  // the cost-weighted prefix of the shared-prefix schedule ([S + 1] ints) is read only
+  // while the warps find their ranges, before any copy is issued: it borrows the fused
+  // step's side buffers where they are large enough, else it has room of its own here
+  static constexpr int kWpreBytes = ((kMaxSeqsPerLaunch + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kSideStageBytes = 2 * D * (kElem < 2 ? 2 : kElem);
+  static constexpr bool kWpreInSide = kWarps * kStages * kSideStageBytes >= kWpreBytes;
+  static constexpr int kTableBytes = (kMaxSeqsPerLaunch + (kMaxSeqsPerLaunch + 1) + kWarps + 3 + 2 * kMaxSeqsPerLaunch) * 4 +
+                                     (kWpreInSide ? 0 : kWpreBytes);
   // score row and running state per warp
   static constexpr int kRows = kMode ? 8 * kMode : 1;
   static constexpr int kStateBytes = kWarps * BS * 4 + kWarps * kRows * (D + 2) * 4;
@@ -82,6 +89,10 @@ struct DecodeShape {
   static constexpr int kSideStage = 2 * D * (kElem < 2 ? 2 : kElem);
   static constexpr int kSmemBytes = kSideOffset + kWarps * kStages * kSideStage;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kSideStage == kSideStageBytes, "side stage");
+  // the regions after the tables hold float2 / float4 accesses: keep every region 16-byte aligned
+  static_assert(kRingBytes % 16 == 0 && kBarBytes % 16 == 0 && kTableBytes % 16 == 0 && kStateBytes % 16 == 0,
+                "shared-memory regions must stay 16-byte aligned");
 };
 
 // Wait for block i's stage.  On timeout record the error and drain the copies
@@ -142,6 +153,9 @@ __device__ __forceinline__ void zero_tail_v(unsigned char* vtile, int rem, int l
 // the token rows of K are loaded in the order perm(), so that S^T's rows line up
 // with the permuted token columns of V^T.
 //
+// Only the 8-column tiles that hold query rows run (nt_ of them; a unit of up to 8
+// heads in a 16-column kernel uses one): block() dispatches to the tile count once.
+//
 // kEarly (16-bit caches): block() is preceded by fetch(), which reads every K and
 // V fragment of the block out of the stage into registers, so the kernel can
 // refill the stage before the math instead of after it.
@@ -161,6 +175,7 @@ struct MmaMath {
     return kFp8 ? 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3) : r;
   }
 
+  int nt_;                 // 8-column tiles in use (rows 0..nh-1): the others are skipped
   uint32_t qb[KS][NH][2];  // Q^T B fragments
   float acc[KS][NH][4];    // O^T accumulators
   uint32_t kf[FM][FK][4], vf[FM][FK][4];  // the block's K and V^T A fragments (kEarly)
@@ -198,13 +213,16 @@ struct MmaMath {
     }
   }
 
-  // B fragments of heads 0..nh-1 of q (row stride D), zero past nh, and the
-  // heads' score factors.
-  __device__ __forceinline__ void load_q(const T* q, int nh, float scale_log2) {
+  // B fragments of query rows 0..nh-1, zero past nh, and the rows' score factors.
+  // Row h is head h % group of sequence h / group: q points at the first row and
+  // seq_stride is the distance between sequences (the rows of one unit, h < group,
+  // are consecutive heads; a shared segment stacks the units of its members).
+  __device__ __forceinline__ void load_q(const T* q, int nh, float scale_log2, int group, long long seq_stride) {
+    nt_ = NH == 1 ? 1 : min(NH, (nh + 7) >> 3);
 #pragma unroll
     for (int n = 0; n < NH; ++n) {
       const int h = 8 * n + g;
-      const T* qh = q + h * D;
+      const T* qh = q + (h / group) * seq_stride + (h % group) * D;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         // operand k = 2t4, 2t4+1 and 2t4+8, 2t4+9 read dims d0, d0+1 and d1, d1+1
@@ -279,7 +297,30 @@ struct MmaMath {
     e4m3x4_to_f16x2(r[3], a1[1], a1[3]);
   }
 
-  __device__ __forceinline__ void block(unsigned char* stage, int tile_bytes, int rem, float scale_log2) {
+  // Column (query row) masks of a shared segment: the member each of this lane's
+  // columns belongs to; a block counts only for the members whose own table holds it.
+  int col_member_[NH][2];
+  __device__ __forceinline__ void set_columns(int group) {
+#pragma unroll
+    for (int n = 0; n < NH; ++n)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) col_member_[n][hh] = (8 * n + 2 * t4 + hh) / group;
+  }
+
+  // One block: `rem` valid tokens; `live` has bit i set for every member i whose
+  // columns take part (all ones outside shared segments).
+  __device__ __forceinline__ void block(unsigned char* stage, int tile_bytes, int rem, float scale_log2,
+                                        uint32_t live = 0xffffffffu) {
+    if (NH == 1 || nt_ == NH)
+      block_t<NH>(stage, tile_bytes, rem, scale_log2, live);
+    else
+      block_t<1>(stage, tile_bytes, rem, scale_log2, live);
+  }
+
+  // block() over the first NT 8-column tiles.
+  template <int NT>
+  __device__ __forceinline__ void block_t(unsigned char* stage, int tile_bytes, int rem, float scale_log2,
+                                          uint32_t live) {
     const uint32_t kb = smem_addr(stage), vb = kb + tile_bytes;
     // S^T = K Q^T for the block's BS tokens.
     float sc[MT][NH][4];
@@ -297,7 +338,7 @@ struct MmaMath {
           uint32_t a0[4], a1[4];
           widen(r, a0, a1);
 #pragma unroll
-          for (int n = 0; n < NH; ++n) {
+          for (int n = 0; n < NT; ++n) {
             mma_16816<OT>(sc[mt][n], a0, qb[2 * kp][n][0], qb[2 * kp][n][1]);
             mma_16816<OT>(sc[mt][n], a1, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
           }
@@ -313,62 +354,82 @@ struct MmaMath {
             ldsm_x4(kb + k_lane_off + (2 * ks * BS + 16 * mt) * 16, a[0], a[1], a[2], a[3]);
           }
 #pragma unroll
-          for (int n = 0; n < NH; ++n) mma_16816<OT>(sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
+          for (int n = 0; n < NT; ++n) mma_16816<OT>(sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
         }
       }
     }
-    // Online softmax update per head (column), log2 domain; tokens past the sequence get -inf.
+    // Online softmax update per head (column), log2 domain; tokens past the sequence
+    // (and every token, for a column whose member does not take this block) get -inf.
+    bool col_ok[NH][2];
+#pragma unroll
+    for (int n = 0; n < NH; ++n)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) col_ok[n][hh] = (live >> col_member_[n][hh]) & 1u;
     float mx[NH][2];
 #pragma unroll
     for (int n = 0; n < NH; ++n) mx[n][0] = mx[n][1] = -INFINITY;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int n = 0; n < NH; ++n)
+      for (int n = 0; n < NT; ++n) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int tok = 16 * mt + ((c >> 1) ? tok1 : tok0);
           const float v = sc[mt][n][c] * hs_[n][c & 1];
-          sc[mt][n][c] = tok < rem ? v : -INFINITY;
+          sc[mt][n][c] = (tok < rem && col_ok[n][c & 1]) ? v : -INFINITY;
           mx[n][c & 1] = fmaxf(mx[n][c & 1], sc[mt][n][c]);
         }
-    float corr[NH][2], ps[NH][2];
+      }
+    // mref: the reference the exponentials are taken against; 0 while a column has
+    // seen no score at all (then every term is 2^-inf = 0, never -inf - -inf)
+    float corr[NH][2], ps[NH][2], mref[NH][2];
 #pragma unroll
     for (int n = 0; n < NH; ++n)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        corr[n][h] = 1.f;
+        ps[n][h] = 0.f;
+        mref[n][h] = 0.f;
+        if (n >= NT) continue;
         float v = mx[n][h];
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
         const float mn = fmaxf(m_[n][h], v);
-        corr[n][h] = exp2f(m_[n][h] - mn);
+        mref[n][h] = mn == -INFINITY ? 0.f : mn;
+        corr[n][h] = exp2f(m_[n][h] - mref[n][h]);
         m_[n][h] = mn;
-        ps[n][h] = 0.f;
       }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int n = 0; n < NH; ++n)
+      for (int n = 0; n < NT; ++n) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          sc[mt][n][c] = exp2f(sc[mt][n][c] - m_[n][c & 1]);
+          sc[mt][n][c] = exp2f(sc[mt][n][c] - mref[n][c & 1]);
           ps[n][c & 1] += sc[mt][n][c];
         }
+      }
 #pragma unroll
     for (int n = 0; n < NH; ++n) {
       l_[n][0] = l_[n][0] * corr[n][0] + ps[n][0];
       l_[n][1] = l_[n][1] * corr[n][1] + ps[n][1];
     }
+    // rescale O only when some column's maximum moved (a factor of exactly 1 changes nothing)
+    bool moved = false;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
+    for (int n = 0; n < NT; ++n) moved |= corr[n][0] != 1.f || corr[n][1] != 1.f;
+    if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-      for (int n = 0; n < NH; ++n) {
-        acc[ks][n][0] *= corr[n][0];
-        acc[ks][n][1] *= corr[n][1];
-        acc[ks][n][2] *= corr[n][0];
-        acc[ks][n][3] *= corr[n][1];
-      }
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          acc[ks][n][0] *= corr[n][0];
+          acc[ks][n][1] *= corr[n][1];
+          acc[ks][n][2] *= corr[n][0];
+          acc[ks][n][3] *= corr[n][1];
+        }
+    }
     // O^T += V^T P^T, one 16-token k-step per 16-token tile of S^T.
 #pragma unroll
     for (int kk = 0; kk < MT; ++kk) {
@@ -377,6 +438,7 @@ struct MmaMath {
       for (int n = 0; n < NH; ++n)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {  // S^T rows 0-7, then rows 8-15
+          if (n >= NT) break;
           const float x = sc[kk][n][2 * r], y = sc[kk][n][2 * r + 1];
           const uint32_t hi = pack2<OT>(x, y);
           const float2 back = unpack2<OT>(hi);
@@ -391,7 +453,7 @@ struct MmaMath {
           uint32_t a0[4], a1[4];
           widen(r, a0, a1);
 #pragma unroll
-          for (int n = 0; n < NH; ++n) {
+          for (int n = 0; n < NT; ++n) {
             mma_16816<OT>(acc[2 * dp][n], a0, bh[n][0], bh[n][1]);
             mma_16816<OT>(acc[2 * dp + 1][n], a1, bh[n][0], bh[n][1]);
             mma_16816<OT>(acc[2 * dp][n], a0, bl[n][0], bl[n][1]);
@@ -409,7 +471,7 @@ struct MmaMath {
             ldsm_x4(vb + v_lane_off + dm * 16 * (BS * 2) + kk * 32, a[0], a[1], a[2], a[3]);
           }
 #pragma unroll
-          for (int n = 0; n < NH; ++n) {
+          for (int n = 0; n < NT; ++n) {
             mma_16816<OT>(acc[dm][n], a, bh[n][0], bh[n][1]);
             mma_16816<OT>(acc[dm][n], a, bl[n][0], bl[n][1]);
           }
@@ -489,7 +551,8 @@ struct MmaMath {
       for (int hh = 0; hh < 2; ++hh) {
         const int h = 8 * n + 2 * t4 + hh;
         const float mn = fmaxf(M[n][hh], m_[n][hh]);
-        const float fo = exp2f(M[n][hh] - mn), fp = exp2f(m_[n][hh] - mn);  // l 2^(m - M') times o = acc / l
+        const float mr = mn == -INFINITY ? 0.f : mn;  // a column with no score yet: both factors 0
+        const float fo = exp2f(M[n][hh] - mr), fp = exp2f(m_[n][hh] - mr);  // l 2^(m - M') times o = acc / l
         if (g == 0) *reinterpret_cast<float2*>(sml + 2 * h) = make_float2(mn, Wt[n][hh] * fo + l_[n][hh] * fp);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks)
@@ -558,13 +621,16 @@ struct SimtMath {
     lpart = 0.f;
   }
 
-  __device__ __forceinline__ void load_q(const T* q, int, float) {
+  __device__ __forceinline__ void load_q(const T* q, int, float, int, long long) {
     const T* qh = q + half * NGH * X;
 #pragma unroll
     for (int k = 0; k < NGH * X; ++k) qv[k] = DType<T>::to_f32(qh[k]);
   }
 
-  __device__ __forceinline__ void block(unsigned char* stage, int tile_bytes, int rem, float scale_log2) {
+  __device__ __forceinline__ void set_columns(int) {}
+
+  __device__ __forceinline__ void block(unsigned char* stage, int tile_bytes, int rem, float scale_log2,
+                                        uint32_t = 0xffffffffu) {
     // Scores of this lane's token(s); each half-warp covers half of the head dims.
     float sc[TP];
 #pragma unroll
@@ -768,6 +834,114 @@ __device__ __forceinline__ void locate(long long g, const int* pre, int S, int U
   j = static_cast<int>(r - (long long)u * nb);
 }
 
+// The cost of a block of a shared segment (two 8-column tiles of query rows) and of
+// an own block (one), relative to each other, for balancing the warps' ranges:
+// measured on GB300, a 16-column block takes ~1.28 times as long as an 8-column one.
+constexpr int kSharedCost = 5, kOwnCost = 4;
+
+// Shared prefixes: the clusters and the work of each sequence (see DecodeParams).
+// On entry nb[k] holds the blocks of sequence tid * PER + k; on exit its blocks of
+// work per unit -- a leader's: its cluster's shared segment plus its own blocks;
+// anyone's own blocks: those past the ones it shares -- and s_info[], s_lead[]
+// the packed layout.
+//   runs: consecutive valid sequences with equal prefix_group; each run is cut
+//   into clusters of `members` consecutive sequences, the first the leader;
+//   sh(m) = prefix_blocks[m] limited to [0, its blocks - 1] (the last block of a
+//   sequence stays its own: the fused step writes it) and to B, the second largest
+//   of them (blocks past B are held by one member only); in a cluster of one, 0;
+//   the cluster's shared segment is its first B blocks, read through the table of
+//   the member with the largest prefix_blocks (the donor).
+// wt[k] receives the cost of the sequence's work per unit (kSharedCost, kOwnCost).
+// s_pre and s_red are scratch here.
+template <int PER>
+__device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre, int* s_info, int* s_lead,
+                                              int* s_red, int (&nb)[PER], int (&wt)[PER], int tid, int warp,
+                                              int lane) {
+  const int S = p.num_seqs, M = p.members;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid * PER + k;
+    if (i < S) s_pre[i] = nb[k];
+  }
+  __syncthreads();
+  int c0[PER], run = -1;  // the start of the run of each sequence (-1: before this thread's first)
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid * PER + k;
+    bool link = false;
+    if (i > 0 && i < S && nb[k] > 0 && s_pre[i - 1] > 0)
+      link = __ldg(p.prefix_group + i) == __ldg(p.prefix_group + i - 1);
+    if (i < S) s_info[i] = nb[k] > 0 ? max(0, min(__ldg(p.prefix_blocks + i), nb[k] - 1)) : 0;
+    if (!link) run = i;
+    c0[k] = run;
+  }
+  int incl = run;  // run starts seen up to this thread: a running maximum
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl = max(incl, x);
+  }
+  if (lane == 31) s_red[warp] = incl;
+  __syncthreads();
+  int before = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) before = -1;
+  for (int w = 0; w < warp; ++w) before = max(before, s_red[w]);
+#pragma unroll
+  for (int k = 0; k < PER; ++k)
+    if (c0[k] < 0) c0[k] = before;
+  // the cluster of a leader: its size (the run continues while the group id does), B and the donor
+  int size_[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid * PER + k;
+    size_[k] = 0;
+    if (i >= S || (i - c0[k]) % M != 0) continue;
+    int size = 1;
+    while (i + size < S && size < M && s_pre[i + size] > 0 && s_pre[i + size - 1] > 0 &&
+           __ldg(p.prefix_group + i + size) == __ldg(p.prefix_group + i + size - 1))
+      ++size;
+    size_[k] = size;
+  }
+  __syncthreads();  // every sh is in s_info
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid * PER + k, size = size_[k];
+    if (size == 0) continue;
+    // B: the second largest sh (blocks past it are held by one member only: its own);
+    // the donor: a member with the largest sh, whose table holds all B blocks
+    int top = 0, B = 0, donor = 0;
+    if (size > 1)
+      for (int m = 0; m < size; ++m) {
+        const int sh = s_info[i + m];
+        if (sh > top) {
+          B = top;
+          top = sh;
+          donor = m;
+        } else if (sh > B) {
+          B = sh;
+        }
+      }
+    // clusters are disjoint: only this thread writes the entries of this one
+    for (int m = 0; m < size; ++m) {
+      const int sh = min(s_info[i + m], B);
+      s_info[i + m] = sh | (m << kInfoOffBits) | (m == 0 ? (size - 1) << 27 : 0);
+    }
+    s_lead[i] = B | (donor << kInfoOffBits);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid * PER + k;
+    wt[k] = 0;
+    if (i < S && nb[k] > 0) {
+      const int B = info_member(s_info[i]) == 0 ? info_off(s_lead[i]) : 0, own = nb[k] - info_off(s_info[i]);
+      nb[k] = B + own;
+      wt[k] = kSharedCost * B + kOwnCost * own;
+    }
+  }
+  __syncthreads();  // s_pre and s_red are rewritten by the prefix sums that follow
+}
+
 // grid = resident CTAs (persistent); kDecodeWarps independent warps per CTA.
 // kMode: 0 = CUDA-core math, 1 or 2 = tensor-core math over 8 or 16 query heads per unit.
 template <typename T, typename TC, int D, int BS, int kMode>
@@ -791,6 +965,10 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   int* s_len = reinterpret_cast<int*>(smem + Sh::kRingBytes + Sh::kBarBytes);
   int* s_pre = s_len + kMaxSeqsPerLaunch;                 // [S + 1] block prefix per unit
   int* s_wsum = s_pre + kMaxSeqsPerLaunch + 1;             // [warps]
+  int* s_info = s_wsum + kDecodeWarps + 3;                 // [S] cluster layout (shared prefixes)
+  int* s_lead = s_info + kMaxSeqsPerLaunch;                // [S] a leader's shared segment and donor
+  // [S + 1] cost-weighted prefix per unit (shared prefixes; see DecodeShape::kWpreBytes)
+  int* s_wpre = Sh::kWpreInSide ? reinterpret_cast<int*>(smem + Sh::kSideOffset) : s_lead + kMaxSeqsPerLaunch;
   float* pw = reinterpret_cast<float*>(smem + Sh::kRingBytes + Sh::kBarBytes + Sh::kTableBytes) + warp * BS;
   // running state of this warp's piece across caller partitions (see fold)
   constexpr int kRows = kMma ? 8 * kMode : 1;
@@ -808,11 +986,12 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   griddep_wait();  // every input may come from the previous kernel in the stream
 
   // Per-sequence tables: length (0 when outside [1, max_seq_len]) and prefix sums
-  // of blocks.  Each thread scans PER consecutive sequences.
+  // of the blocks of work per unit.  Each thread scans PER consecutive sequences.
   const int S = p.num_seqs, U = p.units, PB = p.part_blocks;
+  const bool shared = kMma && p.shared;
   {
     constexpr int PER = (kMaxSeqsPerLaunch + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
-    int nb[PER], sb = 0;
+    int nb[PER], wt[PER];
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
       const int i = tid * PER + k;
@@ -820,38 +999,56 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       if (L < 1 || L > p.max_seq_len) L = 0;
       if (i < S) s_len[i] = L;
       nb[k] = (L + BS - 1) / BS;
-      sb += nb[k];
     }
-    int ib = sb;  // inclusive warp scan
+    if (shared) shared_layout<PER>(p, s_pre, s_info, s_lead, s_wsum, nb, wt, tid, warp, lane);
+    // exclusive prefix sums of v over the sequences into out[0..S]
+    auto scan = [&](const int (&v)[PER], int* out) {
+      int sb = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int xb = __shfl_up_sync(0xffffffffu, ib, o);
-      if (lane >= o) ib += xb;
-    }
-    if (lane == 31) s_wsum[warp] = ib;
-    __syncthreads();
-    int ob = ib - sb;
-    for (int w = 0; w < warp; ++w) ob += s_wsum[w];
+      for (int k = 0; k < PER; ++k) sb += v[k];
+      int ib = sb;  // inclusive warp scan
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int i = tid * PER + k;
-      if (i <= S) s_pre[i] = ob;
-      ob += nb[k];
-    }
-    if (tid == blockDim.x - 1) s_pre[S] = ob;  // the total (also covers S == kMaxSeqsPerLaunch)
-    __syncthreads();
+      for (int o = 1; o < 32; o <<= 1) {
+        const int xb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) ib += xb;
+      }
+      if (lane == 31) s_wsum[warp] = ib;
+      __syncthreads();
+      int ob = ib - sb;
+      for (int w = 0; w < warp; ++w) ob += s_wsum[w];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i = tid * PER + k;
+        if (i <= S) out[i] = ob;
+        ob += v[k];
+      }
+      if (tid == blockDim.x - 1) out[S] = ob;  // the total (also covers S == kMaxSeqsPerLaunch)
+      __syncthreads();
+    };
+    scan(nb, s_pre);
+    if (shared) scan(wt, s_wpre);
   }
+  // segment ids: one per (sequence, unit), or two with shared prefixes (the shared part, then the own part)
+  auto seg_id = [&](int s, int u, int part) { return shared ? 2 * (s * U + u) + part : s * U + u; };
+  // blocks of sequence s's shared segment (s a leader), else 0
+  auto shared_len = [&](int s) { return info_member(s_info[s]) == 0 ? info_off(s_lead[s]) : 0; };
 
   // Sequences outside the contract: record the error, zero their rows, mark their
-  // segments as needing no merge.  One CTA does it.
+  // segments as needing no merge.  One CTA does it, and hands the cluster layout
+  // to the merge kernel.
   if (blockIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       if (s_len[s] != 0) continue;
       if (tid == 0) set_error(p.err, kErrSeqLen);
       T* out = static_cast<T*>(p.out) + (long long)s * p.num_heads * D;
       for (int i = tid; i < p.num_heads * D; i += blockDim.x) out[i] = DType<T>::from_f32(0.f);
-      for (int u = tid; u < U; u += blockDim.x) p.seg_first[s * U + u] = -1;
+      for (int u = tid; u < U; u += blockDim.x) p.seg_first[seg_id(s, u, 1)] = -1;
     }
+    if (shared)
+      for (int s = tid; s < S; s += blockDim.x) {
+        p.seq_info[s] = s_info[s];
+        p.seq_info[S + s] = s_lead[s];
+      }
   }
 
   const int W = gridDim.x * kDecodeWarps;
@@ -934,11 +1131,38 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
     }
   };
 
-  // This warp's range of the T blocks of work.
+  // This warp's range of the T blocks of work: an equal share of the blocks, or with
+  // shared prefixes an equal share of their cost (a shared block costs more).
   const long long T_all = (long long)s_pre[S] * U;
-  const long long qt = T_all / W, rt = T_all % W;
-  const long long start = w * qt + (w * rt) / W;
-  const long long end = (w + 1) * qt + ((w + 1) * rt) / W;
+  long long start, end;
+  if (!shared) {
+    const long long qt = T_all / W, rt = T_all % W;
+    start = w * qt + (w * rt) / W;
+    end = (w + 1) * qt + ((w + 1) * rt) / W;
+  } else {
+    const long long Tw = (long long)s_wpre[S] * U;
+    // the first block whose cost starts at or after t
+    auto block_at = [&](long long t) -> long long {
+      if (t >= Tw) return T_all;
+      int lo = 0, hi = S - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)s_wpre[mid] * U <= t) lo = mid;
+        else hi = mid - 1;
+      }
+      const int s = lo, wl = s_wpre[s + 1] - s_wpre[s], nbl = s_pre[s + 1] - s_pre[s];
+      const long long r = t - (long long)s_wpre[s] * U;
+      const int u = static_cast<int>(r / wl), rr = static_cast<int>(r - (long long)u * wl);
+      const int B = shared_len(s);
+      const int j = rr < kSharedCost * B ? (rr + kSharedCost - 1) / kSharedCost
+                                         : B + (rr - kSharedCost * B + kOwnCost - 1) / kOwnCost;
+      return (long long)s_pre[s] * U + (long long)u * nbl + j;
+    };
+    const long long qt = Tw / W, rt = Tw % W;
+    start = block_at(w * qt + (w * rt) / W);
+    end = block_at((w + 1) * qt + ((w + 1) * rt) / W);
+    __syncthreads();  // every warp has its range: the side buffers may now receive copies
+  }
   const int len = static_cast<int>(end - start);
   if (len <= 0) {
     if (p.fused) write_tokens();
@@ -956,8 +1180,23 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       int s, u, j, h0, nh;
       locate(gpos, s_pre, S, U, s, u, j);
       unit_heads<kMma>(p, u, kvh, h0, nh);
-      phys = __ldg(bt + (long long)s * p.max_blocks_per_seq + j);
-      kvh |= (s << 16) | ((j == s_pre[s + 1] - s_pre[s] - 1) << 30);
+      bool in_shared = false;
+      int row = s;  // the table the block is read through
+      if (shared) {  // position j of the unit's work -> the logical block
+        const int B = shared_len(s);
+        in_shared = j < B;
+        if (in_shared) row = s + info_member(s_lead[s]);
+        else j = info_off(s_info[s]) + j - B;
+      }
+      phys = __ldg(bt + (long long)row * p.max_blocks_per_seq + j);
+      if (in_shared) {  // every member that takes this block must hold it at the same place
+        const int k = info_size(s_info[s]);
+        for (int m = 0; m < k; ++m)
+          if (j < info_off(s_info[s + m]) && __ldg(bt + (long long)(s + m) * p.max_blocks_per_seq + j) != phys)
+            set_error(p.err, kErrShared);
+      }
+      const bool last_blk = !in_shared && j == (s_len[s] + BS - 1) / BS - 1;
+      kvh |= (s << 16) | (static_cast<int>(last_blk) << 30);
     }
   };
   int phys_cur, kvh_cur, phys_nxt, kvh_nxt, group_cur = 0;
@@ -998,28 +1237,56 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   for (int k = 0; k < STAGES && k < len; ++k) issue(k);
   if (p.fused) write_tokens();  // while the first stages are in flight
 
-  // The compute cursor walks the same positions in order.
+  // The compute cursor walks the same positions in order.  Its segment is
+  // (cs, cu, part); cj is the logical block, running from jstart to jend.
   Math math;
   math.init(lane, pw);
+  math.set_columns(p.group);
   int cs, cu, cj;
   locate(start, s_pre, S, U, cs, cu, cj);
-  int L = 0, nblk = 0, kvh = 0, h0 = 0, nh = 0, seg = 0, j0 = cj;
-  bool folded = false;  // earlier partitions of this piece are in the running state
+  int part = 1;
+  if (shared) {  // position cj of the unit's work: in the shared part, or past it in the own part
+    const int B = shared_len(cs);
+    if (cj < B) part = 0;
+    else cj = info_off(s_info[cs]) + cj - B;
+  }
+  int L = 0, nblk = 0, kvh = 0, h0 = 0, nh = 0, seg = 0, jstart = 0, jend = 0, j0 = cj;
+  int my_off = 0;          // lane m < cluster size: the first own block of member m (shared part)
+  bool direct_ok = true;   // a whole segment may go straight to the output
+  bool folded = false;     // earlier partitions of this piece are in the running state
   auto enter = [&]() {
     L = s_len[cs];
-    nblk = s_pre[cs + 1] - s_pre[cs];
+    nblk = (L + BS - 1) / BS;
     unit_heads<kMma>(p, cu, kvh, h0, nh);
-    seg = cs * U + cu;
+    jstart = 0;
+    jend = nblk;
+    direct_ok = true;
+    if (shared) {
+      const int v = s_info[cs];
+      if (part == 0) {  // the cluster's common blocks, for the query rows of all its members
+        const int k = info_size(v);
+        nh = k * p.group;
+        jend = shared_len(cs);
+        my_off = lane < k ? info_off(s_info[cs + lane]) : 0;
+        direct_ok = false;
+      } else {          // this sequence's own blocks; merged with its shared part when it has one
+        jstart = info_off(v);
+        direct_ok = jstart == 0;
+      }
+    }
+    seg = seg_id(cs, cu, part);
     math.reset();
-    math.load_q(static_cast<const T*>(p.q) + ((long long)cs * p.num_heads + h0) * D, nh, p.scale_log2);
+    math.load_q(static_cast<const T*>(p.q) + ((long long)cs * p.num_heads + h0) * D, nh, p.scale_log2, p.group,
+                (long long)p.num_heads * D);
   };
   enter();
 
   for (int k = 0; k < len; ++k) {
     if (!wait_stage<STAGES>(bars, never, p.test_wait_ns, k, len, p.err, lane)) break;
     unsigned char* stage = ring + (k % STAGES) * 2 * TILE;
-    const int rem = L - cj * BS;  // valid tokens in this block (>= 1)
-    if (p.fused && cj == nblk - 1)  // the sequence's new token: from the step's input, not the pool
+    // valid tokens in this block (>= 1); a shared block is full for every member that takes it
+    const int rem = part == 0 ? BS : L - cj * BS;
+    if (p.fused && part != 0 && cj == nblk - 1)  // the sequence's new token: from the step's input, not the pool
     {
       if constexpr (sizeof(TC) == 1)
         inject_token_e4m3<T, D, BS>(stage, TILE, side + (k % STAGES) * Sh::kSideStage, (L - 1) % BS,
@@ -1036,9 +1303,11 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
         issue(k + STAGES);
       }
     }
-    math.block(stage, TILE, rem, p.scale_log2);
+    // the members whose tables hold this block (every column outside shared parts)
+    const uint32_t live = (shared && part == 0) ? __ballot_sync(0xffffffffu, cj < my_off) : 0xffffffffu;
+    math.block(stage, TILE, rem, p.scale_log2, live);
     ++cj;
-    const bool seg_end = cj == nblk, last = k + 1 == len;
+    const bool seg_end = cj == jend, last = k + 1 == len;
     if (seg_end || last) {  // the end of a piece
       math.finish();
       if (folded) {  // close the last caller partition and take the merged state
@@ -1046,7 +1315,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
         math.load_state(st_o, st_ml);
         folded = false;
       }
-      if (j0 == 0 && seg_end) {  // the whole segment: straight to the output
+      if (j0 == jstart && seg_end && direct_ok) {  // the whole segment: straight to the output
         math.store_out(static_cast<T*>(p.out) + ((long long)cs * p.num_heads + h0) * D, nh, p.out_scale);
         if (lane == 0) p.seg_first[seg] = -1;
       } else {
@@ -1055,20 +1324,29 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
         math.store_partial(p.part_o + slot * p.rows * D, p.part_ml + slot * p.rows * 2, nh, p.out_scale);
         if (lane == 0) {
           p.part_tag[slot] = make_int2(seg, static_cast<int>(p.epoch));
-          if (j0 == 0) p.seg_first[seg] = static_cast<int>(slot);
+          if (j0 == jstart) p.seg_first[seg] = static_cast<int>(slot);
           if (seg_end) p.seg_last[seg] = static_cast<int>(slot);
         }
       }
       if (!last) {
-        if (++cu == U) {
-          cu = 0;
-          do {
-            ++cs;
-          } while (s_pre[cs + 1] == s_pre[cs]);
+        if (part == 0) {  // the shared part is followed by the leader's own part of the unit
+          part = 1;
+          cj = info_off(s_info[cs]);
+        } else {
+          if (++cu == U) {
+            cu = 0;
+            do {
+              ++cs;
+            } while (s_pre[cs + 1] == s_pre[cs]);
+          }
+          cj = 0;
+          if (shared) {
+            part = shared_len(cs) > 0 ? 0 : 1;
+            cj = part == 0 ? 0 : info_off(s_info[cs]);
+          }
         }
-        cj = 0;
         enter();
-        j0 = 0;
+        j0 = cj;
       }
     } else if (cj % PB == 0) {  // a caller partition ends inside this piece: fold it
       math.finish();
@@ -1088,115 +1366,140 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
 
 // --- merge of pieces --------------------------------------------------------------------------------
 //
-// One CTA per segment (sequence, head unit).  The segment's pieces are cut into
-// items of (query row, chunk of kMergeChunk consecutive pieces); each warp takes
-// one item per round and issues every load of it at once (the pieces' tags,
-// (m, l) and partial outputs, each lane owning D/32 consecutive head dims), so a
-// round costs one trip to L2.  The item's pieces are combined in registers,
-//     m_c = max m_p,  l_c = sum l_p 2^(m_p - m_c),  o_c = sum l_p 2^(m_p - m_c) o_p,
-// and left in shared memory; then warp r folds the items of row r into its
-// running (M, L, O) with the same formula and finally writes O / L.  Slots whose
-// tag is not (segment, this launch's epoch) weigh nothing and are never read
-// into a sum: when the grid has more warps than blocks of work, a warp with an
-// empty range leaves its slot inside a segment's range unwritten.
-constexpr int kMergeWarps = 16;
-constexpr int kMergeChunk = 8;
+// One warp per output row (sequence, query head); kMergeRows rows per CTA.  The
+// row's pieces are the slots of its own segment and, with shared prefixes, those of
+// its cluster's shared part (where the member's rows sit at row offset
+// member * group).  Lane i reads the tag and (m, l) of piece i of a chunk of up to
+// 32; the chunk's maximum and weights come from warp shuffles,
+//     m_c = max m_p,  w_p = l_p 2^(m_p - m_c),  l_c = sum w_p,  o_c = sum w_p o_p,
+// and the partial outputs are read 8 pieces at a time (each lane D/32 consecutive
+// head dims), so a chunk costs about two trips to L2.  Chunks fold into a running
+// (M, L, O) with the same rule; the row is O / L.  Slots whose tag is not (their
+// segment, this launch's epoch) weigh nothing and are never read into a sum:
+// when the grid has more warps than blocks of work, a warp with an empty range
+// leaves its slot inside a segment's range unwritten.  A piece whose rows saw no
+// block (a member that holds fewer shared blocks than the piece covers) has
+// m = -inf and weighs nothing too.
+constexpr int kMergeRows = 8;
 
 template <typename T, int D, bool kMma>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kMergeRows * 32) decode_merge_kernel(const DecodeParams p) {
   constexpr int CPL = D / 32;  // head dims per lane
   using Vec = std::conditional_t<CPL == 4, float4, float2>;
-  __shared__ __align__(16) float s_o[kMergeWarps][D];
-  __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
-  __shared__ int s_row[kMergeWarps];
   griddep_wait();
   griddep_launch_dependents();
-  const int seg = blockIdx.x;
-  const int first = p.seg_first[seg], last = p.seg_last[seg];
-  if (first < 0 || last < first || last >= p.num_slots) return;  // no merge (or an aborted launch)
-  const int s = seg / p.units, u = seg - s * p.units;
-  int kvh, h0, nh;
-  unit_heads<kMma>(p, u, kvh, h0, nh);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int K = last - first + 1, ep = static_cast<int>(p.epoch);
-  const int chunks = (K + kMergeChunk - 1) / kMergeChunk;
-  const int items = nh * chunks;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kMergeRows + (threadIdx.x >> 5);
+  if (row >= (long long)p.num_seqs * p.num_heads) return;
+  const int s = static_cast<int>(row / p.num_heads), h = static_cast<int>(row - (long long)s * p.num_heads);
+  // the head unit of h and h's row within it
+  int u, r;
+  if (kMma) {
+    const int kvh = h / p.group, hh = h - kvh * p.group;
+    u = kvh * ((p.group + 15) >> 4) + (hh >> 4);
+    r = hh & 15;
+  } else {
+    u = h;
+    r = 0;
+  }
+  const int b = s * p.units + u;
+  const bool shared = kMma && p.shared;
+  const int own = shared ? 2 * b + 1 : b;
+  int first = p.seg_first[own], last = p.seg_last[own];
+  const bool own_ok = first >= 0 && last >= first && last < p.num_slots;
+  if (!own_ok && first >= 0) return;  // an aborted launch
+  if (!own_ok) {                      // the own part went straight to the output
+    first = 0;
+    last = -1;
+  }
+  // the cluster's shared part, if this sequence takes any of its blocks
+  int sfirst = 0, slast = -1, srow = 0, sseg = -1;
+  if (shared) {
+    const int v = p.seq_info[s], mi = info_member(v);
+    if (info_off(v) > 0) {  // its leader is s - mi
+      sseg = 2 * ((s - mi) * p.units + u);
+      sfirst = p.seg_first[sseg];
+      slast = p.seg_last[sseg];
+      srow = mi * p.group;
+      if (sfirst < 0 || slast < sfirst || slast >= p.num_slots) slast = sfirst - 1;  // (an aborted launch)
+    }
+  }
+  const int Ks = slast - sfirst + 1;
+  const int K = Ks + (last - first + 1);
+  if (K <= 0) return;
+  const int ep = static_cast<int>(p.epoch);
+  // piece i: the offset of its row in the partial arrays, and the segment that must have written it
+  auto piece = [&](int i, long long& at, int& seg) {
+    if (i < Ks) {
+      at = (long long)(sfirst + i) * p.rows + srow + r;
+      seg = sseg;
+    } else {
+      at = (long long)(first + (i - Ks)) * p.rows + r;
+      seg = own;
+    }
+  };
 
-  float RM = -INFINITY, RL = 0.f, RO[CPL];  // row `warp`'s running state (warps < nh)
+  float RM = -INFINITY, RL = 0.f, RO[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) RO[c] = 0.f;
-
-  for (int i0 = 0; i0 < items; i0 += kMergeWarps) {
-    const int it = i0 + warp;
-    if (it < items) {
-      const int r = it / chunks, p0 = (it - r * chunks) * kMergeChunk;
-      const int n = min(kMergeChunk, K - p0);
-      float m = -INFINITY, l = 0.f;
-      if (lane < n) {
-        const long long sl = first + p0 + lane;
-        const int2 tag = p.part_tag[sl];
-        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (sl * p.rows + r) * 2);
-        if (tag.x == seg && tag.y == ep) {
-          m = ml.x;
-          l = ml.y;
-        }
+  for (int c0 = 0; c0 < K; c0 += 32) {
+    const int n = min(32, K - c0);
+    float m = -INFINITY, l = 0.f;
+    if (lane < n) {
+      long long at;
+      int sg;
+      piece(c0 + lane, at, sg);
+      const long long slot = at / p.rows;
+      const int2 tag = p.part_tag[slot];
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + at * 2);
+      if (tag.x == sg && tag.y == ep) {
+        m = ml.x;
+        l = ml.y;
       }
-      Vec ov[kMergeChunk];
+    }
+    float mc = m;
 #pragma unroll
-      for (int i = 0; i < kMergeChunk; ++i)
-        if (i < n)
-          ov[i] = *reinterpret_cast<const Vec*>(p.part_o + ((long long)(first + p0 + i) * p.rows + r) * D + CPL * lane);
-      // chunk maximum and weights over lanes 0..n-1
-      float mc = m;
+    for (int o = 1; o < 32; o <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+    const float w = m == -INFINITY ? 0.f : l * exp2f(m - mc);
+    float lc = w;
 #pragma unroll
-      for (int o = 1; o < kMergeChunk; o <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
-      mc = __shfl_sync(0xffffffffu, mc, 0);
-      const float w = m == -INFINITY ? 0.f : l * exp2f(m - mc);
-      float lc = w;
+    for (int o = 1; o < 32; o <<= 1) lc += __shfl_xor_sync(0xffffffffu, lc, o);
+    float oc[CPL];
 #pragma unroll
-      for (int o = 1; o < kMergeChunk; o <<= 1) lc += __shfl_xor_sync(0xffffffffu, lc, o);
-      lc = __shfl_sync(0xffffffffu, lc, 0);
-      float oc[CPL];
+    for (int c = 0; c < CPL; ++c) oc[c] = 0.f;
+    for (int i0 = 0; i0 < n; i0 += 8) {
+      Vec ov[8];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) oc[c] = 0.f;
+      for (int i = 0; i < 8; ++i)
+        if (i0 + i < n) {
+          long long at;
+          int sg;
+          piece(c0 + i0 + i, at, sg);
+          ov[i] = *reinterpret_cast<const Vec*>(p.part_o + at * D + CPL * lane);
+        }
 #pragma unroll
-      for (int i = 0; i < kMergeChunk; ++i) {
-        const float wi = __shfl_sync(0xffffffffu, w, i);
-        if (i < n && wi > 0.f) {  // a slot no piece wrote in this launch holds anything (NaN too)
+      for (int i = 0; i < 8; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, i0 + i);
+        if (i0 + i < n && wi > 0.f) {  // a slot no piece wrote in this launch holds anything (NaN too)
           const float* v = reinterpret_cast<const float*>(&ov[i]);
 #pragma unroll
           for (int c = 0; c < CPL; ++c) oc[c] = fmaf(wi, v[c], oc[c]);
         }
       }
-      *reinterpret_cast<Vec*>(&s_o[warp][CPL * lane]) = *reinterpret_cast<const Vec*>(oc);
-      if (lane == 0) {
-        s_m[warp] = mc;
-        s_l[warp] = lc;
-        s_row[warp] = r;
-      }
-    } else if (lane == 0) {
-      s_row[warp] = -1;
     }
-    __syncthreads();
-    if (warp < nh) {
-      for (int j = 0; j < kMergeWarps; ++j) {
-        if (s_row[j] != warp || !(s_l[j] > 0.f)) continue;
-        const float mn = fmaxf(RM, s_m[j]);
-        const float fa = exp2f(RM - mn), fb = exp2f(s_m[j] - mn);
-        RL = RL * fa + s_l[j] * fb;
+    if (lc > 0.f) {
+      const float mn = fmaxf(RM, mc);
+      const float fa = exp2f(RM - mn), fb = exp2f(mc - mn);
+      RL = RL * fa + lc * fb;
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) RO[c] = RO[c] * fa + fb * s_o[j][CPL * lane + c];
-        RM = mn;
-      }
+      for (int c = 0; c < CPL; ++c) RO[c] = RO[c] * fa + fb * oc[c];
+      RM = mn;
     }
-    __syncthreads();  // the shared arrays are reused by the next round
   }
-  if (warp < nh) {
-    const float il = 1.f / RL;
-    T* out = static_cast<T*>(p.out) + ((long long)s * p.num_heads + h0 + warp) * D + CPL * lane;
+  const float il = 1.f / RL;
+  T* out = static_cast<T*>(p.out) + row * D + CPL * lane;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) out[c] = DType<T>::from_f32(RO[c] * il);
-  }
+  for (int c = 0; c < CPL; ++c) out[c] = DType<T>::from_f32(RO[c] * il);
 }
 
 // --- host-side launch helpers (instantiated per dtype) ------------------------------------------
@@ -1239,7 +1542,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream
                  decode_smem_bytes<TC, D, BS, kMode>(), stream, p);
   if (e != cudaSuccess) return e;
   *launches = 1;
-  e = launch_pdl(decode_merge_kernel<T, D, (kMode != 0)>, dim3(p.num_seqs * p.units), dim3(kMergeWarps * 32), 0, stream, p);
+  const unsigned merge_ctas = static_cast<unsigned>(((long long)p.num_seqs * p.num_heads + kMergeRows - 1) / kMergeRows);
+  e = launch_pdl(decode_merge_kernel<T, D, (kMode != 0)>, dim3(merge_ctas), dim3(kMergeRows * 32), 0, stream, p);
   if (e != cudaSuccess) return e;
   *launches = 2;
   return cudaSuccess;

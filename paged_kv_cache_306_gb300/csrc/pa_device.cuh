@@ -15,7 +15,15 @@ namespace pa {
 
 // ---- device error word ----------------------------------------------------------------
 
-enum : unsigned { kErrNone = 0, kErrBlockId = 1, kErrSeqLen = 2, kErrSlot = 3, kErrTimeout = 4, kErrCopyId = 5 };
+enum : unsigned {
+  kErrNone = 0,
+  kErrBlockId = 1,
+  kErrSeqLen = 2,
+  kErrSlot = 3,
+  kErrTimeout = 4,
+  kErrCopyId = 5,
+  kErrShared = 6  // a block declared shared differs between two sequences' tables
+};
 
 // Record `code` unless an earlier error is already recorded.
 __device__ __forceinline__ void set_error(unsigned* err, unsigned code) {

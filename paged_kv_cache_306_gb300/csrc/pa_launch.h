@@ -70,7 +70,31 @@ struct DecodeParams {
   // > 0 only in the timeout-path test: every warp's first pipeline wait runs out
   // after this many nanoseconds (see pa_set_test_wait_limit)
   unsigned long long test_wait_ns;
+  // Shared prefixes (pa_decode_shared): sequences with the same prefix_group[s]
+  // (consecutive runs) hold the first prefix_blocks[s] blocks of a common prefix,
+  // so any two of them agree on their first min(prefix_blocks) block-table entries.
+  // A run is cut into clusters of up to `members` sequences; a cluster's prefix
+  // blocks are read once for all its members (one segment whose tensor-core
+  // columns are the members' query heads, read through the table of the member
+  // that holds the most of them) and merged with each member's own blocks.
+  // shared == 0: unused.
+  const int32_t* prefix_group;
+  const int32_t* prefix_blocks;
+  int* seq_info;                // [2 S]: the cluster layout (s_info, then s_lead), written by CTA 0 for the merge
+  int shared;
+  int members;
 };
+
+// Packed per-sequence cluster layout (shared prefixes).  info: bits 0..21 the
+// sequence's shared blocks sh (its own segment starts there), bits 22..26 its
+// member index (0 = the cluster's leader), bits 27..31 the cluster size minus one
+// (leaders only).  lead (leaders only): bits 0..21 the length B of the cluster's
+// shared segment (the second largest prefix_blocks of its members: past it only one
+// member holds the blocks), bits 22..26 the member whose table it is read through.
+constexpr int kInfoOffBits = 22;
+__host__ __device__ constexpr int info_off(int v) { return v & ((1 << kInfoOffBits) - 1); }
+__host__ __device__ constexpr int info_member(int v) { return (v >> kInfoOffBits) & 31; }
+__host__ __device__ constexpr int info_size(int v) { return ((v >> 27) & 31) + 1; }
 
 // CUDA cores, or tensor cores with one (up to 8 query heads per kv head) or two
 // 8-head tiles per head unit.

@@ -249,3 +249,20 @@ def test_scaled_fused_step_rejects_bad_arguments_on_the_host(lib):
     assert st(cdt=9) == B.PA_ERR_UNSUPPORTED
     assert st(key=8200) == B.PA_ERR_ALIGNMENT
     assert st(S=0, key=0) == B.PA_OK
+
+
+def test_shared_decode_rejects_bad_arguments_on_the_host(lib):
+    def sd(key=8192, value=8192, sd_=0, npairs=0, grp=8192, blk=8192, S=2, cdt=B.PA_F16, qdt=B.PA_F16, D=128):
+        return lib.pa_decode_shared(A(8192), A(8192), A(key), A(value), A(8192), A(8192), A(sd_), npairs, A(8192), 4,
+                                    A(8192), A(grp), A(blk), S, 16, 8, 2, D, 16, 8, 0.1, 0, None, 0, qdt, cdt, 1.0,
+                                    1.0, None)
+    assert sd(grp=0) == B.PA_ERR_INVALID_ARG                    # no group description
+    assert sd(blk=0) == B.PA_ERR_INVALID_ARG
+    assert sd(key=0) == B.PA_ERR_INVALID_ARG                    # key without value
+    assert sd(key=0, value=0, npairs=1, sd_=8192) == B.PA_ERR_INVALID_ARG   # copies without a step
+    assert sd(grp=8194) == B.PA_ERR_ALIGNMENT
+    assert sd(cdt=9) == B.PA_ERR_UNSUPPORTED
+    assert sd(D=96) == B.PA_ERR_UNSUPPORTED
+    assert sd(S=0, grp=0, blk=0) == B.PA_OK
+    assert lib.pa_decode_shared_workspace_size(4, 8, 2, 96, 64, 16, 0, B.PA_F16) == 0
+

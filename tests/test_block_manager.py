@@ -235,3 +235,24 @@ def test_exhausted_pool_refuses_the_whole_batch():
     assert bm.seq_len(0) == 2 and bm.seq_len(1) == 2 and bm.num_free_blocks == 1
     slots, _ = bm.append_tokens([1])
     assert slots.tolist() == [2 * 2]
+
+
+def test_prefix_groups_match_the_tables():
+    """The manager's description of shared prefixes agrees with one computed from
+    its own block tables, after forks, appends and copy-on-write."""
+    import workloads as W
+    bm = pa.BlockManager(400, 16)
+    bm.add_sequence(0, 100)
+    for c in range(1, 6):
+        bm.fork(0, c)
+    bm.add_sequence(10, 40)
+    bm.fork(10, 11)
+    bm.add_sequence(20, 7)
+    ids = [0, 1, 2, 3, 4, 5, 10, 11, 20]
+    for step in range(40):
+        bm.append_tokens([i for i in ids if (step + i) % 3 != 0])
+    bt, sl = bm.block_tables(ids, 64)
+    grp, blk = bm.prefix_groups(ids)
+    g2, b2 = W.prefix_groups(bt, sl, 16)
+    assert grp.tolist() == g2.tolist() and blk.tolist() == b2.tolist()
+    assert grp.tolist()[:6] == [0] * 6 and blk[8] == 0

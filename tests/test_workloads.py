@@ -158,3 +158,32 @@ def test_no_poison_reaches_a_read_slot_when_sharers_of_a_block_differ_in_length(
             assert np.all(np.isfinite(k[b, :, :, :n, :])) and np.all(np.isfinite(v[b, :, :, :n])), (s, j)
     assert np.all(np.isfinite(oracle.decode(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale, "f32")))
     assert any(int(wl.slot_mapping[s]) // bs in src for s in range(wl.num_seqs)), "no in-place writer to test"
+
+
+def test_prefix_groups_of_crafted_tables():
+    bs = 16
+    bt = np.array([[5, 6, 7, -1],      # group 0 (first block 5)
+                   [5, 6, 9, 10],      # shares 2 with the longest of group 0 (this one: 4 blocks)
+                   [5, 11, -1, -1],    # shares 1
+                   [20, 21, 22, -1],   # a group of one
+                   [30, 31, -1, -1],   # group 4: two sequences sharing 2 blocks
+                   [30, 31, 32, -1]], dtype=np.int32)
+    L = np.array([40, 60, 20, 35, 20, 40], dtype=np.int32)
+    grp, blk = W.prefix_groups(bt, L, bs)
+    assert grp.tolist() == [0, 0, 0, 3, 4, 4]
+    assert blk.tolist() == [2, 4, 1, 0, 2, 3]
+
+
+def test_prefix_groups_of_the_mixed_workload_describe_real_sharing():
+    wl = W.config(5, poison=False, block_size=16)
+    grp, blk = W.prefix_groups(wl.block_tables, wl.seq_lens, 16)
+    for s in range(wl.num_seqs):
+        for t in range(s + 1, wl.num_seqs):
+            if grp[t] != grp[s]:
+                break
+            n = min(blk[s], blk[t])
+            assert np.array_equal(wl.block_tables[s, :n], wl.block_tables[t, :n])
+    # every sampling group of 8 starts a prefix group (a sibling whose only block was
+    # copied on write shares nothing and stands alone)
+    assert set(range(0, wl.num_seqs, 8)) <= set(np.unique(grp).tolist())
+    assert (blk > 16).sum() > 100

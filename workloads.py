@@ -484,6 +484,32 @@ def _config(i, sd, poison, block_size, cache=None, q_dtype=None):
     raise ValueError(i)
 
 
+def prefix_groups(block_tables, seq_lens, block_size):
+    """(prefix_group, prefix_blocks), int32 [S] each: runs of consecutive sequences
+    whose first logical block is one physical block form a group (id: the index of
+    its first sequence); prefix_blocks[s] = how many leading block-table entries
+    sequence s has in common with the longest sequence of its group (0 in a group
+    of one) -- the blocks a fork family still shares."""
+    bt = np.asarray(block_tables)
+    nblk = -(-np.asarray(seq_lens, dtype=np.int64) // block_size)
+    S = len(nblk)
+    grp = np.zeros(S, dtype=np.int32)
+    blk = np.zeros(S, dtype=np.int32)
+    i = 0
+    while i < S:
+        j = i + 1
+        while j < S and nblk[i] > 0 and nblk[j] > 0 and bt[j, 0] == bt[i, 0]:
+            j += 1
+        ref = i + int(np.argmax(nblk[i:j]))
+        for t in range(i, j):
+            n = int(min(nblk[t], nblk[ref]))
+            eq = bt[t, :n] == bt[ref, :n]
+            grp[t] = i
+            blk[t] = 0 if j - i == 1 else (n if eq.all() else int(np.argmin(eq)))
+        i = j
+    return grp, blk
+
+
 def subset(wl, seqs):
     """The same pool with a sub-batch of sequences (for sampled oracle checks)."""
     seqs = np.asarray(seqs, dtype=np.int64)
