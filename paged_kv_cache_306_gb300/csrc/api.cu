@@ -136,7 +136,9 @@ pa_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size
   const int nblk_max = ceil_div(max_seq_len, block_size);
   pl->part_blocks = partition_size > 0 ? partition_size / block_size : (1 << 30);
   long long chunk = num_seqs < pa::kMaxSeqsPerLaunch ? num_seqs : pa::kMaxSeqsPerLaunch;
-  if (chunk > 0x7fffffffLL / nblk_max) chunk = 0x7fffffffLL / nblk_max;
+  // the schedule's cost prefix per unit stays within int32 (see pa::kSegCost)
+  const long long unit_cost = (long long)pa::kSharedCost * nblk_max + 2 * pa::kSegCost;
+  if (chunk > 0x7fffffffLL / unit_cost) chunk = 0x7fffffffLL / unit_cost;
   if (chunk < 1) chunk = 1;
   pl->chunk = static_cast<int>(chunk);
   const int ctas = pa::decode_ctas_per_sm(static_cast<int>(dtype), head_size, block_size, pl->kind);

@@ -834,10 +834,6 @@ __device__ __forceinline__ void locate(long long g, const int* pre, int S, int U
   j = static_cast<int>(r - (long long)u * nb);
 }
 
-// The cost of a block of a shared segment (two 8-column tiles of query rows) and of
-// an own block (one), relative to each other, for balancing the warps' ranges:
-// measured on GB300, a 16-column block takes ~1.28 times as long as an 8-column one.
-constexpr int kSharedCost = 5, kOwnCost = 4;
 
 // Shared prefixes: the clusters and the work of each sequence (see DecodeParams).
 // On entry nb[k] holds the blocks of sequence tid * PER + k; on exit its blocks of
@@ -851,7 +847,7 @@ constexpr int kSharedCost = 5, kOwnCost = 4;
 //   of them (blocks past B are held by one member only); in a cluster of one, 0;
 //   the cluster's shared segment is its first B blocks, read through the table of
 //   the member with the largest prefix_blocks (the donor).
-// wt[k] receives the cost of the sequence's work per unit (kSharedCost, kOwnCost).
+// wt[k] receives the cost of the sequence's work per unit (see kSegCost).
 // s_pre and s_red are scratch here.
 template <int PER>
 __device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre, int* s_info, int* s_lead,
@@ -864,14 +860,21 @@ __device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre,
     if (i < S) s_pre[i] = nb[k];
   }
   __syncthreads();
+  // link: sequence i continues the run of i - 1; kept in bit 30 of s_info[i] (beside sh) until the
+  // leaders have sized their clusters, so that they read shared memory only
+  constexpr int kLinkBit = 1 << 30, kShMask = (1 << kInfoOffBits) - 1;
   int c0[PER], run = -1;  // the start of the run of each sequence (-1: before this thread's first)
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     const int i = tid * PER + k;
     bool link = false;
-    if (i > 0 && i < S && nb[k] > 0 && s_pre[i - 1] > 0)
-      link = __ldg(p.prefix_group + i) == __ldg(p.prefix_group + i - 1);
-    if (i < S) s_info[i] = nb[k] > 0 ? max(0, min(__ldg(p.prefix_blocks + i), nb[k] - 1)) : 0;
+    int sh = 0;
+    if (i < S && nb[k] > 0) {
+      const int gi = __ldg(p.prefix_group + i), pb = __ldg(p.prefix_blocks + i);
+      link = i > 0 && s_pre[i - 1] > 0 && __ldg(p.prefix_group + i - 1) == gi;
+      sh = max(0, min(pb, nb[k] - 1));
+    }
+    if (i < S) s_info[i] = sh | (link ? kLinkBit : 0);
     if (!link) run = i;
     c0[k] = run;
   }
@@ -889,7 +892,8 @@ __device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre,
 #pragma unroll
   for (int k = 0; k < PER; ++k)
     if (c0[k] < 0) c0[k] = before;
-  // the cluster of a leader: its size (the run continues while the group id does), B and the donor
+  __syncthreads();  // every sh and link is in s_info
+  // the cluster of a leader: its size (the run continues while the links do), B and the donor
   int size_[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
@@ -897,12 +901,10 @@ __device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre,
     size_[k] = 0;
     if (i >= S || (i - c0[k]) % M != 0) continue;
     int size = 1;
-    while (i + size < S && size < M && s_pre[i + size] > 0 && s_pre[i + size - 1] > 0 &&
-           __ldg(p.prefix_group + i + size) == __ldg(p.prefix_group + i + size - 1))
-      ++size;
+    while (i + size < S && size < M && (s_info[i + size] & kLinkBit)) ++size;
     size_[k] = size;
   }
-  __syncthreads();  // every sh is in s_info
+  __syncthreads();  // every leader has read the links
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     const int i = tid * PER + k, size = size_[k];
@@ -912,7 +914,7 @@ __device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre,
     int top = 0, B = 0, donor = 0;
     if (size > 1)
       for (int m = 0; m < size; ++m) {
-        const int sh = s_info[i + m];
+        const int sh = s_info[i + m] & kShMask;
         if (sh > top) {
           B = top;
           top = sh;
@@ -923,7 +925,7 @@ __device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre,
       }
     // clusters are disjoint: only this thread writes the entries of this one
     for (int m = 0; m < size; ++m) {
-      const int sh = min(s_info[i + m], B);
+      const int sh = min(s_info[i + m] & kShMask, B);
       s_info[i + m] = sh | (m << kInfoOffBits) | (m == 0 ? (size - 1) << 27 : 0);
     }
     s_lead[i] = B | (donor << kInfoOffBits);
@@ -936,7 +938,7 @@ __device__ __forceinline__ void shared_layout(const DecodeParams& p, int* s_pre,
     if (i < S && nb[k] > 0) {
       const int B = info_member(s_info[i]) == 0 ? info_off(s_lead[i]) : 0, own = nb[k] - info_off(s_info[i]);
       nb[k] = B + own;
-      wt[k] = kSharedCost * B + kOwnCost * own;
+      wt[k] = (B > 0 ? kSegCost + kSharedCost * B : 0) + kSegCost + kOwnCost * own;
     }
   }
   __syncthreads();  // s_pre and s_red are rewritten by the prefix sums that follow
@@ -1000,7 +1002,12 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       if (i < S) s_len[i] = L;
       nb[k] = (L + BS - 1) / BS;
     }
-    if (shared) shared_layout<PER>(p, s_pre, s_info, s_lead, s_wsum, nb, wt, tid, warp, lane);
+    if (shared) {
+      shared_layout<PER>(p, s_pre, s_info, s_lead, s_wsum, nb, wt, tid, warp, lane);
+    } else {
+#pragma unroll
+      for (int k = 0; k < PER; ++k) wt[k] = nb[k] > 0 ? kSegCost + kOwnCost * nb[k] : 0;
+    }
     // exclusive prefix sums of v over the sequences into out[0..S]
     auto scan = [&](const int (&v)[PER], int* out) {
       int sb = 0;
@@ -1026,7 +1033,7 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       __syncthreads();
     };
     scan(nb, s_pre);
-    if (shared) scan(wt, s_wpre);
+    scan(wt, s_wpre);
   }
   // segment ids: one per (sequence, unit), or two with shared prefixes (the shared part, then the own part)
   auto seg_id = [&](int s, int u, int part) { return shared ? 2 * (s * U + u) + part : s * U + u; };
@@ -1131,15 +1138,11 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
     }
   };
 
-  // This warp's range of the T blocks of work: an equal share of the blocks, or with
-  // shared prefixes an equal share of their cost (a shared block costs more).
+  // This warp's range of the T blocks of work: an equal share of their cost (blocks,
+  // shared blocks and segments weighted as kSegCost says).
   const long long T_all = (long long)s_pre[S] * U;
   long long start, end;
-  if (!shared) {
-    const long long qt = T_all / W, rt = T_all % W;
-    start = w * qt + (w * rt) / W;
-    end = (w + 1) * qt + ((w + 1) * rt) / W;
-  } else {
+  {
     const long long Tw = (long long)s_wpre[S] * U;
     // the first block whose cost starts at or after t
     auto block_at = [&](long long t) -> long long {
@@ -1153,9 +1156,11 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
       const int s = lo, wl = s_wpre[s + 1] - s_wpre[s], nbl = s_pre[s + 1] - s_pre[s];
       const long long r = t - (long long)s_wpre[s] * U;
       const int u = static_cast<int>(r / wl), rr = static_cast<int>(r - (long long)u * wl);
-      const int B = shared_len(s);
-      const int j = rr < kSharedCost * B ? (rr + kSharedCost - 1) / kSharedCost
-                                         : B + (rr - kSharedCost * B + kOwnCost - 1) / kOwnCost;
+      // a unit's cost: [segment, shared blocks] (a leader with a shared part), segment, own blocks
+      const int B = shared ? shared_len(s) : 0;
+      const int wS = B > 0 ? kSegCost + kSharedCost * B : 0;
+      const int j = rr < wS ? max(0, rr - kSegCost + kSharedCost - 1) / kSharedCost
+                            : B + max(0, rr - wS - kSegCost + kOwnCost - 1) / kOwnCost;
       return (long long)s_pre[s] * U + (long long)u * nbl + j;
     };
     const long long qt = Tw / W, rt = Tw % W;

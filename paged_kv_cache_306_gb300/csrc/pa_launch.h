@@ -32,6 +32,15 @@ __host__ __device__ constexpr int decode_stages(int stage_bytes, int mode) {
              : 1;
 }
 
+// Costs for balancing the decode warps' ranges (relative units): a block of a
+// shared segment (two 8-column tiles of query rows; measured on GB300, ~1.28 times
+// an 8-column block), an own block, and the fixed work of a segment (its query
+// rows loaded with a global-memory round trip, its state reset, its last block's
+// tail cleared and its result stored) -- about one and a half blocks.  Batches of
+// many short sequences leave some warps with dozens of segments: counted in
+// blocks alone, those warps finish last.
+constexpr int kSharedCost = 5, kOwnCost = 4, kSegCost = 6;
+
 // Everything a decode launch needs; passed to the kernels by value.
 struct DecodeParams {
   void* out;                    // [S, H, D] in the cache dtype
