@@ -78,8 +78,9 @@ struct DecodeShape {
   static constexpr int kWpreBytes = ((kMaxSeqsPerLaunch + 1) * 4 + 15) / 16 * 16;
   static constexpr int kSideStageBytes = 2 * D * (kElem < 2 ? 2 : kElem);
   static constexpr bool kWpreInSide = kWarps * kStages * kSideStageBytes >= kWpreBytes;
-  static constexpr int kTableBytes = (kMaxSeqsPerLaunch + (kMaxSeqsPerLaunch + 1) + kWarps + 3 + 2 * kMaxSeqsPerLaunch) * 4 +
-                                     (kWpreInSide ? 0 : kWpreBytes);
+  static constexpr int kTableBytes =
+      (kMaxSeqsPerLaunch + (kMaxSeqsPerLaunch + 1) + 2 * kWarps + 3 + 2 * kMaxSeqsPerLaunch) * 4 +
+      (kWpreInSide ? 0 : kWpreBytes);
   // score row and running state per warp
   static constexpr int kRows = kMode ? 8 * kMode : 1;
   static constexpr int kStateBytes = kWarps * BS * 4 + kWarps * kRows * (D + 2) * 4;
@@ -966,8 +967,8 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   uint64_t* never = reinterpret_cast<uint64_t*>(smem + Sh::kRingBytes) + kDecodeWarps * STAGES;
   int* s_len = reinterpret_cast<int*>(smem + Sh::kRingBytes + Sh::kBarBytes);
   int* s_pre = s_len + kMaxSeqsPerLaunch;                 // [S + 1] block prefix per unit
-  int* s_wsum = s_pre + kMaxSeqsPerLaunch + 1;             // [warps]
-  int* s_info = s_wsum + kDecodeWarps + 3;                 // [S] cluster layout (shared prefixes)
+  int* s_wsum = s_pre + kMaxSeqsPerLaunch + 1;             // [2 warps]: per-warp sums of the prefix scans
+  int* s_info = s_wsum + 2 * kDecodeWarps + 3;             // [S] cluster layout (shared prefixes)
   int* s_lead = s_info + kMaxSeqsPerLaunch;                // [S] a leader's shared segment and donor
   // [S + 1] cost-weighted prefix per unit (shared prefixes; see DecodeShape::kWpreBytes)
   int* s_wpre = Sh::kWpreInSide ? reinterpret_cast<int*>(smem + Sh::kSideOffset) : s_lead + kMaxSeqsPerLaunch;
@@ -1008,32 +1009,48 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
 #pragma unroll
       for (int k = 0; k < PER; ++k) wt[k] = nb[k] > 0 ? kSegCost + kOwnCost * nb[k] : 0;
     }
-    // exclusive prefix sums of v over the sequences into out[0..S]
-    auto scan = [&](const int (&v)[PER], int* out) {
-      int sb = 0;
+    // exclusive prefix sums over the sequences of the blocks (into s_pre) and of the cost
+    // (into s_wpre) of each one's work per unit, in one pass
+    int sb = 0, sw = 0;
 #pragma unroll
-      for (int k = 0; k < PER; ++k) sb += v[k];
-      int ib = sb;  // inclusive warp scan
+    for (int k = 0; k < PER; ++k) {
+      sb += nb[k];
+      sw += wt[k];
+    }
+    int ib = sb, iw = sw;  // inclusive warp scans
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int xb = __shfl_up_sync(0xffffffffu, ib, o);
-        if (lane >= o) ib += xb;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int xb = __shfl_up_sync(0xffffffffu, ib, o), xw = __shfl_up_sync(0xffffffffu, iw, o);
+      if (lane >= o) {
+        ib += xb;
+        iw += xw;
       }
-      if (lane == 31) s_wsum[warp] = ib;
-      __syncthreads();
-      int ob = ib - sb;
-      for (int w = 0; w < warp; ++w) ob += s_wsum[w];
+    }
+    if (lane == 31) {
+      s_wsum[warp] = ib;
+      s_wsum[kDecodeWarps + warp] = iw;
+    }
+    __syncthreads();
+    int ob = ib - sb, ow = iw - sw;
+    for (int w = 0; w < warp; ++w) {
+      ob += s_wsum[w];
+      ow += s_wsum[kDecodeWarps + w];
+    }
 #pragma unroll
-      for (int k = 0; k < PER; ++k) {
-        const int i = tid * PER + k;
-        if (i <= S) out[i] = ob;
-        ob += v[k];
+    for (int k = 0; k < PER; ++k) {
+      const int i = tid * PER + k;
+      if (i <= S) {
+        s_pre[i] = ob;
+        s_wpre[i] = ow;
       }
-      if (tid == blockDim.x - 1) out[S] = ob;  // the total (also covers S == kMaxSeqsPerLaunch)
-      __syncthreads();
-    };
-    scan(nb, s_pre);
-    scan(wt, s_wpre);
+      ob += nb[k];
+      ow += wt[k];
+    }
+    if (tid == blockDim.x - 1) {  // the totals (also covers S == kMaxSeqsPerLaunch)
+      s_pre[S] = ob;
+      s_wpre[S] = ow;
+    }
+    __syncthreads();
   }
   // segment ids: one per (sequence, unit), or two with shared prefixes (the shared part, then the own part)
   auto seg_id = [&](int s, int u, int part) { return shared ? 2 * (s * U + u) + part : s * U + u; };
