@@ -1392,10 +1392,11 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
 // row's pieces are the slots of its own segment and, with shared prefixes, those of
 // its cluster's shared part (where the member's rows sit at row offset
 // member * group).  Lane i reads the tag and (m, l) of piece i of a chunk of up to
-// 32; the chunk's maximum and weights come from warp shuffles,
-//     m_c = max m_p,  w_p = l_p 2^(m_p - m_c),  l_c = sum w_p,  o_c = sum w_p o_p,
-// and the partial outputs are read 8 pieces at a time (each lane D/32 consecutive
-// head dims), so a chunk costs about two trips to L2.  Chunks fold into a running
+// 32, together with the first batch of the chunk's partial outputs (each lane D/32
+// consecutive head dims; 32 registers' worth), so a chunk of 8 pieces costs one trip
+// to L2; the chunk's
+// maximum and weights come from warp shuffles,
+//     m_c = max m_p,  w_p = l_p 2^(m_p - m_c),  l_c = sum w_p,  o_c = sum w_p o_p.  Chunks fold into a running
 // (M, L, O) with the same rule; the row is O / L.  Slots whose tag is not (their
 // segment, this launch's epoch) weigh nothing and are never read into a sum:
 // when the grid has more warps than blocks of work, a warp with an empty range
@@ -1404,15 +1405,22 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
 // m = -inf and weighs nothing too.
 constexpr int kMergeRows = 8;
 
-template <typename T, int D, bool kMma>
-__global__ void __launch_bounds__(kMergeRows * 32) decode_merge_kernel(const DecodeParams p) {
+//
+// kWide (launches whose segments are cut into many pieces, e.g. a few very long
+// sequences): one CTA per row instead, its warps taking equal runs of the row's
+// pieces, and warp 0 folding their results from shared memory, so that no warp
+// walks a long list of pieces alone.
+template <typename T, int D, bool kMma, bool kWide>
+__global__ void __launch_bounds__(kMergeRows * 32, 2) decode_merge_kernel(const DecodeParams p) {
   constexpr int CPL = D / 32;  // head dims per lane
   using Vec = std::conditional_t<CPL == 4, float4, float2>;
+  __shared__ __align__(16) float s_o[kWide ? kMergeRows : 1][D];
+  __shared__ float s_m[kMergeRows], s_l[kMergeRows];
   griddep_wait();
   griddep_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * kMergeRows + (threadIdx.x >> 5);
-  if (row >= (long long)p.num_seqs * p.num_heads) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long row = kWide ? (long long)blockIdx.x : (long long)blockIdx.x * kMergeRows + warp;
+  if (row >= (long long)p.num_seqs * p.num_heads) return;  // (wide: the whole CTA)
   const int s = static_cast<int>(row / p.num_heads), h = static_cast<int>(row - (long long)s * p.num_heads);
   // the head unit of h and h's row within it
   int u, r;
@@ -1448,36 +1456,46 @@ __global__ void __launch_bounds__(kMergeRows * 32) decode_merge_kernel(const Dec
   }
   const int Ks = slast - sfirst + 1;
   const int K = Ks + (last - first + 1);
-  if (K <= 0) return;
+  if (K <= 0) return;  // (wide: the whole CTA, every warp computed the same)
+  // the pieces this warp folds
+  const int lo = kWide ? (K * warp) / kMergeRows : 0, hi = kWide ? (K * (warp + 1)) / kMergeRows : K;
   const int ep = static_cast<int>(p.epoch);
   // piece i: the offset of its row in the partial arrays, and the segment that must have written it
+  const long long at_s = (long long)sfirst * p.rows + srow + r, at_o = (long long)(first - Ks) * p.rows + r;
   auto piece = [&](int i, long long& at, int& seg) {
-    if (i < Ks) {
-      at = (long long)(sfirst + i) * p.rows + srow + r;
-      seg = sseg;
-    } else {
-      at = (long long)(first + (i - Ks)) * p.rows + r;
-      seg = own;
-    }
+    at = (i < Ks ? at_s : at_o) + (long long)i * p.rows;
+    seg = i < Ks ? sseg : own;
   };
 
   float RM = -INFINITY, RL = 0.f, RO[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) RO[c] = 0.f;
-  for (int c0 = 0; c0 < K; c0 += 32) {
-    const int n = min(32, K - c0);
+  constexpr int kBatch = 32 / CPL;  // partial outputs in flight per lane (32 registers)
+  for (int c0 = lo; c0 < hi; c0 += 32) {
+    const int n = min(32, hi - c0);
+    // the tags and (m, l) of the chunk and the first batch of its partial outputs, all in flight at once
     float m = -INFINITY, l = 0.f;
+    int2 tag = make_int2(-1, 0);
+    int sg_mine = -1;
+    float2 ml = make_float2(0.f, 0.f);
     if (lane < n) {
       long long at;
-      int sg;
-      piece(c0 + lane, at, sg);
-      const long long slot = at / p.rows;
-      const int2 tag = p.part_tag[slot];
-      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + at * 2);
-      if (tag.x == sg && tag.y == ep) {
-        m = ml.x;
-        l = ml.y;
+      piece(c0 + lane, at, sg_mine);
+      tag = p.part_tag[at / p.rows];
+      ml = *reinterpret_cast<const float2*>(p.part_ml + at * 2);
+    }
+    Vec ov[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (i < n) {
+        long long at;
+        int sg;
+        piece(c0 + i, at, sg);
+        ov[i] = *reinterpret_cast<const Vec*>(p.part_o + at * D + CPL * lane);
       }
+    if (lane < n && tag.x == sg_mine && tag.y == ep) {
+      m = ml.x;
+      l = ml.y;
     }
     float mc = m;
 #pragma unroll
@@ -1489,19 +1507,20 @@ __global__ void __launch_bounds__(kMergeRows * 32) decode_merge_kernel(const Dec
     float oc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) oc[c] = 0.f;
-    for (int i0 = 0; i0 < n; i0 += 8) {
-      Vec ov[8];
+    for (int i0 = 0; i0 < n; i0 += kBatch) {
+      if (i0 > 0) {  // the next batch of partial outputs
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i0 + i < n) {
-          long long at;
-          int sg;
-          piece(c0 + i0 + i, at, sg);
-          ov[i] = *reinterpret_cast<const Vec*>(p.part_o + at * D + CPL * lane);
-        }
+        for (int i = 0; i < kBatch; ++i)
+          if (i0 + i < n) {
+            long long at;
+            int sg;
+            piece(c0 + i0 + i, at, sg);
+            ov[i] = *reinterpret_cast<const Vec*>(p.part_o + at * D + CPL * lane);
+          }
+      }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float wi = __shfl_sync(0xffffffffu, w, i0 + i);
+      for (int i = 0; i < kBatch; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, (i0 + i) & 31);
         if (i0 + i < n && wi > 0.f) {  // a slot no piece wrote in this launch holds anything (NaN too)
           const float* v = reinterpret_cast<const float*>(&ov[i]);
 #pragma unroll
@@ -1515,6 +1534,29 @@ __global__ void __launch_bounds__(kMergeRows * 32) decode_merge_kernel(const Dec
       RL = RL * fa + lc * fb;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) RO[c] = RO[c] * fa + fb * oc[c];
+      RM = mn;
+    }
+  }
+  if constexpr (kWide) {  // warp 0 folds the warps' results
+    if (lane == 0) {
+      s_m[warp] = RM;
+      s_l[warp] = RL;
+    }
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) s_o[warp][CPL * lane + c] = RO[c];
+    __syncthreads();
+    if (warp != 0) return;
+    RM = -INFINITY;
+    RL = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) RO[c] = 0.f;
+    for (int j = 0; j < kMergeRows; ++j) {
+      if (!(s_l[j] > 0.f)) continue;
+      const float mn = fmaxf(RM, s_m[j]);
+      const float fa = exp2f(RM - mn), fb = exp2f(s_m[j] - mn);
+      RL = RL * fa + s_l[j] * fb;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) RO[c] = RO[c] * fa + fb * s_o[j][CPL * lane + c];
       RM = mn;
     }
   }
@@ -1564,8 +1606,17 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream
                  decode_smem_bytes<TC, D, BS, kMode>(), stream, p);
   if (e != cudaSuccess) return e;
   *launches = 1;
-  const unsigned merge_ctas = static_cast<unsigned>(((long long)p.num_seqs * p.num_heads + kMergeRows - 1) / kMergeRows);
-  e = launch_pdl(decode_merge_kernel<T, D, (kMode != 0)>, dim3(merge_ctas), dim3(kMergeRows * 32), 0, stream, p);
+  // rows whose segments average 16 pieces or more (a few very long sequences) take a CTA each
+  const long long rows = (long long)p.num_seqs * p.num_heads;
+  const long long segs = (long long)p.num_seqs * p.units;
+  const bool wide = (long long)grid * DecodeShape<TC, D, BS, kMode>::kWarps >= 16 * segs;
+  if (wide)
+    e = launch_pdl(decode_merge_kernel<T, D, (kMode != 0), true>, dim3(static_cast<unsigned>(rows)),
+                   dim3(kMergeRows * 32), 0, stream, p);
+  else
+    e = launch_pdl(decode_merge_kernel<T, D, (kMode != 0), false>,
+                   dim3(static_cast<unsigned>((rows + kMergeRows - 1) / kMergeRows)), dim3(kMergeRows * 32), 0, stream,
+                   p);
   if (e != cudaSuccess) return e;
   *launches = 2;
   return cudaSuccess;
