@@ -77,7 +77,7 @@ cudaError_t encode_v_map(const PrefillParams& p, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// The warp-specialised tcgen05 kernel (prefill_ws.cuh): one CTA per tile of 128 query rows, two per SM.
+// The warp-specialised tcgen05 kernel (prefill_ws.cuh): one CTA per pair of 128-row query tiles, one per SM.
 template <typename T, int D, int BS>
 cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int* launches) {
   using Sh = ws::Shape<T, D, BS>;
@@ -100,10 +100,11 @@ cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int
   if (e != cudaSuccess) return e;
   e = encode_v_map<D, BS>(p, &vmap);
   if (e != cudaSuccess) return e;
-  const long long tiles = (long long)p.num_kv_heads *
-                          (((long long)p.num_query_tokens * p.group + ws::kRows - 1) / ws::kRows + p.num_seqs);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  e = launch_pdl(ws::prefill_ws_kernel<T, D, BS>, dim3(static_cast<unsigned>(tiles)), dim3(ws::kThreads), Sh::kSmem,
+  // sequence s has ceil(ceil(n_s G / 128) / 2) pairs per kv head, at most n_s G / 256 + 1 (rounded up)
+  const long long pairs = (long long)p.num_kv_heads *
+                          (((long long)p.num_query_tokens * p.group + 2 * ws::kRows - 1) / (2 * ws::kRows) + p.num_seqs);
+  if (pairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  e = launch_pdl(ws::prefill_ws_kernel<T, D, BS>, dim3(static_cast<unsigned>(pairs)), dim3(ws::kThreads), Sh::kSmem,
                  stream, p, kmap, vmap);
   if (e == cudaSuccess) *launches = 1;
   return e;

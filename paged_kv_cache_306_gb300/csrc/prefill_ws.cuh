@@ -2,15 +2,17 @@
 //
 // Causal attention of each sequence's chunk of new query tokens over its paged
 // cache (what is computed: see prefill.cu), on sm_103a's tcgen05 MMAs with the
-// accumulators in tensor memory (TMEM).  A CTA owns a
-// tile of 128 query rows -- (token, query head) pairs of one kv head, head
-// fastest -- which are TMEM lanes 0..127, and takes keys 64 at a time.  The
-// phases of a chunk run in different warps that hand over through mbarriers, so
-// the copies, the MMAs and the softmax of neighbouring chunks overlap:
+// accumulators in tensor memory (TMEM).  A query tile is 128 rows -- (token,
+// query head) pairs of one kv head, head fastest -- which are TMEM lanes
+// 0..127; keys are taken 64 at a time (a chunk).  A CTA owns a PAIR of
+// consecutive tiles of one (sequence, kv head): both read the same keys, so each
+// chunk of K and V is copied once and feeds the MMAs of both tiles, and while
+// the tensor cores work for one tile the softmax of the other runs.  The phases
+// run in different warps that hand over through mbarriers:
 //
-//   * warp 4, one thread: the TMA copies of chunk c, through two tensor maps: K
-//     into K buffer c % 2 once S of chunk c - 2 has read it, V into V buffer c % 3
-//     once P V of chunk c - 3 has read it (V is needed last), each on its own
+//   * warp 8, one thread: the TMA copies of chunk c, through two tensor maps: K
+//     into K buffer c % 4 once both tiles' S of chunk c - 4 have read it, V into V
+//     buffer c % 4 once both tiles' P V of chunk c - 4 have read it, each on its own
 //     mbarrier, so S waits only for K and the V copies are well ahead.  K: the pool seen
 //     as rows of 16 keys x 8 dims (one 256-byte run of a K tile [D/8][bs][8]); one
 //     tile::gather4 load per 8-dim chunk fetches the rows of the chunk's 64 keys
@@ -21,18 +23,24 @@
 //     seen as rows of bs keys (one dim of a V tile [D][bs]); each [D rows x 8 keys]
 //     box lands as [D][8], one 8-key group of the [key/8][D][8] layout the P V MMA
 //     reads.  No re-layout pass.
-//   * warp 5, one thread: S(c) = Q K^T into TMEM columns S[c % 2] (once chunk c
-//     has landed and P V(c - 2), which read P from those columns, is done), then
-//     O += P V(c - 1) with P read from TMEM; each group is committed to mbarriers.
-//   * warps 0..3, one thread per row: the softmax of S(c) while the tensor cores
-//     run P V(c - 1) and S(c + 1).  P = exp2(s - m) goes back into the row's own S
+//   * warp 9, one thread: for each chunk c, S_A(c) and S_B(c) = Q K^T into each
+//     tile's TMEM columns S[c % 2] (once chunk c has landed and that tile's
+//     P V(c - 2), which read P from those columns, is done), then O_A += P V(c - 1)
+//     and O_B += P V(c - 1) with P read from TMEM; each group is committed to
+//     mbarriers.  Tile A's softmax of chunk c thus runs under S_B(c), the P V of
+//     chunk c - 1 and the S of chunk c + 1 of both tiles.
+//   * warps 0..3 (tile A) and 4..7 (tile B), one thread per row: the softmax of
+//     S(c).  P = exp2(s - m) goes back into the row's own S
 //     columns as rounded 16-bit high and low parts (two per 32-bit column).  The
 //     running maximum moves only when it grows by more than 2^8; then the row's O
 //     is rescaled in TMEM after P V(c - 1) has finished (rare).  In the last chunk
-//     the V of keys past the sequence (or past the blocks loaded) is zeroed in
-//     shared memory first: P is 0 there, but 0 * NaN would poison O.
+//     tile A's threads zero the V of keys past the sequence (or past the blocks
+//     loaded) in shared memory first: P is 0 there, but 0 * NaN would poison O.
+//     A tile whose rows end before the pair's last chunks sees scores of -inf
+//     there (P = 0).
 //
-// At under 113 KiB of shared memory and 256 TMEM columns, two CTAs share an SM.
+// TMEM: per tile two S/P column groups of 64 and O (D <= 128 columns) in 256, all
+// 512 columns for the pair; one CTA per SM.
 // Every wait is bounded (1 s of %globaltimer); a thread that gives up records
 // PA_DEVERR_TIMEOUT and raises a CTA-wide abort flag that makes every other wait
 // give up at once; the threads that issued copies or MMAs then wait (bounded)
@@ -49,6 +57,7 @@ namespace pa {
 namespace ws {
 
 using tc::commit;
+using tc::elect_one;
 using tc::fence_after;
 using tc::fence_before;
 using tc::idesc;
@@ -57,12 +66,12 @@ using tc::mma;
 using tc::sdesc;
 using tc::st32;
 
-constexpr int kRows = 128;  // query rows per CTA (= TMEM lanes)
+constexpr int kRows = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kKeys = 64;   // keys per chunk
-constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
-constexpr int kVStages = 3;
+constexpr int kSoftmaxThreads = 128;  // per tile
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr int kKStages = 4, kVStages = 4;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -145,16 +154,19 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// The tile of rank `rank` (0-based) in the order of decreasing length -- the chunks of
-// keys it reads -- ties by sequence, kv head and tile index; so the longest tiles of
-// the whole launch start first and the short ones fill the tail.  Every thread of
-// the CTA takes part (thread t owns sequences t * kPer ..); tile j of sequence s
-// covers rows 128 j .. of its n * G rows and reads chunks 0 .. (ctx + (row_hi - 1) / G) / 64,
-// which is non-decreasing in j, so the tiles of s reading >= x chunks are a suffix
-// in j counted in closed form, and the rank-th tile is found by a binary search on x.
-// Writes (sequence, kv head, tile) to out; returns false when rank is past the tiles.
-__device__ bool pick_tile(const PrefillParams& p, int rank, int* red, int* out) {
+// The pair of rank `rank` (0-based) in the order of decreasing length -- the chunks
+// of keys it reads -- ties by sequence, kv head and pair index; so the longest
+// pairs of the whole launch start first and the short ones fill the tail.  Every
+// thread of the CTA takes part (thread t owns sequences t * kPer ..).  Tile j of
+// sequence s covers rows 128 j .. of its n * G rows and reads chunks
+// 0 .. (ctx + (row_hi - 1) / G) / 64, non-decreasing in j; pair k holds tiles 2k and
+// 2k + 1 (if there is one) and reads what its last tile reads.  So the tiles of s
+// reading >= x chunks are a suffix j >= j0 in closed form, the pairs reading >= x
+// are those from j0 / 2 on, and the rank-th pair is found by a binary search on x.
+// Writes (sequence, kv head, pair) to out; returns false when rank is past the pairs.
+__device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) {
   constexpr int kPer = (kMaxSeqsPerLaunch + kThreads - 1) / kThreads;
+  constexpr int kWarpsTotal = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.group, Hkv = p.num_kv_heads;
   int ctx[kPer], rows[kPer], nt[kPer];
@@ -176,12 +188,12 @@ __device__ bool pick_tile(const PrefillParams& p, int rank, int* red, int* out) 
     }
   }
   if (bad && blockIdx.x == 0) set_error(p.err, kErrSeqLen);
-  // tiles of owned sequence i that read >= x chunks
+  // pairs of owned sequence i that read >= x chunks
   auto cnt = [&](int i, int x) -> int {
-    const long long need = (long long)G * (64LL * (x - 1) - ctx[i]) + 1;  // rows the tile must reach
+    const long long need = (long long)G * (64LL * (x - 1) - ctx[i]) + 1;  // rows a tile must reach
     if (nt[i] == 0 || need > rows[i]) return 0;
-    if (need <= 1) return nt[i];
-    return nt[i] - static_cast<int>((need + kRows - 1) / kRows - 1);
+    const int j0 = need <= 1 ? 0 : static_cast<int>((need + kRows - 1) / kRows - 1);  // first tile reading >= x
+    return (nt[i] + 1) / 2 - j0 / 2;
   };
   int buf = 0;
   auto reduce = [&](int v, bool take_max) -> int {
@@ -191,17 +203,17 @@ __device__ bool pick_tile(const PrefillParams& p, int rank, int* red, int* out) 
       v = take_max ? max(v, u) : v + u;
     }
     buf ^= 1;
-    if (lane == 0) red[buf * 8 + warp] = v;
+    if (lane == 0) red[buf * 16 + warp] = v;
     __syncthreads();
-    int t = take_max ? 0 : 0;
+    int t = 0;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) t = take_max ? max(t, red[buf * 8 + w]) : t + red[buf * 8 + w];
+    for (int w = 0; w < kWarpsTotal; ++w) t = take_max ? max(t, red[buf * 16 + w]) : t + red[buf * 16 + w];
     return t;
   };
   int local = 0, longest = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
-    local += nt[i];
+    local += (nt[i] + 1) / 2;
     if (nt[i]) longest = max(longest, (ctx[i] + (rows[i] - 1) / G) / 64 + 1);
   }
   if ((long long)Hkv * reduce(local, false) <= rank) return false;
@@ -214,7 +226,7 @@ __device__ bool pick_tile(const PrefillParams& p, int rank, int* red, int* out) 
     if ((long long)Hkv * reduce(local, false) > rank) lo = mid;
     else hi = mid - 1;
   }
-  // rank among the tiles of exactly lo chunks, ordered by (sequence, kv head, tile)
+  // rank among the pairs of exactly lo chunks, ordered by (sequence, kv head, pair)
   local = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) local += cnt(i, lo + 1);
@@ -232,10 +244,10 @@ __device__ bool pick_tile(const PrefillParams& p, int rank, int* red, int* out) 
     if (lane >= o) incl += u;
   }
   buf ^= 1;
-  if (lane == 31) red[buf * 8 + warp] = incl;
+  if (lane == 31) red[buf * 16 + warp] = incl;
   __syncthreads();
   long long before = incl - mine;
-  for (int w = 0; w < warp; ++w) before += red[buf * 8 + w];
+  for (int w = 0; w < warp; ++w) before += red[buf * 16 + w];
   before *= Hkv;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
@@ -244,7 +256,7 @@ __device__ bool pick_tile(const PrefillParams& p, int rank, int* red, int* out) 
       const int q = static_cast<int>(r - before);
       out[0] = tid * kPer + i;
       out[1] = q / e[i];
-      out[2] = nt[i] - cnt(i, lo) + q % e[i];
+      out[2] = (nt[i] + 1) / 2 - cnt(i, lo) + q % e[i];
     }
     before += span;
   }
@@ -256,51 +268,62 @@ template <typename T, int D, int BS>
 struct Shape {
   static constexpr int kTile = D * BS * 2;                 // one block's K (or V) tile
   static constexpr int kBlocks = kKeys / BS;               // blocks per chunk
-  static constexpr int kQBytes = kRows * D * 2;            // Q, core-matrix layout
+  static constexpr int kQTile = kRows * D * 2;             // one tile's Q, core-matrix layout
   static constexpr int kKBytes = kKeys * D * 2;  // a chunk's K as [D/8][64][8]
   static constexpr int kVBytes = kKeys * D * 2;  // a chunk's V as [key/8][D][8]
-  static constexpr int kOffK = kQBytes;          // K ring: 2 buffers
-  static constexpr int kOffV = kOffK + 2 * kKBytes;  // V ring: 3 buffers (V is read last)
+  static constexpr int kOffK = 2 * kQTile;                  // K ring
+  static constexpr int kOffV = kOffK + kKStages * kKBytes;  // V ring
   static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-  static constexpr int kNumBars = 2 + kVStages + 2 + 2 + 2 + kVStages + 1;  // the last: nothing completes it
-  static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][8] ints: block reductions
-  static constexpr int kSmem = kOffRed + 2 * 8 * 4;            // <= 113 KiB: two CTAs per SM
-  static constexpr int kTmemCols = 256;  // S/P[0]: 0..63, S/P[1]: 64..127, O: 128..128+D
+  // fullk[K], fullv[V], kfree[K], vfree[V], per tile sfull[2], pfull[2], pvdone[2], never
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 6 + 1;
+  static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][16] ints: block reductions
+  // more than half an SM's shared memory, so one CTA per SM: it takes all of TMEM
+  static constexpr int kSmem = kOffRed + 2 * 16 * 4 > 116 * 1024 ? kOffRed + 2 * 16 * 4 : 116 * 1024;
+  static constexpr int kTmemCols = 512;  // tile X at 256 X: S/P[0] 0..63, S/P[1] 64..127, O 128..128+D
 };
 
 template <typename T, int D, int BS>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_ws_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
   using Sh = Shape<T, D, BS>;
+  static_assert(Sh::kSmem > 114 * 1024, "two CTAs on one SM would contend for TMEM");
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* sQ = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);
-  uint64_t* fullk = bars;                   // [2] K buffer landed (TMA bytes)
-  uint64_t* fullv = fullk + 2;              // [kVStages] V buffer landed (TMA bytes)
-  uint64_t* sfull = fullv + kVStages;       // [2] S in TMEM, the K buffer read (commit)
-  uint64_t* pfull = sfull + 2;              // [2] P in TMEM, O rescaled and V tail zeroed where needed (128 arrivals)
-  uint64_t* pvdone = pfull + 2;             // [2] P V done: P's columns and O are free (commit)
-  uint64_t* vfree = pvdone + 2;             // [kVStages] P V done with the V buffer (commit)
-  uint64_t* never = vfree + kVStages;       // nothing completes it: the timeout-path test waits on it
+  uint64_t* fullk = bars;                   // [kKStages] K buffer landed (TMA bytes)
+  uint64_t* fullv = fullk + kKStages;       // [kVStages] V buffer landed (TMA bytes)
+  uint64_t* kfree = fullv + kVStages;       // [kKStages] both tiles' S read the K buffer (commit)
+  uint64_t* vfree = kfree + kKStages;       // [kVStages] both tiles' P V read the V buffer (commit)
+  uint64_t* tbars = vfree + kVStages;       // per tile X at 6 X: sfull[2], pfull[2], pvdone[2]
+  uint64_t* never = tbars + 12;             // nothing completes it: the timeout-path test waits on it
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
-  int* s_tile = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, tile (or -1)
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tile + 3);  // a thread gave up
+  int* s_pair = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, pair (or -1)
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_pair + 3);  // a thread gave up
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // S in TMEM, the K buffer read (commit); P in TMEM, O rescaled, V tail zeroed (128 arrivals);
+  // P V done: P's columns and O free (commit)
+  auto sfull = [&](int X, int i) { return tbars + 6 * X + i; };
+  auto pfull = [&](int X, int i) { return tbars + 6 * X + 2 + i; };
+  auto pvdone = [&](int X, int i) { return tbars + 6 * X + 4 + i; };
 
   griddep_launch_dependents();
   griddep_wait();
 
-  // ---- which tile: the longest first over the whole launch
-  const bool has_tile = pick_tile(p, static_cast<int>(blockIdx.x), reinterpret_cast<int*>(smem + Sh::kOffRed), s_tile);
+  // ---- which pair: the longest first over the whole launch
+  const bool has_pair = pick_pair(p, static_cast<int>(blockIdx.x), reinterpret_cast<int*>(smem + Sh::kOffRed), s_pair);
   if (tid == 0) {
-    if (!has_tile) s_tile[0] = -1;
+    if (!has_pair) s_pair[0] = -1;
     *s_abort = 0;
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&fullk[i], 1);
-      mbar_init(&sfull[i], 1);
-      mbar_init(&pfull[i], kSoftmaxThreads);
-      mbar_init(&pvdone[i], 1);
+      mbar_init(&kfree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      for (int X = 0; X < 2; ++X) {
+        mbar_init(sfull(X, i), 1);
+        mbar_init(pfull(X, i), kSoftmaxThreads);
+        mbar_init(pvdone(X, i), 1);
+      }
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&fullv[i], 1);
@@ -310,14 +333,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_barrier_init();
   }
   __syncthreads();
-  const int s = s_tile[0];
-  if (s < 0) return;  // no tile for this CTA (before any TMEM is taken)
-  const int kvh = s_tile[1], tile = s_tile[2];
+  const int s = s_pair[0];
+  if (s < 0) return;  // no pair for this CTA (before any TMEM is taken)
+  const int kvh = s_pair[1], pair = s_pair[2];
   const int G = p.group;
   const int L = p.seq_lens[s], tok0 = p.query_start_loc[s], n = p.query_start_loc[s + 1] - tok0;
-  const int rows = n * G, row_lo = tile * kRows, row_hi = min(rows, row_lo + kRows);
+  const int rows = n * G, pair_lo = 2 * pair * kRows, pair_hi = min(rows, pair_lo + 2 * kRows);
+  const bool two = pair_lo + kRows < rows;    // the pair has a tile B
   const int ctx = L - n;
-  const int p_max = ctx + (row_hi - 1) / G;  // last position any row of the tile has
+  const int p_max = ctx + (pair_hi - 1) / G;  // last position any row of the pair has
   const int nblk = p_max / BS + 1;            // blocks holding keys 0..p_max
   const int nchunks = (p_max + kKeys) / kKeys;
 
@@ -326,10 +350,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                  "r"(Sh::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // the softmax threads' rows; Q into shared memory (core matrices: 8 rows x 16 bytes)
-  const int r = tid & (kRows - 1), row = row_lo + r;
-  const bool valid = row < row_hi;
-  if (tid < kSoftmaxThreads) {
+  // the softmax threads' tile and row; Q of both tiles into shared memory (core matrices: 8 rows x 16 bytes)
+  const int X = tid >= kSoftmaxThreads ? 1 : 0;  // (softmax threads only)
+  const int r = tid & (kRows - 1), row = pair_lo + X * kRows + r;
+  const bool valid = row < pair_hi;
+  if (tid < 2 * kSoftmaxThreads) {
+    unsigned char* sQ = smem + X * Sh::kQTile;
     const T* q = static_cast<const T*>(p.q) +
                  ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) * D;
 #pragma unroll
@@ -343,131 +369,135 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t t_o = tmem + 2 * kKeys;
   auto wait = [&](uint64_t* bar, int parity) { return wait_or_abort(bar, parity, s_abort, p.err); };
   int issued_k = 0, issued_v = 0;  // chunks whose K (V) copies the producer issued
 
-  if (warp < 4) {
-    // ================= softmax: row r, all keys of each chunk =================
-    const int pos = valid ? ctx + row / G : p_max;  // a padding row behaves as the last real one
-    const int kz = min(L, nblk * BS);               // first key whose V must read as zero
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int c = 0; c < nchunks; ++c) {
-      const int sb = c & 1;
-      // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them
-      // is taken by the whole warp, so each wait's outcome is agreed across the warp
-      if (!__all_sync(0xffffffffu, wait(&sfull[sb], (c >> 1) & 1))) {
-        ok = false;
-        break;
-      }
-      fence_after();
-      const uint32_t t_s = tmem + lane_base + sb * kKeys;
-      float sv[kKeys];
-      ld64(t_s, sv);
-      const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
-      if (lim < kKeys - 1) {           // the diagonal chunk (or past it): hide the later keys
-#pragma unroll
-        for (int j = 0; j < kKeys; ++j)
-          if (j > lim) sv[j] = -INFINITY;
-      }
-      // the row maximum of the raw scores, as a tree (scale > 0 keeps the order)
-      float mx;
-      {
-        float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = sv[i];
-#pragma unroll
-        for (int j = 8; j < kKeys; ++j) t[j & 7] = fmaxf(t[j & 7], sv[j]);
-        mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7]))) * sl2;
-      }
-      float corr = 1.f;
-      const bool move = mx > m + 8.f;
-      if (move) {
-        corr = m == -INFINITY ? 0.f : exp2f(m - mx);
-        m = mx;
-        l *= corr;
-      }
-      // O holds P V up to chunk c - 1 once that group is done: rescale the row if the maximum moved
-      // (the whole warp takes the branch when one of its rows needs it; the others scale by 1)
-      const bool rescale = c > 0 && move && corr != 1.f;
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!__all_sync(0xffffffffu, wait(&pvdone[(c - 1) & 1], ((c - 1) >> 1) & 1))) {
+  if (warp < 8) {
+    // ================= softmax: tile X, row r, all keys of each chunk =================
+    if (X == 0 || two) {
+      const uint32_t tbase = tmem + 256 * X;
+      const uint32_t t_o = tbase + 2 * kKeys;
+      const int pos = valid ? ctx + row / G : ctx + (pair_hi - 1) / G;  // a padding row behaves as a real one
+      const int kz = min(L, nblk * BS);  // first key whose V must read as zero
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      const float sl2 = p.scale_log2;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int c = 0; c < nchunks; ++c) {
+        const int sb = c & 1;
+        // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them
+        // is taken by the whole warp, so each wait's outcome is agreed across the warp
+        if (!__all_sync(0xffffffffu, wait(sfull(X, sb), (c >> 1) & 1))) {
           ok = false;
           break;
         }
         fence_after();
-        const float f = rescale ? corr : 1.f;
+        const uint32_t t_s = tbase + lane_base + sb * kKeys;
+        float sv[kKeys];
+        ld64(t_s, sv);
+        const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
+        if (lim < kKeys - 1) {           // the diagonal chunk (or past it): hide the later keys
+#pragma unroll
+          for (int j = 0; j < kKeys; ++j)
+            if (j > lim) sv[j] = -INFINITY;
+        }
+        // the row maximum of the raw scores, as a tree (scale > 0 keeps the order)
+        float mx;
+        {
+          float t[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = sv[i];
+#pragma unroll
+          for (int j = 8; j < kKeys; ++j) t[j & 7] = fmaxf(t[j & 7], sv[j]);
+          mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7]))) * sl2;
+        }
+        float corr = 1.f;
+        const bool move = mx > m + 8.f;
+        if (move) {
+          corr = m == -INFINITY ? 0.f : exp2f(m - mx);
+          m = mx;
+          l *= corr;
+        }
+        // O holds P V up to chunk c - 1 once that group is done: rescale the row if the maximum moved
+        // (the whole warp takes the branch when one of its rows needs it; the others scale by 1)
+        const bool rescale = c > 0 && move && corr != 1.f;
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (!__all_sync(0xffffffffu, wait(pvdone(X, (c - 1) & 1), ((c - 1) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const float f = rescale ? corr : 1.f;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float o[32];
+            ld32(t_o + lane_base + c0, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] *= f;
+            st32(t_o + lane_base + c0, o);
+          }
+        }
+        // P into the row's S columns: high parts in 0..31, low parts in 32..63
+        {
+          float hi[32], lo[32];
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
+            const float x0 = ex2(fmaf(sv[2 * j], sl2, -m)), x1 = ex2(fmaf(sv[2 * j + 1], sl2, -m));
+            ps[j & 3] += x0 + x1;
+            const uint32_t h = pack2<T>(x0, x1);
+            const float2 back = unpack2<T>(h);
+            hi[j] = __uint_as_float(h);
+            lo[j] = __uint_as_float(pack2<T>(x0 - back.x, x1 - back.y));
+          }
+          st32(t_s, hi);
+          st32(t_s + 32, lo);
+          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        }
+        // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as
+        // zero; tile A's threads clear it before either tile's P V of the chunk is issued
+        if (X == 0 && c == nchunks - 1 && kz < (c + 1) * kKeys) {
+          if (!__all_sync(0xffffffffu, wait(&fullv[c % kVStages], (c / kVStages) & 1))) {
+            ok = false;
+            break;
+          }
+          unsigned char* vbase = smem + Sh::kOffV + (c % kVStages) * Sh::kVBytes;
+          const int k0 = kz - c * kKeys, cnt = (kKeys - k0) * D;
+          for (int i = tid; i < cnt; i += kSoftmaxThreads) {
+            const int kk = k0 + i / D, d = i % D;
+            *reinterpret_cast<T*>(vbase + (kk / 8) * (D * 16) + d * 16 + (kk % 8) * 2) = DType<T>::from_f32(0.f);
+          }
+          fence_proxy_async_smem();
+        }
+        fence_before();
+        mbar_arrive(pfull(X, sb));
+      }
+      if (__all_sync(0xffffffffu, ok && wait(pvdone(X, (nchunks - 1) & 1), ((nchunks - 1) >> 1) & 1))) {
+        fence_after();
+        const float inv = 1.f / l;
+        T* out = static_cast<T*>(p.out) +
+                 ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) *
+                     D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
           ld32(t_o + lane_base + c0, o);
+          if (valid) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] *= f;
-          st32(t_o + lane_base + c0, o);
-        }
-      }
-      // P into the row's S columns: high parts in 0..31, low parts in 32..63
-      {
-        float hi[32], lo[32];
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
-          const float x0 = ex2(fmaf(sv[2 * j], sl2, -m)), x1 = ex2(fmaf(sv[2 * j + 1], sl2, -m));
-          ps[j & 3] += x0 + x1;
-          const uint32_t h = pack2<T>(x0, x1);
-          const float2 back = unpack2<T>(h);
-          hi[j] = __uint_as_float(h);
-          lo[j] = __uint_as_float(pack2<T>(x0 - back.x, x1 - back.y));
-        }
-        st32(t_s, hi);
-        st32(t_s + 32, lo);
-        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      }
-      // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as zero
-      if (c == nchunks - 1 && kz < (c + 1) * kKeys) {
-        if (!__all_sync(0xffffffffu, wait(&fullv[c % kVStages], (c / kVStages) & 1))) {
-          ok = false;
-          break;
-        }
-        unsigned char* vbase = smem + Sh::kOffV + (c % kVStages) * Sh::kVBytes;
-        const int k0 = kz - c * kKeys, cnt = (kKeys - k0) * D;
-        for (int i = tid; i < cnt; i += kSoftmaxThreads) {
-          const int kk = k0 + i / D, d = i % D;
-          *reinterpret_cast<T*>(vbase + (kk / 8) * (D * 16) + d * 16 + (kk % 8) * 2) = DType<T>::from_f32(0.f);
-        }
-        fence_proxy_async_smem();
-      }
-      fence_before();
-      mbar_arrive(&pfull[sb]);
-    }
-    if (__all_sync(0xffffffffu, ok && wait(&pvdone[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1))) {
-      fence_after();
-      const float inv = 1.f / l;
-      T* out = static_cast<T*>(p.out) +
-               ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) *
-                   D;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float o[32];
-        ld32(t_o + lane_base + c0, o);
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 w;
-            w.x = pack2<T>(o[j] * inv, o[j + 1] * inv);
-            w.y = pack2<T>(o[j + 2] * inv, o[j + 3] * inv);
-            w.z = pack2<T>(o[j + 4] * inv, o[j + 5] * inv);
-            w.w = pack2<T>(o[j + 6] * inv, o[j + 7] * inv);
-            *reinterpret_cast<uint4*>(out + c0 + j) = w;
+            for (int j = 0; j < 32; j += 8) {
+              uint4 w;
+              w.x = pack2<T>(o[j] * inv, o[j + 1] * inv);
+              w.y = pack2<T>(o[j + 2] * inv, o[j + 3] * inv);
+              w.z = pack2<T>(o[j + 4] * inv, o[j + 5] * inv);
+              w.w = pack2<T>(o[j + 6] * inv, o[j + 7] * inv);
+              *reinterpret_cast<uint4*>(out + c0 + j) = w;
+            }
           }
         }
       }
     }
   } else if (warp == kProducerWarp) {
-    // ================= TMA copies of chunk c into stage c % 2 =================
+    // ================= TMA copies of chunk c =================
     if (lane == 0) {
       const int32_t* bt = p.block_tables + (long long)s * p.max_blocks_per_seq;
       int phys[Sh::kBlocks];
@@ -481,12 +511,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       load_table(0);
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
-        const int sb = c & 1;
-        if (c >= 2 && !wait(&sfull[sb], ((c - 2) >> 1) & 1)) {  // S(c-2) is done with the stage's K
+        const int kb = c % kKStages;
+        if (c >= kKStages && !wait(&kfree[kb], ((c - kKStages) / kKStages) & 1)) {  // both tiles' S read it
           ok = false;
           break;
         }
-        unsigned char* sk = smem + Sh::kOffK + sb * Sh::kKBytes;
+        unsigned char* sk = smem + Sh::kOffK + kb * Sh::kKBytes;
         const int vb = c % kVStages;
         unsigned char* sv_ = smem + Sh::kOffV + vb * Sh::kVBytes;
         int nv = 0;
@@ -505,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           tl[b] = (long long)ph * p.num_kv_heads + kvh;
         }
-        mbar_arrive_expect_tx(&fullk[sb], Sh::kKBytes);
+        mbar_arrive_expect_tx(&fullk[kb], Sh::kKBytes);
         // K: per 8-dim chunk dc, the rows (16 keys each) of the chunk's 64 keys
 #pragma unroll
         for (int dc = 0; dc < D / 8; ++dc) {
@@ -515,10 +545,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int b = (16 * q) / BS, h = (16 * q) % BS / 16;
             rw[q] = static_cast<int>((tl[b] * (D / 8) + dc) * (BS / 16) + h);
           }
-          tma_gather4_g2s(sk + dc * (kKeys * 16), &tmap_k, rw, &fullk[sb]);
+          tma_gather4_g2s(sk + dc * (kKeys * 16), &tmap_k, rw, &fullk[kb]);
         }
         issued_k = c + 1;
-        if (c >= kVStages && !wait(&vfree[vb], ((c - kVStages) / kVStages) & 1)) {  // P V(c-3) read the buffer
+        if (c >= kVStages && !wait(&vfree[vb], ((c - kVStages) / kVStages) & 1)) {  // both tiles' P V read it
           ok = false;
           break;
         }
@@ -535,56 +565,77 @@ __global__ void __launch_bounds__(kThreads, 2)
         issued_v = c + 1;
         load_table(c + 1);  // lands while this chunk is in flight
       }
+      (void)ok;
     }
   } else {
-    // ================= MMA issue: S(c), then O += P V(c - 1) =================
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc<T>(kRows, kKeys), kIdO = idesc<T>(kRows, D);
-      // the timeout-path test: the first wait runs out on `never` (no MMA issued yet);
-      // the producer then drains its copies with the normal limit
-      bool ok = !p.test_wait_ns || wait_or_abort(never, 0, s_abort, p.err, p.test_wait_ns);
-      int last_s = -1, last_pv = -1;  // last groups committed
-      for (int c = 0; c <= nchunks && ok; ++c) {
-        if (c < nchunks) {
-          const int sb = c & 1;
-          ok = wait(&fullk[sb], (c >> 1) & 1);
-          if (ok && c >= 2) ok = wait(&pvdone[sb], ((c - 2) >> 1) & 1);  // P(c-2) read from S[sb]
-          if (!ok) break;
+    // ================= MMA issue: S of both tiles for chunk c, then their P V(c - 1) =================
+    // The whole warp runs the loop and the waits (so the loop state and the descriptors
+    // stay warp-uniform); one elected lane issues the MMAs and the commits.
+    constexpr uint32_t kIdS = idesc<T>(kRows, kKeys), kIdO = idesc<T>(kRows, D);
+    const int ntiles = two ? 2 : 1;
+    const bool leader = elect_one();
+    // descriptors of the first Q tile, K buffer and V buffer; a step moves the address
+    // field (bits 0..13, 16-byte units), which stays below 2^14 for any shared address
+    const uint64_t dq0 = sdesc(smem_addr(smem), 128, (D / 8) * 128);
+    const uint64_t dk0 = sdesc(smem_addr(smem + Sh::kOffK), kKeys * 16, 128);
+    const uint64_t dv0 = sdesc(smem_addr(smem + Sh::kOffV), D * 16, 128);
+    auto wait_all = [&](uint64_t* bar, int parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
+    uint64_t* last_bar = nullptr;  // the last barrier a commit was issued to, and its phase
+    int last_par = 0;
+    auto commit_to = [&](uint64_t* bar, int parity) {
+      if (leader) commit(bar);
+      __syncwarp();
+      last_bar = bar;
+      last_par = parity;
+    };
+    // the timeout-path test: the first wait runs out on `never` (no MMA issued yet);
+    // the producer then drains its copies with the normal limit
+    bool ok = __all_sync(0xffffffffu, !p.test_wait_ns || wait_or_abort(never, 0, s_abort, p.err, p.test_wait_ns));
+    for (int c = 0; c <= nchunks && ok; ++c) {
+      if (c < nchunks) {
+        const int sb = c & 1, kb = c % kKStages;
+        ok = wait_all(&fullk[kb], (c / kKStages) & 1);
+        for (int Xm = 0; Xm < ntiles && ok; ++Xm) {
+          if (c >= 2 && !(ok = wait_all(pvdone(Xm, sb), ((c - 2) >> 1) & 1))) break;  // P(c-2) read from S[sb]
           fence_after();
-          const unsigned char* st = smem + Sh::kOffK + sb * Sh::kKBytes;
+          if (leader) {
+            const uint64_t da = dq0 + Xm * (Sh::kQTile >> 4), db = dk0 + kb * (Sh::kKBytes >> 4);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t da = sdesc(smem_addr(sQ) + ks * 256, 128, (D / 8) * 128);
-            const uint64_t db = sdesc(smem_addr(st) + ks * 2 * (kKeys * 16), kKeys * 16, 128);
-            mma(tmem + sb * kKeys, da, db, kIdS, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+              mma(tmem + 256 * Xm + sb * kKeys, da + ks * 16, db + ks * (2 * kKeys), kIdS, ks > 0);
           }
-          commit(&sfull[sb]);
-          last_s = c;
+          commit_to(sfull(Xm, sb), (c >> 1) & 1);
         }
-        if (c >= 1) {
-          const int c1 = c - 1, sb = c1 & 1;
-          const int vb = c1 % kVStages;
-          if (!(ok = wait(&pfull[sb], (c1 >> 1) & 1) && wait(&fullv[vb], (c1 / kVStages) & 1))) break;
+        if (!ok) break;
+        commit_to(&kfree[kb], (c / kKStages) & 1);
+      }
+      if (c >= 1) {
+        const int c1 = c - 1, sb = c1 & 1;
+        const int vb = c1 % kVStages;
+        if (!(ok = wait_all(&fullv[vb], (c1 / kVStages) & 1))) break;
+        for (int Xm = 0; Xm < ntiles && ok; ++Xm) {
+          if (!(ok = wait_all(pfull(Xm, sb), (c1 >> 1) & 1))) break;
           fence_after();
-          const uint32_t sV = smem_addr(smem + Sh::kOffV + vb * Sh::kVBytes);
+          if (leader) {
+            const uint64_t db = dv0 + vb * (Sh::kVBytes >> 4);
+            const uint32_t tb = tmem + 256 * Xm;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
+            for (int part = 0; part < 2; ++part) {
 #pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint64_t db = sdesc(sV + kk * 2 * (D * 16), D * 16, 128);
-              mma_ts(t_o, tmem + sb * kKeys + part * 32 + kk * 8, db, kIdO, c1 > 0 || part > 0 || kk > 0);
+              for (int kk = 0; kk < kKeys / 16; ++kk)
+                mma_ts(tb + 2 * kKeys, tb + sb * kKeys + part * 32 + kk * 8, db + kk * (2 * D), kIdO,
+                       c1 > 0 || part > 0 || kk > 0);
             }
           }
-          commit(&pvdone[sb]);
-          commit(&vfree[vb]);
-          last_pv = c1;
+          commit_to(pvdone(Xm, sb), (c1 >> 1) & 1);
         }
-      }
-      if (!ok) {  // MMAs committed but maybe not finished: wait (bounded) for the last of each kind
-        if (last_s >= 0) mbar_wait_bounded(&sfull[last_s & 1], (last_s >> 1) & 1, kWaitNs / 8);
-        if (last_pv >= 0) mbar_wait_bounded(&pvdone[last_pv & 1], (last_pv >> 1) & 1, kWaitNs / 8);
+        if (!ok) break;
+        commit_to(&vfree[vb], (c1 / kVStages) & 1);
       }
     }
+    // MMAs committed but maybe not finished: a commit tracks every earlier MMA of the
+    // issuing thread, so the last commit's barrier covers them all
+    if (!ok && last_bar != nullptr) mbar_wait_bounded(last_bar, last_par, kWaitNs / 8);
   }
 
   fence_before();
@@ -593,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   // consumer waits for the copies still landing: the producer waits (bounded) for the
   // last chunks it issued, so nothing lands after the CTA exits.
   if (*s_abort && warp == kProducerWarp && lane == 0) {
-    for (int c = issued_k - 2; c < issued_k; ++c)
-      if (c >= 0) mbar_wait_bounded(&fullk[c & 1], (c >> 1) & 1, kWaitNs / 8);
+    for (int c = issued_k - kKStages; c < issued_k; ++c)
+      if (c >= 0) mbar_wait_bounded(&fullk[c % kKStages], (c / kKStages) & 1, kWaitNs / 8);
     for (int c = issued_v - kVStages; c < issued_v; ++c)
       if (c >= 0) mbar_wait_bounded(&fullv[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
   }
