@@ -10,9 +10,9 @@
 // over K, V gathered through the block table, as decode does for one token.
 //
 // The kernel is in prefill_ws.cuh (tcgen05 MMAs with accumulators in tensor
-// memory, warp-specialised); this file holds its host-side launch: the two
-// tensor maps its TMA copies read the pools through, and the dispatch over
-// dtype, head size and block size.
+// memory, warp-specialised); this file holds its host-side launch: the tensor
+// map its TMA copies read the K pool through, and the dispatch over dtype, head
+// size and block size.
 #include <math.h>
 
 #include <type_traits>
@@ -55,25 +55,7 @@ cudaError_t encode_k_map(const PrefillParams& p, CUtensorMap* map) {
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(p.k_cache), dims, strides, box,
                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// The V pool [NB][Hkv][D][bs] seen as NB * Hkv * D rows of bs 16-bit elements; a box is
-// [D rows][8 elements]: one 8-key group of one (block, kv head) tile, landing as [D][8].
-template <int D, int BS>
-cudaError_t encode_v_map(const PrefillParams& p, CUtensorMap* map) {
-  const EncodeTiledFn enc = encoder();
-  if (!enc) return cudaErrorNotSupported;
-  const unsigned long long rows = (unsigned long long)p.num_blocks * p.num_kv_heads * D;
-  if (rows > 0x7fffffffULL) return cudaErrorInvalidValue;  // box rows are addressed with int32 coordinates
-  const cuuint64_t dims[2] = {(cuuint64_t)BS, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)BS * 2};
-  const cuuint32_t box[2] = {8, (cuuint32_t)D};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(p.v_cache), dims, strides, box,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -95,17 +77,15 @@ cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int
     if (e != cudaSuccess) return e;
     if (dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
   }
-  CUtensorMap kmap, vmap;
+  // sequence s has ceil(ceil(n_s G / 128) / 2) pairs per kv head, at most n_s G / 256 + 1 (rounded up)
+  CUtensorMap kmap;
   e = encode_k_map<D, BS>(p, &kmap);
   if (e != cudaSuccess) return e;
-  e = encode_v_map<D, BS>(p, &vmap);
-  if (e != cudaSuccess) return e;
-  // sequence s has ceil(ceil(n_s G / 128) / 2) pairs per kv head, at most n_s G / 256 + 1 (rounded up)
   const long long pairs = (long long)p.num_kv_heads *
                           (((long long)p.num_query_tokens * p.group + 2 * ws::kRows - 1) / (2 * ws::kRows) + p.num_seqs);
   if (pairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   e = launch_pdl(ws::prefill_ws_kernel<T, D, BS>, dim3(static_cast<unsigned>(pairs)), dim3(ws::kThreads), Sh::kSmem,
-                 stream, p, kmap, vmap);
+                 stream, p, kmap);
   if (e == cudaSuccess) *launches = 1;
   return e;
 }

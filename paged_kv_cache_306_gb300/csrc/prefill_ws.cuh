@@ -4,42 +4,40 @@
 // cache (what is computed: see prefill.cu), on sm_103a's tcgen05 MMAs with the
 // accumulators in tensor memory (TMEM).  A query tile is 128 rows -- (token,
 // query head) pairs of one kv head, head fastest -- which are TMEM lanes
-// 0..127; keys are taken 64 at a time (a chunk).  A CTA owns a PAIR of
-// consecutive tiles of one (sequence, kv head): both read the same keys, so each
-// chunk of K and V is copied once and feeds the MMAs of both tiles, and while
-// the tensor cores work for one tile the softmax of the other runs.  The phases
-// run in different warps that hand over through mbarriers:
+// 0..127; keys are taken 128 at a time (a chunk).  A CTA owns a PAIR of
+// consecutive tiles A and B of one (sequence, kv head): both read the same keys,
+// so each chunk of K and V is copied once and feeds the MMAs of both tiles.  The
+// two tiles take turns: while the softmax of one runs, the tensor cores run the
+// other's P V and its next S (ping-pong).  The phases run in different warps that
+// hand over through mbarriers:
 //
-//   * warp 8, one thread: the TMA copies of chunk c, through two tensor maps: K
-//     into K buffer c % 4 once both tiles' S of chunk c - 4 have read it, V into V
-//     buffer c % 4 once both tiles' P V of chunk c - 4 have read it, each on its own
-//     mbarrier, so S waits only for K and the V copies are well ahead.  K: the pool seen
-//     as rows of 16 keys x 8 dims (one 256-byte run of a K tile [D/8][bs][8]); one
-//     tile::gather4 load per 8-dim chunk fetches the rows of the chunk's 64 keys
-//     (from up to four blocks anywhere in the pool) and lands them as [64][8]:
-//     the K operand of S = Q K^T becomes [D/8][64 keys][8], core matrices with one
-//     uniform stride, so S is one MMA of N = 64 per 16 dims (a block-by-block S
-//     of N = bs took four times the MMAs and was the largest cost).  V: the pool
-//     seen as rows of bs keys (one dim of a V tile [D][bs]); each [D rows x 8 keys]
-//     box lands as [D][8], one 8-key group of the [key/8][D][8] layout the P V MMA
-//     reads.  No re-layout pass.
-//   * warp 9, one thread: for each chunk c, S_A(c) and S_B(c) = Q K^T into each
-//     tile's TMEM columns S[c % 2] (once chunk c has landed and that tile's
-//     P V(c - 2), which read P from those columns, is done), then O_A += P V(c - 1)
-//     and O_B += P V(c - 1) with P read from TMEM; each group is committed to
-//     mbarriers.  Tile A's softmax of chunk c thus runs under S_B(c), the P V of
-//     chunk c - 1 and the S of chunk c + 1 of both tiles.
+//   * warps 8, 10 and 11: the copies of chunk c, K into K buffer c % 2 once both
+//     tiles' S of chunk c - 2 have read it, V into V buffer c % 2 once both tiles'
+//     P V of chunk c - 2 have read it, each on its own mbarrier; 16 bytes per lane
+//     and step through the load/store unit (cp.async), consecutive lanes on
+//     consecutive bytes of a block's tile.  K: the 8 dims of one key of a K tile
+//     [D/8][bs][8] land as one row of [D/8][128 keys][8], the K operand of
+//     S = Q K^T as core matrices with one uniform stride, so S is one MMA of
+//     N = 128 per 16 dims.  V: the 8 keys of one dim of a V tile [D][bs] land as one
+//     row of the [key/8][D][8] layout the P V MMA reads.  (TMA was tried: one
+//     tile::gather4 load per 8-dim slice and 64 keys, and [D x 8-key] boxes for V,
+//     whose 16-byte rows made the copy engine the slowest stage of a chunk.)
+//   * warp 9: the MMAs, in the order P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1): a
+//     tile's S(c + 1) overwrites the P(c) its P V(c) reads, so it waits for that
+//     P V to finish.  The whole warp runs the loop and the waits; one elected lane
+//     issues the MMAs and commits them to mbarriers.
 //   * warps 0..3 (tile A) and 4..7 (tile B), one thread per row: the softmax of
-//     S(c).  P = exp2(s - m) goes back into the row's own S
-//     columns as rounded 16-bit high and low parts (two per 32-bit column).  The
-//     running maximum moves only when it grows by more than 2^8; then the row's O
-//     is rescaled in TMEM after P V(c - 1) has finished (rare).  In the last chunk
-//     tile A's threads zero the V of keys past the sequence (or past the blocks
-//     loaded) in shared memory first: P is 0 there, but 0 * NaN would poison O.
-//     A tile whose rows end before the pair's last chunks sees scores of -inf
-//     there (P = 0).
+//     S(c).  P = exp2(s - m) goes back into the row's own S columns as 16-bit
+//     values, two per 32-bit column: the 16 columns of keys 16 k .. 16 k + 15
+//     become 8 columns of P rounded to fp16 or, for bf16, 8 columns of rounded high
+//     parts and 8 of low parts (~16 significant bits; P V is then two MMA groups).  The running maximum moves only when it grows
+//     by more than 2^8; then the row's O is rescaled in TMEM (P V(c - 1) is done by
+//     then: S(c) was issued after it).  In the last chunk tile A's threads zero the
+//     V of keys past the sequence (or past the blocks loaded) in shared memory
+//     first: P is 0 there, but 0 * NaN would poison O.  A tile whose rows end
+//     before the pair's last chunk sees scores of -inf there (P = 0).
 //
-// TMEM: per tile two S/P column groups of 64 and O (D <= 128 columns) in 256, all
+// TMEM: tile X at column 256 X: S/P in 0..127, O (D <= 128 columns) from 128; all
 // 512 columns for the pair; one CTA per SM.
 // Every wait is bounded (1 s of %globaltimer); a thread that gives up records
 // PA_DEVERR_TIMEOUT and raises a CTA-wide abort flag that makes every other wait
@@ -67,11 +65,12 @@ using tc::sdesc;
 using tc::st32;
 
 constexpr int kRows = 128;  // query rows per tile (= TMEM lanes)
-constexpr int kKeys = 64;   // keys per chunk
+constexpr int kKeys = 128;  // keys per chunk
 constexpr int kSoftmaxThreads = 128;  // per tile
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
-constexpr int kKStages = 4, kVStages = 4;
+constexpr int kKWarp = 8, kMmaWarp = 9;     // warps 10 and 11 copy V
+constexpr int kVThreads = 2 * 32;
+constexpr int kThreads = 12 * 32;
+constexpr int kKStages = 2, kVStages = 2;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -86,14 +85,19 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b), "r"(id), "r"((uint32_t)accumulate));
 }
 
-// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait
-__device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r[64];
+// 128 consecutive fp32 columns of this thread's TMEM lane: four loads, one wait (in one
+// statement, so no use of the registers can be scheduled before the wait)
+__device__ __forceinline__ void ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
@@ -102,12 +106,37 @@ __device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
         "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
         "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
         "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr), "r"(taddr + 32)
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
       : "memory");
 #pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane; no wait (wait_st before
+// the columns are handed over)
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 2^x by the hardware's approximate exponential (|relative error| below 2^-22; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
@@ -116,13 +145,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2-D tensor-map copy global -> shared (box at element coordinates x, y)
-__device__ __forceinline__ void tma_2d_g2s(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_addr(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
+// 16 bytes global -> shared through the load/store unit, cached in L2 only
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+// one arrival on `bar` once every earlier cp.async of this thread has landed (the
+// barrier's count includes it)
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // tile::gather4 tensor-map copy: four rows (element row indices rows[0..3]) of a 2-D
@@ -159,7 +189,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // pairs of the whole launch start first and the short ones fill the tail.  Every
 // thread of the CTA takes part (thread t owns sequences t * kPer ..).  Tile j of
 // sequence s covers rows 128 j .. of its n * G rows and reads chunks
-// 0 .. (ctx + (row_hi - 1) / G) / 64, non-decreasing in j; pair k holds tiles 2k and
+// 0 .. (ctx + (row_hi - 1) / G) / 128, non-decreasing in j; pair k holds tiles 2k and
 // 2k + 1 (if there is one) and reads what its last tile reads.  So the tiles of s
 // reading >= x chunks are a suffix j >= j0 in closed form, the pairs reading >= x
 // are those from j0 / 2 on, and the rank-th pair is found by a binary search on x.
@@ -190,7 +220,7 @@ __device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) 
   if (bad && blockIdx.x == 0) set_error(p.err, kErrSeqLen);
   // pairs of owned sequence i that read >= x chunks
   auto cnt = [&](int i, int x) -> int {
-    const long long need = (long long)G * (64LL * (x - 1) - ctx[i]) + 1;  // rows a tile must reach
+    const long long need = (long long)G * ((long long)kKeys * (x - 1) - ctx[i]) + 1;  // rows a tile must reach
     if (nt[i] == 0 || need > rows[i]) return 0;
     const int j0 = need <= 1 ? 0 : static_cast<int>((need + kRows - 1) / kRows - 1);  // first tile reading >= x
     return (nt[i] + 1) / 2 - j0 / 2;
@@ -214,7 +244,7 @@ __device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) 
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     local += (nt[i] + 1) / 2;
-    if (nt[i]) longest = max(longest, (ctx[i] + (rows[i] - 1) / G) / 64 + 1);
+    if (nt[i]) longest = max(longest, (ctx[i] + (rows[i] - 1) / G) / kKeys + 1);
   }
   if ((long long)Hkv * reduce(local, false) <= rank) return false;
   int lo = 1, hi = reduce(longest, true);  // C(lo) > rank
@@ -269,42 +299,46 @@ struct Shape {
   static constexpr int kTile = D * BS * 2;                 // one block's K (or V) tile
   static constexpr int kBlocks = kKeys / BS;               // blocks per chunk
   static constexpr int kQTile = kRows * D * 2;             // one tile's Q, core-matrix layout
-  static constexpr int kKBytes = kKeys * D * 2;  // a chunk's K as [D/8][64][8]
+  static constexpr int kKBytes = kKeys * D * 2;  // a chunk's K as [D/8][128][8]
   static constexpr int kVBytes = kKeys * D * 2;  // a chunk's V as [key/8][D][8]
   static constexpr int kOffK = 2 * kQTile;                  // K ring
   static constexpr int kOffV = kOffK + kKStages * kKBytes;  // V ring
   static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-  // fullk[K], fullv[V], kfree[K], vfree[V], per tile sfull[2], pfull[2], pvdone[2], never
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 6 + 1;
+  // fullk[K], fullv[V], kfree[K], vfree[V], per tile sfull, pfull, pvdone, never
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 3 + 1;
   static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][16] ints: block reductions
   // more than half an SM's shared memory, so one CTA per SM: it takes all of TMEM
   static constexpr int kSmem = kOffRed + 2 * 16 * 4 > 116 * 1024 ? kOffRed + 2 * 16 * 4 : 116 * 1024;
-  static constexpr int kTmemCols = 512;  // tile X at 256 X: S/P[0] 0..63, S/P[1] 64..127, O 128..128+D
+  static constexpr int kTmemCols = 512;  // tile X at 256 X: S/P 0..127, O 128..128+D
 };
 
 template <typename T, int D, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_ws_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v) {
+    prefill_ws_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k) {
   using Sh = Shape<T, D, BS>;
   static_assert(Sh::kSmem > 114 * 1024, "two CTAs on one SM would contend for TMEM");
+  static_assert(kKeys % BS == 0, "a chunk is whole blocks");
+  // P in one 16-bit part for fp16 (11 significant bits, the operands' own precision); for
+  // bf16 a high and a low part (~16 bits), since one bf16 part (8 bits) would add
+  // errors as large as the output's own rounding
+  constexpr int kParts = std::is_same<T, __half>::value ? 1 : 2;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);
   uint64_t* fullk = bars;                   // [kKStages] K buffer landed (TMA bytes)
-  uint64_t* fullv = fullk + kKStages;       // [kVStages] V buffer landed (TMA bytes)
+  uint64_t* fullv = fullk + kKStages;       // [kVStages] V buffer landed (the V lanes' copies)
   uint64_t* kfree = fullv + kVStages;       // [kKStages] both tiles' S read the K buffer (commit)
   uint64_t* vfree = kfree + kKStages;       // [kVStages] both tiles' P V read the V buffer (commit)
-  uint64_t* tbars = vfree + kVStages;       // per tile X at 6 X: sfull[2], pfull[2], pvdone[2]
-  uint64_t* never = tbars + 12;             // nothing completes it: the timeout-path test waits on it
+  uint64_t* tbars = vfree + kVStages;       // per tile X at 3 X: sfull, pfull, pvdone
+  uint64_t* never = tbars + 6;              // nothing completes it: the timeout-path test waits on it
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
   int* s_pair = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, pair (or -1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_pair + 3);  // a thread gave up
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // S in TMEM, the K buffer read (commit); P in TMEM, O rescaled, V tail zeroed (128 arrivals);
-  // P V done: P's columns and O free (commit)
-  auto sfull = [&](int X, int i) { return tbars + 6 * X + i; };
-  auto pfull = [&](int X, int i) { return tbars + 6 * X + 2 + i; };
-  auto pvdone = [&](int X, int i) { return tbars + 6 * X + 4 + i; };
+  // S(c) in TMEM (commit); P(c) in TMEM, O rescaled, V tail zeroed (128 arrivals);
+  // P V(c) done: P's columns free, O final after the last chunk (commit)
+  auto sfull = [&](int X) { return tbars + 3 * X; };
+  auto pfull = [&](int X) { return tbars + 3 * X + 1; };
+  auto pvdone = [&](int X) { return tbars + 3 * X + 2; };
 
   griddep_launch_dependents();
   griddep_wait();
@@ -318,16 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&fullk[i], 1);
       mbar_init(&kfree[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      for (int X = 0; X < 2; ++X) {
-        mbar_init(sfull(X, i), 1);
-        mbar_init(pfull(X, i), kSoftmaxThreads);
-        mbar_init(pvdone(X, i), 1);
-      }
-    }
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&fullv[i], 1);
+      mbar_init(&fullv[i], kVThreads);  // one cp.async arrival per V lane
       mbar_init(&vfree[i], 1);
+    }
+    for (int X = 0; X < 2; ++X) {
+      mbar_init(sfull(X), 1);
+      mbar_init(pfull(X), kSoftmaxThreads);
+      mbar_init(pvdone(X), 1);
     }
     mbar_init(never, 1);
     fence_barrier_init();
@@ -369,32 +401,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *s_tmem;
+  int issued_k = 0;  // chunks whose K copies warp 8 issued
   auto wait = [&](uint64_t* bar, int parity) { return wait_or_abort(bar, parity, s_abort, p.err); };
-  int issued_k = 0, issued_v = 0;  // chunks whose K (V) copies the producer issued
 
   if (warp < 8) {
     // ================= softmax: tile X, row r, all keys of each chunk =================
     if (X == 0 || two) {
-      const uint32_t tbase = tmem + 256 * X;
-      const uint32_t t_o = tbase + 2 * kKeys;
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t t_s = tmem + 256 * X + lane_base;
+      const uint32_t t_o = t_s + kKeys;
       const int pos = valid ? ctx + row / G : ctx + (pair_hi - 1) / G;  // a padding row behaves as a real one
       const int kz = min(L, nblk * BS);  // first key whose V must read as zero
-      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
       const float sl2 = p.scale_log2;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
-        const int sb = c & 1;
         // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them
         // is taken by the whole warp, so each wait's outcome is agreed across the warp
-        if (!__all_sync(0xffffffffu, wait(sfull(X, sb), (c >> 1) & 1))) {
+        if (!__all_sync(0xffffffffu, wait(sfull(X), c & 1))) {
           ok = false;
           break;
         }
         fence_after();
-        const uint32_t t_s = tbase + lane_base + sb * kKeys;
         float sv[kKeys];
-        ld64(t_s, sv);
+        ld128(t_s, sv);
         const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
         if (lim < kKeys - 1) {           // the diagonal chunk (or past it): hide the later keys
 #pragma unroll
@@ -418,41 +448,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
           l *= corr;
         }
-        // O holds P V up to chunk c - 1 once that group is done: rescale the row if the maximum moved
-        // (the whole warp takes the branch when one of its rows needs it; the others scale by 1)
+        // P over the row's S columns, 16 keys at a time: the 16 columns of keys 16 k ..
+        // 16 k + 15 become 8 columns of high parts (then, for bf16, 8 of low parts)
+        {
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k = 0; k < kKeys / 16; ++k) {
+            uint32_t blk[8 * kParts];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
+              const float x0 = ex2(fmaf(sv[16 * k + 2 * j], sl2, -m)), x1 = ex2(fmaf(sv[16 * k + 2 * j + 1], sl2, -m));
+              ps[j & 3] += x0 + x1;
+              blk[j] = pack2<T>(x0, x1);
+              if constexpr (kParts == 2) {
+                const float2 back = unpack2<T>(blk[j]);
+                blk[8 + j] = pack2<T>(x0 - back.x, x1 - back.y);
+              }
+            }
+            if constexpr (kParts == 2) st16(t_s + 16 * k, blk);
+            else st8(t_s + 16 * k, blk);
+          }
+          wait_st();
+          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        }
+        // O holds P V up to chunk c - 1, finished (S(c) was issued after it): rescale the
+        // row if the maximum moved (the whole warp takes the branch when one of its rows
+        // needs it; the others scale by 1)
         const bool rescale = c > 0 && move && corr != 1.f;
         if (__any_sync(0xffffffffu, rescale)) {
-          if (!__all_sync(0xffffffffu, wait(pvdone(X, (c - 1) & 1), ((c - 1) >> 1) & 1))) {
-            ok = false;
-            break;
-          }
-          fence_after();
           const float f = rescale ? corr : 1.f;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             float o[32];
-            ld32(t_o + lane_base + c0, o);
+            ld32(t_o + c0, o);
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] *= f;
-            st32(t_o + lane_base + c0, o);
+            st32(t_o + c0, o);
           }
-        }
-        // P into the row's S columns: high parts in 0..31, low parts in 32..63
-        {
-          float hi[32], lo[32];
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
-            const float x0 = ex2(fmaf(sv[2 * j], sl2, -m)), x1 = ex2(fmaf(sv[2 * j + 1], sl2, -m));
-            ps[j & 3] += x0 + x1;
-            const uint32_t h = pack2<T>(x0, x1);
-            const float2 back = unpack2<T>(h);
-            hi[j] = __uint_as_float(h);
-            lo[j] = __uint_as_float(pack2<T>(x0 - back.x, x1 - back.y));
-          }
-          st32(t_s, hi);
-          st32(t_s + 32, lo);
-          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         }
         // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as
         // zero; tile A's threads clear it before either tile's P V of the chunk is issued
@@ -462,17 +494,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           unsigned char* vbase = smem + Sh::kOffV + (c % kVStages) * Sh::kVBytes;
-          const int k0 = kz - c * kKeys, cnt = (kKeys - k0) * D;
-          for (int i = tid; i < cnt; i += kSoftmaxThreads) {
+          const int k0 = kz - c * kKeys;      // first key to clear (0 <= k0 < kKeys)
+          const int g0 = (k0 + 7) / 8;        // first whole 8-key group
+          for (int i = tid; i < (g0 * 8 - k0) * D; i += kSoftmaxThreads) {  // the group holding k0
             const int kk = k0 + i / D, d = i % D;
             *reinterpret_cast<T*>(vbase + (kk / 8) * (D * 16) + d * 16 + (kk % 8) * 2) = DType<T>::from_f32(0.f);
           }
+          for (int i = tid; i < (kKeys / 8 - g0) * D; i += kSoftmaxThreads)  // whole groups: 8 keys of one dim
+            *reinterpret_cast<uint4*>(vbase + (g0 + i / D) * (D * 16) + (i % D) * 16) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         fence_before();
-        mbar_arrive(pfull(X, sb));
+        mbar_arrive(pfull(X));
       }
-      if (__all_sync(0xffffffffu, ok && wait(pvdone(X, (nchunks - 1) & 1), ((nchunks - 1) >> 1) & 1))) {
+      if (__all_sync(0xffffffffu, ok && wait(pvdone(X), (nchunks - 1) & 1))) {
         fence_after();
         const float inv = 1.f / l;
         T* out = static_cast<T*>(p.out) +
@@ -481,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
-          ld32(t_o + lane_base + c0, o);
+          ld32(t_o + c0, o);
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
@@ -496,79 +531,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kProducerWarp) {
-    // ================= TMA copies of chunk c =================
-    if (lane == 0) {
-      const int32_t* bt = p.block_tables + (long long)s * p.max_blocks_per_seq;
-      int phys[Sh::kBlocks];
-      auto load_table = [&](int c) {
-#pragma unroll
-        for (int b = 0; b < Sh::kBlocks; ++b) {
-          const int gb = c * Sh::kBlocks + b;
-          phys[b] = gb < nblk ? __ldg(bt + gb) : -1;
-        }
-      };
-      load_table(0);
-      bool ok = true;
-      for (int c = 0; c < nchunks; ++c) {
+  } else if (warp != kMmaWarp) {
+    // ================= copies of chunk c: K (warp 8, TMA), V (warps 10 and 11, cp.async) =================
+    const int32_t* bt = p.block_tables + (long long)s * p.max_blocks_per_seq;
+    auto phys_of = [&](int c) {  // lane b: the physical block of the chunk's block b (-1 past the keys)
+      const int gb = c * Sh::kBlocks + lane;
+      return lane < Sh::kBlocks && gb < nblk ? __ldg(bt + gb) : -1;
+    };
+    static_assert(Sh::kBlocks <= 32, "one block per lane");
+    int ph = phys_of(0);  // the next chunk's table entries land while a chunk is in flight
+    bool ok = true;
+    if (warp == kKWarp) {
+      // lane i issues the i-th gather4 load of a chunk: 8-dim slice dc, keys 64 h .. 64 h + 63
+      constexpr int kGathers = (D / 8) * (kKeys / 64);
+      static_assert(kGathers <= 32, "one gather per lane");
+      const int dc = lane / (kKeys / 64), h = lane % (kKeys / 64);
+      for (int c = 0; c < nchunks && ok; ++c) {
         const int kb = c % kKStages;
-        if (c >= kKStages && !wait(&kfree[kb], ((c - kKStages) / kKStages) & 1)) {  // both tiles' S read it
-          ok = false;
+        const bool live = lane < Sh::kBlocks && c * Sh::kBlocks + lane < nblk;
+        const bool bad = ph < 0 || ph >= p.num_blocks;
+        if (live && bad) set_error(p.err, kErrBlockId);
+        const int ph0 = __shfl_sync(0xffffffffu, bad ? 0 : ph, 0);  // block 0 of a chunk always holds keys
+        // a block past the keys: any rows do (S there is masked)
+        const long long tl = (long long)(live ? (bad ? 0 : ph) : ph0) * p.num_kv_heads + kvh;
+        int rw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // the rows (16 keys each) of this lane's 64 keys
+          const int key = 64 * h + 16 * q;
+          const long long tb = __shfl_sync(0xffffffffu, tl, key / BS);
+          rw[q] = static_cast<int>((tb * (D / 8) + dc) * (BS / 16) + (key % BS) / 16);
+        }
+        if (c >= kKStages &&  // both tiles' S read the buffer
+            !(ok = __all_sync(0xffffffffu, wait(&kfree[kb], ((c - kKStages) / kKStages) & 1))))
           break;
-        }
-        unsigned char* sk = smem + Sh::kOffK + kb * Sh::kKBytes;
-        const int vb = c % kVStages;
-        unsigned char* sv_ = smem + Sh::kOffV + vb * Sh::kVBytes;
-        int nv = 0;
-        long long tl[Sh::kBlocks];
-#pragma unroll
-        for (int b = 0; b < Sh::kBlocks; ++b) {
-          int ph = phys[b];
-          if (c * Sh::kBlocks + b < nblk) {
-            ++nv;
-            if (ph < 0 || ph >= p.num_blocks) {
-              set_error(p.err, kErrBlockId);
-              ph = 0;
-            }
-          } else {
-            ph = phys[0] < 0 || phys[0] >= p.num_blocks ? 0 : phys[0];  // a block past the keys: any rows do
-          }
-          tl[b] = (long long)ph * p.num_kv_heads + kvh;
-        }
-        mbar_arrive_expect_tx(&fullk[kb], Sh::kKBytes);
-        // K: per 8-dim chunk dc, the rows (16 keys each) of the chunk's 64 keys
-#pragma unroll
-        for (int dc = 0; dc < D / 8; ++dc) {
-          int rw[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int b = (16 * q) / BS, h = (16 * q) % BS / 16;
-            rw[q] = static_cast<int>((tl[b] * (D / 8) + dc) * (BS / 16) + h);
-          }
-          tma_gather4_g2s(sk + dc * (kKeys * 16), &tmap_k, rw, &fullk[kb]);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&fullk[kb], Sh::kKBytes);
+        __syncwarp();
+        if (lane < kGathers)  // lands as [64 keys][8 dims] in the slice's rows
+          tma_gather4_g2s(smem + Sh::kOffK + kb * Sh::kKBytes + dc * (kKeys * 16) + h * (64 * 16), &tmap_k, rw,
+                          &fullk[kb]);
         issued_k = c + 1;
-        if (c >= kVStages && !wait(&vfree[vb], ((c - kVStages) / kVStages) & 1)) {  // both tiles' P V read it
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&fullv[vb], nv * Sh::kTile);
-        // V: per block and 8-key group, [D][8]
-#pragma unroll
-        for (int b = 0; b < Sh::kBlocks; ++b) {
-          if (c * Sh::kBlocks + b >= nblk) continue;
-#pragma unroll
-          for (int g = 0; g < BS / 8; ++g)  // V rows tl*D .. tl*D+D-1, keys 8g .. 8g+7 of the block
-            tma_2d_g2s(sv_ + ((b * BS) / 8 + g) * (D * 16), &tmap_v, g * 8, static_cast<int>(tl[b] * D),
-                       &fullv[vb]);
-        }
-        issued_v = c + 1;
-        load_table(c + 1);  // lands while this chunk is in flight
+        ph = phys_of(c + 1);
       }
-      (void)ok;
+    } else {
+      // V: 16 bytes (8 keys of one dim of a V tile [D][bs]) per lane and step, one row of
+      // the [key/8][D][8] layout; consecutive lanes on consecutive bytes of a block's tile
+      constexpr int kPerBlockV = D * (BS / 8);
+      constexpr int kSteps = (Sh::kBlocks * kPerBlockV + kVThreads - 1) / kVThreads;
+      const int gid = (warp - 10) * 32 + lane;
+      const unsigned char* vpool = static_cast<const unsigned char*>(p.v_cache);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int vb = c % kVStages;
+        if (lane < Sh::kBlocks && c * Sh::kBlocks + lane < nblk && (ph < 0 || ph >= p.num_blocks)) ph = 0;
+        const long long tl = (long long)ph * p.num_kv_heads + kvh;  // lanes past the keys: unused
+        const int nlive = min(Sh::kBlocks, nblk - c * Sh::kBlocks);  // blocks of the chunk holding keys
+        if (c >= kVStages &&  // both tiles' P V read the buffer
+            !(ok = __all_sync(0xffffffffu, wait(&vfree[vb], ((c - kVStages) / kVStages) & 1))))
+          break;
+        unsigned char* sv_ = smem + Sh::kOffV + vb * Sh::kVBytes;
+#pragma unroll 4
+        for (int step = 0; step < kSteps; ++step) {  // the same trip count on every lane (the shuffle)
+          const int i = step * kVThreads + gid, b = min(i / kPerBlockV, Sh::kBlocks - 1);
+          const long long tb = __shfl_sync(0xffffffffu, tl, b);
+          const int r = i - b * kPerBlockV, d = r / (BS / 8), grp = r % (BS / 8);
+          if (i < nlive * kPerBlockV)  // V past the keys: zeroed by the softmax threads instead
+            cp_async16(sv_ + ((b * BS) / 8 + grp) * (D * 16) + d * 16, vpool + (tb * kPerBlockV + r) * 16);
+        }
+        cp_async_arrive(&fullv[vb]);
+        ph = phys_of(c + 1);
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of this lane lands after the CTA exits
     }
   } else {
-    // ================= MMA issue: S of both tiles for chunk c, then their P V(c - 1) =================
+    // ================= MMAs (warp 9): P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1) =================
     // The whole warp runs the loop and the waits (so the loop state and the descriptors
     // stay warp-uniform); one elected lane issues the MMAs and the commits.
     constexpr uint32_t kIdS = idesc<T>(kRows, kKeys), kIdO = idesc<T>(kRows, D);
@@ -588,49 +622,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_bar = bar;
       last_par = parity;
     };
+    auto issue_s = [&](int Xm, int c) {  // S_X(c) = Q_X K(c)^T into X's S columns
+      if (leader) {
+        const uint64_t da = dq0 + Xm * (Sh::kQTile >> 4), db = dk0 + (c % kKStages) * (Sh::kKBytes >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma(tmem + 256 * Xm, da + ks * 16, db + ks * (2 * kKeys), kIdS, ks > 0);
+      }
+      commit_to(sfull(Xm), c & 1);
+    };
+    auto issue_pv = [&](int Xm, int c) {  // O_X += P_X(c) V(c): high parts, then low parts
+      if (leader) {
+        const uint64_t db = dv0 + (c % kVStages) * (Sh::kVBytes >> 4);
+        const uint32_t tb = tmem + 256 * Xm;
+#pragma unroll
+        for (int part = 0; part < kParts; ++part) {
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)  // keys 16 kk ..: high parts in 8 columns, low in the next 8
+            mma_ts(tb + kKeys, tb + 16 * kk + 8 * part, db + kk * (2 * D), kIdO, c > 0 || part > 0 || kk > 0);
+        }
+      }
+      commit_to(pvdone(Xm), c & 1);
+    };
     // the timeout-path test: the first wait runs out on `never` (no MMA issued yet);
     // the producer then drains its copies with the normal limit
     bool ok = __all_sync(0xffffffffu, !p.test_wait_ns || wait_or_abort(never, 0, s_abort, p.err, p.test_wait_ns));
-    for (int c = 0; c <= nchunks && ok; ++c) {
-      if (c < nchunks) {
-        const int sb = c & 1, kb = c % kKStages;
-        ok = wait_all(&fullk[kb], (c / kKStages) & 1);
-        for (int Xm = 0; Xm < ntiles && ok; ++Xm) {
-          if (c >= 2 && !(ok = wait_all(pvdone(Xm, sb), ((c - 2) >> 1) & 1))) break;  // P(c-2) read from S[sb]
+    if (ok && (ok = wait_all(&fullk[0], 0))) {
+      fence_after();
+      for (int Xm = 0; Xm < ntiles; ++Xm) issue_s(Xm, 0);
+      commit_to(&kfree[0], 0);
+    }
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int vb = c % kVStages, c1 = c + 1;
+      if (!(ok = wait_all(&fullv[vb], (c / kVStages) & 1))) break;
+      fence_proxy_async_smem();  // V landed through the generic proxy; the MMAs read it through the async one
+      for (int Xm = 0; Xm < ntiles && ok; ++Xm) {
+        if (!(ok = wait_all(pfull(Xm), c & 1))) break;  // the softmax wrote P_X(c)
+        fence_after();
+        issue_pv(Xm, c);
+        if (Xm == ntiles - 1) commit_to(&vfree[vb], (c / kVStages) & 1);
+        if (c1 < nchunks) {
+          if (Xm == 0 && !(ok = wait_all(&fullk[c1 % kKStages], (c1 / kKStages) & 1))) break;
+          if (!(ok = wait_all(pvdone(Xm), c & 1))) break;  // P_X(c) read before S_X(c + 1) overwrites it
           fence_after();
-          if (leader) {
-            const uint64_t da = dq0 + Xm * (Sh::kQTile >> 4), db = dk0 + kb * (Sh::kKBytes >> 4);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              mma(tmem + 256 * Xm + sb * kKeys, da + ks * 16, db + ks * (2 * kKeys), kIdS, ks > 0);
-          }
-          commit_to(sfull(Xm, sb), (c >> 1) & 1);
+          issue_s(Xm, c1);
+          if (Xm == ntiles - 1) commit_to(&kfree[c1 % kKStages], (c1 / kKStages) & 1);
         }
-        if (!ok) break;
-        commit_to(&kfree[kb], (c / kKStages) & 1);
-      }
-      if (c >= 1) {
-        const int c1 = c - 1, sb = c1 & 1;
-        const int vb = c1 % kVStages;
-        if (!(ok = wait_all(&fullv[vb], (c1 / kVStages) & 1))) break;
-        for (int Xm = 0; Xm < ntiles && ok; ++Xm) {
-          if (!(ok = wait_all(pfull(Xm, sb), (c1 >> 1) & 1))) break;
-          fence_after();
-          if (leader) {
-            const uint64_t db = dv0 + vb * (Sh::kVBytes >> 4);
-            const uint32_t tb = tmem + 256 * Xm;
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-              for (int kk = 0; kk < kKeys / 16; ++kk)
-                mma_ts(tb + 2 * kKeys, tb + sb * kKeys + part * 32 + kk * 8, db + kk * (2 * D), kIdO,
-                       c1 > 0 || part > 0 || kk > 0);
-            }
-          }
-          commit_to(pvdone(Xm, sb), (c1 >> 1) & 1);
-        }
-        if (!ok) break;
-        commit_to(&vfree[vb], (c1 / kVStages) & 1);
       }
     }
     // MMAs committed but maybe not finished: a commit tracks every earlier MMA of the
@@ -640,14 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   fence_before();
   __syncthreads();
-  // After an abort (whoever raised it, before or after the producer's loop ended) no
-  // consumer waits for the copies still landing: the producer waits (bounded) for the
-  // last chunks it issued, so nothing lands after the CTA exits.
-  if (*s_abort && warp == kProducerWarp && lane == 0) {
+  // After an abort no consumer waits for the K copies still landing: warp 8 waits
+  // (bounded) for the last chunks it issued, so nothing lands after the CTA exits.
+  if (*s_abort && warp == kKWarp && lane == 0) {
     for (int c = issued_k - kKStages; c < issued_k; ++c)
       if (c >= 0) mbar_wait_bounded(&fullk[c % kKStages], (c / kKStages) & 1, kWaitNs / 8);
-    for (int c = issued_v - kVStages; c < issued_v; ++c)
-      if (c >= 0) mbar_wait_bounded(&fullv[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
   }
   if (warp == 0) {
     fence_after();

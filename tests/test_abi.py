@@ -214,9 +214,9 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert pf(q=8200) == B.PA_ERR_ALIGNMENT
     assert pf(T=0) == B.PA_OK and pf(S=0) == B.PA_OK
     # null pointers: the row-count check comes first, and without it the null check would refuse
-    big = lib.pa_prefill(None, None, None, None, None, 4, None, None, 2, 8, 64, 8, 2, 128, 16, 1 << 24, 0.1,
+    big = lib.pa_prefill(None, None, None, None, None, 4, None, None, 2, 8, 64, 8, 2, 128, 16, 1 << 27, 0.1,
                          B.PA_F16, None)
-    assert big == B.PA_ERR_UNSUPPORTED     # 2^24 blocks x 2 kv heads x 128 dims: past the tensor maps' rows
+    assert big == B.PA_ERR_UNSUPPORTED     # 2^27 blocks x 2 kv heads x 16 slices: past the tensor map's rows
 
 
 def test_fused_step_rejects_bad_arguments_on_the_host(lib):
