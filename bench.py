@@ -442,14 +442,27 @@ def device_error_check(where):
         raise RuntimeError(f"device error {code} ({pa.DEVICE_ERRORS.get(code)}) {where}")
 
 
-def roofline_of(wl, fused, call_ms, peak, peak_kind):
+def traffic_key(wl, shared):
+    """The name a call's DRAM record is kept under: a batch of forked sequences taken
+    through the plain call (--plain) is a different call from the shared one."""
+    return wl.name + ("-plain" if "group_size" in wl.meta and not shared else "")
+
+
+def roofline_of(wl, fused, call_ms, peak, peak_kind, shared=False):
     nbytes = call_bytes(wl, fused)
     med = float(np.median(call_ms))
     achieved = nbytes / (med * 1e-3) / 1e9
+    if shared:
+        kernel = ("shared-prefix call: copy_blocks_kernel (when the step has copies) + decode_kernel (new tokens, "
+                  "decode) + decode_merge_kernel")
+    elif fused:
+        kernel = ("fused step call: copy_blocks_kernel (when the step has copies) + decode_kernel (new tokens, "
+                  "decode) + decode_merge_kernel")
+    else:
+        kernel = "decode call: decode_kernel + decode_merge_kernel"
     return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": load_traffic(wl, fused),
-            "kernel": ("fused step call: decode_kernel (copies, new tokens, decode) + decode_merge_kernel"
-                       if fused else "decode call: decode_kernel + decode_merge_kernel"),
+            "frac": round(achieved / peak, 4), "traffic": load_traffic(wl, fused, shared),
+            "kernel": kernel,
             "bytes_per_launch": int(nbytes), "launch_us": spread(call_ms), "calls": len(call_ms),
             "peak_source": f"{peak_kind} hbm_gbs (of {peak_kind})"}
 
@@ -486,7 +499,7 @@ def run_ours(args, wl, cfg, world_size, rank, local_rank):
         "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(wl),
         "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": config_dict(args, wl, cfg),
-        "roofline": roofline_of(wl, r.fused, call_ms, peak, peak_kind),
+        "roofline": roofline_of(wl, r.fused, call_ms, peak, peak_kind, r.shared),
         "tokens_per_s_per_layer": round(world_size * wl.num_seqs / (ms_step * 1e-3), 1),
         "detail": {"decode_bytes": int(decode_bytes(wl)), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
                    "write_bytes": int(write_bytes(wl)), "step_bytes": int(sbytes),
@@ -535,7 +548,7 @@ def run_subrecord(args, key, dev, stream, peak, peak_kind):
     device_error_check(f"in sub-record {key}")
     ms_step = ms / steps
     sbytes = step_bytes(wl)
-    roof = roofline_of(wl, r.fused, call_ms, peak, peak_kind)
+    roof = roofline_of(wl, r.fused, call_ms, peak, peak_kind, r.shared)
     rec = {"workload": wl.name, "dtype": dtype_label(wl), "partition_size": "auto" if r.ps == -1 else int(r.ps),
            "call_us": roof["launch_us"], "calls": len(call_ms), "bytes_per_call": roof["bytes_per_launch"],
            "call_gbs": roof["achieved"], "frac": roof["frac"], "traffic": roof["traffic"],
@@ -620,7 +633,7 @@ def run_e2e(args, r):
             "d2h_bytes_per_step": int(d2h), "copies_per_step": 2}
 
 
-def load_traffic(wl, fused):
+def load_traffic(wl, fused, shared=False):
     """DRAM bytes per timed call from the committed ncu summary, if it was taken on the
     current kernel source and on the same kind of call; otherwise null."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
@@ -632,10 +645,27 @@ def load_traffic(wl, fused):
         src = open(os.path.join(ROOT, "paged_kv_cache_306_gb300", "csrc", "decode_kernels.cuh"), "rb").read()
         if d.get("kernel_sha256") != hashlib.sha256(src).hexdigest():
             return None
-        ent = d.get("workloads", {}).get(wl.name)
+        ent = d.get("workloads", {}).get(traffic_key(wl, shared))
         if not ent or ent.get("fused", True) != fused:
             return None
         return ent.get("dram_bytes_per_launch")
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def load_prefill_traffic(wl):
+    """DRAM bytes per prefill launch from the committed ncu summary, if it was taken on
+    the current prefill kernel source; otherwise null."""
+    p = os.path.join(ROOT, "profiles", "prefill_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        import hashlib
+        d = json.load(open(p))
+        src = open(os.path.join(ROOT, "paged_kv_cache_306_gb300", "csrc", "prefill_ws.cuh"), "rb").read()
+        if d.get("kernel_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return d.get("workloads", {}).get(wl.name, {}).get("dram_bytes_per_launch")
     except (OSError, ValueError, KeyError):
         return None
 
@@ -831,7 +861,7 @@ def run_prefill(args, world_size, rank, local_rank):
             "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)", "config": cfg,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_ws_kernel",
+                         "frac": round(achieved / peak, 4), "traffic": load_prefill_traffic(wl), "kernel": "prefill_ws_kernel",
                          "flops_per_launch": int(flops), "launch_us": spread(pre_ms), "calls": kn,
                          "peak_source": f"{kind} bf16_tflops (of {kind}; fp16 runs at the bf16 rate)"},
             "detail": {"flops_per_step": int(flops), "parallelism": f"replicas x{world_size}"},

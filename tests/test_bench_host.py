@@ -160,3 +160,17 @@ def test_cpu_baseline_reports_all_threads_and_one():
     cb = bench.cpu_baseline(wl, seconds=0.5)
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["single_core_value"] > 0
     assert cb["cores"] >= 1 and cb["all_vs_single"] > 0
+
+
+def test_plain_and_shared_calls_keep_separate_traffic_records():
+    wl = W.config(5, poison=False, block_size=16)
+    assert bench.traffic_key(wl, True) == wl.name
+    assert bench.traffic_key(wl, False) == wl.name + "-plain"
+    q = W.config(2, poison=False)
+    assert bench.traffic_key(q, False) == q.name
+
+
+def test_prefill_traffic_record_needs_the_current_kernel_source(tmp_path, monkeypatch):
+    wl = W.make_prefill("f", "f16", [0, 5], [3, 17], 8, 2, 64, 16, seed=1, poison=False)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_prefill_traffic(wl) is None
