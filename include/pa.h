@@ -44,6 +44,13 @@
  *     device: the offending access is skipped or clamped into the pool, the
  *     affected outputs are unspecified, and the first such error is recorded
  *     for pa_get_device_error().
+ *   - Kernels are chained by programmatic dependent launch: a decode kernel may
+ *     start while the previous kernel in the stream (another call of this
+ *     library) finishes, and reads seq_lens and the prefix groups before it waits
+ *     for that kernel; everything else it reads or writes it touches after.  A
+ *     caller kernel that writes seq_lens or the prefix groups must not release
+ *     its dependents early (griddepcontrol.launch_dependents) before those writes;
+ *     an ordinary kernel never does.
  *   - Thread safety: calls may be made from several host threads; the
  *     device-error word and the launch counter are shared per process.
  *   - The library looks up the device addresses of its own device-side objects

@@ -986,10 +986,12 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   }
   __syncwarp();
   griddep_launch_dependents();
-  griddep_wait();  // every input may come from the previous kernel in the stream
 
   // Per-sequence tables: length (0 when outside [1, max_seq_len]) and prefix sums
   // of the blocks of work per unit.  Each thread scans PER consecutive sequences.
+  // They come from seq_lens and the prefix groups, which no kernel of this library
+  // writes, so they are built while the previous kernel in the stream may still be
+  // running (see griddep_wait below).
   const int S = p.num_seqs, U = p.units, PB = p.part_blocks;
   const bool shared = kMma && p.shared;
   {
@@ -1056,6 +1058,10 @@ __global__ void __launch_bounds__(DecodeShape<TC, D, BS, kMode>::kWarps * 32, 1)
   auto seg_id = [&](int s, int u, int part) { return shared ? 2 * (s * U + u) + part : s * U + u; };
   // blocks of sequence s's shared segment (s a leader), else 0
   auto shared_len = [&](int s) { return info_member(s_info[s]) == 0 ? info_off(s_lead[s]) : 0; };
+
+  // Everything from here on may touch memory the previous kernel in the stream
+  // writes (the pools, the output, the workspace a previous call's merge still reads).
+  griddep_wait();
 
   // Sequences outside the contract: record the error, zero their rows, mark their
   // segments as needing no merge.  One CTA does it, and hands the cluster layout
