@@ -323,12 +323,15 @@ struct MmaMath {
   __device__ __forceinline__ void block_t(unsigned char* stage, int tile_bytes, int rem, float scale_log2,
                                           uint32_t live) {
     const uint32_t kb = smem_addr(stage), vb = kb + tile_bytes;
-    // S^T = K Q^T for the block's BS tokens.
-    float sc[MT][NH][4];
+    // S^T = K Q^T for the block's BS tokens, the even and the odd 16-dim k-steps in two
+    // accumulators (two dependent chains of KS/2 MMAs, added at the end)
+    float sc[MT][NH][4], so[MT][NH][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int n = 0; n < NH; ++n) sc[mt][n][0] = sc[mt][n][1] = sc[mt][n][2] = sc[mt][n][3] = 0.f;
+      for (int n = 0; n < NH; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[mt][n][c] = so[mt][n][c] = 0.f;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       if constexpr (kFp8) {
@@ -341,7 +344,7 @@ struct MmaMath {
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
             mma_16816<OT>(sc[mt][n], a0, qb[2 * kp][n][0], qb[2 * kp][n][1]);
-            mma_16816<OT>(sc[mt][n], a1, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
+            mma_16816<OT>(so[mt][n], a1, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
           }
         }
       } else {
@@ -355,9 +358,14 @@ struct MmaMath {
             ldsm_x4(kb + k_lane_off + (2 * ks * BS + 16 * mt) * 16, a[0], a[1], a[2], a[3]);
           }
 #pragma unroll
-          for (int n = 0; n < NT; ++n) mma_16816<OT>(sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
+          for (int n = 0; n < NT; ++n)
+            mma_16816<OT>((ks & 1) ? so[mt][n] : sc[mt][n], a, qb[ks][n][0], qb[ks][n][1]);
         }
       }
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[mt][n][c] += so[mt][n][c];
     }
     // Online softmax update per head (column), log2 domain; tokens past the sequence
     // (and every token, for a column whose member does not take this block) get -inf.
