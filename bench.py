@@ -558,7 +558,8 @@ def run_subrecord(args, key, dev, stream, peak, peak_kind):
            "tokens_per_s_per_layer": round(wl.num_seqs / (ms_step * 1e-3), 1),
            "decode_bytes": int(decode_bytes(wl)), "decode_unique_bytes": int(decode_bytes(wl, unique=True)),
            "step": "fused" if r.fused else "separate", "pool_copies_rotated": r.copies,
-           "call": "pa_decode_shared" if r.shared else ("pa_decode_step" if r.fused else "pa_decode")}
+           "call": "pa_decode_shared" if r.shared else (("pa_decode_step_scaled" if wl.dtype == "fp8" else "pa_decode_step")
+                                                   if r.fused else "pa_decode")}
     if cfg == 1:
         rec["note"] = "latency-bound batch (4 short sequences): no roofline claim"
     del r
