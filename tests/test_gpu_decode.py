@@ -129,6 +129,43 @@ def test_non_default_stream():
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("bs", [16, 32])
+def test_reshape_and_cache_of_many_tokens_is_bit_exact(dtype, bs):
+    """A write of many tokens (the tiled kernel: 32 tokens of one kv head per CTA):
+    chunks of consecutive slots at every alignment within a block, crossing blocks,
+    scattered slots, padding, and a ragged last tile; bit-identical with the oracle."""
+    import paged_kv_cache_306_gb300 as pa
+    rng = np.random.default_rng(zlib.crc32(repr(("tiled write", dtype, bs)).encode()))
+    Hkv, D, NB = 8, 128, 400
+    perm = rng.permutation(NB)
+    slots, b = [], 0
+    for n in (1, 5, 31, 32, 33, 100, 257, 500):  # runs of consecutive positions through private blocks
+        start = int(rng.integers(0, bs))
+        nblk = -(-(start + n) // bs)
+        table = perm[b:b + nblk]
+        b += nblk
+        pos = start + np.arange(n)
+        slots += list(table[pos // bs] * bs + pos % bs)
+    free = np.setdiff1d(np.arange(NB * bs), np.array(slots))
+    slots += list(rng.choice(free, size=200, replace=False))  # scattered
+    slots = np.array(slots, dtype=np.int64)
+    slots[rng.choice(len(slots), size=20, replace=False)] = -1  # padding
+    T = len(slots)
+    assert (T + 31) // 32 * Hkv >= 256 and T % 32 != 0
+    wl = W.make_private("w", dtype, [bs] * 2, Hkv, Hkv, D, bs, seed=23, num_blocks=NB, poison=False)
+    key = W.randn(rng, (T, Hkv, D), dtype)
+    value = W.randn(rng, (T, Hkv, D), dtype)
+    t = upload(wl)
+    pa.pa_reshape_and_cache(W.to_torch(key, dtype, "cuda"), W.to_torch(value, dtype, "cuda"), t["k_cache"],
+                            t["v_cache"], torch.from_numpy(slots).cuda())
+    assert pa.pa_get_device_error() == 0
+    k, v = wl.clone_pools()
+    oracle.reshape_and_cache(key, value, k, v, slots, dtype)
+    assert np.array_equal(W.from_torch(t["k_cache"], dtype).view(np.uint8), k.view(np.uint8))
+    assert np.array_equal(W.from_torch(t["v_cache"], dtype).view(np.uint8), v.view(np.uint8))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("bs", [16, 32])
 def test_reshape_and_cache_is_bit_exact(dtype, bs):
     import paged_kv_cache_306_gb300 as pa
     rng = np.random.default_rng(21)
