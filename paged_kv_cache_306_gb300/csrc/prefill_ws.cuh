@@ -11,17 +11,19 @@
 // other's P V and its next S (ping-pong).  The phases run in different warps that
 // hand over through mbarriers:
 //
-//   * warps 8, 10 and 11: the copies of chunk c, K into K buffer c % 2 once both
-//     tiles' S of chunk c - 2 have read it, V into V buffer c % 2 once both tiles'
-//     P V of chunk c - 2 have read it, each on its own mbarrier; 16 bytes per lane
-//     and step through the load/store unit (cp.async), consecutive lanes on
-//     consecutive bytes of a block's tile.  K: the 8 dims of one key of a K tile
-//     [D/8][bs][8] land as one row of [D/8][128 keys][8], the K operand of
-//     S = Q K^T as core matrices with one uniform stride, so S is one MMA of
-//     N = 128 per 16 dims.  V: the 8 keys of one dim of a V tile [D][bs] land as one
-//     row of the [key/8][D][8] layout the P V MMA reads.  (TMA was tried: one
-//     tile::gather4 load per 8-dim slice and 64 keys, and [D x 8-key] boxes for V,
-//     whose 16-byte rows made the copy engine the slowest stage of a chunk.)
+//   * warp 8 copies K, warps 10 and 11 copy V, chunk c into buffer c % 2 once both
+//     tiles' S (P V) of chunk c - 2 have read it, each on its own mbarrier.  K
+//     through TMA: the pool seen as rows of 16 keys x 8 dims (one 256-byte run of a
+//     K tile [D/8][bs][8]); lane i issues the i-th tile::gather4 load (one per 8-dim
+//     slice and 64 keys), which fetches four such rows from blocks anywhere in the
+//     pool and lands them as [64][8]: the K operand of S = Q K^T is
+//     [D/8][128 keys][8], core matrices with one uniform stride, so S is one MMA of
+//     N = 128 per 16 dims.  V through the load/store unit (cp.async, 16 bytes per
+//     lane, consecutive lanes on consecutive bytes of a block's tile): the 8 keys of
+//     one dim of a V tile [D][bs] land as one row of the [key/8][D][8] layout the
+//     P V MMA reads.  No re-layout pass.  (TMA carries about as many bytes per cycle
+//     as the load/store unit does here; with both K and V on it -- V as [D x 8-key]
+//     boxes, or as whole swizzled [D][bs] tiles -- it was the slowest stage.)
 //   * warp 9: the MMAs, in the order P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1): a
 //     tile's S(c + 1) overwrites the P(c) its P V(c) reads, so it waits for that
 //     P V to finish.  The whole warp runs the loop and the waits; one elected lane
@@ -30,8 +32,8 @@
 //     S(c).  P = exp2(s - m) goes back into the row's own S columns as 16-bit
 //     values, two per 32-bit column: the 16 columns of keys 16 k .. 16 k + 15
 //     become 8 columns of P rounded to fp16 or, for bf16, 8 columns of rounded high
-//     parts and 8 of low parts (~16 significant bits; P V is then two MMA groups).  The running maximum moves only when it grows
-//     by more than 2^8; then the row's O is rescaled in TMEM (P V(c - 1) is done by
+//     parts and 8 of low parts (~16 significant bits; P V is then two MMA groups).
+//     The running maximum moves only when it grows by more than 2^8; then the row's O is rescaled in TMEM (P V(c - 1) is done by
 //     then: S(c) was issued after it).  In the last chunk tile A's threads zero the
 //     V of keys past the sequence (or past the blocks loaded) in shared memory
 //     first: P is 0 there, but 0 * NaN would poison O.  A tile whose rows end
