@@ -369,10 +369,9 @@ PA_API void pa_set_test_wait_limit(uint64_t nanoseconds);
  *
  * No workspace.  A sequence whose length lies outside [1, max_seq_len] or whose
  * chunk is longer than itself is recorded as PA_DEVERR_SEQ_LEN and its rows of
- * out are unspecified.  num_blocks * num_kv_heads * head_size / 8 *
- * block_size / 16 (the rows of 16 keys x 8 dims the K pool holds) must stay below
- * 2^31 (PA_ERR_UNSUPPORTED otherwise).  The kernel reads the K pool through a TMA
- * tensor map encoded on the host at every call (cuTensorMapEncodeTiled, found
+ * out are unspecified.  num_blocks * num_kv_heads * head_size must stay below
+ * 2^31 (PA_ERR_UNSUPPORTED otherwise).  The kernel reads the pools through TMA
+ * tensor maps encoded on the host at every call (cuTensorMapEncodeTiled, found
  * through the CUDA runtime; PA_ERR_CUDA if the driver does not provide it).
  * Asynchronous on `stream`.
  */

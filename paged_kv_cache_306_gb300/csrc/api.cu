@@ -574,12 +574,11 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
     return fail(PA_ERR_INVALID_ARG, "max_seq_len %d exceeds max_blocks_per_seq %d * block_size %d", max_seq_len,
                 max_blocks_per_seq, block_size);
   if (num_blocks < 1) return fail(PA_ERR_INVALID_ARG, "num_blocks %lld < 1", (long long)num_blocks);
-  // the kernel's tensor map addresses the K pool in rows of 16 keys x 8 dims of one
-  // (block, kv head) with int32 coordinates
-  if ((long long)num_blocks * num_kv_heads * (head_size / 8) * (block_size / 16) > 0x7fffffffLL)
-    return fail(PA_ERR_UNSUPPORTED, "prefill addresses at most 2^31 - 1 K rows (num_blocks * num_kv_heads * "
-                                    "head_size / 8 * block_size / 16 = %lld)",
-                (long long)num_blocks * num_kv_heads * (head_size / 8) * (block_size / 16));
+  // the kernel's tensor maps address the pools in rows with int32 coordinates: the V
+  // pool in rows of one dim of one (block, kv head), the most rows of the two maps
+  if ((long long)num_blocks * num_kv_heads * head_size > 0x7fffffffLL)
+    return fail(PA_ERR_UNSUPPORTED, "prefill addresses at most 2^31 - 1 V rows (num_blocks * num_kv_heads * "
+                                    "head_size = %lld)", (long long)num_blocks * num_kv_heads * head_size);
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
   if (num_seqs == 0 || num_query_tokens == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc)

@@ -10,8 +10,8 @@
 // over K, V gathered through the block table, as decode does for one token.
 //
 // The kernel is in prefill_ws.cuh (tcgen05 MMAs with accumulators in tensor
-// memory, warp-specialised); this file holds its host-side launch: the tensor
-// map its TMA copies read the K pool through, and the dispatch over dtype, head
+// memory, warp-specialised); this file holds its host-side launch: the two tensor
+// maps its TMA copies read the pools through, and the dispatch over dtype, head
 // size and block size.
 #include <math.h>
 
@@ -59,7 +59,28 @@ cudaError_t encode_k_map(const PrefillParams& p, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// The warp-specialised tcgen05 kernel (prefill_ws.cuh): one CTA per pair of 128-row query tiles, one per SM.
+// The V pool [NB][Hkv][D][bs] seen as NB * Hkv * D rows of bs 16-bit elements; a box
+// is one (block, kv head) tile, [D rows][bs keys], landing with the 32-byte (bs 16) or
+// 64-byte (bs 32) swizzle: the K-major layout the P V MMA reads with the same swizzle.
+template <int D, int BS>
+cudaError_t encode_v_map(const PrefillParams& p, CUtensorMap* map) {
+  const EncodeTiledFn enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const unsigned long long rows = (unsigned long long)p.num_blocks * p.num_kv_heads * D;
+  if (rows > 0x7fffffffULL) return cudaErrorInvalidValue;  // box rows are addressed with int32 coordinates
+  const cuuint64_t dims[2] = {(cuuint64_t)BS, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)BS * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BS, (cuuint32_t)D};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(p.v_cache), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         BS == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The warp-specialised tcgen05 kernel (prefill_ws.cuh): clusters of two CTAs, each CTA a pair of 128-row query
+// tiles, one CTA per SM.
 template <typename T, int D, int BS>
 cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int* launches) {
   using Sh = ws::Shape<T, D, BS>;
@@ -77,15 +98,32 @@ cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int
     if (e != cudaSuccess) return e;
     if (dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
   }
-  // sequence s has ceil(ceil(n_s G / 128) / 2) pairs per kv head, at most n_s G / 256 + 1 (rounded up)
-  CUtensorMap kmap;
+  CUtensorMap kmap, vmap;
   e = encode_k_map<D, BS>(p, &kmap);
   if (e != cudaSuccess) return e;
-  const long long pairs = (long long)p.num_kv_heads *
-                          (((long long)p.num_query_tokens * p.group + 2 * ws::kRows - 1) / (2 * ws::kRows) + p.num_seqs);
-  if (pairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  e = launch_pdl(ws::prefill_ws_kernel<T, D, BS>, dim3(static_cast<unsigned>(pairs)), dim3(ws::kThreads), Sh::kSmem,
-                 stream, p, kmap);
+  e = encode_v_map<D, BS>(p, &vmap);
+  if (e != cudaSuccess) return e;
+  // sequence s has ceil(ceil(n_s G / 128) / 4) units of four tiles per kv head, at most
+  // n_s G / 512 + 1 (rounded up); a unit is one cluster of two CTAs
+  const long long units = (long long)p.num_kv_heads * (((long long)p.num_query_tokens * p.group + ws::kUnitTiles * ws::kRows - 1) /
+                                                           (ws::kUnitTiles * ws::kRows) +
+                                                       p.num_seqs);
+  if (units * ws::kCluster > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * ws::kCluster));
+  cfg.blockDim = dim3(ws::kThreads);
+  cfg.dynamicSmemBytes = Sh::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = ws::kCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, ws::prefill_ws_kernel<T, D, BS>, p, kmap, vmap);
   if (e == cudaSuccess) *launches = 1;
   return e;
 }

@@ -11,19 +11,19 @@
 // other's P V and its next S (ping-pong).  The phases run in different warps that
 // hand over through mbarriers:
 //
-//   * warp 8 copies K, warps 10 and 11 copy V, chunk c into buffer c % 2 once both
-//     tiles' S (P V) of chunk c - 2 have read it, each on its own mbarrier.  K
-//     through TMA: the pool seen as rows of 16 keys x 8 dims (one 256-byte run of a
-//     K tile [D/8][bs][8]); lane i issues the i-th tile::gather4 load (one per 8-dim
-//     slice and 64 keys), which fetches four such rows from blocks anywhere in the
-//     pool and lands them as [64][8]: the K operand of S = Q K^T is
-//     [D/8][128 keys][8], core matrices with one uniform stride, so S is one MMA of
-//     N = 128 per 16 dims.  V through the load/store unit (cp.async, 16 bytes per
-//     lane, consecutive lanes on consecutive bytes of a block's tile): the 8 keys of
-//     one dim of a V tile [D][bs] land as one row of the [key/8][D][8] layout the
-//     P V MMA reads.  No re-layout pass.  (TMA carries about as many bytes per cycle
-//     as the load/store unit does here; with both K and V on it -- V as [D x 8-key]
-//     boxes, or as whole swizzled [D][bs] tiles -- it was the slowest stage.)
+//   * warp 8: the TMA copies of chunk c, K into K buffer c % 2 once both tiles' S
+//     of chunk c - 2 have read it, V into V buffer c % 2 once both tiles' P V of
+//     chunk c - 2 have read it, each on its own mbarrier.  K: the pool seen as rows
+//     of 16 keys x 8 dims (one 256-byte run of a K tile [D/8][bs][8]); lane i issues
+//     the i-th tile::gather4 load (one per 8-dim slice and 64 keys), which fetches
+//     four such rows from blocks anywhere in the pool and lands them as [64][8]: the
+//     K operand of S = Q K^T is [D/8][128 keys][8], core matrices with one uniform
+//     stride, so S is one MMA of N = 128 per 16 dims.  V: lane b issues one box per
+//     block, the (block, kv head) tile [D][bs] with the 32-byte (bs 16) or 64-byte
+//     (bs 32) swizzle, which is the K-major operand layout of P V with the same
+//     swizzle: no re-layout pass.  (V was first copied as [D x 8-key] boxes of
+//     16-byte rows, 16 per chunk, whose copies held the K gathers back, and then
+//     with cp.async from two warps of its own.)
 //   * warp 9: the MMAs, in the order P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1): a
 //     tile's S(c + 1) overwrites the P(c) its P V(c) reads, so it waits for that
 //     P V to finish.  The whole warp runs the loop and the waits; one elected lane
@@ -69,9 +69,13 @@ using tc::st32;
 constexpr int kRows = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kKeys = 128;  // keys per chunk
 constexpr int kSoftmaxThreads = 128;  // per tile
-constexpr int kKWarp = 8, kMmaWarp = 9;     // warps 10 and 11 copy V
-constexpr int kVThreads = 2 * 32;
-constexpr int kThreads = 12 * 32;
+constexpr int kCopyWarp = 8, kMmaWarp = 9;
+// A cluster of two CTAs on two SMs takes a unit of four consecutive tiles of one
+// (sequence, kv head), a pair per CTA; each CTA copies half of every chunk of K and V
+// with TMA multicast into both, so each SM fetches half of the bytes its MMAs read.
+constexpr int kCluster = 2, kUnitTiles = 2 * kCluster;
+constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
+constexpr int kThreads = 10 * 32;
 constexpr int kKStages = 2, kVStages = 2;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -147,24 +151,57 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 16 bytes global -> shared through the load/store unit, cached in L2 only
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-// one arrival on `bar` once every earlier cp.async of this thread has landed (the
-// barrier's count includes it)
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+// Shared-memory matrix descriptor (tcgen05), K-major with the 32-byte (mode 6) or
+// 64-byte (mode 4) swizzle: rows of 32 or 64 bytes, sbo = the distance between groups
+// of 8 rows; the leading offset is unused when one MMA's K extent fits a row.
+__device__ __forceinline__ uint64_t sdesc_swizzled(uint32_t addr, uint32_t sbo, uint32_t mode) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)mode << 61);
 }
 
 // tile::gather4 tensor-map copy: four rows (element row indices rows[0..3]) of a 2-D
-// map whose box is one row high, landing one after another in shared memory
-__device__ __forceinline__ void tma_gather4_g2s(void* dst, const CUtensorMap* map, const int (&rows)[4], uint64_t* bar) {
+// map whose box is one row high, landing one after another at the same offset of
+// shared memory in every CTA of the cluster in `mask`, each signalling its own
+// mbarrier at `bar`'s offset
+__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* map, const int (&rows)[4], uint64_t* bar,
+                                               uint16_t mask) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3]), "r"(smem_addr(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3]), "r"(smem_addr(bar)), "h"(mask)
       : "memory");
+}
+
+// 2-D tensor-map copy (box at element coordinates x, y) into every CTA of `mask`, as above
+__device__ __forceinline__ void tma_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                          uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+
+// One arrival on the mbarrier at `bar`'s offset in every CTA of `mask` once every
+// earlier MMA of this thread has completed
+__device__ __forceinline__ void commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs of the cluster: the mbarrier inits (and any shared-memory
+// writes before it) are visible cluster-wide afterwards
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // A bounded wait that also gives up at once when another thread of the CTA has
@@ -186,17 +223,19 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// The pair of rank `rank` (0-based) in the order of decreasing length -- the chunks
-// of keys it reads -- ties by sequence, kv head and pair index; so the longest
-// pairs of the whole launch start first and the short ones fill the tail.  Every
-// thread of the CTA takes part (thread t owns sequences t * kPer ..).  Tile j of
-// sequence s covers rows 128 j .. of its n * G rows and reads chunks
-// 0 .. (ctx + (row_hi - 1) / G) / 128, non-decreasing in j; pair k holds tiles 2k and
-// 2k + 1 (if there is one) and reads what its last tile reads.  So the tiles of s
-// reading >= x chunks are a suffix j >= j0 in closed form, the pairs reading >= x
-// are those from j0 / 2 on, and the rank-th pair is found by a binary search on x.
-// Writes (sequence, kv head, pair) to out; returns false when rank is past the pairs.
-__device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) {
+// The unit of rank `rank` (0-based) in the order of decreasing length -- the chunks
+// of keys it reads -- ties by sequence, kv head and unit index; so the longest
+// units of the whole launch start first and the short ones fill the tail.  A unit
+// is kUnitTiles consecutive tiles of one (sequence, kv head), the work of one
+// cluster.  Every thread of the CTA takes part (thread t owns sequences
+// t * kPer ..).  Tile j of sequence s covers rows 128 j .. of its n * G rows and
+// reads chunks 0 .. (ctx + (row_hi - 1) / G) / 128, non-decreasing in j; unit k holds
+// tiles kUnitTiles k .. (those that exist) and reads what its last tile reads.  So
+// the tiles of s reading >= x chunks are a suffix j >= j0 in closed form, the units
+// reading >= x are those from j0 / kUnitTiles on, and the rank-th unit is found by
+// a binary search on x.  Writes (sequence, kv head, unit) to out; returns false
+// when rank is past the units.
+__device__ bool pick_unit(const PrefillParams& p, int rank, int* red, int* out) {
   constexpr int kPer = (kMaxSeqsPerLaunch + kThreads - 1) / kThreads;
   constexpr int kWarpsTotal = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -220,12 +259,12 @@ __device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) 
     }
   }
   if (bad && blockIdx.x == 0) set_error(p.err, kErrSeqLen);
-  // pairs of owned sequence i that read >= x chunks
+  // units of owned sequence i that read >= x chunks
   auto cnt = [&](int i, int x) -> int {
     const long long need = (long long)G * ((long long)kKeys * (x - 1) - ctx[i]) + 1;  // rows a tile must reach
     if (nt[i] == 0 || need > rows[i]) return 0;
     const int j0 = need <= 1 ? 0 : static_cast<int>((need + kRows - 1) / kRows - 1);  // first tile reading >= x
-    return (nt[i] + 1) / 2 - j0 / 2;
+    return (nt[i] + kUnitTiles - 1) / kUnitTiles - j0 / kUnitTiles;
   };
   int buf = 0;
   auto reduce = [&](int v, bool take_max) -> int {
@@ -245,7 +284,7 @@ __device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) 
   int local = 0, longest = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
-    local += (nt[i] + 1) / 2;
+    local += (nt[i] + kUnitTiles - 1) / kUnitTiles;
     if (nt[i]) longest = max(longest, (ctx[i] + (rows[i] - 1) / G) / kKeys + 1);
   }
   if ((long long)Hkv * reduce(local, false) <= rank) return false;
@@ -258,7 +297,7 @@ __device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) 
     if ((long long)Hkv * reduce(local, false) > rank) lo = mid;
     else hi = mid - 1;
   }
-  // rank among the pairs of exactly lo chunks, ordered by (sequence, kv head, pair)
+  // rank among the units of exactly lo chunks, ordered by (sequence, kv head, unit)
   local = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) local += cnt(i, lo + 1);
@@ -288,7 +327,7 @@ __device__ bool pick_pair(const PrefillParams& p, int rank, int* red, int* out) 
       const int q = static_cast<int>(r - before);
       out[0] = tid * kPer + i;
       out[1] = q / e[i];
-      out[2] = (nt[i] + 1) / 2 - cnt(i, lo) + q % e[i];
+      out[2] = (nt[i] + kUnitTiles - 1) / kUnitTiles - cnt(i, lo) + q % e[i];
     }
     before += span;
   }
@@ -302,7 +341,7 @@ struct Shape {
   static constexpr int kBlocks = kKeys / BS;               // blocks per chunk
   static constexpr int kQTile = kRows * D * 2;             // one tile's Q, core-matrix layout
   static constexpr int kKBytes = kKeys * D * 2;  // a chunk's K as [D/8][128][8]
-  static constexpr int kVBytes = kKeys * D * 2;  // a chunk's V as [key/8][D][8]
+  static constexpr int kVBytes = kKeys * D * 2;  // a chunk's V: kBlocks swizzled tiles [D][bs]
   static constexpr int kOffK = 2 * kQTile;                  // K ring
   static constexpr int kOffV = kOffK + kKStages * kKBytes;  // V ring
   static constexpr int kOffBar = kOffV + kVStages * kVBytes;
@@ -316,7 +355,8 @@ struct Shape {
 
 template <typename T, int D, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_ws_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k) {
+    prefill_ws_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
   using Sh = Shape<T, D, BS>;
   static_assert(Sh::kSmem > 114 * 1024, "two CTAs on one SM would contend for TMEM");
   static_assert(kKeys % BS == 0, "a chunk is whole blocks");
@@ -327,13 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kOffBar);
   uint64_t* fullk = bars;                   // [kKStages] K buffer landed (TMA bytes)
-  uint64_t* fullv = fullk + kKStages;       // [kVStages] V buffer landed (the V lanes' copies)
-  uint64_t* kfree = fullv + kVStages;       // [kKStages] both tiles' S read the K buffer (commit)
-  uint64_t* vfree = kfree + kKStages;       // [kVStages] both tiles' P V read the V buffer (commit)
+  uint64_t* fullv = fullk + kKStages;       // [kVStages] V buffer landed (TMA bytes)
+  uint64_t* kfree = fullv + kVStages;       // [kKStages] both CTAs' S read the K buffer (a commit from each)
+  uint64_t* vfree = kfree + kKStages;       // [kVStages] both CTAs' P V read the V buffer (a commit from each)
   uint64_t* tbars = vfree + kVStages;       // per tile X at 3 X: sfull, pfull, pvdone
   uint64_t* never = tbars + 6;              // nothing completes it: the timeout-path test waits on it
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
-  int* s_pair = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, pair (or -1)
+  int* s_pair = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, unit (or -1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_pair + 3);  // a thread gave up
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // S(c) in TMEM (commit); P(c) in TMEM, O rescaled, V tail zeroed (128 arrivals);
@@ -345,18 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   griddep_wait();
 
-  // ---- which pair: the longest first over the whole launch
-  const bool has_pair = pick_pair(p, static_cast<int>(blockIdx.x), reinterpret_cast<int*>(smem + Sh::kOffRed), s_pair);
+  // ---- which unit: the longest first over the whole launch (both CTAs of a cluster pick the same)
+  const uint32_t crank = cluster_rank();
+  const bool has_unit =
+      pick_unit(p, static_cast<int>(blockIdx.x / kCluster), reinterpret_cast<int*>(smem + Sh::kOffRed), s_pair);
   if (tid == 0) {
-    if (!has_pair) s_pair[0] = -1;
+    if (!has_unit) s_pair[0] = -1;
     *s_abort = 0;
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&fullk[i], 1);
-      mbar_init(&kfree[i], 1);
+      mbar_init(&kfree[i], kCluster);
     }
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&fullv[i], kVThreads);  // one cp.async arrival per V lane
-      mbar_init(&vfree[i], 1);
+      mbar_init(&fullv[i], 1);
+      mbar_init(&vfree[i], kCluster);
     }
     for (int X = 0; X < 2; ++X) {
       mbar_init(sfull(X), 1);
@@ -367,15 +409,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  cluster_sync_all();  // both CTAs' mbarriers are initialised before either copies into the other
   const int s = s_pair[0];
-  if (s < 0) return;  // no pair for this CTA (before any TMEM is taken)
-  const int kvh = s_pair[1], pair = s_pair[2];
+  if (s < 0) return;  // no unit for this cluster: both CTAs leave here, before any TMEM is taken
+  const int kvh = s_pair[1], unit = s_pair[2];
   const int G = p.group;
   const int L = p.seq_lens[s], tok0 = p.query_start_loc[s], n = p.query_start_loc[s + 1] - tok0;
-  const int rows = n * G, pair_lo = 2 * pair * kRows, pair_hi = min(rows, pair_lo + 2 * kRows);
-  const bool two = pair_lo + kRows < rows;    // the pair has a tile B
+  // this CTA's pair: tiles kUnitTiles unit + 2 crank and the next (either may be past the rows)
+  const int rows = n * G, pair_lo = (kUnitTiles * unit + 2 * static_cast<int>(crank)) * kRows,
+            pair_hi = min(rows, pair_lo + 2 * kRows);
+  const int ntiles = pair_lo >= rows ? 0 : (pair_lo + kRows < rows ? 2 : 1);  // tiles with rows: A, then B
+  // keys: what the unit's last row sees, the same in both CTAs (they share every chunk)
+  const int unit_hi = min(rows, (kUnitTiles * unit + kUnitTiles) * kRows);
   const int ctx = L - n;
-  const int p_max = ctx + (pair_hi - 1) / G;  // last position any row of the pair has
+  const int p_max = ctx + (unit_hi - 1) / G;  // last position any row of the unit has
   const int nblk = p_max / BS + 1;            // blocks holding keys 0..p_max
   const int nchunks = (p_max + kKeys) / kKeys;
 
@@ -403,12 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *s_tmem;
-  int issued_k = 0;  // chunks whose K copies warp 8 issued
+  int issued_k = 0, issued_v = 0;  // chunks whose K (V) copies warp 8 issued
   auto wait = [&](uint64_t* bar, int parity) { return wait_or_abort(bar, parity, s_abort, p.err); };
 
   if (warp < 8) {
     // ================= softmax: tile X, row r, all keys of each chunk =================
-    if (X == 0 || two) {
+    if (ntiles > X) {
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
       const uint32_t t_s = tmem + 256 * X + lane_base;
       const uint32_t t_o = t_s + kKeys;
@@ -495,15 +542,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // block b's tile [D][bs]: dim d's keys 8 g .. 8 g + 7 are the 16 bytes at d * 2 bs + 16 g
+          // within the row, moved by the swizzle (16-byte unit bits xor'ed with bits 7 and up)
           unsigned char* vbase = smem + Sh::kOffV + (c % kVStages) * Sh::kVBytes;
-          const int k0 = kz - c * kKeys;      // first key to clear (0 <= k0 < kKeys)
-          const int g0 = (k0 + 7) / 8;        // first whole 8-key group
-          for (int i = tid; i < (g0 * 8 - k0) * D; i += kSoftmaxThreads) {  // the group holding k0
-            const int kk = k0 + i / D, d = i % D;
-            *reinterpret_cast<T*>(vbase + (kk / 8) * (D * 16) + d * 16 + (kk % 8) * 2) = DType<T>::from_f32(0.f);
+          constexpr int kRow = 2 * BS, kUnits = kRow / 16;
+          const int k0 = kz - c * kKeys;  // first key to clear (0 <= k0 < kKeys)
+          const int g0 = k0 / 8;          // the 8-key group holding it
+          for (int i = tid; i < (kKeys / 8 - g0) * D; i += kSoftmaxThreads) {
+            const int g = g0 + i / D, d = i % D;  // keys 8 g .. 8 g + 7 of dim d
+            const int a = d * kRow + ((8 * g) % BS) * 2;
+            unsigned char* u = vbase + ((8 * g) / BS) * Sh::kTile + (a ^ (((a >> 7) & (kUnits - 1)) << 4));
+            if (8 * g >= k0) {
+              *reinterpret_cast<uint4*>(u) = make_uint4(0, 0, 0, 0);
+            } else {
+              for (int k = k0 - 8 * g; k < 8; ++k) *reinterpret_cast<T*>(u + 2 * k) = DType<T>::from_f32(0.f);
+            }
           }
-          for (int i = tid; i < (kKeys / 8 - g0) * D; i += kSoftmaxThreads)  // whole groups: 8 keys of one dim
-            *reinterpret_cast<uint4*>(vbase + (g0 + i / D) * (D * 16) + (i % D) * 16) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         fence_before();
@@ -533,93 +587,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp != kMmaWarp) {
-    // ================= copies of chunk c: K (warp 8, TMA), V (warps 10 and 11, cp.async) =================
+  } else if (warp == kCopyWarp) {
+    // ================= copies of chunk c (warp 8): K gathers, then V boxes =================
+    // This CTA issues its half of the chunk's copies, each into both CTAs of the
+    // cluster: lane i the gather4 load crank * kGathers / 2 + i of K (8-dim slice dc,
+    // keys 64 h .. 64 h + 63), lane b the V box of the chunk's block b when b % 2 is
+    // its rank.  Each CTA's full barriers expect the whole chunk.
+    constexpr int kGathers = (D / 8) * (kKeys / 64), kMine = kGathers / kCluster;
+    static_assert(kGathers <= 32 && Sh::kBlocks <= 32 && kGathers % kCluster == 0, "one copy per lane");
     const int32_t* bt = p.block_tables + (long long)s * p.max_blocks_per_seq;
     auto phys_of = [&](int c) {  // lane b: the physical block of the chunk's block b (-1 past the keys)
       const int gb = c * Sh::kBlocks + lane;
       return lane < Sh::kBlocks && gb < nblk ? __ldg(bt + gb) : -1;
     };
-    static_assert(Sh::kBlocks <= 32, "one block per lane");
+    const int gi = static_cast<int>(crank) * kMine + lane;  // this lane's gather (lanes < kMine)
+    const int dc = gi / (kKeys / 64), h = gi % (kKeys / 64);
     int ph = phys_of(0);  // the next chunk's table entries land while a chunk is in flight
     bool ok = true;
-    if (warp == kKWarp) {
-      // lane i issues the i-th gather4 load of a chunk: 8-dim slice dc, keys 64 h .. 64 h + 63
-      constexpr int kGathers = (D / 8) * (kKeys / 64);
-      static_assert(kGathers <= 32, "one gather per lane");
-      const int dc = lane / (kKeys / 64), h = lane % (kKeys / 64);
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int kb = c % kKStages;
-        const bool live = lane < Sh::kBlocks && c * Sh::kBlocks + lane < nblk;
-        const bool bad = ph < 0 || ph >= p.num_blocks;
-        if (live && bad) set_error(p.err, kErrBlockId);
-        const int ph0 = __shfl_sync(0xffffffffu, bad ? 0 : ph, 0);  // block 0 of a chunk always holds keys
-        // a block past the keys: any rows do (S there is masked)
-        const long long tl = (long long)(live ? (bad ? 0 : ph) : ph0) * p.num_kv_heads + kvh;
-        int rw[4];
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int kb = c % kKStages, vb = c % kVStages;
+      const bool live = lane < Sh::kBlocks && c * Sh::kBlocks + lane < nblk;
+      const bool bad = ph < 0 || ph >= p.num_blocks;
+      if (live && bad) set_error(p.err, kErrBlockId);
+      const int ph0 = __shfl_sync(0xffffffffu, bad ? 0 : ph, 0);  // block 0 of a chunk always holds keys
+      // a block past the keys: any rows do (S there is masked; its V is not copied)
+      const long long tl = (long long)(live ? (bad ? 0 : ph) : ph0) * p.num_kv_heads + kvh;
+      const int nlive = __popc(__ballot_sync(0xffffffffu, live));
+      int rw[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // the rows (16 keys each) of this lane's 64 keys
-          const int key = 64 * h + 16 * q;
-          const long long tb = __shfl_sync(0xffffffffu, tl, key / BS);
-          rw[q] = static_cast<int>((tb * (D / 8) + dc) * (BS / 16) + (key % BS) / 16);
-        }
-        if (c >= kKStages &&  // both tiles' S read the buffer
-            !(ok = __all_sync(0xffffffffu, wait(&kfree[kb], ((c - kKStages) / kKStages) & 1))))
-          break;
-        if (lane == 0) mbar_arrive_expect_tx(&fullk[kb], Sh::kKBytes);
-        __syncwarp();
-        if (lane < kGathers)  // lands as [64 keys][8 dims] in the slice's rows
-          tma_gather4_g2s(smem + Sh::kOffK + kb * Sh::kKBytes + dc * (kKeys * 16) + h * (64 * 16), &tmap_k, rw,
-                          &fullk[kb]);
-        issued_k = c + 1;
-        ph = phys_of(c + 1);
+      for (int q = 0; q < 4; ++q) {  // the rows (16 keys each) of this lane's 64 keys
+        const int key = 64 * h + 16 * q;
+        const long long tb = __shfl_sync(0xffffffffu, tl, key / BS);
+        rw[q] = static_cast<int>((tb * (D / 8) + dc) * (BS / 16) + (key % BS) / 16);
       }
-    } else {
-      // V: 16 bytes (8 keys of one dim of a V tile [D][bs]) per lane and step, one row of
-      // the [key/8][D][8] layout; consecutive lanes on consecutive bytes of a block's tile
-      constexpr int kPerBlockV = D * (BS / 8);
-      constexpr int kSteps = (Sh::kBlocks * kPerBlockV + kVThreads - 1) / kVThreads;
-      const int gid = (warp - 10) * 32 + lane;
-      const unsigned char* vpool = static_cast<const unsigned char*>(p.v_cache);
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int vb = c % kVStages;
-        if (lane < Sh::kBlocks && c * Sh::kBlocks + lane < nblk && (ph < 0 || ph >= p.num_blocks)) ph = 0;
-        const long long tl = (long long)ph * p.num_kv_heads + kvh;  // lanes past the keys: unused
-        const int nlive = min(Sh::kBlocks, nblk - c * Sh::kBlocks);  // blocks of the chunk holding keys
-        if (c >= kVStages &&  // both tiles' P V read the buffer
-            !(ok = __all_sync(0xffffffffu, wait(&vfree[vb], ((c - kVStages) / kVStages) & 1))))
-          break;
-        unsigned char* sv_ = smem + Sh::kOffV + vb * Sh::kVBytes;
-#pragma unroll 4
-        for (int step = 0; step < kSteps; ++step) {  // the same trip count on every lane (the shuffle)
-          const int i = step * kVThreads + gid, b = min(i / kPerBlockV, Sh::kBlocks - 1);
-          const long long tb = __shfl_sync(0xffffffffu, tl, b);
-          const int r = i - b * kPerBlockV, d = r / (BS / 8), grp = r % (BS / 8);
-          if (i < nlive * kPerBlockV)  // V past the keys: zeroed by the softmax threads instead
-            cp_async16(sv_ + ((b * BS) / 8 + grp) * (D * 16) + d * 16, vpool + (tb * kPerBlockV + r) * 16);
-        }
-        cp_async_arrive(&fullv[vb]);
-        ph = phys_of(c + 1);
-      }
-      asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of this lane lands after the CTA exits
+      if (c >= kKStages &&  // both CTAs' S read the buffer (in both CTAs)
+          !(ok = __all_sync(0xffffffffu, wait(&kfree[kb], ((c - kKStages) / kKStages) & 1))))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(&fullk[kb], Sh::kKBytes);
+      __syncwarp();
+      if (lane < kMine)  // lands as [64 keys][8 dims] in the slice's rows, in both CTAs
+        tma_gather4_mc(smem + Sh::kOffK + kb * Sh::kKBytes + dc * (kKeys * 16) + h * (64 * 16), &tmap_k, rw,
+                       &fullk[kb], kClusterMask);
+      issued_k = c + 1;
+      if (c >= kVStages &&  // both CTAs' P V read the buffer (in both CTAs)
+          !(ok = __all_sync(0xffffffffu, wait(&vfree[vb], ((c - kVStages) / kVStages) & 1))))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(&fullv[vb], nlive * Sh::kTile);
+      __syncwarp();
+      if (live && lane % kCluster == static_cast<int>(crank))  // the (block, kv head) tile [D][bs], swizzled;
+        tma_2d_mc(smem + Sh::kOffV + vb * Sh::kVBytes + lane * Sh::kTile, &tmap_v, 0,  // V past the keys is zeroed
+                  static_cast<int>(tl * D), &fullv[vb], kClusterMask);                // by the softmax threads
+      issued_v = c + 1;
+      ph = phys_of(c + 1);
     }
   } else {
     // ================= MMAs (warp 9): P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1) =================
     // The whole warp runs the loop and the waits (so the loop state and the descriptors
     // stay warp-uniform); one elected lane issues the MMAs and the commits.
+    // A CTA without rows (the unit's second pair missing) still frees each buffer
+    // for its partner: it commits to the free barriers of both CTAs with no MMA before.
     constexpr uint32_t kIdS = idesc<T>(kRows, kKeys), kIdO = idesc<T>(kRows, D);
-    const int ntiles = two ? 2 : 1;
     const bool leader = elect_one();
     // descriptors of the first Q tile, K buffer and V buffer; a step moves the address
     // field (bits 0..13, 16-byte units), which stays below 2^14 for any shared address
     const uint64_t dq0 = sdesc(smem_addr(smem), 128, (D / 8) * 128);
     const uint64_t dk0 = sdesc(smem_addr(smem + Sh::kOffK), kKeys * 16, 128);
-    const uint64_t dv0 = sdesc(smem_addr(smem + Sh::kOffV), D * 16, 128);
+    // V: one [D][bs] tile per block, rows of 2 bs bytes with the matching swizzle; the keys
+    // 16 kk .. 16 kk + 15 are block 16 kk / bs, at byte 2 (16 kk % bs) of its rows
+    const uint64_t dv0 = sdesc_swizzled(smem_addr(smem + Sh::kOffV), 8 * BS * 2, BS == 16 ? 6u : 4u);
     auto wait_all = [&](uint64_t* bar, int parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
     uint64_t* last_bar = nullptr;  // the last barrier a commit was issued to, and its phase
     int last_par = 0;
-    auto commit_to = [&](uint64_t* bar, int parity) {
-      if (leader) commit(bar);
+    auto commit_to = [&](uint64_t* bar, int parity, bool both = false) {  // both: the free barriers of both CTAs
+      if (leader) {
+        if (both) commit_mc(bar, kClusterMask);
+        else commit(bar);
+      }
       __syncwarp();
       last_bar = bar;
       last_par = parity;
@@ -641,7 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int part = 0; part < kParts; ++part) {
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)  // keys 16 kk ..: high parts in 8 columns, low in the next 8
-            mma_ts(tb + kKeys, tb + 16 * kk + 8 * part, db + kk * (2 * D), kIdO, c > 0 || part > 0 || kk > 0);
+            mma_ts(tb + kKeys, tb + 16 * kk + 8 * part,
+                   db + (((16 * kk) / BS) * Sh::kTile + ((16 * kk) % BS) * 2) / 16, kIdO, c > 0 || part > 0 || kk > 0);
         }
       }
       commit_to(pvdone(Xm), c & 1);
@@ -652,25 +696,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && (ok = wait_all(&fullk[0], 0))) {
       fence_after();
       for (int Xm = 0; Xm < ntiles; ++Xm) issue_s(Xm, 0);
-      commit_to(&kfree[0], 0);
+      commit_to(&kfree[0], 0, true);
     }
     for (int c = 0; c < nchunks && ok; ++c) {
       const int vb = c % kVStages, c1 = c + 1;
       if (!(ok = wait_all(&fullv[vb], (c / kVStages) & 1))) break;
-      fence_proxy_async_smem();  // V landed through the generic proxy; the MMAs read it through the async one
       for (int Xm = 0; Xm < ntiles && ok; ++Xm) {
         if (!(ok = wait_all(pfull(Xm), c & 1))) break;  // the softmax wrote P_X(c)
         fence_after();
         issue_pv(Xm, c);
-        if (Xm == ntiles - 1) commit_to(&vfree[vb], (c / kVStages) & 1);
+        if (Xm == ntiles - 1) commit_to(&vfree[vb], (c / kVStages) & 1, true);
         if (c1 < nchunks) {
           if (Xm == 0 && !(ok = wait_all(&fullk[c1 % kKStages], (c1 / kKStages) & 1))) break;
           if (!(ok = wait_all(pvdone(Xm), c & 1))) break;  // P_X(c) read before S_X(c + 1) overwrites it
           fence_after();
           issue_s(Xm, c1);
-          if (Xm == ntiles - 1) commit_to(&kfree[c1 % kKStages], (c1 / kKStages) & 1);
+          if (Xm == ntiles - 1) commit_to(&kfree[c1 % kKStages], (c1 / kKStages) & 1, true);
         }
       }
+      if (ntiles == 0 && ok) {  // no rows: free the buffers for the partner as they land
+        commit_to(&vfree[vb], (c / kVStages) & 1, true);
+        if (c1 < nchunks) {
+          if (!(ok = wait_all(&fullk[c1 % kKStages], (c1 / kKStages) & 1))) break;
+          commit_to(&kfree[c1 % kKStages], (c1 / kKStages) & 1, true);
+        }
+      }
+    }
+    // The partner's last commits arrive on this CTA's free barriers: wait (bounded) for
+    // their final phases, so nothing lands in this CTA's shared memory after it exits.
+    if (ok) {
+      for (int c = max(0, nchunks - kKStages); c < nchunks; ++c)
+        mbar_wait_bounded(&kfree[c % kKStages], (c / kKStages) & 1, kWaitNs / 8);
+      for (int c = max(0, nchunks - kVStages); c < nchunks; ++c)
+        mbar_wait_bounded(&vfree[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
     }
     // MMAs committed but maybe not finished: a commit tracks every earlier MMA of the
     // issuing thread, so the last commit's barrier covers them all
@@ -679,12 +737,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   fence_before();
   __syncthreads();
-  // After an abort no consumer waits for the K copies still landing: warp 8 waits
+  // After an abort no consumer waits for the copies still landing: warp 8 waits
   // (bounded) for the last chunks it issued, so nothing lands after the CTA exits.
-  if (*s_abort && warp == kKWarp && lane == 0) {
+  if (*s_abort && warp == kCopyWarp && lane == 0) {
     for (int c = issued_k - kKStages; c < issued_k; ++c)
       if (c >= 0) mbar_wait_bounded(&fullk[c % kKStages], (c / kKStages) & 1, kWaitNs / 8);
+    for (int c = issued_v - kVStages; c < issued_v; ++c)
+      if (c >= 0) mbar_wait_bounded(&fullv[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
   }
+  // Neither CTA of the cluster leaves while the other may still copy into it or
+  // commit to its barriers (every wait above is bounded, so both arrive here).
+  __syncthreads();
+  cluster_sync_all();
   if (warp == 0) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Sh::kTmemCols));

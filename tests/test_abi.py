@@ -216,7 +216,7 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     # null pointers: the row-count check comes first, and without it the null check would refuse
     big = lib.pa_prefill(None, None, None, None, None, 4, None, None, 2, 8, 64, 8, 2, 128, 16, 1 << 27, 0.1,
                          B.PA_F16, None)
-    assert big == B.PA_ERR_UNSUPPORTED     # 2^27 blocks x 2 kv heads x 16 slices: past the tensor map's rows
+    assert big == B.PA_ERR_UNSUPPORTED     # 2^27 blocks x 2 kv heads x 128 dims: past the V tensor map's rows
 
 
 def test_fused_step_rejects_bad_arguments_on_the_host(lib):
