@@ -25,9 +25,9 @@
 //     16-byte rows, 16 per chunk, whose copies held the K gathers back, and then
 //     with cp.async from two warps of its own.)
 //   * warp 9: the MMAs, in the order P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1): a
-//     tile's S(c + 1) overwrites the P(c) its P V(c) reads, so it waits for that
-//     P V to finish.  The whole warp runs the loop and the waits; one elected lane
-//     issues the MMAs and commits them to mbarriers.
+//     tile's S(c + 1) overwrites the P(c) its P V(c) reads and is issued right behind
+//     it (the MMAs of one thread run in issue order).  The whole warp runs the loop
+//     and the waits; one elected lane issues the MMAs and commits them to mbarriers.
 //   * warps 0..3 (tile A) and 4..7 (tile B), one thread per row: the softmax of
 //     S(c).  P = exp2(s - m) goes back into the row's own S columns as 16-bit
 //     values, two per 32-bit column: the 16 columns of keys 16 k .. 16 k + 15
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_before();
         mbar_arrive(pfull(X));
       }
-      if (__all_sync(0xffffffffu, ok && wait(pvdone(X), (nchunks - 1) & 1))) {
+      if (__all_sync(0xffffffffu, ok && wait(pvdone(X), 0))) {  // one phase: the last P V
         fence_after();
         const float inv = 1.f / l;
         T* out = static_cast<T*>(p.out) +
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    db + (((16 * kk) / BS) * Sh::kTile + ((16 * kk) % BS) * 2) / 16, kIdO, c > 0 || part > 0 || kk > 0);
         }
       }
-      commit_to(pvdone(Xm), c & 1);
+      if (c == nchunks - 1) commit_to(pvdone(Xm), 0);  // O_X is complete
     };
     // the timeout-path test: the first wait runs out on `never` (no MMA issued yet);
     // the producer then drains its copies with the normal limit
@@ -708,7 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (Xm == ntiles - 1) commit_to(&vfree[vb], (c / kVStages) & 1, true);
         if (c1 < nchunks) {
           if (Xm == 0 && !(ok = wait_all(&fullk[c1 % kKStages], (c1 / kKStages) & 1))) break;
-          if (!(ok = wait_all(pvdone(Xm), c & 1))) break;  // P_X(c) read before S_X(c + 1) overwrites it
+          // S_X(c + 1) overwrites the columns P V_X(c) reads, issued right behind it: MMAs
+          // of one thread run in issue order, so no wait is needed between the two
           fence_after();
           issue_s(Xm, c1);
           if (Xm == ntiles - 1) commit_to(&kfree[c1 % kKStages], (c1 / kKStages) & 1, true);
