@@ -435,15 +435,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int X = tid >= kSoftmaxThreads ? 1 : 0;  // (softmax threads only)
   const int r = tid & (kRows - 1), row = pair_lo + X * kRows + r;
   const bool valid = row < pair_hi;
-  if (tid < 2 * kSoftmaxThreads) {
-    unsigned char* sQ = smem + X * Sh::kQTile;
+  if (tid < 2 * kSoftmaxThreads) {  // all 16-byte pieces of the row in flight at once, zeros for a padding row
+    const uint32_t sq = smem_addr(smem + X * Sh::kQTile + (r / 8) * (D / 8) * 128 + (r % 8) * 16);
     const T* q = static_cast<const T*>(p.q) +
                  ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) * D;
+    const uint32_t nbytes = valid ? 16u : 0u;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(q) + c) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sQ + (r / 8) * (D / 8) * 128 + c * 128 + (r % 8) * 16) = v;
-    }
+    for (int c = 0; c < D / 8; ++c)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sq + c * 128), "l"(q + 8 * c), "r"(nbytes)
+                   : "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
   }
   fence_proxy_async_smem();  // Q's generic stores before the MMAs read it
   fence_before();
