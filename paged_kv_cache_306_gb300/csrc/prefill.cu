@@ -89,14 +89,36 @@ cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static unsigned done = 0;
-  if (dev >= 32 || !(__atomic_load_n(&done, __ATOMIC_ACQUIRE) & (1u << dev))) {
+  static int resident[32];  // clusters that fit on device d at once
+  const bool cached = dev < 32 && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & (1u << dev));
+  int clusters_resident = cached ? __atomic_load_n(&resident[dev], __ATOMIC_RELAXED) : 0;
+  if (!cached) {
     e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&ws::prefill_ws_kernel<T, D, BS>),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&ws::prefill_ws_kernel<T, D, BS>),
                              cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    if (dev < 32) __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(ws::kCluster);
+    q.blockDim = dim3(ws::kThreads);
+    q.dynamicSmemBytes = Sh::kSmem;
+    cudaLaunchAttribute ca;
+    ca.id = cudaLaunchAttributeClusterDimension;
+    ca.val.clusterDim.x = ws::kCluster;
+    ca.val.clusterDim.y = 1;
+    ca.val.clusterDim.z = 1;
+    q.attrs = &ca;
+    q.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&ws::prefill_ws_kernel<T, D, BS>), &q);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    clusters_resident = n;
+    if (dev < 32) {
+      __atomic_store_n(&resident[dev], n, __ATOMIC_RELAXED);
+      __atomic_fetch_or(&done, 1u << dev, __ATOMIC_RELEASE);
+    }
   }
   CUtensorMap kmap, vmap;
   e = encode_k_map<D, BS>(p, &kmap);
@@ -104,13 +126,13 @@ cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int
   e = encode_v_map<D, BS>(p, &vmap);
   if (e != cudaSuccess) return e;
   // sequence s has ceil(ceil(n_s G / 128) / 4) units of four tiles per kv head, at most
-  // n_s G / 512 + 1 (rounded up); a unit is one cluster of two CTAs
+  // n_s G / 512 + 1 (rounded up); each cluster of two CTAs takes units until none is left
   const long long units = (long long)p.num_kv_heads * (((long long)p.num_query_tokens * p.group + ws::kUnitTiles * ws::kRows - 1) /
                                                            (ws::kUnitTiles * ws::kRows) +
                                                        p.num_seqs);
-  if (units * ws::kCluster > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long clusters = units < clusters_resident ? units : clusters_resident;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * ws::kCluster));
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * ws::kCluster));
   cfg.blockDim = dim3(ws::kThreads);
   cfg.dynamicSmemBytes = Sh::kSmem;
   cfg.stream = stream;

@@ -4,16 +4,25 @@
 // cache (what is computed: see prefill.cu), on sm_103a's tcgen05 MMAs with the
 // accumulators in tensor memory (TMEM).  A query tile is 128 rows -- (token,
 // query head) pairs of one kv head, head fastest -- which are TMEM lanes
-// 0..127; keys are taken 128 at a time (a chunk).  A CTA owns a PAIR of
-// consecutive tiles A and B of one (sequence, kv head): both read the same keys,
-// so each chunk of K and V is copied once and feeds the MMAs of both tiles.  The
-// two tiles take turns: while the softmax of one runs, the tensor cores run the
-// other's P V and its next S (ping-pong).  The phases run in different warps that
-// hand over through mbarriers:
+// 0..127; keys are taken 128 at a time (a chunk).  A unit is four consecutive
+// tiles of one (sequence, kv head); a cluster of two CTAs on two SMs takes a unit
+// at a time, each CTA a PAIR of its tiles, A and B.  All four read the same keys,
+// so each chunk of K and V is copied once per cluster (half by each CTA, with TMA
+// multicast into both) and feeds the MMAs of both tiles of both CTAs.  The two
+// tiles of a CTA take turns: while the softmax of one runs, the tensor cores run
+// the other's P V and its next S (ping-pong).  The kernel is persistent: as many
+// clusters as fit on the GPU at once, each taking units in the order of
+// decreasing length until none is left; the K/V rings, the barriers' phases and
+// the TMEM columns carry on from one unit to the next, so a unit's first copies,
+// its Q and its first S overlap the previous unit's last chunk and its output.
+// The phases run in different warps that hand over through mbarriers:
 //
-//   * warp 8: the TMA copies of chunk c, K into K buffer c % 2 once both tiles' S
-//     of chunk c - 2 have read it, V into V buffer c % 2 once both tiles' P V of
-//     chunk c - 2 have read it, each on its own mbarrier.  K: the pool seen as rows
+//   * warp 10: the unit ring.  It works out this cluster's units (ranks cid,
+//     cid + clusters, ..: see pick_unit) up to four ahead; each is read by
+//     every other warp.
+//   * warp 8: the TMA copies of chunk c (counted over all units), K into K buffer
+//     c % 2 once both tiles' S of chunk c - 2 have read it, V into V buffer c % 2
+//     once both tiles' P V of chunk c - 2 have read it, each on its own mbarrier.  K: the pool seen as rows
 //     of 16 keys x 8 dims (one 256-byte run of a K tile [D/8][bs][8]); lane i issues
 //     the i-th tile::gather4 load (one per 8-dim slice and 64 keys), which fetches
 //     four such rows from blocks anywhere in the pool and lands them as [64][8]: the
@@ -29,18 +38,21 @@
 //     it (the MMAs of one thread run in issue order).  The whole warp runs the loop
 //     and the waits; one elected lane issues the MMAs and commits them to mbarriers.
 //   * warps 0..3 (tile A) and 4..7 (tile B), one thread per row: the softmax of
-//     S(c).  P = exp2(s - m) goes back into the row's own S columns as 16-bit
-//     values, two per 32-bit column: the 16 columns of keys 16 k .. 16 k + 15
-//     become 8 columns of P rounded to fp16 or, for bf16, 8 columns of rounded high
-//     parts and 8 of low parts (~16 significant bits; P V is then two MMA groups).
-//     The running maximum moves only when it grows by more than 2^8; then the row's O is rescaled in TMEM (P V(c - 1) is done by
-//     then: S(c) was issued after it).  In the last chunk tile A's threads zero the
+//     S(c), then the unit's output out of TMEM; during a unit's last chunk they
+//     load the next unit's Q (its S(0) waits for it, its first P V for the output).
+//     P = exp2(s - m) goes back into the row's own S columns as 16-bit values, two
+//     per 32-bit column: the 16 columns of keys 16 k .. 16 k + 15 become 8 columns
+//     of P rounded to fp16 or, for bf16, 8 columns of rounded high parts and 8 of
+//     low parts (~16 significant bits; P V is then two MMA groups).  The running
+//     maximum moves only when it grows by more than 2^8; then the row's O is
+//     rescaled in TMEM (P V(c - 1) is done by then: S(c) was issued after it).  In the last chunk tile A's threads zero the
 //     V of keys past the sequence (or past the blocks loaded) in shared memory
 //     first: P is 0 there, but 0 * NaN would poison O.  A tile whose rows end
 //     before the pair's last chunk sees scores of -inf there (P = 0).
 //
 // TMEM: tile X at column 256 X: S/P in 0..127, O (D <= 128 columns) from 128; all
-// 512 columns for the pair; one CTA per SM.
+// 512 columns for the pair; one CTA per SM.  A unit's first P V_X overwrites O_X
+// only after the softmax threads have read the previous unit's O_X out.
 // Every wait is bounded (1 s of %globaltimer); a thread that gives up records
 // PA_DEVERR_TIMEOUT and raises a CTA-wide abort flag that makes every other wait
 // give up at once; the threads that issued copies or MMAs then wait (bounded)
@@ -69,13 +81,16 @@ using tc::st32;
 constexpr int kRows = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kKeys = 128;  // keys per chunk
 constexpr int kSoftmaxThreads = 128;  // per tile
-constexpr int kCopyWarp = 8, kMmaWarp = 9;
+constexpr int kCopyWarp = 8, kMmaWarp = 9, kSchedWarp = 10;
 // A cluster of two CTAs on two SMs takes a unit of four consecutive tiles of one
 // (sequence, kv head), a pair per CTA; each CTA copies half of every chunk of K and V
 // with TMA multicast into both, so each SM fetches half of the bytes its MMAs read.
 constexpr int kCluster = 2, kUnitTiles = 2 * kCluster;
 constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
-constexpr int kThreads = 10 * 32;
+constexpr int kThreads = 11 * 32;
+// The unit ring: the scheduler warp writes up to kUnitSlots units ahead; each is
+// read by the 8 softmax warps, the copy warp and the MMA warp.
+constexpr int kUnitSlots = 4, kUnitReaders = 10;
 constexpr int kKStages = 2, kVStages = 2;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -223,116 +238,108 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// The unit of rank `rank` (0-based) in the order of decreasing length -- the chunks
-// of keys it reads -- ties by sequence, kv head and unit index; so the longest
-// units of the whole launch start first and the short ones fill the tail.  A unit
-// is kUnitTiles consecutive tiles of one (sequence, kv head), the work of one
-// cluster.  Every thread of the CTA takes part (thread t owns sequences
-// t * kPer ..).  Tile j of sequence s covers rows 128 j .. of its n * G rows and
-// reads chunks 0 .. (ctx + (row_hi - 1) / G) / 128, non-decreasing in j; unit k holds
-// tiles kUnitTiles k .. (those that exist) and reads what its last tile reads.  So
-// the tiles of s reading >= x chunks are a suffix j >= j0 in closed form, the units
-// reading >= x are those from j0 / kUnitTiles on, and the rank-th unit is found by
-// a binary search on x.  Writes (sequence, kv head, unit) to out; returns false
-// when rank is past the units.
-__device__ bool pick_unit(const PrefillParams& p, int rank, int* red, int* out) {
-  constexpr int kPer = (kMaxSeqsPerLaunch + kThreads - 1) / kThreads;
-  constexpr int kWarpsTotal = kThreads / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = p.group, Hkv = p.num_kv_heads;
-  int ctx[kPer], rows[kPer], nt[kPer];
+// The per-sequence figures unit selection needs, in shared memory (3 kMaxSeqsPerLaunch
+// ints): ctx = tokens before the chunk, rows = its n G query rows, and its tiles.
+// One warp fills it once per CTA (lane i: sequences i, i + 32, ..) and checks the
+// lengths; returns the number of units of the launch (all kv heads) and, in
+// *longest, the most chunks any unit reads.
+__device__ long long build_seq_table(const PrefillParams& p, int* tab, int* longest_out) {
+  const int lane = threadIdx.x & 31, G = p.group, S = p.num_seqs;
   bool bad = false;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int s = tid * kPer + i;
-    ctx[i] = rows[i] = nt[i] = 0;
-    if (s < p.num_seqs) {
-      const int L = __ldg(p.seq_lens + s), a = __ldg(p.query_start_loc + s), b = __ldg(p.query_start_loc + s + 1);
-      const int n = b - a;
-      if (L < 1 || L > p.max_seq_len || a < 0 || b > p.num_query_tokens || n < 0 || n > L) {
-        bad = true;
-      } else {
-        ctx[i] = L - n;
-        rows[i] = n * G;
-        nt[i] = (rows[i] + kRows - 1) / kRows;
-      }
+  int units = 0, longest = 0;
+  for (int s = lane; s < S; s += 32) {
+    const int L = __ldg(p.seq_lens + s), a = __ldg(p.query_start_loc + s), b = __ldg(p.query_start_loc + s + 1);
+    const int n = b - a;
+    int ctx = 0, rows = 0, nt = 0;
+    if (L < 1 || L > p.max_seq_len || a < 0 || b > p.num_query_tokens || n < 0 || n > L) {
+      bad = true;
+    } else {
+      ctx = L - n;
+      rows = n * G;
+      nt = (rows + kRows - 1) / kRows;
     }
+    tab[s] = ctx;
+    tab[kMaxSeqsPerLaunch + s] = rows;
+    tab[2 * kMaxSeqsPerLaunch + s] = nt;
+    units += (nt + kUnitTiles - 1) / kUnitTiles;
+    if (nt) longest = max(longest, (ctx + (rows - 1) / G) / kKeys + 1);
   }
   if (bad && blockIdx.x == 0) set_error(p.err, kErrSeqLen);
-  // units of owned sequence i that read >= x chunks
-  auto cnt = [&](int i, int x) -> int {
-    const long long need = (long long)G * ((long long)kKeys * (x - 1) - ctx[i]) + 1;  // rows a tile must reach
-    if (nt[i] == 0 || need > rows[i]) return 0;
-    const int j0 = need <= 1 ? 0 : static_cast<int>((need + kRows - 1) / kRows - 1);  // first tile reading >= x
-    return (nt[i] + kUnitTiles - 1) / kUnitTiles - j0 / kUnitTiles;
-  };
-  int buf = 0;
-  auto reduce = [&](int v, bool take_max) -> int {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const int u = __shfl_xor_sync(0xffffffffu, v, o);
-      v = take_max ? max(v, u) : v + u;
-    }
-    buf ^= 1;
-    if (lane == 0) red[buf * 16 + warp] = v;
-    __syncthreads();
-    int t = 0;
-#pragma unroll
-    for (int w = 0; w < kWarpsTotal; ++w) t = take_max ? max(t, red[buf * 16 + w]) : t + red[buf * 16 + w];
-    return t;
-  };
-  int local = 0, longest = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    local += (nt[i] + kUnitTiles - 1) / kUnitTiles;
-    if (nt[i]) longest = max(longest, (ctx[i] + (rows[i] - 1) / G) / kKeys + 1);
+  for (int o = 16; o > 0; o >>= 1) {
+    units += __shfl_xor_sync(0xffffffffu, units, o);
+    longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
   }
-  if ((long long)Hkv * reduce(local, false) <= rank) return false;
-  int lo = 1, hi = reduce(longest, true);  // C(lo) > rank
+  __syncwarp();
+  *longest_out = longest;
+  return (long long)p.num_kv_heads * units;
+}
+
+// The unit of rank `rank` (0-based) in the order of decreasing length -- the chunks
+// of keys it reads -- ties by sequence, kv head and unit index; so the longest
+// units of the whole launch are taken first and the short ones fill the tail.  A
+// unit is kUnitTiles consecutive tiles of one (sequence, kv head), the work of one
+// cluster.  Tile j of sequence s covers rows 128 j .. of its n * G rows and reads
+// chunks 0 .. (ctx + (row_hi - 1) / G) / 128, non-decreasing in j; unit k holds tiles
+// kUnitTiles k .. (those that exist) and reads what its last tile reads.  So the
+// tiles of s reading >= x chunks are a suffix j >= j0 in closed form, the units
+// reading >= x are those from j0 / kUnitTiles on, and the rank-th unit is found by a
+// binary search on x.  One warp, on the table of build_seq_table (every count a warp
+// sum); rank must be below the launch's `total` units.  Returns (sequence, kv head,
+// unit) in every lane.
+__device__ int3 pick_unit(const PrefillParams& p, const int* tab, long long rank, int longest) {
+  const int lane = threadIdx.x & 31, G = p.group, Hkv = p.num_kv_heads, S = p.num_seqs;
+  const int* t_ctx = tab;
+  const int* t_rows = tab + kMaxSeqsPerLaunch;
+  const int* t_nt = tab + 2 * kMaxSeqsPerLaunch;
+  auto cnt = [&](int s, int x) -> int {  // units of sequence s that read >= x chunks
+    const int nt = t_nt[s], rows = t_rows[s];
+    const long long need = (long long)G * ((long long)kKeys * (x - 1) - t_ctx[s]) + 1;  // rows a tile must reach
+    if (nt == 0 || need > rows) return 0;
+    const int j0 = need <= 1 ? 0 : static_cast<int>((need + kRows - 1) / kRows - 1);  // first tile reading >= x
+    return (nt + kUnitTiles - 1) / kUnitTiles - j0 / kUnitTiles;
+  };
+  auto count = [&](int x) {  // units of the launch (all kv heads) reading >= x chunks
+    int v = 0;
+    for (int s = lane; s < S; s += 32) v += cnt(s, x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return (long long)Hkv * v;
+  };
+  int lo = 1, hi = longest;  // count(lo) > rank
   while (lo < hi) {
     const int mid = (lo + hi + 1) / 2;
-    local = 0;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) local += cnt(i, mid);
-    if ((long long)Hkv * reduce(local, false) > rank) lo = mid;
+    if (count(mid) > rank) lo = mid;
     else hi = mid - 1;
   }
-  // rank among the units of exactly lo chunks, ordered by (sequence, kv head, unit)
-  local = 0;
+  // rank among the units of exactly lo chunks, ordered by (sequence, kv head, unit):
+  // sequences in rounds of 32, an inclusive scan over the lanes within a round
+  long long r = rank - count(lo + 1);
+  int3 u = make_int3(0, 0, 0);
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s = s0 + lane;
+    const int e = s < S ? cnt(s, lo) - cnt(s, lo + 1) : 0;
+    int incl = e;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) local += cnt(i, lo + 1);
-  const long long r = rank - (long long)Hkv * reduce(local, false);
-  int e[kPer], mine = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    e[i] = cnt(i, lo) - cnt(i, lo + 1);
-    mine += e[i];
-  }
-  int incl = mine;  // inclusive scan over threads (sequence order)
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  buf ^= 1;
-  if (lane == 31) red[buf * 16 + warp] = incl;
-  __syncthreads();
-  long long before = incl - mine;
-  for (int w = 0; w < warp; ++w) before += red[buf * 16 + w];
-  before *= Hkv;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const long long span = (long long)Hkv * e[i];
-    if (r >= before && r < before + span) {
-      const int q = static_cast<int>(r - before);
-      out[0] = tid * kPer + i;
-      out[1] = q / e[i];
-      out[2] = (nt[i] + kUnitTiles - 1) / kUnitTiles - cnt(i, lo) + q % e[i];
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
-    before += span;
+    const long long before = (long long)Hkv * (incl - e), span = (long long)Hkv * e;
+    const bool here = e > 0 && r >= before && r < before + span;
+    const unsigned who = __ballot_sync(0xffffffffu, here);
+    if (who) {
+      const int src = __ffs(who) - 1;
+      const int q = static_cast<int>(r - before);
+      const int3 mine = make_int3(s, here ? q / e : 0, here ? (t_nt[s] + kUnitTiles - 1) / kUnitTiles - cnt(s, lo) + q % e : 0);
+      u.x = __shfl_sync(0xffffffffu, mine.x, src);
+      u.y = __shfl_sync(0xffffffffu, mine.y, src);
+      u.z = __shfl_sync(0xffffffffu, mine.z, src);
+      break;
+    }
+    r -= (long long)Hkv * __shfl_sync(0xffffffffu, incl, 31);
   }
-  __syncthreads();
-  return true;
+  return u;
 }
 
 template <typename T, int D, int BS>
@@ -345,13 +352,44 @@ struct Shape {
   static constexpr int kOffK = 2 * kQTile;                  // K ring
   static constexpr int kOffV = kOffK + kKStages * kKBytes;  // V ring
   static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-  // fullk[K], fullv[V], kfree[K], vfree[V], per tile sfull, pfull, pvdone, never
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 3 + 1;
-  static constexpr int kOffRed = kOffBar + kNumBars * 8 + 32;  // [2][16] ints: block reductions
+  // fullk[K], fullv[V], kfree[K], vfree[V], per tile 5 (sfull, pfull, pvdone, qfull,
+  // ofree), ufull[U], uempty[U], never
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 * kUnitSlots + 1;
+  static constexpr int kOffMisc = kOffBar + (kNumBars * 8 + 15) / 16 * 16;  // TMEM address, abort flag
+  static constexpr int kOffUnits = kOffMisc + 16;                           // [kUnitSlots] int4: the unit ring
+  static constexpr int kOffTab = kOffUnits + kUnitSlots * 16;               // unit selection's table
+  static constexpr int kEnd = kOffTab + 3 * kMaxSeqsPerLaunch * 4;
   // more than half an SM's shared memory, so one CTA per SM: it takes all of TMEM
-  static constexpr int kSmem = kOffRed + 2 * 16 * 4 > 116 * 1024 ? kOffRed + 2 * 16 * 4 : 116 * 1024;
+  static constexpr int kSmem = kEnd > 116 * 1024 ? kEnd : 116 * 1024;
   static constexpr int kTmemCols = 512;  // tile X at 256 X: S/P 0..127, O 128..128+D
 };
+
+// The figures of one unit that every role needs: the same in every role, and in both
+// CTAs of the cluster except for the pair, which is this CTA's.
+struct UnitView {
+  int s, kvh, L, tok0, pair_lo, pair_hi, ntiles, ctx, nblk, nchunks;
+};
+template <int BS>
+__device__ __forceinline__ UnitView unit_view(const PrefillParams& p, int4 u, uint32_t crank) {
+  UnitView v;
+  v.s = u.x;
+  v.kvh = u.y;
+  const int G = p.group;
+  v.L = p.seq_lens[v.s];
+  v.tok0 = p.query_start_loc[v.s];
+  const int n = p.query_start_loc[v.s + 1] - v.tok0, rows = n * G;
+  // this CTA's pair: tiles kUnitTiles unit + 2 crank and the next (either may be past the rows)
+  v.pair_lo = (kUnitTiles * u.z + 2 * static_cast<int>(crank)) * kRows;
+  v.pair_hi = min(rows, v.pair_lo + 2 * kRows);
+  v.ntiles = v.pair_lo >= rows ? 0 : (v.pair_lo + kRows < rows ? 2 : 1);  // tiles with rows: A, then B
+  // keys: what the unit's last row sees (the same in both CTAs: they share every chunk)
+  const int unit_hi = min(rows, (kUnitTiles * u.z + kUnitTiles) * kRows);
+  v.ctx = v.L - n;
+  const int p_max = v.ctx + (unit_hi - 1) / G;  // last position any row of the unit has
+  v.nblk = p_max / BS + 1;                      // blocks holding keys 0..p_max
+  v.nchunks = (p_max + kKeys) / kKeys;
+  return v;
+}
 
 template <typename T, int D, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -359,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmap_v) {
   using Sh = Shape<T, D, BS>;
   static_assert(Sh::kSmem > 114 * 1024, "two CTAs on one SM would contend for TMEM");
+  static_assert(Sh::kSmem <= 227 * 1024, "shared memory per CTA");
   static_assert(kKeys % BS == 0, "a chunk is whole blocks");
   // P in one 16-bit part for fp16 (11 significant bits, the operands' own precision); for
   // bf16 a high and a low part (~16 bits), since one bf16 part (8 bits) would add
@@ -370,27 +409,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* fullv = fullk + kKStages;       // [kVStages] V buffer landed (TMA bytes)
   uint64_t* kfree = fullv + kVStages;       // [kKStages] both CTAs' S read the K buffer (a commit from each)
   uint64_t* vfree = kfree + kKStages;       // [kVStages] both CTAs' P V read the V buffer (a commit from each)
-  uint64_t* tbars = vfree + kVStages;       // per tile X at 3 X: sfull, pfull, pvdone
-  uint64_t* never = tbars + 6;              // nothing completes it: the timeout-path test waits on it
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + Sh::kNumBars);
-  int* s_pair = reinterpret_cast<int*>(s_tmem + 1);                     // sequence, kv head, unit (or -1)
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_pair + 3);  // a thread gave up
+  uint64_t* tbars = vfree + kVStages;       // per tile X at 5 X: sfull, pfull, pvdone, qfull, ofree
+  uint64_t* ufull = tbars + 10;             // [kUnitSlots] the scheduler wrote the slot
+  uint64_t* uempty = ufull + kUnitSlots;    // [kUnitSlots] every reader took the slot
+  uint64_t* never = uempty + kUnitSlots;    // nothing completes it: the timeout-path test waits on it
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Sh::kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);  // a thread gave up
+  volatile int* s_unit = reinterpret_cast<volatile int*>(smem + Sh::kOffUnits);  // [kUnitSlots][4]
+  int* tab = reinterpret_cast<int*>(smem + Sh::kOffTab);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // S(c) in TMEM (commit); P(c) in TMEM, O rescaled, V tail zeroed (128 arrivals);
-  // P V(c) done: P's columns free, O final after the last chunk (commit)
-  auto sfull = [&](int X) { return tbars + 3 * X; };
-  auto pfull = [&](int X) { return tbars + 3 * X + 1; };
-  auto pvdone = [&](int X) { return tbars + 3 * X + 2; };
+  // S(c) in TMEM (commit); P(c) in TMEM, O rescaled, V tail zeroed (128 arrivals); the
+  // unit's last P V done (commit); the next unit's Q in shared memory (128 arrivals);
+  // the unit's O read out of TMEM (128 arrivals)
+  auto sfull = [&](int X) { return tbars + 5 * X; };
+  auto pfull = [&](int X) { return tbars + 5 * X + 1; };
+  auto pvdone = [&](int X) { return tbars + 5 * X + 2; };
+  auto qfull = [&](int X) { return tbars + 5 * X + 3; };
+  auto ofree = [&](int X) { return tbars + 5 * X + 4; };
 
   griddep_launch_dependents();
   griddep_wait();
-
-  // ---- which unit: the longest first over the whole launch (both CTAs of a cluster pick the same)
   const uint32_t crank = cluster_rank();
-  const bool has_unit =
-      pick_unit(p, static_cast<int>(blockIdx.x / kCluster), reinterpret_cast<int*>(smem + Sh::kOffRed), s_pair);
   if (tid == 0) {
-    if (!has_unit) s_pair[0] = -1;
     *s_abort = 0;
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&fullk[i], 1);
@@ -404,248 +444,317 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sfull(X), 1);
       mbar_init(pfull(X), kSoftmaxThreads);
       mbar_init(pvdone(X), 1);
+      mbar_init(qfull(X), kSoftmaxThreads);
+      mbar_init(ofree(X), kSoftmaxThreads);
+    }
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(&ufull[i], 1);
+      mbar_init(&uempty[i], kUnitReaders);
     }
     mbar_init(never, 1);
     fence_barrier_init();
   }
-  __syncthreads();
-  cluster_sync_all();  // both CTAs' mbarriers are initialised before either copies into the other
-  const int s = s_pair[0];
-  if (s < 0) return;  // no unit for this cluster: both CTAs leave here, before any TMEM is taken
-  const int kvh = s_pair[1], unit = s_pair[2];
-  const int G = p.group;
-  const int L = p.seq_lens[s], tok0 = p.query_start_loc[s], n = p.query_start_loc[s + 1] - tok0;
-  // this CTA's pair: tiles kUnitTiles unit + 2 crank and the next (either may be past the rows)
-  const int rows = n * G, pair_lo = (kUnitTiles * unit + 2 * static_cast<int>(crank)) * kRows,
-            pair_hi = min(rows, pair_lo + 2 * kRows);
-  const int ntiles = pair_lo >= rows ? 0 : (pair_lo + kRows < rows ? 2 : 1);  // tiles with rows: A, then B
-  // keys: what the unit's last row sees, the same in both CTAs (they share every chunk)
-  const int unit_hi = min(rows, (kUnitTiles * unit + kUnitTiles) * kRows);
-  const int ctx = L - n;
-  const int p_max = ctx + (unit_hi - 1) / G;  // last position any row of the unit has
-  const int nblk = p_max / BS + 1;            // blocks holding keys 0..p_max
-  const int nchunks = (p_max + kKeys) / kKeys;
-
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(s_tmem)),
                  "r"(Sh::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // the softmax threads' tile and row; Q of both tiles into shared memory (core matrices: 8 rows x 16 bytes)
-  const int X = tid >= kSoftmaxThreads ? 1 : 0;  // (softmax threads only)
-  const int r = tid & (kRows - 1), row = pair_lo + X * kRows + r;
-  const bool valid = row < pair_hi;
-  if (tid < 2 * kSoftmaxThreads) {  // all 16-byte pieces of the row in flight at once, zeros for a padding row
-    const uint32_t sq = smem_addr(smem + X * Sh::kQTile + (r / 8) * (D / 8) * 128 + (r % 8) * 16);
-    const T* q = static_cast<const T*>(p.q) +
-                 ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) * D;
-    const uint32_t nbytes = valid ? 16u : 0u;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sq + c * 128), "l"(q + 8 * c), "r"(nbytes)
-                   : "memory");
-    asm volatile("cp.async.wait_all;" ::: "memory");
-  }
-  fence_proxy_async_smem();  // Q's generic stores before the MMAs read it
   fence_before();
   __syncthreads();
   fence_after();
+  cluster_sync_all();  // both CTAs' mbarriers are initialised before either copies into the other
   const uint32_t tmem = *s_tmem;
-  int issued_k = 0, issued_v = 0;  // chunks whose K (V) copies warp 8 issued
+  const int G = p.group;
+  int issued_k = 0, issued_v = 0;  // chunks (of all units) whose K (V) copies warp 8 issued
   auto wait = [&](uint64_t* bar, int parity) { return wait_or_abort(bar, parity, s_abort, p.err); };
+  // the k-th unit of the ring (the slot's ufull phase k / kUnitSlots); every reader
+  // takes it once and frees it with one arrival per warp
+  auto take_unit = [&](int k, int4& u) -> bool {
+    const int slot = k % kUnitSlots;
+    if (!__all_sync(0xffffffffu, wait(&ufull[slot], (k / kUnitSlots) & 1))) return false;
+    u = make_int4(s_unit[4 * slot], s_unit[4 * slot + 1], s_unit[4 * slot + 2], 0);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&uempty[slot]);
+    return true;
+  };
 
   if (warp < 8) {
-    // ================= softmax: tile X, row r, all keys of each chunk =================
-    if (ntiles > X) {
-      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-      const uint32_t t_s = tmem + 256 * X + lane_base;
-      const uint32_t t_o = t_s + kKeys;
-      const int pos = valid ? ctx + row / G : ctx + (pair_hi - 1) / G;  // a padding row behaves as a real one
-      const int kz = min(L, nblk * BS);  // first key whose V must read as zero
-      const float sl2 = p.scale_log2;
-      float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int c = 0; c < nchunks; ++c) {
-        // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them
-        // is taken by the whole warp, so each wait's outcome is agreed across the warp
-        if (!__all_sync(0xffffffffu, wait(sfull(X), c & 1))) {
-          ok = false;
-          break;
+    // ================= softmax: tile X, row r, all keys of each chunk of each unit =================
+    const int X = warp >> 2, r = tid & (kRows - 1);
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + 256 * X + lane_base;
+    const uint32_t t_o = t_s + kKeys;
+    const float sl2 = p.scale_log2;
+    const uint32_t sq = smem_addr(smem + X * Sh::kQTile + (r / 8) * (D / 8) * 128 + (r % 8) * 16);
+    // this thread's row of Q_X for unit v into shared memory: every 16-byte piece in
+    // flight at once, zeros for a padding row (completed by wait_q)
+    auto load_q = [&](const UnitView& v) {
+      const int row = v.pair_lo + X * kRows + r;
+      const bool valid = row < v.pair_hi;
+      const T* q = static_cast<const T*>(p.q) +
+                   ((long long)(v.tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)v.kvh * G +
+                    (valid ? row % G : 0)) * D;
+      const uint32_t nbytes = valid ? 16u : 0u;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sq + c * 128), "l"(q + 8 * c), "r"(nbytes)
+                     : "memory");
+    };
+    auto q_landed = [&]() {  // the Q copies done, visible to the MMAs, handed over
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      fence_proxy_async_smem();
+      mbar_arrive(qfull(X));
+    };
+    int cx = 0, ux = 0;  // chunks and units this tile had rows in: the phases of its barriers
+    int g = 0;           // chunks of all units before this one: the K/V ring positions
+    int4 u;
+    bool ok = take_unit(0, u);
+    UnitView U{};
+    if (ok && u.x >= 0) {
+      U = unit_view<BS>(p, u, crank);
+      if (U.ntiles > X) {
+        load_q(U);
+        q_landed();
+      }
+    }
+    for (int k = 0; ok && u.x >= 0; ++k) {
+      int4 un = make_int4(-1, 0, 0, 0);  // the next unit, taken during this one's last chunk
+      UnitView N{};
+      auto next = [&]() {
+        if (!(ok = take_unit(k + 1, un))) return;
+        if (un.x >= 0) {
+          N = unit_view<BS>(p, un, crank);
+          if (N.ntiles > X) load_q(N);  // Q_X is free: the last S_X of this unit is done
         }
-        fence_after();
-        float sv[kKeys];
-        ld128(t_s, sv);
-        const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
-        if (lim < kKeys - 1) {           // the diagonal chunk (or past it): hide the later keys
+      };
+      if (U.ntiles > X) {
+        const int row = U.pair_lo + X * kRows + r;
+        const bool valid = row < U.pair_hi;
+        const int pos = valid ? U.ctx + row / G : U.ctx + (U.pair_hi - 1) / G;  // a padding row behaves as a real one
+        const int kz = min(U.L, U.nblk * BS);  // first key whose V must read as zero
+        float m = -INFINITY, l = 0.f;
+        for (int c = 0; c < U.nchunks; ++c, ++cx) {
+          // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them
+          // is taken by the whole warp, so each wait's outcome is agreed across the warp
+          if (!(ok = __all_sync(0xffffffffu, wait(sfull(X), cx & 1)))) break;
+          fence_after();
+          if (c == U.nchunks - 1) {
+            next();
+            if (!ok) break;
+          }
+          float sv[kKeys];
+          ld128(t_s, sv);
+          const int lim = pos - c * kKeys;  // keys 0..lim of the chunk are visible to the row
+          if (lim < kKeys - 1) {           // the diagonal chunk (or past it): hide the later keys
 #pragma unroll
-          for (int j = 0; j < kKeys; ++j)
-            if (j > lim) sv[j] = -INFINITY;
-        }
-        // the row maximum of the raw scores, as a tree (scale > 0 keeps the order)
-        float mx;
-        {
-          float t[8];
+            for (int j = 0; j < kKeys; ++j)
+              if (j > lim) sv[j] = -INFINITY;
+          }
+          // the row maximum of the raw scores, as a tree (scale > 0 keeps the order)
+          float mx;
+          {
+            float t[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) t[i] = sv[i];
+            for (int i = 0; i < 8; ++i) t[i] = sv[i];
 #pragma unroll
-          for (int j = 8; j < kKeys; ++j) t[j & 7] = fmaxf(t[j & 7], sv[j]);
-          mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7]))) * sl2;
-        }
-        float corr = 1.f;
-        const bool move = mx > m + 8.f;
-        if (move) {
-          corr = m == -INFINITY ? 0.f : exp2f(m - mx);
-          m = mx;
-          l *= corr;
-        }
-        // P over the row's S columns, 16 keys at a time: the 16 columns of keys 16 k ..
-        // 16 k + 15 become 8 columns of high parts (then, for bf16, 8 of low parts)
-        {
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 8; j < kKeys; ++j) t[j & 7] = fmaxf(t[j & 7], sv[j]);
+            mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7]))) * sl2;
+          }
+          float corr = 1.f;
+          const bool move = mx > m + 8.f;
+          if (move) {
+            corr = m == -INFINITY ? 0.f : exp2f(m - mx);
+            m = mx;
+            l *= corr;
+          }
+          // P over the row's S columns, 16 keys at a time: the 16 columns of keys 16 k ..
+          // 16 k + 15 become 8 columns of high parts (then, for bf16, 8 of low parts)
+          {
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int k = 0; k < kKeys / 16; ++k) {
-            uint32_t blk[8 * kParts];
+            for (int k2 = 0; k2 < kKeys / 16; ++k2) {
+              uint32_t blk[8 * kParts];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
-              const float x0 = ex2(fmaf(sv[16 * k + 2 * j], sl2, -m)), x1 = ex2(fmaf(sv[16 * k + 2 * j + 1], sl2, -m));
-              ps[j & 3] += x0 + x1;
-              blk[j] = pack2<T>(x0, x1);
-              if constexpr (kParts == 2) {
-                const float2 back = unpack2<T>(blk[j]);
-                blk[8 + j] = pack2<T>(x0 - back.x, x1 - back.y);
+              for (int j = 0; j < 8; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
+                const float x0 = ex2(fmaf(sv[16 * k2 + 2 * j], sl2, -m)), x1 = ex2(fmaf(sv[16 * k2 + 2 * j + 1], sl2, -m));
+                ps[j & 3] += x0 + x1;
+                blk[j] = pack2<T>(x0, x1);
+                if constexpr (kParts == 2) {
+                  const float2 back = unpack2<T>(blk[j]);
+                  blk[8 + j] = pack2<T>(x0 - back.x, x1 - back.y);
+                }
+              }
+              if constexpr (kParts == 2) st16(t_s + 16 * k2, blk);
+              else st8(t_s + 16 * k2, blk);
+            }
+            wait_st();
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          }
+          // O holds P V up to chunk c - 1, finished (S(c) was issued after it): rescale the
+          // row if the maximum moved (the whole warp takes the branch when one of its rows
+          // needs it; the others scale by 1)
+          const bool rescale = c > 0 && move && corr != 1.f;
+          if (__any_sync(0xffffffffu, rescale)) {
+            const float f = rescale ? corr : 1.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              float o[32];
+              ld32(t_o + c0, o);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] *= f;
+              st32(t_o + c0, o);
+            }
+          }
+          // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as
+          // zero; tile A's threads clear it before either tile's P V of the chunk is issued
+          if (X == 0 && c == U.nchunks - 1 && kz < (c + 1) * kKeys) {
+            const int gc = g + c;
+            if (!(ok = __all_sync(0xffffffffu, wait(&fullv[gc % kVStages], (gc / kVStages) & 1)))) break;
+            // block b's tile [D][bs]: dim d's keys 8 g .. 8 g + 7 are the 16 bytes at d * 2 bs + 16 g
+            // within the row, moved by the swizzle (16-byte unit bits xor'ed with bits 7 and up)
+            unsigned char* vbase = smem + Sh::kOffV + (gc % kVStages) * Sh::kVBytes;
+            constexpr int kRow = 2 * BS, kUnits = kRow / 16;
+            const int k0 = kz - c * kKeys;  // first key to clear (0 <= k0 < kKeys)
+            const int g0 = k0 / 8;          // the 8-key group holding it
+            for (int i = tid; i < (kKeys / 8 - g0) * D; i += kSoftmaxThreads) {
+              const int g8 = g0 + i / D, d = i % D;  // keys 8 g8 .. 8 g8 + 7 of dim d
+              const int a = d * kRow + ((8 * g8) % BS) * 2;
+              unsigned char* ptr = vbase + ((8 * g8) / BS) * Sh::kTile + (a ^ (((a >> 7) & (kUnits - 1)) << 4));
+              if (8 * g8 >= k0) {
+                *reinterpret_cast<uint4*>(ptr) = make_uint4(0, 0, 0, 0);
+              } else {
+                for (int kk = k0 - 8 * g8; kk < 8; ++kk) *reinterpret_cast<T*>(ptr + 2 * kk) = DType<T>::from_f32(0.f);
               }
             }
-            if constexpr (kParts == 2) st16(t_s + 16 * k, blk);
-            else st8(t_s + 16 * k, blk);
+            fence_proxy_async_smem();
           }
-          wait_st();
-          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          fence_before();
+          mbar_arrive(pfull(X));
         }
-        // O holds P V up to chunk c - 1, finished (S(c) was issued after it): rescale the
-        // row if the maximum moved (the whole warp takes the branch when one of its rows
-        // needs it; the others scale by 1)
-        const bool rescale = c > 0 && move && corr != 1.f;
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? corr : 1.f;
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            float o[32];
-            ld32(t_o + c0, o);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] *= f;
-            st32(t_o + c0, o);
-          }
-        }
-        // the last chunk: V of keys past the sequence (or past the blocks loaded) reads as
-        // zero; tile A's threads clear it before either tile's P V of the chunk is issued
-        if (X == 0 && c == nchunks - 1 && kz < (c + 1) * kKeys) {
-          if (!__all_sync(0xffffffffu, wait(&fullv[c % kVStages], (c / kVStages) & 1))) {
-            ok = false;
-            break;
-          }
-          // block b's tile [D][bs]: dim d's keys 8 g .. 8 g + 7 are the 16 bytes at d * 2 bs + 16 g
-          // within the row, moved by the swizzle (16-byte unit bits xor'ed with bits 7 and up)
-          unsigned char* vbase = smem + Sh::kOffV + (c % kVStages) * Sh::kVBytes;
-          constexpr int kRow = 2 * BS, kUnits = kRow / 16;
-          const int k0 = kz - c * kKeys;  // first key to clear (0 <= k0 < kKeys)
-          const int g0 = k0 / 8;          // the 8-key group holding it
-          for (int i = tid; i < (kKeys / 8 - g0) * D; i += kSoftmaxThreads) {
-            const int g = g0 + i / D, d = i % D;  // keys 8 g .. 8 g + 7 of dim d
-            const int a = d * kRow + ((8 * g) % BS) * 2;
-            unsigned char* u = vbase + ((8 * g) / BS) * Sh::kTile + (a ^ (((a >> 7) & (kUnits - 1)) << 4));
-            if (8 * g >= k0) {
-              *reinterpret_cast<uint4*>(u) = make_uint4(0, 0, 0, 0);
-            } else {
-              for (int k = k0 - 8 * g; k < 8; ++k) *reinterpret_cast<T*>(u + 2 * k) = DType<T>::from_f32(0.f);
-            }
-          }
-          fence_proxy_async_smem();
-        }
-        fence_before();
-        mbar_arrive(pfull(X));
-      }
-      if (__all_sync(0xffffffffu, ok && wait(pvdone(X), 0))) {  // one phase: the last P V
+        if (!ok) break;
+        if (un.x >= 0 && N.ntiles > X) q_landed();  // the next unit's first S_X may go
+        // the unit's output: O / l, read out of TMEM (then the columns are free for the
+        // next unit's P V), rounded to T, stored as the row's D contiguous elements
+        if (!(ok = __all_sync(0xffffffffu, wait(pvdone(X), ux & 1)))) break;
         fence_after();
         const float inv = 1.f / l;
-        T* out = static_cast<T*>(p.out) +
-                 ((long long)(tok0 + (valid ? row / G : 0)) * p.num_heads + (long long)kvh * G + (valid ? row % G : 0)) *
-                     D;
+        uint32_t o16[D / 2];
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
           ld32(t_o + c0, o);
-          if (valid) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 w;
-              w.x = pack2<T>(o[j] * inv, o[j + 1] * inv);
-              w.y = pack2<T>(o[j + 2] * inv, o[j + 3] * inv);
-              w.z = pack2<T>(o[j + 4] * inv, o[j + 5] * inv);
-              w.w = pack2<T>(o[j + 6] * inv, o[j + 7] * inv);
-              *reinterpret_cast<uint4*>(out + c0 + j) = w;
-            }
-          }
+          for (int j = 0; j < 32; j += 2) o16[(c0 + j) / 2] = pack2<T>(o[j] * inv, o[j + 1] * inv);
         }
+        fence_before();
+        mbar_arrive(ofree(X));
+        if (valid) {
+          T* out = static_cast<T*>(p.out) +
+                   ((long long)(U.tok0 + row / G) * p.num_heads + (long long)U.kvh * G + row % G) * D;
+#pragma unroll
+          for (int j = 0; j < D / 8; ++j)
+            reinterpret_cast<uint4*>(out)[j] = make_uint4(o16[4 * j], o16[4 * j + 1], o16[4 * j + 2], o16[4 * j + 3]);
+        }
+        ++ux;
+      } else {  // no rows of this tile in the unit: only the next unit's Q
+        next();
+        if (!ok) break;
+        if (un.x >= 0 && N.ntiles > X) q_landed();
       }
+      g += U.nchunks;
+      u = un;
+      U = N;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no Q copy lands after the CTA exits
   } else if (warp == kCopyWarp) {
-    // ================= copies of chunk c (warp 8): K gathers, then V boxes =================
-    // This CTA issues its half of the chunk's copies, each into both CTAs of the
+    // ================= copies (warp 8): K gathers, then V boxes, chunk after chunk of each unit =================
+    // This CTA issues its half of each chunk's copies, each into both CTAs of the
     // cluster: lane i the gather4 load crank * kGathers / 2 + i of K (8-dim slice dc,
     // keys 64 h .. 64 h + 63), lane b the V box of the chunk's block b when b % 2 is
-    // its rank.  Each CTA's full barriers expect the whole chunk.
+    // its rank.  Each CTA's full barriers expect the whole chunk.  Buffer positions run
+    // on over the units (g counts the chunks of all units so far).
     constexpr int kGathers = (D / 8) * (kKeys / 64), kMine = kGathers / kCluster;
     static_assert(kGathers <= 32 && Sh::kBlocks <= 32 && kGathers % kCluster == 0, "one copy per lane");
-    const int32_t* bt = p.block_tables + (long long)s * p.max_blocks_per_seq;
-    auto phys_of = [&](int c) {  // lane b: the physical block of the chunk's block b (-1 past the keys)
-      const int gb = c * Sh::kBlocks + lane;
-      return lane < Sh::kBlocks && gb < nblk ? __ldg(bt + gb) : -1;
-    };
     const int gi = static_cast<int>(crank) * kMine + lane;  // this lane's gather (lanes < kMine)
     const int dc = gi / (kKeys / 64), h = gi % (kKeys / 64);
-    int ph = phys_of(0);  // the next chunk's table entries land while a chunk is in flight
     bool ok = true;
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int kb = c % kKStages, vb = c % kVStages;
-      const bool live = lane < Sh::kBlocks && c * Sh::kBlocks + lane < nblk;
-      const bool bad = ph < 0 || ph >= p.num_blocks;
-      if (live && bad) set_error(p.err, kErrBlockId);
-      const int ph0 = __shfl_sync(0xffffffffu, bad ? 0 : ph, 0);  // block 0 of a chunk always holds keys
-      // a block past the keys: any rows do (S there is masked; its V is not copied)
-      const long long tl = (long long)(live ? (bad ? 0 : ph) : ph0) * p.num_kv_heads + kvh;
-      const int nlive = __popc(__ballot_sync(0xffffffffu, live));
-      int rw[4];
+    int g = 0;
+    for (int k = 0; ok; ++k) {
+      int4 u;
+      if (!(ok = take_unit(k, u)) || u.x < 0) break;
+      const UnitView U = unit_view<BS>(p, u, crank);
+      const int32_t* bt = p.block_tables + (long long)U.s * p.max_blocks_per_seq;
+      auto phys_of = [&](int c) {  // lane b: the physical block of the chunk's block b (-1 past the keys)
+        const int gb = c * Sh::kBlocks + lane;
+        return lane < Sh::kBlocks && gb < U.nblk ? __ldg(bt + gb) : -1;
+      };
+      int ph = phys_of(0);  // the next chunk's table entries land while a chunk is in flight
+      for (int c = 0; c < U.nchunks; ++c) {
+        const int gc = g + c, kb = gc % kKStages, vb = gc % kVStages;
+        const bool live = lane < Sh::kBlocks && c * Sh::kBlocks + lane < U.nblk;
+        const bool bad = ph < 0 || ph >= p.num_blocks;
+        if (live && bad) set_error(p.err, kErrBlockId);
+        const int ph0 = __shfl_sync(0xffffffffu, bad ? 0 : ph, 0);  // block 0 of a chunk always holds keys
+        // a block past the keys: any rows do (S there is masked; its V is not copied)
+        const long long tl = (long long)(live ? (bad ? 0 : ph) : ph0) * p.num_kv_heads + U.kvh;
+        const int nlive = __popc(__ballot_sync(0xffffffffu, live));
+        int rw[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {  // the rows (16 keys each) of this lane's 64 keys
-        const int key = 64 * h + 16 * q;
-        const long long tb = __shfl_sync(0xffffffffu, tl, key / BS);
-        rw[q] = static_cast<int>((tb * (D / 8) + dc) * (BS / 16) + (key % BS) / 16);
+        for (int q = 0; q < 4; ++q) {  // the rows (16 keys each) of this lane's 64 keys
+          const int key = 64 * h + 16 * q;
+          const long long tb = __shfl_sync(0xffffffffu, tl, key / BS);
+          rw[q] = static_cast<int>((tb * (D / 8) + dc) * (BS / 16) + (key % BS) / 16);
+        }
+        if (gc >= kKStages &&  // both CTAs' S read the buffer (in both CTAs)
+            !(ok = __all_sync(0xffffffffu, wait(&kfree[kb], ((gc - kKStages) / kKStages) & 1))))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(&fullk[kb], Sh::kKBytes);
+        __syncwarp();
+        if (lane < kMine)  // lands as [64 keys][8 dims] in the slice's rows, in both CTAs
+          tma_gather4_mc(smem + Sh::kOffK + kb * Sh::kKBytes + dc * (kKeys * 16) + h * (64 * 16), &tmap_k, rw,
+                         &fullk[kb], kClusterMask);
+        issued_k = gc + 1;
+        if (gc >= kVStages &&  // both CTAs' P V read the buffer (in both CTAs)
+            !(ok = __all_sync(0xffffffffu, wait(&vfree[vb], ((gc - kVStages) / kVStages) & 1))))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(&fullv[vb], nlive * Sh::kTile);
+        __syncwarp();
+        if (live && lane % kCluster == static_cast<int>(crank))  // the (block, kv head) tile [D][bs], swizzled;
+          tma_2d_mc(smem + Sh::kOffV + vb * Sh::kVBytes + lane * Sh::kTile, &tmap_v, 0,  // V past the keys is zeroed
+                    static_cast<int>(tl * D), &fullv[vb], kClusterMask);                // by the softmax threads
+        issued_v = gc + 1;
+        ph = phys_of(c + 1);
       }
-      if (c >= kKStages &&  // both CTAs' S read the buffer (in both CTAs)
-          !(ok = __all_sync(0xffffffffu, wait(&kfree[kb], ((c - kKStages) / kKStages) & 1))))
+      g += U.nchunks;
+    }
+  } else if (warp == kSchedWarp) {
+    // ================= the unit ring (warp 10): this cluster's units, in rank order =================
+    // Rank cid, cid + clusters, ..: the longest units are spread over the clusters first.
+    // Both CTAs of a cluster write the same sequence; a unit with x < 0 ends it.
+    int longest = 0;
+    const long long total = build_seq_table(p, tab, &longest);
+    const long long cid = blockIdx.x / kCluster, ncl = gridDim.x / kCluster;
+    for (int k = 0;; ++k) {
+      const long long rank = cid + k * ncl;
+      int3 t = make_int3(-1, 0, 0);
+      if (rank < total) t = pick_unit(p, tab, rank, longest);
+      const int slot = k % kUnitSlots;
+      if (k >= kUnitSlots && !__all_sync(0xffffffffu, wait(&uempty[slot], ((k - kUnitSlots) / kUnitSlots) & 1)))
         break;
-      if (lane == 0) mbar_arrive_expect_tx(&fullk[kb], Sh::kKBytes);
+      if (lane == 0) {
+        s_unit[4 * slot] = t.x;
+        s_unit[4 * slot + 1] = t.y;
+        s_unit[4 * slot + 2] = t.z;
+        mbar_arrive(&ufull[slot]);  // release: the slot's words before the phase completes
+      }
       __syncwarp();
-      if (lane < kMine)  // lands as [64 keys][8 dims] in the slice's rows, in both CTAs
-        tma_gather4_mc(smem + Sh::kOffK + kb * Sh::kKBytes + dc * (kKeys * 16) + h * (64 * 16), &tmap_k, rw,
-                       &fullk[kb], kClusterMask);
-      issued_k = c + 1;
-      if (c >= kVStages &&  // both CTAs' P V read the buffer (in both CTAs)
-          !(ok = __all_sync(0xffffffffu, wait(&vfree[vb], ((c - kVStages) / kVStages) & 1))))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(&fullv[vb], nlive * Sh::kTile);
-      __syncwarp();
-      if (live && lane % kCluster == static_cast<int>(crank))  // the (block, kv head) tile [D][bs], swizzled;
-        tma_2d_mc(smem + Sh::kOffV + vb * Sh::kVBytes + lane * Sh::kTile, &tmap_v, 0,  // V past the keys is zeroed
-                  static_cast<int>(tl * D), &fullv[vb], kClusterMask);                // by the softmax threads
-      issued_v = c + 1;
-      ph = phys_of(c + 1);
+      if (t.x < 0) break;
     }
   } else {
-    // ================= MMAs (warp 9): P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1) =================
+    // ================= MMAs (warp 9): per unit S_X(0), then per chunk P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1) =================
     // The whole warp runs the loop and the waits (so the loop state and the descriptors
-    // stay warp-uniform); one elected lane issues the MMAs and the commits.
-    // A CTA without rows (the unit's second pair missing) still frees each buffer
+    // stay warp-uniform); one elected lane issues the MMAs and the commits.  A CTA
+    // without rows in a unit (the unit's second pair missing) still frees each buffer
     // for its partner: it commits to the free barriers of both CTAs with no MMA before.
     constexpr uint32_t kIdS = idesc<T>(kRows, kKeys), kIdO = idesc<T>(kRows, D);
     const bool leader = elect_one();
@@ -668,68 +777,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_bar = bar;
       last_par = parity;
     };
-    auto issue_s = [&](int Xm, int c) {  // S_X(c) = Q_X K(c)^T into X's S columns
+    int cx[2] = {0, 0}, ux[2] = {0, 0};  // per tile: chunks (S, P V) and units it had rows in
+    auto issue_s = [&](int Xm, int gc) {  // S_X = Q_X K(gc)^T into X's S columns
       if (leader) {
-        const uint64_t da = dq0 + Xm * (Sh::kQTile >> 4), db = dk0 + (c % kKStages) * (Sh::kKBytes >> 4);
+        const uint64_t da = dq0 + Xm * (Sh::kQTile >> 4), db = dk0 + (gc % kKStages) * (Sh::kKBytes >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma(tmem + 256 * Xm, da + ks * 16, db + ks * (2 * kKeys), kIdS, ks > 0);
       }
-      commit_to(sfull(Xm), c & 1);
+      commit_to(sfull(Xm), cx[Xm] & 1);
     };
-    auto issue_pv = [&](int Xm, int c) {  // O_X += P_X(c) V(c): high parts, then low parts
+    auto issue_pv = [&](int Xm, int gc, bool first) {  // O_X (+)= P_X V(gc): high parts, then low parts
       if (leader) {
-        const uint64_t db = dv0 + (c % kVStages) * (Sh::kVBytes >> 4);
+        const uint64_t db = dv0 + (gc % kVStages) * (Sh::kVBytes >> 4);
         const uint32_t tb = tmem + 256 * Xm;
 #pragma unroll
         for (int part = 0; part < kParts; ++part) {
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)  // keys 16 kk ..: high parts in 8 columns, low in the next 8
             mma_ts(tb + kKeys, tb + 16 * kk + 8 * part,
-                   db + (((16 * kk) / BS) * Sh::kTile + ((16 * kk) % BS) * 2) / 16, kIdO, c > 0 || part > 0 || kk > 0);
+                   db + (((16 * kk) / BS) * Sh::kTile + ((16 * kk) % BS) * 2) / 16, kIdO, !first || part > 0 || kk > 0);
         }
       }
-      if (c == nchunks - 1) commit_to(pvdone(Xm), 0);  // O_X is complete
     };
     // the timeout-path test: the first wait runs out on `never` (no MMA issued yet);
     // the producer then drains its copies with the normal limit
     bool ok = __all_sync(0xffffffffu, !p.test_wait_ns || wait_or_abort(never, 0, s_abort, p.err, p.test_wait_ns));
-    if (ok && (ok = wait_all(&fullk[0], 0))) {
-      fence_after();
-      for (int Xm = 0; Xm < ntiles; ++Xm) issue_s(Xm, 0);
-      commit_to(&kfree[0], 0, true);
-    }
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int vb = c % kVStages, c1 = c + 1;
-      if (!(ok = wait_all(&fullv[vb], (c / kVStages) & 1))) break;
-      for (int Xm = 0; Xm < ntiles && ok; ++Xm) {
-        if (!(ok = wait_all(pfull(Xm), c & 1))) break;  // the softmax wrote P_X(c)
+    int g = 0;  // chunks of all units so far
+    for (int k = 0; ok; ++k) {
+      int4 u;
+      if (!(ok = take_unit(k, u)) || u.x < 0) break;
+      const UnitView U = unit_view<BS>(p, u, crank);
+      const int nt = U.ntiles, nc = U.nchunks;
+      // S of the unit's first chunk, for each tile as soon as its Q has landed (the
+      // previous unit's P V run ahead of it on the tensor cores)
+      if (!(ok = wait_all(&fullk[g % kKStages], (g / kKStages) & 1))) break;
+      for (int Xm = 0; Xm < nt && ok; ++Xm) {
+        if (!(ok = wait_all(qfull(Xm), ux[Xm] & 1))) break;
         fence_after();
-        issue_pv(Xm, c);
-        if (Xm == ntiles - 1) commit_to(&vfree[vb], (c / kVStages) & 1, true);
-        if (c1 < nchunks) {
-          if (Xm == 0 && !(ok = wait_all(&fullk[c1 % kKStages], (c1 / kKStages) & 1))) break;
-          // S_X(c + 1) overwrites the columns P V_X(c) reads, issued right behind it: MMAs
-          // of one thread run in issue order, so no wait is needed between the two
+        issue_s(Xm, g);
+      }
+      if (!ok) break;
+      commit_to(&kfree[g % kKStages], (g / kKStages) & 1, true);
+      for (int c = 0; c < nc && ok; ++c) {
+        const int gc = g + c, vb = gc % kVStages, g1 = gc + 1;
+        if (!(ok = wait_all(&fullv[vb], (gc / kVStages) & 1))) break;
+        for (int Xm = 0; Xm < nt && ok; ++Xm) {
+          if (!(ok = wait_all(pfull(Xm), cx[Xm] & 1))) break;  // the softmax wrote P_X(c)
+          // the first P V of a unit overwrites O_X: the previous unit's O_X is read out
+          if (c == 0 && ux[Xm] > 0 && !(ok = wait_all(ofree(Xm), (ux[Xm] - 1) & 1))) break;
           fence_after();
-          issue_s(Xm, c1);
-          if (Xm == ntiles - 1) commit_to(&kfree[c1 % kKStages], (c1 / kKStages) & 1, true);
+          issue_pv(Xm, gc, c == 0);
+          if (Xm == nt - 1) commit_to(&vfree[vb], (gc / kVStages) & 1, true);
+          if (c == nc - 1) commit_to(pvdone(Xm), ux[Xm] & 1);  // O_X is complete
+          ++cx[Xm];
+          if (c + 1 < nc) {
+            if (Xm == 0 && !(ok = wait_all(&fullk[g1 % kKStages], (g1 / kKStages) & 1))) break;
+            // S_X(c + 1) overwrites the columns P V_X(c) reads, issued right behind it: MMAs
+            // of one thread run in issue order, so no wait is needed between the two
+            fence_after();
+            issue_s(Xm, g1);
+            if (Xm == nt - 1) commit_to(&kfree[g1 % kKStages], (g1 / kKStages) & 1, true);
+          }
+        }
+        if (nt == 0 && ok) {  // no rows: free the buffers for the partner as they land
+          commit_to(&vfree[vb], (gc / kVStages) & 1, true);
+          if (c + 1 < nc) {
+            if (!(ok = wait_all(&fullk[g1 % kKStages], (g1 / kKStages) & 1))) break;
+            commit_to(&kfree[g1 % kKStages], (g1 / kKStages) & 1, true);
+          }
         }
       }
-      if (ntiles == 0 && ok) {  // no rows: free the buffers for the partner as they land
-        commit_to(&vfree[vb], (c / kVStages) & 1, true);
-        if (c1 < nchunks) {
-          if (!(ok = wait_all(&fullk[c1 % kKStages], (c1 / kKStages) & 1))) break;
-          commit_to(&kfree[c1 % kKStages], (c1 / kKStages) & 1, true);
-        }
-      }
+      for (int Xm = 0; Xm < nt; ++Xm) ++ux[Xm];
+      g += nc;
     }
     // The partner's last commits arrive on this CTA's free barriers: wait (bounded) for
     // their final phases, so nothing lands in this CTA's shared memory after it exits.
     if (ok) {
-      for (int c = max(0, nchunks - kKStages); c < nchunks; ++c)
+      for (int c = max(0, g - kKStages); c < g; ++c)
         mbar_wait_bounded(&kfree[c % kKStages], (c / kKStages) & 1, kWaitNs / 8);
-      for (int c = max(0, nchunks - kVStages); c < nchunks; ++c)
+      for (int c = max(0, g - kVStages); c < g; ++c)
         mbar_wait_bounded(&vfree[c % kVStages], (c / kVStages) & 1, kWaitNs / 8);
     }
     // MMAs committed but maybe not finished: a commit tracks every earlier MMA of the
