@@ -130,7 +130,8 @@ cudaError_t launch_prefill_ws_t(const PrefillParams& p, cudaStream_t stream, int
   const long long units = (long long)p.num_kv_heads * (((long long)p.num_query_tokens * p.group + ws::kUnitTiles * ws::kRows - 1) /
                                                            (ws::kUnitTiles * ws::kRows) +
                                                        p.num_seqs);
-  const long long clusters = units < clusters_resident ? units : clusters_resident;
+  long long clusters = units < clusters_resident ? units : clusters_resident;
+  if (clusters > 32 * ws::kLoadsPerLane) clusters = 32 * ws::kLoadsPerLane;  // the scheduler's table of loads
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * ws::kCluster));
   cfg.blockDim = dim3(ws::kThreads);

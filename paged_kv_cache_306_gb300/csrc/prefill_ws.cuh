@@ -17,9 +17,10 @@
 // its Q and its first S overlap the previous unit's last chunk and its output.
 // The phases run in different warps that hand over through mbarriers:
 //
-//   * warp 10: the unit ring.  It works out this cluster's units (ranks cid,
-//     cid + clusters, ..: see pick_unit) up to four ahead; each is read by
-//     every other warp.
+//   * warp 10: the unit ring.  It replays a greedy assignment of all units,
+//     longest first, each to the cluster with the least work so far, and puts
+//     this cluster's units into a ring up to four ahead; each is read by every
+//     other warp.
 //   * warp 8: the TMA copies of chunk c (counted over all units), K into K buffer
 //     c % 2 once both tiles' S of chunk c - 2 have read it, V into V buffer c % 2
 //     once both tiles' P V of chunk c - 2 have read it, each on its own mbarrier.  K: the pool seen as rows
@@ -91,6 +92,9 @@ constexpr int kThreads = 11 * 32;
 // The unit ring: the scheduler warp writes up to kUnitSlots units ahead; each is
 // read by the 8 softmax warps, the copy warp and the MMA warp.
 constexpr int kUnitSlots = 4, kUnitReaders = 10;
+constexpr int kLoadsPerLane = 4;  // the scheduler's greedy assignment: up to 128 clusters
+// A unit's fixed cost in chunk periods (its first S and its output; measured ~2.8)
+constexpr int kUnitCost = 3;
 constexpr int kKStages = 2, kVStages = 2;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -241,12 +245,11 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // The per-sequence figures unit selection needs, in shared memory (3 kMaxSeqsPerLaunch
 // ints): ctx = tokens before the chunk, rows = its n G query rows, and its tiles.
 // One warp fills it once per CTA (lane i: sequences i, i + 32, ..) and checks the
-// lengths; returns the number of units of the launch (all kv heads) and, in
-// *longest, the most chunks any unit reads.
-__device__ long long build_seq_table(const PrefillParams& p, int* tab, int* longest_out) {
+// lengths; returns the most chunks any unit reads.
+__device__ int build_seq_table(const PrefillParams& p, int* tab) {
   const int lane = threadIdx.x & 31, G = p.group, S = p.num_seqs;
   bool bad = false;
-  int units = 0, longest = 0;
+  int longest = 0;
   for (int s = lane; s < S; s += 32) {
     const int L = __ldg(p.seq_lens + s), a = __ldg(p.query_start_loc + s), b = __ldg(p.query_start_loc + s + 1);
     const int n = b - a;
@@ -261,85 +264,27 @@ __device__ long long build_seq_table(const PrefillParams& p, int* tab, int* long
     tab[s] = ctx;
     tab[kMaxSeqsPerLaunch + s] = rows;
     tab[2 * kMaxSeqsPerLaunch + s] = nt;
-    units += (nt + kUnitTiles - 1) / kUnitTiles;
     if (nt) longest = max(longest, (ctx + (rows - 1) / G) / kKeys + 1);
   }
   if (bad && blockIdx.x == 0) set_error(p.err, kErrSeqLen);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    units += __shfl_xor_sync(0xffffffffu, units, o);
-    longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
-  }
+  for (int o = 16; o > 0; o >>= 1) longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
   __syncwarp();
-  *longest_out = longest;
-  return (long long)p.num_kv_heads * units;
+  return longest;
 }
 
-// The unit of rank `rank` (0-based) in the order of decreasing length -- the chunks
-// of keys it reads -- ties by sequence, kv head and unit index; so the longest
-// units of the whole launch are taken first and the short ones fill the tail.  A
-// unit is kUnitTiles consecutive tiles of one (sequence, kv head), the work of one
-// cluster.  Tile j of sequence s covers rows 128 j .. of its n * G rows and reads
-// chunks 0 .. (ctx + (row_hi - 1) / G) / 128, non-decreasing in j; unit k holds tiles
-// kUnitTiles k .. (those that exist) and reads what its last tile reads.  So the
-// tiles of s reading >= x chunks are a suffix j >= j0 in closed form, the units
-// reading >= x are those from j0 / kUnitTiles on, and the rank-th unit is found by a
-// binary search on x.  One warp, on the table of build_seq_table (every count a warp
-// sum); rank must be below the launch's `total` units.  Returns (sequence, kv head,
-// unit) in every lane.
-__device__ int3 pick_unit(const PrefillParams& p, const int* tab, long long rank, int longest) {
-  const int lane = threadIdx.x & 31, G = p.group, Hkv = p.num_kv_heads, S = p.num_seqs;
-  const int* t_ctx = tab;
-  const int* t_rows = tab + kMaxSeqsPerLaunch;
-  const int* t_nt = tab + 2 * kMaxSeqsPerLaunch;
-  auto cnt = [&](int s, int x) -> int {  // units of sequence s that read >= x chunks
-    const int nt = t_nt[s], rows = t_rows[s];
-    const long long need = (long long)G * ((long long)kKeys * (x - 1) - t_ctx[s]) + 1;  // rows a tile must reach
-    if (nt == 0 || need > rows) return 0;
-    const int j0 = need <= 1 ? 0 : static_cast<int>((need + kRows - 1) / kRows - 1);  // first tile reading >= x
-    return (nt + kUnitTiles - 1) / kUnitTiles - j0 / kUnitTiles;
-  };
-  auto count = [&](int x) {  // units of the launch (all kv heads) reading >= x chunks
-    int v = 0;
-    for (int s = lane; s < S; s += 32) v += cnt(s, x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return (long long)Hkv * v;
-  };
-  int lo = 1, hi = longest;  // count(lo) > rank
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) / 2;
-    if (count(mid) > rank) lo = mid;
-    else hi = mid - 1;
-  }
-  // rank among the units of exactly lo chunks, ordered by (sequence, kv head, unit):
-  // sequences in rounds of 32, an inclusive scan over the lanes within a round
-  long long r = rank - count(lo + 1);
-  int3 u = make_int3(0, 0, 0);
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    const int s = s0 + lane;
-    const int e = s < S ? cnt(s, lo) - cnt(s, lo + 1) : 0;
-    int incl = e;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const long long before = (long long)Hkv * (incl - e), span = (long long)Hkv * e;
-    const bool here = e > 0 && r >= before && r < before + span;
-    const unsigned who = __ballot_sync(0xffffffffu, here);
-    if (who) {
-      const int src = __ffs(who) - 1;
-      const int q = static_cast<int>(r - before);
-      const int3 mine = make_int3(s, here ? q / e : 0, here ? (t_nt[s] + kUnitTiles - 1) / kUnitTiles - cnt(s, lo) + q % e : 0);
-      u.x = __shfl_sync(0xffffffffu, mine.x, src);
-      u.y = __shfl_sync(0xffffffffu, mine.y, src);
-      u.z = __shfl_sync(0xffffffffu, mine.z, src);
-      break;
-    }
-    r -= (long long)Hkv * __shfl_sync(0xffffffffu, incl, 31);
-  }
-  return u;
+// Units of sequence s (per kv head) that read >= x chunks of keys, from the table of
+// build_seq_table.  Tile j of s covers rows 128 j .. of its n G rows and reads chunks
+// 0 .. (ctx + (row_hi - 1) / G) / 128, non-decreasing in j; a unit holds kUnitTiles
+// consecutive tiles (those that exist) and reads what its last tile reads.  So the
+// tiles reading >= x chunks are a suffix j >= j0 in closed form, and the units
+// reading >= x are the last ones, from j0 / kUnitTiles on.
+__device__ __forceinline__ int units_reading(const int* tab, int G, int s, int x) {
+  const int ctx = tab[s], rows = tab[kMaxSeqsPerLaunch + s], nt = tab[2 * kMaxSeqsPerLaunch + s];
+  const long long need = (long long)G * ((long long)kKeys * (x - 1) - ctx) + 1;  // rows a tile must reach
+  if (nt == 0 || need > rows) return 0;
+  const int j0 = need <= 1 ? 0 : static_cast<int>((need + kRows - 1) / kRows - 1);  // first tile reading >= x
+  return (nt + kUnitTiles - 1) / kUnitTiles - j0 / kUnitTiles;
 }
 
 template <typename T, int D, int BS>
@@ -728,28 +673,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       g += U.nchunks;
     }
   } else if (warp == kSchedWarp) {
-    // ================= the unit ring (warp 10): this cluster's units, in rank order =================
-    // Rank cid, cid + clusters, ..: the longest units are spread over the clusters first.
-    // Both CTAs of a cluster write the same sequence; a unit with x < 0 ends it.
-    int longest = 0;
-    const long long total = build_seq_table(p, tab, &longest);
-    const long long cid = blockIdx.x / kCluster, ncl = gridDim.x / kCluster;
-    for (int k = 0;; ++k) {
-      const long long rank = cid + k * ncl;
-      int3 t = make_int3(-1, 0, 0);
-      if (rank < total) t = pick_unit(p, tab, rank, longest);
+    // ================= the unit ring (warp 10): this cluster's units =================
+    // Every cluster replays the same greedy assignment of all units of the launch:
+    // longest first (ties by sequence, kv head, unit), each to the cluster with the
+    // least work so far (ties to the lowest index), a unit's work being its chunks +
+    // kUnitCost;
+    // this cluster's units enter the ring in that order.  Both CTAs of a cluster write
+    // the same sequence; a unit with x < 0 ends it.
+    const int longest = build_seq_table(p, tab);
+    const int cid = blockIdx.x / kCluster, ncl = gridDim.x / kCluster;  // ncl <= 32 kLoadsPerLane
+    long long load[kLoadsPerLane];  // work of cluster lane + 32 i
+#pragma unroll
+    for (int i = 0; i < kLoadsPerLane; ++i) load[i] = lane + 32 * i < ncl ? 0 : LLONG_MAX;
+    int k = 0;
+    bool ok = true;
+    auto push = [&](int s, int kvh, int ui) {  // the next unit of this cluster into the ring
       const int slot = k % kUnitSlots;
-      if (k >= kUnitSlots && !__all_sync(0xffffffffu, wait(&uempty[slot], ((k - kUnitSlots) / kUnitSlots) & 1)))
-        break;
+      if (k >= kUnitSlots && !__all_sync(0xffffffffu, wait(&uempty[slot], ((k - kUnitSlots) / kUnitSlots) & 1))) {
+        ok = false;
+        return;
+      }
       if (lane == 0) {
-        s_unit[4 * slot] = t.x;
-        s_unit[4 * slot + 1] = t.y;
-        s_unit[4 * slot + 2] = t.z;
+        s_unit[4 * slot] = s;
+        s_unit[4 * slot + 1] = kvh;
+        s_unit[4 * slot + 2] = ui;
         mbar_arrive(&ufull[slot]);  // release: the slot's words before the phase completes
       }
       __syncwarp();
-      if (t.x < 0) break;
+      ++k;
+    };
+    const int S = p.num_seqs, Hkv = p.num_kv_heads;
+    for (int x = longest; x >= 1 && ok; --x) {
+      for (int s0 = 0; s0 < S && ok; s0 += 32) {  // lane i: sequence s0 + i's units of exactly x chunks
+        const int s = s0 + lane;
+        int e = 0, first = 0;
+        if (s < S) {
+          const int a = units_reading(tab, G, s, x), b = units_reading(tab, G, s, x + 1);
+          e = a - b;
+          first = (tab[2 * kMaxSeqsPerLaunch + s] + kUnitTiles - 1) / kUnitTiles - a;
+        }
+        for (unsigned m = __ballot_sync(0xffffffffu, e > 0); m && ok; m &= m - 1) {
+          const int src = __ffs(m) - 1;
+          const int ee = __shfl_sync(0xffffffffu, e, src), ff = __shfl_sync(0xffffffffu, first, src);
+          for (int kvh = 0; kvh < Hkv && ok; ++kvh)
+            for (int jj = 0; jj < ee && ok; ++jj) {
+              long long best = load[0];
+              int bi = lane;
+#pragma unroll
+              for (int i = 1; i < kLoadsPerLane; ++i)
+                if (load[i] < best) {
+                  best = load[i];
+                  bi = lane + 32 * i;
+                }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) {
+                const long long ob = __shfl_xor_sync(0xffffffffu, best, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ob < best || (ob == best && oi < bi)) {
+                  best = ob;
+                  bi = oi;
+                }
+              }
+              if (bi == cid) push(s0 + src, kvh, ff + jj);
+#pragma unroll
+              for (int i = 0; i < kLoadsPerLane; ++i)
+                if (bi == lane + 32 * i) load[i] += x + kUnitCost;
+            }
+        }
+      }
     }
+    if (ok) push(-1, 0, 0);
   } else {
     // ================= MMAs (warp 9): per unit S_X(0), then per chunk P V_A(c), S_A(c + 1), P V_B(c), S_B(c + 1) =================
     // The whole warp runs the loop and the waits (so the loop state and the descriptors
