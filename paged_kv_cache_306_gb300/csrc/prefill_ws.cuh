@@ -163,6 +163,35 @@ __device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&v)[8]) {
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Packed pairs of fp32 values (low = first) and the paired fp32 operations of sm_100+:
+// one instruction for both halves, each rounded as its scalar form
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return make_float2(a, b);
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// the largest of three (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 2^x by the hardware's approximate exponential (|relative error| below 2^-22; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -495,15 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < kKeys; ++j)
               if (j > lim) sv[j] = -INFINITY;
           }
-          // the row maximum of the raw scores, as a tree (scale > 0 keeps the order)
+          // the row maximum of the raw scores, as a tree of three-input maxima in 8 chains
+          // (scale > 0 keeps the order)
           float mx;
           {
+            static_assert(kKeys % 16 == 0, "8 chains, two keys a step");
             float t[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = sv[i];
+            for (int i = 0; i < 8; ++i) t[i] = fmaxf(sv[i], sv[8 + i]);
 #pragma unroll
-            for (int j = 8; j < kKeys; ++j) t[j & 7] = fmaxf(t[j & 7], sv[j]);
-            mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7]))) * sl2;
+            for (int j = 16; j < kKeys; j += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) t[i] = max3(t[i], sv[j + i], sv[j + 8 + i]);
+            mx = fmaxf(max3(t[0], t[1], t[2]), max3(max3(t[3], t[4], t[5]), t[6], t[7])) * sl2;
           }
           float corr = 1.f;
           const bool move = mx > m + 8.f;
@@ -515,14 +548,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P over the row's S columns, 16 keys at a time: the 16 columns of keys 16 k ..
           // 16 k + 15 become 8 columns of high parts (then, for bf16, 8 of low parts)
           {
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            // P = 2^(scale * s - m) (s = -inf gives 0): the scaling of a pair of scores and
+            // the row sums in paired fp32 operations
+            const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-m, -m);
+            uint64_t ps2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
             for (int k2 = 0; k2 < kKeys / 16; ++k2) {
               uint32_t blk[8 * kParts];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {  // P = 2^(scale * s - m), s = -inf gives 0
-                const float x0 = ex2(fmaf(sv[16 * k2 + 2 * j], sl2, -m)), x1 = ex2(fmaf(sv[16 * k2 + 2 * j + 1], sl2, -m));
-                ps[j & 3] += x0 + x1;
+              for (int j = 0; j < 8; ++j) {
+                const float2 y = f2unpack(fma2(f2pack(sv[16 * k2 + 2 * j], sv[16 * k2 + 2 * j + 1]), sl2x2, negm2));
+                const float x0 = ex2(y.x), x1 = ex2(y.y);
+                ps2[j & 1] = add2(ps2[j & 1], f2pack(x0, x1));
                 blk[j] = pack2<T>(x0, x1);
                 if constexpr (kParts == 2) {
                   const float2 back = unpack2<T>(blk[j]);
@@ -533,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               else st8(t_s + 16 * k2, blk);
             }
             wait_st();
-            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            const float2 s0 = f2unpack(ps2[0]), s1 = f2unpack(ps2[1]);
+            l += (s0.x + s0.y) + (s1.x + s1.y);
           }
           // O holds P V up to chunk c - 1, finished (S(c) was issued after it): rescale the
           // row if the maximum moved (the whole warp takes the branch when one of its rows
