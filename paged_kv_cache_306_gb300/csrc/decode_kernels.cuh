@@ -160,6 +160,15 @@ __device__ __forceinline__ void zero_tail_v(unsigned char* vtile, int rem, int l
 // kEarly (16-bit caches): block() is preceded by fetch(), which reads every K and
 // V fragment of the block out of the stage into registers, so the kernel can
 // refill the stage before the math instead of after it.
+// 2^x by the hardware's approximate exponential, one instruction (|relative error|
+// below 2^-22, results below 2^-126 flushed to 0, 2^-inf = 0): the P of a block and
+// the rescale factors, which are rounded to 16 bits (P) or enter fp32 sums
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T, typename TC, int D, int BS, int NH, bool kEarly>
 struct MmaMath {
   static constexpr int MT = BS / 16;  // 16-token tiles of a block
@@ -406,7 +415,7 @@ struct MmaMath {
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
         const float mn = fmaxf(m_[n][h], v);
         mref[n][h] = mn == -INFINITY ? 0.f : mn;
-        corr[n][h] = exp2f(m_[n][h] - mref[n][h]);
+        corr[n][h] = ex2_approx(m_[n][h] - mref[n][h]);
         m_[n][h] = mn;
       }
 #pragma unroll
@@ -415,7 +424,7 @@ struct MmaMath {
       for (int n = 0; n < NT; ++n) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          sc[mt][n][c] = exp2f(sc[mt][n][c] - mref[n][c & 1]);
+          sc[mt][n][c] = ex2_approx(sc[mt][n][c] - mref[n][c & 1]);
           ps[n][c & 1] += sc[mt][n][c];
         }
       }
