@@ -138,9 +138,9 @@ __device__ __forceinline__ void zero_tail_v(unsigned char* vtile, int rem, int l
 // row holds 16 bytes of dims of one token, a V-pool row the tokens of one dim);
 // Q^T stays in registers for the whole segment.  A kv head with at most 8 query
 // heads fills one 8-column tile, so no tensor-core work goes to padding rows.
-// P^T comes from S^T's accumulators through movmatrix (8x8 transposes), split
-// into a rounded 16-bit high part and the rounded remainder, so that P V keeps
-// ~16 significant bits.
+// P^T comes from S^T's accumulators through movmatrix (8x8 transposes): for bf16
+// operands split into a rounded high part and the rounded remainder, so that P V
+// keeps ~16 significant bits; for fp16 operands one rounded part (11 bits).
 //
 // T is the query / output type; TC is the cache element type: T itself (the
 // operands are then T), or FP8 E4M3.  An FP8 cache is widened in registers to
@@ -176,6 +176,10 @@ struct MmaMath {
   static constexpr bool kFp8 = sizeof(TC) == 1;
   using OT = std::conditional_t<kFp8, __half, T>;  // tensor-core operand type
   static constexpr bool kRescaleQ = kFp8 && !std::is_same<T, __half>::value;
+  // P^T in one rounded part for fp16 operands (11 significant bits, the operands' own
+  // precision); for bf16 a rounded high part and the rounded remainder (~16 bits),
+  // since one bf16 part (8 bits) can exceed the error bound on short sequences
+  static constexpr bool kSplitP = !std::is_same<OT, __half>::value;
   static_assert(!(kEarly && kFp8), "early release is for 16-bit caches");
   static constexpr bool kFetch = kEarly;
   static constexpr int FM = kEarly ? MT : 1, FK = kEarly ? KS : 1;
@@ -459,9 +463,11 @@ struct MmaMath {
           if (n >= NT) break;
           const float x = sc[kk][n][2 * r], y = sc[kk][n][2 * r + 1];
           const uint32_t hi = pack2<OT>(x, y);
-          const float2 back = unpack2<OT>(hi);
           bh[n][r] = movmatrix_trans(hi);
-          bl[n][r] = movmatrix_trans(pack2<OT>(x - back.x, y - back.y));
+          if constexpr (kSplitP) {
+            const float2 back = unpack2<OT>(hi);
+            bl[n][r] = movmatrix_trans(pack2<OT>(x - back.x, y - back.y));
+          }
         }
       if constexpr (kFp8) {
 #pragma unroll
@@ -474,8 +480,10 @@ struct MmaMath {
           for (int n = 0; n < NT; ++n) {
             mma_16816<OT>(acc[2 * dp][n], a0, bh[n][0], bh[n][1]);
             mma_16816<OT>(acc[2 * dp + 1][n], a1, bh[n][0], bh[n][1]);
-            mma_16816<OT>(acc[2 * dp][n], a0, bl[n][0], bl[n][1]);
-            mma_16816<OT>(acc[2 * dp + 1][n], a1, bl[n][0], bl[n][1]);
+            if constexpr (kSplitP) {
+              mma_16816<OT>(acc[2 * dp][n], a0, bl[n][0], bl[n][1]);
+              mma_16816<OT>(acc[2 * dp + 1][n], a1, bl[n][0], bl[n][1]);
+            }
           }
         }
       } else {
@@ -491,7 +499,7 @@ struct MmaMath {
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
             mma_16816<OT>(acc[dm][n], a, bh[n][0], bh[n][1]);
-            mma_16816<OT>(acc[dm][n], a, bl[n][0], bl[n][1]);
+            if constexpr (kSplitP) mma_16816<OT>(acc[dm][n], a, bl[n][0], bl[n][1]);
           }
         }
       }
