@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const uint32_t sq = smem_addr(smem + X * Sh::kQTile + (r / 8) * (D / 8) * 128 + (r % 8) * 16);
     // this thread's row of Q_X for unit v into shared memory: every 16-byte piece in
-    // flight at once, zeros for a padding row (completed by wait_q)
+    // flight at once, zeros for a padding row (completed and handed over by q_landed)
     auto load_q = [&](const UnitView& v) {
       const int row = v.pair_lo + X * kRows + r;
       const bool valid = row < v.pair_hi;
