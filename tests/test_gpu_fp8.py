@@ -137,6 +137,37 @@ def test_fp8_seq_len_one_returns_the_dequantised_v0_bit_exactly(q_dtype, G):
 
 @pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("G", [1, 4])
+def test_fp8_decode_widens_every_finite_code_exactly(q_dtype, G):
+    """Every finite E4M3 code goes through the decode kernel's widening: one-token
+    sequences whose cached V rows hold all 254 finite codes (each twice; the two NaN
+    codes replaced by 0), their K rows code 0, read by a decode-only call (G = 4 takes
+    the tensor-core path, G = 1 the CUDA-core one).  With one token P = 1, so each output
+    element is its code's value times v_scale (a power of two), exact in fp16 and in
+    bf16 (E4M3 values have at most 4 significant bits): it must equal the oracle's
+    decoding of the same code exactly."""
+    D, bs = 128, 16
+    wl = W.make_private("codes8", "fp8", [1, 1, 1, 1], 2 * G, 2, D, bs, seed=61, partition_size=0, q_dtype=q_dtype)
+    assert np.log2(wl.v_scale) == np.round(np.log2(wl.v_scale))
+    k, v = wl.k_cache.view(np.uint8), wl.v_cache.view(np.uint8)  # [NB, Hkv, D/16, bs, 16], [NB, Hkv, D, bs]
+    expect = np.zeros((4, 2 * G, D))
+    for s in range(4):
+        blk = int(wl.block_tables[s][0])
+        for h in range(2):
+            codes = ((np.arange(D) + (2 * s + h) * D) % 256).astype(np.uint8)
+            codes[(codes == 0x7F) | (codes == 0xFF)] = 0
+            v[blk, h, :, 0] = codes
+            k[blk, h, :, 0, :] = 0
+            expect[s, h * G:(h + 1) * G, :] = oracle.widen(codes, "fp8") * wl.v_scale
+    covered = {int(c) for s in range(4) for h in range(2) for c in v[int(wl.block_tables[s][0]), h, :, 0]}
+    assert covered == set(range(256)) - {0x7F, 0xFF}
+    out, _ = gpu_step(wl, write=False)
+    want = torch.from_numpy(expect).to(out.dtype).cuda()
+    # equal values (the code of -0 comes out as +0: the attention sum starts from +0)
+    assert torch.equal(out.float(), want.float())
+
+
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("G", [1, 4])
 def test_fp8_physical_permutation_is_bit_identical(q_dtype, G):
     wl = W.make_private("perm8", "fp8", [700, 33, 256, 1], 2 * G, 2, 128, 16, seed=36, partition_size=-1,
                         q_dtype=q_dtype)
