@@ -146,6 +146,29 @@ __device__ __forceinline__ void ld128(uint32_t taddr, float (&v)[128]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait
+__device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane; no wait (wait_st before
 // the columns are handed over)
 __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -178,6 +201,11 @@ __device__ __forceinline__ float2 f2unpack(uint64_t v) {
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
@@ -621,13 +649,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = __all_sync(0xffffffffu, wait(pvdone(X), ux & 1)))) break;
         fence_after();
         const float inv = 1.f / l;
+        const uint64_t inv2 = f2pack(inv, inv);
         uint32_t o16[D / 2];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float o[32];
-          ld32(t_o + c0, o);
+        static_assert(D % 64 == 0, "O read 64 columns at a time");
+        for (int c0 = 0; c0 < D; c0 += 64) {  // 64 columns per wait
+          float o[64];
+          ld64(t_o + c0, o);
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) o16[(c0 + j) / 2] = pack2<T>(o[j] * inv, o[j + 1] * inv);
+          for (int j = 0; j < 64; j += 2) {
+            const float2 v = f2unpack(mul2(f2pack(o[j], o[j + 1]), inv2));
+            o16[(c0 + j) / 2] = pack2<T>(v.x, v.y);
+          }
         }
         fence_before();
         mbar_arrive(ofree(X));
